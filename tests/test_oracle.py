@@ -1,0 +1,363 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each test below checks one oracle function against a closed form, a textbook special
+case, a library routine, a brute-force unroll on tiny inputs, or numbers printed on the
+pages (tests/golden).  They are chosen so that a dropped term, a wrong sign, a wrong
+index or a transposed operand in the oracle fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from recurrent_state_cache_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _unit_rows(r, T, K):
+    x = r.standard_normal((T, K))
+    return x / np.linalg.norm(x, axis=1, keepdims=True)
+
+
+def _head_case(seed, T, K, V, s0_std=0.3):
+    r = np.random.default_rng(seed)
+    q = _unit_rows(r, T, K)
+    k = _unit_rows(r, T, K)
+    v = r.standard_normal((T, V))
+    g = -np.logaddexp(0.0, r.standard_normal((T, K)))
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
+    S0 = r.standard_normal((V, K)) * s0_std
+    return q, k, v, g, beta, S0
+
+
+# ----------------------------------------------------------------------- storage dtype
+
+def test_bf16_round_matches_torch_rne():
+    torch = pytest.importorskip("torch")
+    r = np.random.default_rng(1)
+    x = (r.standard_normal(20000) * np.exp(r.uniform(-30, 30, 20000))).astype(np.float32)
+    # exact ties (low half == 0x8000) with even and odd kept mantissa
+    ties = (np.arange(1, 2001, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties, np.float32([0.0, -0.0, 1e-40, 3.0e38])])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+# ----------------------------------------------------------------------- short conv
+
+@pytest.mark.parametrize("T", [1, 2, 3, 7])
+def test_conv_is_direct_four_tap_filter(T):
+    r = np.random.default_rng(2)
+    D = 37
+    win = r.standard_normal((3, D))
+    x = r.standard_normal((T, D))
+    w = r.standard_normal((D, 4)).astype(np.float32)
+    new_win, y = oracle.conv_sequence(win, x, w)
+    ext = np.concatenate([win, x], axis=0)  # oldest first
+    for c in range(D):
+        ref = np.correlate(ext[:, c], w[c].astype(np.float64), mode="valid")
+        np.testing.assert_allclose(y[:, c], ref, rtol=1e-13, atol=1e-13)
+    # the window is the last three raw inputs, bit for bit
+    assert np.array_equal(new_win, ext[-3:])
+
+
+# ----------------------------------------------------------------------- delta rule
+
+def test_beta_zero_alpha_one_leaves_state_unchanged():
+    q, k, v, _, _, S0 = _head_case(3, T=5, K=8, V=6)
+    S, o, _ = oracle.recurrent_head(q, k, v, np.zeros((5, 8)), np.zeros(5), S0)
+    assert np.array_equal(S, S0)
+    np.testing.assert_allclose(o, q @ S0.T, rtol=1e-14, atol=1e-14)
+
+
+def test_single_token_from_zero_state():
+    q, k, v, g, beta, _ = _head_case(4, T=1, K=8, V=6)
+    S, o, d = oracle.recurrent_head(q, k, v, g, beta, np.zeros((6, 8)))
+    np.testing.assert_allclose(S, beta[0] * np.outer(v[0], k[0]), rtol=1e-14, atol=1e-15)
+    # the output reads the updated state: o = beta (k . q) v
+    np.testing.assert_allclose(o[0], beta[0] * (k[0] @ q[0]) * v[0], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(d[0], beta[0] * v[0], rtol=1e-14)
+
+
+def test_beta_one_writes_value_at_key():
+    q, k, v, g, _, S0 = _head_case(5, T=4, K=16, V=12)
+    S = S0
+    for t in range(4):  # after each token with beta = 1 and |k| = 1: S_new k = v
+        S, _, _ = oracle.recurrent_head(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1],
+                                        np.ones(1), S)
+        np.testing.assert_allclose(S @ k[t], v[t], rtol=1e-12, atol=1e-12)
+
+
+def _product_unroll(q, k, v, g, beta, S0):
+    """S_T = S0 prod_t M_t + sum_t beta_t v_t k_t^T prod_{u>t} M_u with
+    M_t = Diag(alpha_t) (I - beta_t k_t k_t^T); o_t = S_t q_t."""
+    T, K = k.shape
+    M = [np.diag(np.exp(g[t])) @ (np.eye(K) - beta[t] * np.outer(k[t], k[t])) for t in range(T)]
+    outs, S_list = [], []
+    for t_end in range(1, T + 1):
+        acc = S0.copy()
+        for t in range(t_end):
+            acc = acc @ M[t]
+        for t in range(t_end):
+            term = beta[t] * np.outer(v[t], k[t])
+            for u in range(t + 1, t_end):
+                term = term @ M[u]
+            acc = acc + term
+        S_list.append(acc)
+        outs.append(acc @ q[t_end - 1])
+    return S_list[-1], np.array(outs)
+
+
+@pytest.mark.parametrize("seed", [6, 7, 8])
+def test_matches_brute_force_product_unroll(seed):
+    # V != K so that a transposed state or operand cannot pass
+    q, k, v, g, beta, S0 = _head_case(seed, T=6, K=3, V=4)
+    S, o, _ = oracle.recurrent_head(q, k, v, g, beta, S0)
+    S_ref, o_ref = _product_unroll(q, k, v, g, beta, S0)
+    np.testing.assert_allclose(S, S_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_with_unit_gate_is_plain_delta_rule():
+    # alpha = 1: S <- S (I - beta k k^T) + beta v k^T, the textbook DeltaNet update
+    q, k, v, _, beta, S0 = _head_case(9, T=5, K=6, V=5)
+    S, _, _ = oracle.recurrent_head(q, k, v, np.zeros((5, 6)), beta, S0)
+    ref = S0.copy()
+    for t in range(5):
+        ref = ref @ (np.eye(6) - beta[t] * np.outer(k[t], k[t])) + beta[t] * np.outer(v[t], k[t])
+    np.testing.assert_allclose(S, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_unrolled_closed_form_of_the_pages():
+    # S_m = S_0 Diag(prod_i alpha_i) + sum_j d_j (k_j . prod_{i>j} alpha_i)^T
+    q, k, v, g, beta, S0 = _head_case(10, T=9, K=7, V=5)
+    S, _, d = oracle.recurrent_head(q, k, v, g, beta, S0)
+    G = np.cumsum(g, axis=0)
+    ref = S0 * np.exp(G[-1])[None, :]
+    for j in range(9):
+        ref = ref + np.outer(d[j], k[j] * np.exp(G[-1] - G[j]))
+    np.testing.assert_allclose(S, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,K,V", [(1, 16, 16), (63, 16, 8), (64, 16, 16), (65, 8, 16),
+                                   (130, 16, 16), (1312, 32, 32)])
+def test_chunkwise_equals_recurrence(T, K, V):
+    q, k, v, g, beta, S0 = _head_case(11 + T, T=T, K=K, V=V)
+    S_r, o_r, _ = oracle.recurrent_head(q, k, v, g, beta, S0)
+    S_c, o_c = oracle.chunkwise_head(q, k, v, g, beta, S0, C=64)
+    scale_o = np.max(np.abs(o_r))
+    scale_s = np.max(np.abs(S_r))
+    assert np.max(np.abs(o_c - o_r)) <= 1e-11 * scale_o
+    assert np.max(np.abs(S_c - S_r)) <= 1e-11 * scale_s
+
+
+# ----------------------------------------------------------------------- layer step
+
+def _pool_case(seed, H=2, K=8, V=6, P=5, st=oracle.F32, io=oracle.F32, gate=oracle.KDA):
+    r = np.random.default_rng(seed)
+    ssm, conv = inputs.pool_arrays(r, 1, P, H, K, V, st, io)
+    pool = oracle.Pool(1, P, H, K, V, st, io, gate, ssm, conv)
+    w = inputs.conv_weights(r, H, K, V)
+    return r, pool, w
+
+
+def test_layer_split_order_and_output_of_value_channels():
+    """S = 0, beta = 1 and identical raw q and k channels: each head's output is
+    (|k|^2 / (|k|^2 + eps)) times its conv'd value channels."""
+    H, K, V = 3, 8, 5
+    r, pool, w = _pool_case(12, H=H, K=K, V=V)
+    D = pool.D
+    pool.ssm[...] = 0
+    w[H * K:2 * H * K] = w[:H * K]                     # same taps for the k block as the q block
+    pool.conv[0, 2, :, H * K:2 * H * K] = pool.conv[0, 2, :, :H * K]
+    x = r.standard_normal(D).astype(np.float32)
+    x[H * K:2 * H * K] = x[:H * K]
+    g = np.zeros((1, H, K), np.float32)
+    beta = np.ones((1, H), np.float32)
+    ext = np.concatenate([pool.conv[0, 2].astype(np.float64), x[None].astype(np.float64)])
+    y = np.array([ext[:, c] @ w[c].astype(np.float64) for c in range(D)])
+    out = oracle.decode_step(pool, 0, [2], x[None], w, g, beta)
+    for h in range(H):
+        kk = y[H * K + h * K:H * K + (h + 1) * K]
+        ss = kk @ kk
+        vv = y[2 * H * K + h * V:2 * H * K + (h + 1) * V]
+        np.testing.assert_allclose(out[0, h], ss / (ss + 1e-6) * vv, rtol=1e-6, atol=1e-7)
+
+
+def test_layer_query_is_normalised_conv_of_q_block():
+    """beta = 0, alpha = 1: the state stays and o_h = S_h q_hat with q_hat the L2-normalised
+    conv output of head h's q channels (eps = 1e-6)."""
+    H, K, V = 2, 8, 6
+    r, pool, w = _pool_case(13, H=H, K=K, V=V)
+    D = pool.D
+    S0 = pool.ssm[0, 3].astype(np.float64).copy()
+    x = r.standard_normal(D).astype(np.float32)
+    ext = np.concatenate([pool.conv[0, 3].astype(np.float64), x[None].astype(np.float64)])
+    y = np.array([ext[:, c] @ w[c].astype(np.float64) for c in range(D)])
+    out = oracle.decode_step(pool, 0, [3], x[None], w, np.zeros((1, H, K), np.float32),
+                             np.zeros((1, H), np.float32))
+    for h in range(H):
+        qq = y[h * K:(h + 1) * K]
+        qh = qq / np.sqrt(qq @ qq + 1e-6)
+        np.testing.assert_allclose(out[0, h], S0[h] @ qh, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(pool.ssm[0, 3], S0, rtol=1e-7, atol=0)
+
+
+def test_gdn_gate_is_one_scalar_per_head():
+    H, K, V = 2, 8, 6
+    r, pool_k, w = _pool_case(14, H=H, K=K, V=V, gate=oracle.KDA)
+    pool_g = oracle.Pool(1, 5, H, K, V, oracle.F32, oracle.F32, oracle.GDN,
+                         pool_k.ssm, pool_k.conv)
+    x = r.standard_normal((1, pool_k.D)).astype(np.float32)
+    gh = -np.abs(r.standard_normal((1, H))).astype(np.float32)
+    beta = np.full((1, H), 0.7, np.float32)
+    o_g = oracle.decode_step(pool_g, 0, [1], x, w, gh, beta)
+    o_k = oracle.decode_step(pool_k, 0, [1], x, w, np.repeat(gh[..., None], K, -1), beta)
+    assert np.array_equal(o_g, o_k)
+    assert np.array_equal(pool_g.ssm, pool_k.ssm)
+
+
+def test_decode_touches_only_its_slots():
+    r, pool, w = _pool_case(15, P=6)
+    before_s, before_c = pool.ssm.copy(), pool.conv.copy()
+    slots = np.int32([4, 1])
+    x = inputs.projections(r, (2,), pool.H, pool.K, pool.V, oracle.F32)
+    g, beta = inputs.gates(r, (2,), pool.H, pool.K, oracle.KDA)
+    oracle.decode_step(pool, 0, slots, x, w, g, beta)
+    untouched = [s for s in range(7) if s not in (1, 4)]
+    assert np.array_equal(pool.ssm[0, untouched], before_s[0, untouched])
+    assert np.array_equal(pool.conv[0, untouched], before_c[0, untouched])
+    # window: rows shift up by one and the new raw input lands in the last row
+    for b, s in enumerate(slots):
+        assert np.array_equal(pool.conv[0, s, :2], before_c[0, s, 1:])
+        assert np.array_equal(pool.conv[0, s, 2], x[b])
+
+
+def test_bf16_storage_rounds_only_at_store():
+    """bf16 decode = fp32-storage decode of the same widened inputs, then bf16 rounding of
+    the stored state and output (rounding happens once, at the store)."""
+    H, K, V = 2, 8, 6
+    r = np.random.default_rng(16)
+    ssm, conv = inputs.pool_arrays(r, 1, 4, H, K, V, oracle.BF16, oracle.BF16)
+    w = inputs.conv_weights(r, H, K, V)
+    x = inputs.projections(r, (2,), H, K, V, oracle.BF16)
+    g, beta = inputs.gates(r, (2,), H, K, oracle.KDA)
+    pb = oracle.Pool(1, 4, H, K, V, oracle.BF16, oracle.BF16, oracle.KDA, ssm, conv)
+    ob = oracle.decode_step(pb, 0, [1, 3], x, w, g, beta)
+    # the same step in fp64 storage precision via the head recurrence
+    for b, s in enumerate([1, 3]):
+        win = oracle.bf16_to_f64(conv[0, s])
+        xin = oracle.bf16_to_f64(x[b])
+        new_win, y = oracle.conv_sequence(win, xin[None], w)
+        assert np.array_equal(oracle.bf16_round(new_win), pb.conv[0, s])
+        for h in range(H):
+            qq = y[0, h * K:(h + 1) * K]
+            kk = y[0, H * K + h * K:H * K + (h + 1) * K]
+            vv = y[0, 2 * H * K + h * V:2 * H * K + (h + 1) * V]
+            qh, kh = qq / np.sqrt(qq @ qq + 1e-6), kk / np.sqrt(kk @ kk + 1e-6)
+            S, o, _ = oracle.recurrent_head(qh[None], kh[None], vv[None], g[b, h][None],
+                                            beta[b, h:h + 1], oracle.bf16_to_f64(ssm[0, s, h]))
+            assert np.array_equal(oracle.bf16_round(S), pb.ssm[0, s, h])
+            assert np.array_equal(oracle.bf16_round(o[0]), ob[b, h])
+
+
+# ----------------------------------------------------------------------- prefill
+
+def test_prefill_equals_decode_steps():
+    """Prefill of T tokens = T decode steps, except that storage rounding happens once at
+    the end (fp32 storage: agreement to fp32 rounding)."""
+    H, K, V, T = 2, 8, 6, 7
+    r, pool, w = _pool_case(17, H=H, K=K, V=V)
+    pool2 = oracle.Pool(1, 5, H, K, V, oracle.F32, oracle.F32, oracle.KDA, pool.ssm, pool.conv)
+    x = inputs.projections(r, (T,), H, K, V, oracle.F32)
+    g, beta = inputs.gates(r, (T,), H, K, oracle.KDA)
+    out = oracle.prefill(pool, 0, [2], [0, T], x, w, g, beta)
+    outs = [oracle.decode_step(pool2, 0, [2], x[t:t + 1], w, g[t:t + 1], beta[t:t + 1])[0]
+            for t in range(T)]
+    np.testing.assert_allclose(out, np.stack(outs), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(pool.ssm, pool2.ssm, rtol=1e-5, atol=1e-6)
+    assert np.array_equal(pool.conv, pool2.conv)
+
+
+def test_prefill_fresh_state_and_packed_sequences():
+    H, K, V = 2, 8, 6
+    r, pool, w = _pool_case(18, H=H, K=K, V=V)
+    lens = [5, 2, 9]
+    cu = inputs.cu_seqlens(lens)
+    x = inputs.projections(r, (cu[-1],), H, K, V, oracle.F32)
+    g, beta = inputs.gates(r, (cu[-1],), H, K, oracle.KDA)
+    ref = oracle.Pool(1, 5, H, K, V, oracle.F32, oracle.F32, oracle.KDA, pool.ssm, pool.conv)
+    out = oracle.prefill(pool, 0, [3, 1, 5], cu, x, w, g, beta, has_init=[1, 0, 1])
+    # each sequence alone gives the same result; the fresh one starts from zeros
+    ref.ssm[0, 1] = 0
+    ref.conv[0, 1] = 0
+    for n, s in enumerate([3, 1, 5]):
+        a, b = cu[n], cu[n + 1]
+        o_n = oracle.prefill(ref, 0, [s], [0, b - a], x[a:b], w, g[a:b], beta[a:b])
+        assert np.array_equal(o_n, out[a:b])
+    assert np.array_equal(ref.ssm, pool.ssm)
+    assert np.array_equal(ref.conv, pool.conv)
+
+
+# ----------------------------------------------------------------------- copy and spec
+
+def test_slot_copy_bytes_and_mask():
+    r, pool, _ = _pool_case(19, P=6, st=oracle.BF16, io=oracle.BF16)
+    before_s, before_c = pool.ssm.copy(), pool.conv.copy()
+    oracle.slot_copy(pool, -1, [1, 2, 3], [4, 5, 6], mask=[1, 0, 1])
+    assert np.array_equal(pool.ssm[:, 4], before_s[:, 1])
+    assert np.array_equal(pool.conv[:, 6], before_c[:, 3])
+    assert np.array_equal(pool.ssm[:, 5], before_s[:, 5])   # masked out
+    assert np.array_equal(pool.ssm[:, :4], before_s[:, :4])
+
+
+@pytest.mark.parametrize("st", [oracle.F32, oracle.BF16])
+def test_spec_commit_equals_accepted_decode_steps(st):
+    """COMMIT(a) after VERIFY of T tokens = a+1 decode steps: windows bit-exact; states
+    equal up to the storage rounding that decode applies after every step."""
+    H, K, V, T, Lc = 2, 8, 6, 5, 8
+    r, pool, w = _pool_case(20, H=H, K=K, V=V, st=st, io=st)
+    B = 3
+    slots = np.int32([5, 2, 4])
+    x = inputs.projections(r, (B, T), H, K, V, st)
+    g, beta = inputs.gates(r, (B, T), H, K, oracle.KDA)
+    accept = np.int32([0, 4, 2])
+    ref = oracle.Pool(1, 5, H, K, V, st, st, oracle.KDA, pool.ssm, pool.conv)
+    before = pool.ssm.copy(), pool.conv.copy()
+    sS, sC, out = oracle.spec_verify(pool, 0, slots, T, Lc, x, w, g, beta)
+    assert np.array_equal(pool.ssm, before[0]) and np.array_equal(pool.conv, before[1])
+    oracle.spec_commit(pool, 0, slots, T, Lc, sS, sC, accept)
+    tol = 1e-6 if st == oracle.F32 else 2e-2
+    for b in range(B):
+        for t in range(accept[b] + 1):
+            o = oracle.decode_step(ref, 0, slots[b:b + 1], x[b, t:t + 1], w, g[b, t:t + 1],
+                                   beta[b, t:t + 1])
+            err = np.max(np.abs(oracle.to_f64(o[0], st) - oracle.to_f64(out[b, t], st)))
+            assert err <= tol * np.max(np.abs(oracle.to_f64(o[0], st)))
+        s = slots[b]
+        assert np.array_equal(pool.conv[0, s], ref.conv[0, s])
+        a, e = oracle.to_f64(pool.ssm[0, s], st), oracle.to_f64(ref.ssm[0, s], st)
+        assert np.max(np.abs(a - e)) <= tol * np.max(np.abs(e))
+
+
+# ----------------------------------------------------------------------- pool layout
+
+def test_pool_bytes_reproduce_logged_sizes():
+    gold = json.load(open(os.path.join(GOLDEN, "pool_sizes.json")))
+    shp = gold["shape"]
+    dt = {"f32": oracle.F32, "bf16": oracle.BF16}
+    for p in gold["pools"]:
+        s, c = oracle.pool_bytes(shp["layers"], p["slots"], shp["H"], shp["K"], shp["V"],
+                                 dt[p["state_dtype"]], dt[p["conv_dtype"]])
+        assert round(s / 2**30, 2) == p["ssm_gib"], p
+        assert round(c / 2**30, 2) == p["conv_gib"], p
+    pr = gold["per_request"]
+    # one slot of all layers = one row per layer: (slots + 1) rows with slots = 0
+    s, c = oracle.pool_bytes(pr["layers"], 0, pr["H"], pr["K"], pr["V"], oracle.BF16, oracle.BF16)
+    assert round(s / 2**20, 1) == pr["ssm_mib"]
+    assert round(c / 2**20, 2) == pr["conv_mib"]
+    assert round((pr["ssm_mib"] + pr["conv_mib"]) * 8, 1) == pr["tp8_total_mib"]
