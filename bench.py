@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the slot-indexed recurrent-state layer step on one GB300 (or N replicas).
+
+Headline (one JSON line on stdout): KDA decode over a Kimi-K3 TP8-shard pool -- 69
+layers, H=12 heads, K=V=128, bf16 state and io, 320 usable slots, 64 requests with
+distinct random slots, one token per request per step.  A step runs all 69 layer
+launches (replayed from a CUDA graph); value = decode tokens/s per layer =
+batch * layers / step time.  The per-step state working set (64 x 69 x 786 KB moved)
+is ~14x the 129 MB L2, so no flush is needed between steps.
+
+Legs reported in the same line (each timed separately with CUDA events):
+  gdn_decode   GDN decode, H=32, K=V=128, fp32 state, 48 layers, 1024-slot pool,
+               batch 1/16/64/256
+  prefill      one KDA layer, 13600 tokens in chunked-prefill calls of 6144/6144/1312,
+               a slot snapshot (ssm_slot_copy) after each call
+  slot_copy    64 (src, dst) pairs of the 69-layer decode pool, all layers, one launch
+  spec         verify of 8 tokens (anchor + 7 drafts) for 64 requests into a 16-deep
+               cache, then commit of a seeded accept count per request
+The oracle (plain fp64 C, one host core) is timed on a bounded sample as cpu_baseline.
+
+--impl reference times the oracle itself on the same workload (rank 0 only).
+Multi-GPU: replicas only (the layer step has no exchange between requests or heads);
+under torchrun every rank runs the full workload on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE_METRIC = "decode tokens/s per layer and achieved HBM GB/s (% of peak); prefill tok/s"
+
+
+# --------------------------------------------------------------------------- plumbing
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec or all/none")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while a region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); smax.append(float(f[2])); power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def timed(fn, steps, warmup, stream, dist=None):
+    """Run fn warmup times, then time exactly `steps` calls with CUDA events on `stream`,
+    bracketed by barrier + synchronize.  Returns milliseconds per step."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1) / steps
+
+
+def graph_of(fn, stream):
+    """Capture fn (a sequence of library launches on `stream`) into a CUDA graph."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm: loads every kernel module before capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+# --------------------------------------------------------------------------- workloads
+
+def _softplus_neg(t):
+    import torch
+    return -torch.nn.functional.softplus(t)
+
+
+class DecodeWorkload:
+    """Per-layer inputs of one decode step, resident on the device; seeded."""
+
+    def __init__(self, dev, layers, P, B, H, K, V, st, io, gate, seed=0):
+        import torch
+        import recurrent_state_cache_gb300 as rsc
+        from recurrent_state_cache_gb300 import inputs
+        self.rsc = rsc
+        self.layers, self.P, self.B, self.H, self.K, self.V = layers, P, B, H, K, V
+        self.st, self.io, self.gate = st, io, gate
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        sdt, idt = rsc.binding.TORCH_DTYPE[st], rsc.binding.TORCH_DTYPE[io]
+        D = H * (2 * K + V)
+        self.D = D
+        ssm = torch.empty((layers, P + 1, H, V, K), dtype=sdt, device=dev).normal_(0, 0.1, generator=gen)
+        conv = torch.empty((layers, P + 1, 3, D), dtype=idt, device=dev).normal_(0, 0.1, generator=gen)
+        self.pool = rsc.SlotPool(layers, P, H, K, V, st, io, gate, dev, ssm=ssm, conv=conv)
+        r = inputs.rng(seed)
+        self.slots = torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev)
+        gshape = (layers, B, H, K) if gate == rsc.KDA else (layers, B, H)
+        self.qkv = torch.empty((layers, B, D), dtype=idt, device=dev).normal_(0, 1, generator=gen)
+        self.g = _softplus_neg(torch.empty(gshape, device=dev).normal_(0, 1, generator=gen))
+        self.beta = torch.sigmoid(torch.empty((layers, B, H), device=dev).normal_(0, 1, generator=gen))
+        self.w = torch.empty((layers, D, 4), device=dev).normal_(0, 0.5, generator=gen)
+        self.out = torch.empty((layers, B, H, V), dtype=idt, device=dev)
+
+    def step(self):
+        rsc = self.rsc
+        for l in range(self.layers):
+            rsc.kda_decode_step(self.pool, l, self.slots, self.qkv[l], self.w[l], self.g[l],
+                                self.beta[l], self.out[l])
+
+    def bytes_per_launch(self):
+        """Algorithmic bytes of one layer launch: per request the state read + written,
+        window read + written, qkv, g, beta, out and its slot id; plus the layer's taps."""
+        ss = 4 if self.st == 0 else 2
+        io = 4 if self.io == 0 else 2
+        H, K, V, D = self.H, self.K, self.V, self.D
+        gw = K if self.gate == 0 else 1
+        per_req = (2 * H * V * K * ss + 2 * 3 * D * io + D * io + H * gw * 4 + H * 4
+                   + H * V * io + 4)
+        return self.B * per_req + D * 4 * 4
+
+
+# --------------------------------------------------------------------------- legs
+
+def leg_gdn(dev, peaks, stream, batches=(1, 16, 64, 256)):
+    import torch
+    from recurrent_state_cache_gb300 import binding as b
+    res = {"config": "GDN decode, H=32, K=V=128, fp32 state, bf16 io, 48 layers, 1024 slots"}
+    wl = DecodeWorkload(dev, 48, 1024, max(batches), 32, 128, 128, b.F32, b.BF16, b.GDN, seed=1)
+    full_slots = wl.slots
+    rows = []
+    for B in batches:
+        wl.B = B
+        wl.slots = full_slots[:B].contiguous()
+        sub = (wl.qkv, wl.g, wl.beta, wl.out)
+        wl.qkv, wl.g, wl.beta, wl.out = (x[:, :B].contiguous() for x in sub)
+        graph = graph_of(wl.step, stream)
+        ms = timed(graph.replay, 20, 3, stream)
+        wl.qkv, wl.g, wl.beta, wl.out = sub
+        per_launch = ms / wl.layers
+        gbs = wl.bytes_per_launch() / (per_launch * 1e-3) / 1e9
+        rows.append({"batch": B, "us_per_layer": round(per_launch * 1e3, 3),
+                     "tokens_per_s_per_layer": round(B / (per_launch * 1e-3), 1),
+                     "hbm_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)})
+    res["sweep"] = rows
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_prefill(dev, peaks, stream):
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    from recurrent_state_cache_gb300 import binding as b, inputs
+    H, K, V = 12, 128, 128
+    chunks = (6144, 6144, 1312)
+    T = sum(chunks)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    D = H * (2 * K + V)
+    pool = rsc.SlotPool(1, 8, H, K, V, b.BF16, b.BF16, b.KDA, dev)
+    qkv = torch.empty((T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((T, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((T, H), device=dev).normal_(0, 1, generator=gen))
+    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
+    out = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(rsc.kda_prefill_workspace_size(pool, 1, max(chunks)), dtype=torch.uint8, device=dev)
+    slot = torch.tensor([1], dtype=torch.int32, device=dev)
+    snaps = [torch.tensor([s], dtype=torch.int32, device=dev) for s in (2, 3, 4)]
+    fresh = torch.tensor([0], dtype=torch.uint8, device=dev)
+    cus = [torch.tensor([0, c], dtype=torch.int32, device=dev) for c in chunks]
+    offs = np.cumsum((0,) + chunks)
+
+    def run():
+        for i, c in enumerate(chunks):
+            a, e = int(offs[i]), int(offs[i + 1])
+            rsc.kda_prefill_chunk(pool, 0, slot, cus[i], qkv[a:e], w, g[a:e], beta[a:e],
+                                  has_initial_state=fresh if i == 0 else None, out=out[a:e],
+                                  workspace=ws)
+            rsc.ssm_slot_copy(pool, 0, slot, snaps[i])
+
+    graph = graph_of(run, stream)
+    ms = timed(graph.replay, 5, 2, stream)
+    flops = T * H * (6 * 64 * K + 4 * 64 * V + 6 * K * V)
+    io_bytes = T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2
+    res = {"config": "1 KDA layer, H=12, K=V=128, bf16, 13600 tokens as 6144/6144/1312, snapshot copy after each",
+           "ms_per_prefill": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+           "algorithmic_tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+           "tensor_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
+           "io_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
+           "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "path": "token-serial fp32 recurrence"}
+    return res
+
+
+def leg_copy(dev, peaks, stream, wl):
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    from recurrent_state_cache_gb300 import inputs
+    r = inputs.rng(3)
+    perm = r.permutation(wl.P) + 1
+    src = torch.from_numpy(perm[:64].astype(np.int32)).to(dev)
+    dst = torch.from_numpy(perm[64:128].astype(np.int32)).to(dev)
+    fn = lambda: rsc.ssm_slot_copy(wl.pool, -1, src, dst)
+    ms = timed(fn, 10, 3, stream)
+    ss, io = 2, 2
+    row = wl.H * wl.V * wl.K * ss + 3 * wl.D * io
+    nbytes = 2 * row * wl.layers * 64
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"config": "64 pairs x 69 layers of the decode pool, one launch pair",
+            "ms": round(ms, 4), "bytes": nbytes, "hbm_gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
+def leg_spec(dev, peaks, stream):
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    from recurrent_state_cache_gb300 import binding as b, inputs
+    H, K, V, B, T, L, P = 12, 128, 128, 64, 8, 16, 320
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    D = H * (2 * K + V)
+    ssm = torch.empty((1, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    conv = torch.empty((1, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    pool = rsc.SlotPool(1, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
+    r = inputs.rng(4)
+    slots = torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev)
+    accept = torch.from_numpy(inputs.accept_counts(r, B, T)).to(dev)
+    qkv = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((B, T, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((B, T, H), device=dev).normal_(0, 1, generator=gen))
+    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
+    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    spec_ssm = torch.empty((B, L, H, V, K), dtype=torch.bfloat16, device=dev)
+    spec_conv = torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev)
+    verify = lambda: rsc.kda_spec_verify_commit(pool, 0, rsc.VERIFY, slots, T, L, spec_ssm, spec_conv,
+                                                qkv, w, g, beta, out)
+    commit = lambda: rsc.kda_spec_verify_commit(pool, 0, rsc.COMMIT, slots, T, L, spec_ssm, spec_conv,
+                                                accept=accept)
+    ms_v = timed(verify, 10, 3, stream)
+    ms_c = timed(commit, 10, 3, stream)
+    S, Wb = H * V * K * 2, 3 * D * 2
+    vb = B * (S + T * S + Wb + T * Wb + T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2 + 4)
+    cb = B * 2 * (S + Wb)
+    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), cache depth 16",
+            "verify_ms": round(ms_v, 4), "verify_gbs": round(vb / (ms_v * 1e-3) / 1e9, 1),
+            "verify_frac": round(vb / (ms_v * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "commit_ms": round(ms_c, 4), "commit_gbs": round(cb / (ms_c * 1e-3) / 1e9, 1),
+            "commit_frac": round(cb / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+class OracleDecodeSample:
+    """One layer-step of the headline workload (64 requests, H=12, K=V=128, bf16 state
+    and io, KDA gate) on the CPU oracle; inputs built once, outside any timing."""
+
+    def __init__(self, seed=0):
+        import oracle
+        from recurrent_state_cache_gb300 import inputs
+        self.oracle = oracle
+        H, K, V, B = 12, 128, 128, 64
+        self.B = B
+        r = inputs.rng(seed)
+        ssm, conv = inputs.pool_arrays(r, 1, B, H, K, V, oracle.BF16, oracle.BF16)
+        self.pool = oracle.Pool(1, B, H, K, V, oracle.BF16, oracle.BF16, oracle.KDA, ssm, conv)
+        self.w = inputs.conv_weights(r, H, K, V)
+        self.slots = inputs.distinct_slots(r, B, B)
+        self.x = inputs.projections(r, (B,), H, K, V, oracle.BF16)
+        self.g, self.beta = inputs.gates(r, (B,), H, K, oracle.KDA)
+
+    def step(self):
+        self.oracle.decode_step(self.pool, 0, self.slots, self.x, self.w, self.g, self.beta)
+
+
+def oracle_decode_sample(seconds: float, seed=0):
+    """Time oracle layer-steps of the headline workload until `seconds` of CPU work;
+    returns (tokens/s per layer, description of the sample)."""
+    s = OracleDecodeSample(seed)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        s.step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return s.B * n / el, f"{n} layer-steps of 64 requests (H=12, K=V=128, bf16) in {el:.1f} s"
+
+
+# --------------------------------------------------------------------------- main
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    total_t0 = time.perf_counter()
+    sample = OracleDecodeSample(0)
+    for _ in range(args.warmup):
+        sample.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample.step()
+    ms = 1e3 * (time.perf_counter() - t0) / args.steps
+    value = 64 / (ms * 1e-3)
+    line = {"metric": HEADLINE_METRIC, "value": round(value, 3), "unit": "tokens/s per layer",
+            "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "kda_decode_kimi_k3_tp8_shard", "layers_per_step": 1,
+                       "batch": 64, "H": 12, "K": 128, "V": 128, "state_dtype": "bf16"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s per layer", "cores": 1,
+                             "kind": "oracle",
+                             "sample": "each step: one layer-step of 64 requests of the headline workload"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s per layer",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - total_t0, 1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    from recurrent_state_cache_gb300 import _build, binding as b
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    # ---- headline: Kimi-K3 shard KDA decode, 69 layers, batch 64
+    wl = DecodeWorkload(dev, 69, 320, 64, 12, 128, 128, b.BF16, b.BF16, b.KDA, seed=0)
+    graph = graph_of(wl.step, stream)
+    with ClockSampler(local) as clk:
+        ms = timed(graph.replay, args.steps, args.warmup, stream, dist)
+    ms_max = max_over_ranks(ms, dist, dev)
+    units = wl.B * wl.layers
+    value = sum_over_ranks(units, dist, dev) / (ms_max * 1e-3)
+    per_launch_s = ms * 1e-3 / wl.layers
+    bpl = wl.bytes_per_launch()
+    achieved = bpl / per_launch_s / 1e9
+
+    # ---- e2e through the public API with pinned host buffers
+    h_qkv = wl.qkv.cpu().pin_memory()
+    h_g, h_beta = wl.g.cpu().pin_memory(), wl.beta.cpu().pin_memory()
+    h_out = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+
+    def e2e_step():
+        wl.qkv.copy_(h_qkv, non_blocking=True)
+        wl.g.copy_(h_g, non_blocking=True)
+        wl.beta.copy_(h_beta, non_blocking=True)
+        wl.step()
+        h_out.copy_(wl.out, non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 200))
+    ms_e2e = timed(e2e_step, e2e_steps, args.warmup, stream, dist)
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
+    h2d = h_qkv.numel() * h_qkv.element_size() + h_g.numel() * 4 + h_beta.numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+
+    legs = {}
+    want = set(["gdn", "prefill", "copy", "spec"] if args.legs == "all" else
+               ([] if args.legs == "none" else args.legs.split(",")))
+    if "copy" in want:
+        legs["slot_copy"] = leg_copy(dev, peaks, stream, wl)
+    del graph
+    if "spec" in want:
+        legs["spec"] = leg_spec(dev, peaks, stream)
+    if "prefill" in want:
+        legs["prefill"] = leg_prefill(dev, peaks, stream)
+    del wl
+    torch.cuda.empty_cache()
+    if "gdn" in want:
+        legs["gdn_decode"] = leg_gdn(dev, peaks, stream)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample = oracle_decode_sample(args.cpu_seconds)
+        cpu = {"value": round(v, 3), "unit": "tokens/s per layer", "cores": 1, "kind": "oracle",
+               "sample": sample}
+
+    clocks = clk.summary()
+    line = {
+        "metric": HEADLINE_METRIC, "value": round(value, 1), "unit": "tokens/s per layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "kda_decode_kimi_k3_tp8_shard", "layers": 69, "batch": 64,
+                   "pool_slots": 320, "H": 12, "K": 128, "V": 128, "state_dtype": "bf16",
+                   "io_dtype": "bf16", "tokens_per_request_per_step": 1,
+                   "l2": "inputs larger than L2: 1.74 GB of state moved per step, no flush",
+                   "launch": "69 kda_decode_step launches per step replayed from a CUDA graph",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None, "kernel": "kda_decode_kernel",
+                     "bytes_per_launch": bpl, "peak_source": peaks["source"]},
+        "e2e": {"value": round(sum_over_ranks(units, dist, dev) / (ms_e2e * 1e-3), 1),
+                "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 69 * args.steps,
+        "clocks": clocks,
+        "legs": legs,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+/*
+ * rsc.h -- C ABI of the GB300 slot-indexed recurrent-state cache (librsc.so).
+ *
+ * The library runs one layer step of a KDA / GDN linear-attention layer over a pool of
+ * per-request recurrent states, entirely in hand-written sm_103a CUDA kernels:
+ *   short conv (kernel 4, depthwise, causal) over the projected q/k/v with the slot's
+ *   window of the last three raw inputs, L2 normalisation of q and k, and the gated
+ *   delta rule on the slot's state S[H][V][K]:
+ *       S <- S Diag(alpha);  d = beta (v - S k);  S <- S + d k^T;  o = S q
+ *   with alpha = exp(g) per key channel (KDA) or per head (GDN).
+ * Sources (web pages; cited by title and section):
+ *   [p1] "SGLang Qwen3/kimi-k3 Hybrid Linear Mamba KV cache管理" (xxmr.cn/news/181459):
+ *        "Conv state" (window of the last 3 q/k/v vectors), the KDA recurrent update and
+ *        its ReplaySSM replay steps (normalised key, alpha = exp(g), decay, delta, rank-1),
+ *        the speculative conv-window snapshots and their scatter commit, and the masked
+ *        track copy of conv and ssm state between slots.
+ *   [p2] "SGLang之KV Cache内存池机制" (yuyanqi.com) §8.2 (pool shapes, row 0 padding)
+ *        and §8.5 (forward_decode / forward_extend: state looked up by cache_indices,
+ *        updated in place; chunked extend with chunk 64 and cu_seqlens).
+ *   [p4] "sglang-mamba-kv-cache-kimi-k3" (treerouter.ai) §3.2 (conv and SSM state shapes).
+ *
+ * Conventions for every call
+ *   - Every pointer argument documented "device" is CUDA device memory owned by the
+ *     caller; the library never allocates, frees or retains device memory, except where
+ *     a call says otherwise.  Pointers documented "host" are read before the call returns.
+ *   - Device arrays read or written with 16-byte vector accesses must be 16-byte
+ *     aligned: pool bases, qkv, out, conv_w, spec caches, workspace, and g of a
+ *     prefill.  Other arrays need their element alignment.  Otherwise RSC_EALIGN.
+ *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Host-side validation failures return a negative status before anything
+ *     is launched.  A CUDA launch failure returns RSC_ECUDA.
+ *   - Values the host cannot see (slot ids, accept counts, sequence offsets: all device
+ *     arrays) are checked on the device.  A bad row is skipped (nothing of that row is
+ *     written) and a bit is OR-ed into the pool's device error word; read it with
+ *     rsc_get_device_error.  No kernel traps or asserts.
+ *   - Slot ids within one call must be distinct (states are updated in place); slot 0
+ *     is the padding row and is a legal target for padded batch entries.
+ *   - Calls that touch the same slots must be ordered on one stream by the caller.
+ */
+#ifndef RSC_H
+#define RSC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+#define RSC_OK        0
+#define RSC_EINVAL   -1 /* null pointer, bad count, bad mode                        */
+#define RSC_ERANGE   -2 /* layer, batch, length or cache depth out of range         */
+#define RSC_EDTYPE   -3 /* unsupported dtype, gate, head dims or conv kernel        */
+#define RSC_EALIGN   -4 /* a vector-accessed pointer is not 16-byte aligned         */
+#define RSC_ECUDA    -5 /* a CUDA runtime call or launch failed                      */
+#define RSC_ENOSPACE -6 /* caller-provided workspace too small                       */
+
+/* Bits of the device error word. */
+#define RSC_DEVERR_SLOT   1 /* a slot id outside [0, num_slots]                      */
+#define RSC_DEVERR_ACCEPT 2 /* an accept count outside [0, T-1]                      */
+#define RSC_DEVERR_SEQ    4 /* cu_seqlens not non-decreasing within [0, total]       */
+
+typedef enum { RSC_F32 = 0, RSC_BF16 = 1 } rsc_dtype;
+typedef enum { RSC_GATE_KDA = 0, RSC_GATE_GDN = 1 } rsc_gate;
+typedef enum { RSC_SPEC_VERIFY = 0, RSC_SPEC_COMMIT = 1 } rsc_spec_mode;
+
+/* Pool layout ([p2] §8.2; [p1] "Conv state"; [p4] §3.2), D = H*(2K+V):
+ *   ssm  [num_layers][num_slots+1][H][V][K]  state_dtype, K contiguous
+ *   conv [num_layers][num_slots+1][3][D]     conv_dtype, row 0 the oldest input;
+ *        channels [q: H*K | k: H*K | v: H*V], head-major inside each block
+ * Row 0 of each layer is padding.  conv_dtype is also the dtype of the projected
+ * inputs (qkv) and of the outputs of every call.
+ * Supported: head_k in {64, 128}, head_v in {64, 128}, conv_kernel == 4,
+ * state_dtype and conv_dtype each RSC_F32 or RSC_BF16, gate KDA or GDN. */
+typedef struct rsc_pool_desc {
+  int32_t num_layers;
+  int32_t num_slots;    /* usable slots P; the arrays hold P+1 rows per layer       */
+  int32_t num_heads;    /* H (heads of this GPU's shard)                           */
+  int32_t head_k;       /* K                                                       */
+  int32_t head_v;       /* V                                                       */
+  int32_t conv_kernel;  /* must be 4                                               */
+  int32_t state_dtype;  /* rsc_dtype of ssm                                        */
+  int32_t conv_dtype;   /* rsc_dtype of conv, qkv and outputs                      */
+  int32_t gate;         /* rsc_gate                                                */
+  void *ssm_base;       /* device, 16-byte aligned, caller-owned                    */
+  void *conv_base;      /* device, 16-byte aligned, caller-owned                    */
+  int32_t *dev_error;   /* device, one int32 zeroed by the caller, caller-owned      */
+} rsc_pool_desc;
+
+typedef struct rsc_pool rsc_pool; /* opaque host handle */
+
+/* Validate a pool description and record its layout in a host handle (*out).  Owns no
+ * device memory; performs no CUDA call.  Errors: RSC_EINVAL (null), RSC_ERANGE (counts),
+ * RSC_EDTYPE (dims, dtypes, gate, conv kernel), RSC_EALIGN (bases). */
+int ssm_pool_create(const rsc_pool_desc *desc, rsc_pool **out);
+
+/* Free the host handle (NULL is a no-op).  Device memory stays the caller's. */
+int ssm_pool_destroy(rsc_pool *pool);
+
+/* Bytes the caller must allocate for ssm_base and conv_base of a description (only
+ * the counts, dims and dtypes of desc are read).  Host only. */
+int ssm_pool_bytes(const rsc_pool_desc *desc, uint64_t *ssm_bytes, uint64_t *conv_bytes);
+
+/* Decode: one token per request ([p2] §8.5 forward_decode).
+ *   slot_ids [batch]      device int32, distinct, each in [0, num_slots]
+ *   qkv      [batch][D]   device, conv_dtype: projected inputs before the conv
+ *   conv_w   [D][4]       device fp32: taps 0..2 act on window rows 0..2, tap 3 on qkv
+ *   g        [batch][H][K] (KDA) or [batch][H] (GDN)  device fp32 log-decay, alpha=exp(g)
+ *   beta     [batch][H]   device fp32
+ *   out      [batch][H][V] device, conv_dtype: o = S q from the updated state
+ * Each slot's window rolls (rows 1,2 move to 0,1; qkv lands in row 2) and its state is
+ * updated in place; both are rounded once to their storage dtype.  batch == 0 is a
+ * no-op.  Errors: RSC_EINVAL, RSC_ERANGE (layer), RSC_EALIGN, RSC_ECUDA. */
+int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                    const void *qkv, const float *conv_w, const float *g,
+                    const float *beta, void *out, void *stream);
+
+/* Workspace bytes kda_prefill_chunk needs for num_seqs sequences of total_tokens
+ * tokens (host only). */
+int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tokens,
+                               size_t *bytes);
+
+/* Chunked prefill ([p2] §8.5 forward_extend: initial state from the pool, final state
+ * written back in place; sequences packed along tokens by cu_seqlens).  The result is
+ * the token-by-token recurrence over each sequence; state and window are rounded once,
+ * at the end of the call.
+ *   slot_ids          [num_seqs]    device int32, distinct
+ *   cu_seqlens        [num_seqs+1]  device int32, cu[0] = 0, non-decreasing, cu[N] = total
+ *   has_initial_state [num_seqs]    device uint8 or NULL (= all 1); 0 starts that
+ *                                   sequence from a zero state and a zero window
+ *   qkv [total][D], g [total][H][K] or [total][H], beta [total][H], out [total][H][V]
+ *   workspace         device, >= kda_prefill_workspace_size bytes, 16-byte aligned
+ * bf16-state pools run the chunkwise form (chunk 64, intra-chunk products on the
+ * tensor cores); fp32-state pools run the recurrence token by token in fp32.
+ * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ENOSPACE, RSC_ECUDA. */
+int kda_prefill_chunk(rsc_pool *pool, int layer, const int32_t *slot_ids,
+                      const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                      const uint8_t *has_initial_state, const void *qkv,
+                      const float *conv_w, const float *g, const float *beta, void *out,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Slot copy ([p1] masked track copy: conv[dst] = conv[src], ssm[dst] = ssm[src]).
+ *   layer  >= 0 copies that layer, -1 copies every layer
+ *   src, dst [n] device int32; dst distinct and disjoint from src
+ *   mask     [n] device uint8 or NULL (= copy all); rows with mask 0 are skipped
+ * Bytes are copied unchanged.  Errors: RSC_EINVAL, RSC_ERANGE, RSC_ECUDA. */
+int ssm_slot_copy(rsc_pool *pool, int layer, const int32_t *src, const int32_t *dst,
+                  const uint8_t *mask, int n, void *stream);
+
+/* Speculative verify / commit ([p1] speculative decoding conv-state section: per-step
+ * window snapshots, scatter of the last accepted step; the SSM intermediate cache works
+ * the same way).
+ *   VERIFY: for each request b run T tokens (anchor + drafts) from its slot state and
+ *     store, after token t, S_t into spec_ssm[b][t] and the window into spec_conv[b][t]
+ *     (rounded to their storage dtypes); out[b][t] = o_t.  The slot is not modified;
+ *     the running state stays fp32 across the T tokens.  accept is ignored.
+ *   COMMIT: slot_ids[b] <- entry accept[b] of request b (S and window), bytes unchanged.
+ *     accept[b] = accepted drafts in [0, T-1].  qkv, conv_w, g, beta, out are ignored.
+ *   spec_ssm  [batch][L][H][V][K] device, state_dtype;  spec_conv [batch][L][3][D]
+ *   qkv [batch][T][D], g [batch][T][H][K] or [batch][T][H], beta [batch][T][H],
+ *   out [batch][T][H][V];  1 <= T <= L, L a power of two.
+ * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ECUDA. */
+int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *slot_ids,
+                           int batch, int T, int L, void *spec_ssm, void *spec_conv,
+                           const void *qkv, const float *conv_w, const float *g,
+                           const float *beta, void *out, const int32_t *accept,
+                           void *stream);
+
+/* Read the pool's device error word into *code and clear it.  Synchronises `stream`.
+ * Errors: RSC_EINVAL, RSC_ECUDA. */
+int rsc_get_device_error(rsc_pool *pool, int32_t *code, void *stream);
+
+/* Static text for a status code (host only). */
+const char *rsc_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSC_H */

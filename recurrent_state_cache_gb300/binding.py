@@ -1,0 +1,273 @@
+"""ctypes binding of librsc.so (include/rsc.h) with the same entry-point names.
+
+Argument marshalling only: torch tensors are checked for dtype, device, shape and
+contiguity, then their device pointers and the current CUDA stream are handed to the C
+ABI.  Every step of the layer runs in the library's CUDA kernels; there is no fallback
+of any kind, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+F32, BF16 = 0, 1
+KDA, GDN = 0, 1
+VERIFY, COMMIT = 0, 1
+
+RSC_OK, RSC_EINVAL, RSC_ERANGE, RSC_EDTYPE, RSC_EALIGN, RSC_ECUDA, RSC_ENOSPACE = (
+    0, -1, -2, -3, -4, -5, -6)
+DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ = 1, 2, 4
+
+TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
+
+# Every symbol include/rsc.h declares.
+EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
+           "kda_prefill_workspace_size", "kda_prefill_chunk", "ssm_slot_copy",
+           "kda_spec_verify_commit", "rsc_get_device_error", "rsc_status_string")
+
+
+class RscError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status} ({status_string(status)})")
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32), ("head_k", ctypes.c_int32),
+        ("head_v", ctypes.c_int32), ("conv_kernel", ctypes.c_int32),
+        ("state_dtype", ctypes.c_int32), ("conv_dtype", ctypes.c_int32),
+        ("gate", ctypes.c_int32),
+        ("ssm_base", ctypes.c_void_p), ("conv_base", ctypes.c_void_p),
+        ("dev_error", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded librsc.so.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"librsc.so is missing at {path}: build it with "
+                               "recurrent_state_cache_gb300._build.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        pd = ctypes.POINTER(PoolDesc)
+        L.ssm_pool_create.argtypes = [pd, ctypes.POINTER(vp)]
+        L.ssm_pool_destroy.argtypes = [vp]
+        L.ssm_pool_bytes.argtypes = [pd, ctypes.POINTER(ctypes.c_uint64),
+                                     ctypes.POINTER(ctypes.c_uint64)]
+        L.kda_decode_step.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
+        L.kda_prefill_chunk.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
+                                        vp, sz, vp]
+        L.ssm_slot_copy.argtypes = [vp, i32, vp, vp, vp, i32, vp]
+        L.kda_spec_verify_commit.argtypes = [vp, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp,
+                                             vp, vp, vp, vp, vp]
+        L.rsc_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        L.rsc_status_string.argtypes = [i32]
+        L.rsc_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name != "rsc_status_string":
+                getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().rsc_status_string(status).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != RSC_OK:
+        raise RscError(rc, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+class SlotPool:
+    """A slot pool in device memory allocated by torch, plus the library's host handle.
+
+    ssm  [num_layers][num_slots+1][H][V][K]  state dtype
+    conv [num_layers][num_slots+1][3][D]     conv dtype (also the io dtype)
+    """
+
+    def __init__(self, num_layers, num_slots, H, K, V, state_dtype=BF16, conv_dtype=BF16,
+                 gate=KDA, device="cuda", ssm=None, conv=None):
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.num_layers, self.num_slots = num_layers, num_slots
+        self.H, self.K, self.V = H, K, V
+        self.D = H * (2 * K + V)
+        self.state_dtype, self.conv_dtype, self.gate = state_dtype, conv_dtype, gate
+        rows = num_slots + 1
+        shp_s, shp_c = (num_layers, rows, H, V, K), (num_layers, rows, 3, self.D)
+        self.ssm = (torch.zeros(shp_s, dtype=TORCH_DTYPE[state_dtype], device=self.device)
+                    if ssm is None else ssm)
+        self.conv = (torch.zeros(shp_c, dtype=TORCH_DTYPE[conv_dtype], device=self.device)
+                     if conv is None else conv)
+        _need(self.ssm, "ssm", TORCH_DTYPE[state_dtype], shp_s, self.device)
+        _need(self.conv, "conv", TORCH_DTYPE[conv_dtype], shp_c, self.device)
+        self.dev_error = torch.zeros(4, dtype=torch.int32, device=self.device)
+        self.desc = PoolDesc(num_layers, num_slots, H, K, V, 4, state_dtype, conv_dtype, gate,
+                             self.ssm.data_ptr(), self.conv.data_ptr(),
+                             self.dev_error.data_ptr())
+        h = ctypes.c_void_p()
+        _check(lib().ssm_pool_create(ctypes.byref(self.desc), ctypes.byref(h)),
+               "ssm_pool_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().ssm_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def io_dtype(self):
+        return TORCH_DTYPE[self.conv_dtype]
+
+    def gate_shape(self, lead):
+        return tuple(lead) + ((self.H, self.K) if self.gate == KDA else (self.H,))
+
+
+def ssm_pool_bytes(num_layers, num_slots, H, K, V, state_dtype, conv_dtype, gate=KDA):
+    d = PoolDesc(num_layers, num_slots, H, K, V, 4, state_dtype, conv_dtype, gate, None, None,
+                 None)
+    s, c = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib().ssm_pool_bytes(ctypes.byref(d), ctypes.byref(s), ctypes.byref(c)),
+           "ssm_pool_bytes")
+    return s.value, c.value
+
+
+def kda_decode_step(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, out=None,
+                    stream=None):
+    B = slot_ids.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (B, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(g, "g", torch.float32, pool.gate_shape((B,)), dev)
+    _need(beta, "beta", torch.float32, (B, pool.H), dev)
+    if out is None:
+        out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
+    _check(lib().kda_decode_step(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                 _p(g), _p(beta), _p(out), _stream(stream)),
+           "kda_decode_step")
+    return out
+
+
+def kda_prefill_workspace_size(pool: SlotPool, num_seqs, total_tokens) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kda_prefill_workspace_size(pool.handle, num_seqs, total_tokens,
+                                            ctypes.byref(n)), "kda_prefill_workspace_size")
+    return n.value
+
+
+def kda_prefill_chunk(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, conv_w, g, beta,
+                      has_initial_state=None, out=None, workspace=None, stream=None):
+    N = slot_ids.shape[0]
+    T = qkv.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (T, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(g, "g", torch.float32, pool.gate_shape((T,)), dev)
+    _need(beta, "beta", torch.float32, (T, pool.H), dev)
+    if has_initial_state is not None:
+        _need(has_initial_state, "has_initial_state", torch.uint8, (N,), dev)
+    if out is None:
+        out = torch.empty((T, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (T, pool.H, pool.V), dev)
+    need = kda_prefill_workspace_size(pool, N, T)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if workspace.dtype != torch.uint8 or workspace.device != dev:
+        raise ValueError("workspace: a uint8 tensor on the pool's device")
+    _check(lib().kda_prefill_chunk(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N, T,
+                                   _p(has_initial_state), _p(qkv), _p(conv_w), _p(g), _p(beta),
+                                   _p(out), _p(workspace), workspace.numel(), _stream(stream)),
+           "kda_prefill_chunk")
+    return out
+
+
+def ssm_slot_copy(pool: SlotPool, layer, src, dst, mask=None, stream=None):
+    n = src.shape[0]
+    dev = pool.device
+    _need(src, "src", torch.int32, (n,), dev)
+    _need(dst, "dst", torch.int32, (n,), dev)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, (n,), dev)
+    _check(lib().ssm_slot_copy(pool.handle, layer, _p(src), _p(dst), _p(mask), n,
+                               _stream(stream)), "ssm_slot_copy")
+
+
+def kda_spec_verify_commit(pool: SlotPool, layer, mode, slot_ids, T, L, spec_ssm, spec_conv,
+                           qkv=None, conv_w=None, g=None, beta=None, out=None, accept=None,
+                           stream=None):
+    B = slot_ids.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(spec_ssm, "spec_ssm", TORCH_DTYPE[pool.state_dtype], (B, L, pool.H, pool.V, pool.K), dev)
+    _need(spec_conv, "spec_conv", pool.io_dtype, (B, L, 3, pool.D), dev)
+    if mode == VERIFY:
+        _need(qkv, "qkv", pool.io_dtype, (B, T, pool.D), dev)
+        _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+        _need(g, "g", torch.float32, pool.gate_shape((B, T)), dev)
+        _need(beta, "beta", torch.float32, (B, T, pool.H), dev)
+        if out is None:
+            out = torch.empty((B, T, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+        _need(out, "out", pool.io_dtype, (B, T, pool.H, pool.V), dev)
+    else:
+        _need(accept, "accept", torch.int32, (B,), dev)
+    _check(lib().kda_spec_verify_commit(pool.handle, layer, mode, _p(slot_ids), B, T, L,
+                                        _p(spec_ssm), _p(spec_conv), _p(qkv), _p(conv_w), _p(g),
+                                        _p(beta), _p(out), _p(accept), _stream(stream)),
+           "kda_spec_verify_commit")
+    return out
+
+
+def rsc_get_device_error(pool: SlotPool, stream=None) -> int:
+    code = ctypes.c_int32()
+    _check(lib().rsc_get_device_error(pool.handle, ctypes.byref(code), _stream(stream)),
+           "rsc_get_device_error")
+    return code.value

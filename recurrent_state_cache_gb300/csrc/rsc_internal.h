@@ -1,0 +1,78 @@
+// rsc_internal.h -- launchers behind the C ABI (host side).  Arguments have already
+// been validated by rsc_api.cu when these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rsc_common.cuh"
+
+namespace rsc {
+
+struct LayerArgs {
+  PoolView pv;
+  int st, io, gate;   // state dtype, conv/io dtype, gate kind
+  int layer;
+};
+
+int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
+                  const float *conv_w, const float *g, const float *beta, void *out,
+                  cudaStream_t s);
+
+int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, int L,
+                       void *spec_ssm, void *spec_conv, const void *qkv,
+                       const float *conv_w, const float *g, const float *beta, void *out,
+                       cudaStream_t s);
+
+int launch_spec_commit(const LayerArgs &a, const int32_t *slots, int B, int T, int L,
+                       const void *spec_ssm, const void *spec_conv, const int32_t *accept,
+                       cudaStream_t s);
+
+int launch_slot_copy(const PoolView &pv, int st, int io, int layer0, int nlayers,
+                     const int32_t *src, const int32_t *dst, const uint8_t *mask, int n,
+                     cudaStream_t s);
+
+size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T);
+
+int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_seqlens,
+                   int N, int T, const uint8_t *has_init, const void *qkv,
+                   const float *conv_w, const float *g, const float *beta, void *out,
+                   void *ws, size_t ws_bytes, cudaStream_t s);
+
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? RSC_OK : RSC_ECUDA;
+}
+
+// Compile-time dispatch over (state dtype, io dtype, K, V, gate) onto L<ST,IO,K,V,GATE>::run.
+template <template <typename, typename, int, int, int> class L, typename ST, typename IO,
+          int K, int V, typename... A>
+int dispatch_gate(int gate, A... a) {
+  return gate == RSC_GATE_KDA ? L<ST, IO, K, V, RSC_GATE_KDA>::run(a...)
+                              : L<ST, IO, K, V, RSC_GATE_GDN>::run(a...);
+}
+template <template <typename, typename, int, int, int> class L, typename ST, typename IO,
+          int K, typename... A>
+int dispatch_v(int V, int gate, A... a) {
+  if (V == 64) return dispatch_gate<L, ST, IO, K, 64>(gate, a...);
+  if (V == 128) return dispatch_gate<L, ST, IO, K, 128>(gate, a...);
+  return RSC_EDTYPE;
+}
+template <template <typename, typename, int, int, int> class L, typename ST, typename IO,
+          typename... A>
+int dispatch_k(int K, int V, int gate, A... a) {
+  if (K == 64) return dispatch_v<L, ST, IO, 64>(V, gate, a...);
+  if (K == 128) return dispatch_v<L, ST, IO, 128>(V, gate, a...);
+  return RSC_EDTYPE;
+}
+template <template <typename, typename, int, int, int> class L, typename... A>
+int dispatch_all(int st, int io, int K, int V, int gate, A... a) {
+  if (st == RSC_F32) {
+    return io == RSC_F32 ? dispatch_k<L, float, float>(K, V, gate, a...)
+                         : dispatch_k<L, float, bf16>(K, V, gate, a...);
+  }
+  return io == RSC_F32 ? dispatch_k<L, bf16, float>(K, V, gate, a...)
+                       : dispatch_k<L, bf16, bf16>(K, V, gate, a...);
+}
+
+}  // namespace rsc

@@ -1,0 +1,84 @@
+// rsc_step.cuh -- the per-token delta-rule update of one CTA's tile of S rows.
+//
+// A CTA of 128 threads owns VT consecutive rows of one head's state S[V][K] (K
+// contiguous).  Each row is covered by LPR lanes holding one 16-byte vector each (EPL
+// elements), so a warp touches RPW whole rows per pass and a pass of the CTA covers
+// RPP rows: every global access of S is a fully coalesced 16-byte vector access.  Rows
+// of S evolve independently under the gated delta rule (the update acts on S from the
+// right), which is what lets a head be split across CTAs by rows.
+#pragma once
+
+#include "rsc_common.cuh"
+
+namespace rsc {
+
+template <typename ST, int K, int VT>
+struct TileGeom {
+  static constexpr int EPL = VecTraits<ST>::N;  // elements per 16-byte vector
+  static constexpr int LPR = K / EPL;           // lanes per row
+  static constexpr int RPW = 32 / LPR;          // rows per warp per pass
+  static constexpr int RPP = 4 * RPW;           // rows per CTA per pass
+  static constexpr int NP = VT / RPP;           // passes
+  static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must fit a warp");
+  static_assert(NP >= 1 && NP * RPP == VT, "tile rows must be whole passes");
+  __device__ static __forceinline__ int row(int p) {
+    return p * RPP + (threadIdx.x >> 5) * RPW + (threadIdx.x & 31) / LPR;
+  }
+  __device__ static __forceinline__ int kofs() { return ((threadIdx.x & 31) % LPR) * EPL; }
+};
+
+// Load / store this thread's part of the tile (rows base[row(p)*K + kofs()]).
+template <typename ST, int K, int VT>
+__device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL]) {
+  using G = TileGeom<ST, K, VT>;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p)
+    unpack16(ld16_stream(base + (size_t)G::row(p) * K + G::kofs()), s[p]);
+}
+
+template <typename ST, int K, int VT>
+__device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL]) {
+  using G = TileGeom<ST, K, VT>;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p) st16(base + (size_t)G::row(p) * K + G::kofs(), pack16(s[p]));
+}
+
+// One token of the gated delta rule on the tile, for every row r of the tile:
+//   s <- s . alpha            (decay, S Diag(alpha))
+//   u  = s . k_hat ;  w = s . q_hat          (one pass, two row dots)
+//   d  = beta (v_r - u)
+//   s <- s + d k_hat          (rank-1 write)
+//   o_r = w + d (k_hat . q_hat)
+// The last line is S_new q_hat written out: (S Diag(alpha) + d k^T) q = w + d (k.q), so
+// the output of the updated state costs no second pass over the row.
+template <typename ST, int K, int VT>
+__device__ __forceinline__ void delta_rule_tile(
+    float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL],
+    const float (&qh)[TileGeom<ST, K, VT>::EPL], const float (&kh)[TileGeom<ST, K, VT>::EPL],
+    const float (&al)[TileGeom<ST, K, VT>::EPL], float beta, float kq, const float *v_rows,
+    float (&o)[TileGeom<ST, K, VT>::NP]) {
+  using G = TileGeom<ST, K, VT>;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p) {
+    float u = 0.f, w = 0.f;
+#pragma unroll
+    for (int e = 0; e < G::EPL; ++e) {
+      s[p][e] *= al[e];
+      u = fmaf(s[p][e], kh[e], u);
+      w = fmaf(s[p][e], qh[e], w);
+    }
+    u = group_sum<G::LPR>(u);
+    w = group_sum<G::LPR>(w);
+    const float d = beta * (v_rows[G::row(p)] - u);
+#pragma unroll
+    for (int e = 0; e < G::EPL; ++e) s[p][e] = fmaf(d, kh[e], s[p][e]);
+    o[p] = fmaf(d, kq, w);
+  }
+}
+
+// The conv of one channel: taps 0..2 on the window rows (oldest first), tap 3 on x.
+__device__ __forceinline__ float conv4(const float4 &w, float w0, float w1, float w2, float x) {
+  return fmaf(w.w, x, fmaf(w.z, w2, fmaf(w.y, w1, w.x * w0)));
+}
+
+}  // namespace rsc

@@ -1,0 +1,199 @@
+// spec.cu -- speculative verify (T tokens per request, every intermediate state and
+// window saved) and commit (the accepted entry gathered back into the slot).
+//
+// Source: "SGLang Qwen3/kimi-k3 Hybrid Linear Mamba KV cache管理", speculative-decoding
+// conv-state section: the verify pass stores the conv window after each token into a
+// per-step cache and the commit scatters the snapshot of the last accepted step into
+// the persistent state; the intermediate SSM cache does the same for S.
+//
+// VERIFY runs the decode body of decode.cu T times with the state tile held in
+// registers (fp32) across tokens; the slot is only read.  Each CTA keeps its own copy
+// of the head's q/k windows plus its value rows' windows in registers and rolls them
+// token by token, so no CTA ever writes memory another one reads: no cluster needed.
+// Each window channel of a cache entry is written by exactly one CTA (q/k channels
+// partitioned over the NVT tiles of the head, value channels by tile), each S entry
+// tile by its owner.
+#include "rsc_internal.h"
+#include "rsc_step.cuh"
+
+namespace rsc {
+
+template <typename ST, typename IO, int K, int V, int NVT, int GATE>
+__global__ void __launch_bounds__(128)
+kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
+                       int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
+                       const IO *__restrict__ qkv, const float *__restrict__ conv_w,
+                       const float *__restrict__ g, const float *__restrict__ beta,
+                       IO *__restrict__ out) {
+  constexpr int VT = V / NVT;
+  using G = TileGeom<ST, K, VT>;
+  constexpr int QK_T = 2 * K / 128;
+  constexpr int OWN = 2 * K / NVT;
+
+  __shared__ float s_qk[2 * K];
+  __shared__ float s_v[VT];
+  __shared__ float s_red[12];
+
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int H = pv.H, D = pv.D;
+
+  const int slot = slots[b];
+  if (slot < 0 || slot > pv.P) {
+    if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
+    return;
+  }
+  const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+
+  const ST *S = reinterpret_cast<const ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
+  float s[G::NP][G::EPL];
+  tile_load<ST, K, VT>(S, s);
+
+  // Window registers (raw io values, row 0 oldest) and taps of this thread's channels.
+  const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
+  IO win[QK_T][3];
+  float4 wt[QK_T];
+  int cqk[QK_T];
+#pragma unroll
+  for (int u = 0; u < QK_T; ++u) {
+    const int i2 = tid + u * 128;
+    cqk[u] = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
+    wt[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cqk[u]);
+    win[u][0] = W[cqk[u]]; win[u][1] = W[D + cqk[u]]; win[u][2] = W[2 * D + cqk[u]];
+  }
+  IO winv[3];
+  float4 wtv = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int cv = 2 * H * K + h * V + j * VT + tid;
+  if (tid < VT) {
+    wtv = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cv);
+    winv[0] = W[cv]; winv[1] = W[D + cv]; winv[2] = W[2 * D + cv];
+  }
+
+  const int k0 = G::kofs();
+  for (int t = 0; t < T; ++t) {
+    const size_t bt = (size_t)b * T + t;
+    const IO *x = qkv + bt * D;
+    IO *E = spec_conv + ((size_t)b * L + t) * 3 * (size_t)D;
+    if (t > 0) __syncthreads();  // previous token's readers of s_qk / s_v are done
+#pragma unroll
+    for (int u = 0; u < QK_T; ++u) {
+      const IO xc = x[cqk[u]];
+      s_qk[tid + u * 128] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]),
+                                  to_f32(win[u][2]), to_f32(xc));
+      win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
+      const int i2 = tid + u * 128;
+      if (i2 >= j * OWN && i2 < (j + 1) * OWN) {
+        E[cqk[u]] = win[u][0]; E[D + cqk[u]] = win[u][1]; E[2 * D + cqk[u]] = win[u][2];
+      }
+    }
+    if (tid < VT) {
+      const IO xc = x[cv];
+      s_v[tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
+      winv[0] = winv[1]; winv[1] = winv[2]; winv[2] = xc;
+      E[cv] = winv[0]; E[D + cv] = winv[1]; E[2 * D + cv] = winv[2];
+    }
+    __syncthreads();
+
+    float qq = 0.f, kk = 0.f, qk = 0.f;
+    if (tid < K) {
+      const float a = s_qk[tid], c = s_qk[K + tid];
+      qq = a * a; kk = c * c; qk = a * c;
+    }
+    block3_sum_128(qq, kk, qk, s_red);
+    const float rq = 1.0f / sqrtf(qq + kNormEps);
+    const float rk = 1.0f / sqrtf(kk + kNormEps);
+    const float kq = qk * rq * rk;
+
+    float qh[G::EPL], kh[G::EPL], al[G::EPL];
+#pragma unroll
+    for (int e = 0; e < G::EPL; ++e) {
+      qh[e] = s_qk[k0 + e] * rq;
+      kh[e] = s_qk[K + k0 + e] * rk;
+    }
+    if (GATE == RSC_GATE_KDA) {
+      const float *gg = g + (bt * H + h) * K + k0;
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) al[e] = expf(gg[e]);
+    } else {
+      const float a = expf(g[bt * H + h]);
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) al[e] = a;
+    }
+    const float bta = beta[bt * H + h];
+
+    float o[G::NP];
+    delta_rule_tile<ST, K, VT>(s, qh, kh, al, bta, kq, s_v, o);
+    ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
+    tile_store<ST, K, VT>(Se, s);
+    if (k0 == 0) {
+      IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
+#pragma unroll
+      for (int p = 0; p < G::NP; ++p) ob[G::row(p)] = from_f32<IO>(o[p]);
+    }
+    // the block reduction scratch is rewritten next token only after the barrier at
+    // the top of the loop, which every thread reaches after its reads of s_red above
+  }
+}
+
+template <typename ST, typename IO, int K, int V, int GATE>
+struct VerifyLaunch {
+  static int run(const LayerArgs *a, const int32_t *slots, int B, int T, int L,
+                 void *spec_ssm, void *spec_conv, const void *qkv, const float *conv_w,
+                 const float *g, const float *beta, void *out, cudaStream_t s) {
+    constexpr int NVT = V / 32;
+    dim3 grid(NVT, a->pv.H, B);
+    kda_spec_verify_kernel<ST, IO, K, V, NVT, GATE><<<grid, 128, 0, s>>>(
+        a->pv, a->layer, slots, T, L, static_cast<ST *>(spec_ssm),
+        static_cast<IO *>(spec_conv), static_cast<const IO *>(qkv), conv_w, g, beta,
+        static_cast<IO *>(out));
+    return launch_status();
+  }
+};
+
+int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, int L,
+                       void *spec_ssm, void *spec_conv, const void *qkv,
+                       const float *conv_w, const float *g, const float *beta, void *out,
+                       cudaStream_t s) {
+  return dispatch_all<VerifyLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, T, L,
+                                    spec_ssm, spec_conv, qkv, conv_w, g, beta, out, s);
+}
+
+// COMMIT: slot <- cache entry accept[b], for S (which == 0) or the window (which == 1).
+// Grid (chunks of kCopyChunk bytes, batch).  Bad slot or accept count: row skipped.
+__global__ void __launch_bounds__(128)
+kda_spec_commit_kernel(PoolView pv, int layer, size_t row_bytes, int which,
+                       const int32_t *__restrict__ slots, int T, int L,
+                       const char *__restrict__ cache, const int32_t *__restrict__ accept) {
+  const int b = blockIdx.y;
+  const int slot = slots[b], a = accept[b];
+  const bool bad_slot = slot < 0 || slot > pv.P, bad_acc = a < 0 || a >= T;
+  if (bad_slot || bad_acc) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && which == 0)
+      flag_error(pv.err, (bad_slot ? RSC_DEVERR_SLOT : 0) | (bad_acc ? RSC_DEVERR_ACCEPT : 0));
+    return;
+  }
+  const size_t off = (size_t)blockIdx.x * kCopyChunk;
+  if (off >= row_bytes) return;
+  char *base = reinterpret_cast<char *>(which == 0 ? pv.ssm : pv.conv);
+  char *dst = base + ((size_t)layer * (pv.P + 1) + slot) * row_bytes;
+  const char *src = cache + ((size_t)b * L + a) * row_bytes;
+  copy_chunk(dst, src, row_bytes, off);
+}
+
+int launch_spec_commit(const LayerArgs &a, const int32_t *slots, int B, int T, int L,
+                       const void *spec_ssm, const void *spec_conv, const int32_t *accept,
+                       cudaStream_t s) {
+  const size_t ssz = a.st == RSC_F32 ? 4 : 2, csz = a.io == RSC_F32 ? 4 : 2;
+  const size_t sb = (size_t)a.pv.H * a.pv.V * a.pv.K * ssz;
+  const size_t cb = (size_t)3 * a.pv.D * csz;
+  dim3 gs((unsigned)((sb + kCopyChunk - 1) / kCopyChunk), B);
+  kda_spec_commit_kernel<<<gs, 128, 0, s>>>(a.pv, a.layer, sb, 0, slots, T, L,
+                                            static_cast<const char *>(spec_ssm), accept);
+  if (launch_status() != RSC_OK) return RSC_ECUDA;
+  dim3 gc((unsigned)((cb + kCopyChunk - 1) / kCopyChunk), B);
+  kda_spec_commit_kernel<<<gc, 128, 0, s>>>(a.pv, a.layer, cb, 1, slots, T, L,
+                                            static_cast<const char *>(spec_conv), accept);
+  return launch_status();
+}
+
+}  // namespace rsc

@@ -1,0 +1,217 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on identical seeded
+inputs.  Tolerances: max relative error (max |got-ref| / max |ref|) <= 1e-4 for tensors
+stored in fp32, <= 2e-2 for tensors stored in bf16 (states by the state dtype, outputs by
+the io dtype); windows, slot copies and commits bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import recurrent_state_cache_gb300 as rsc
+from recurrent_state_cache_gb300 import inputs
+from tests.devio import to_dev, to_np, widen
+from tests.tolerances import TOL, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+class Case:
+    """One pool held twice: by the oracle (numpy) and on the device (torch)."""
+
+    def __init__(self, dev, seed, L, P, H, K, V, st, io, gate):
+        self.r = inputs.rng(seed)
+        self.st, self.io, self.gate = st, io, gate
+        self.H, self.K, self.V = H, K, V
+        ssm, conv = inputs.pool_arrays(self.r, L, P, H, K, V, st, io)
+        self.ref = oracle.Pool(L, P, H, K, V, st, io, gate, ssm, conv)
+        self.pool = rsc.SlotPool(L, P, H, K, V, st, io, gate, dev,
+                                 ssm=to_dev(ssm, dev), conv=to_dev(conv, dev))
+        self.w = inputs.conv_weights(self.r, H, K, V)
+        self.w_dev = to_dev(self.w, dev)
+        self.dev = dev
+        self.D = self.pool.D
+
+    def gates(self, lead):
+        return inputs.gates(self.r, lead, self.H, self.K, self.gate)
+
+    def proj(self, lead):
+        return inputs.projections(self.r, lead, self.H, self.K, self.V, self.io)
+
+    def check_pool(self, tol=None):
+        tol = TOL[self.st] if tol is None else tol
+        s_gpu, c_gpu = to_np(self.pool.ssm), to_np(self.pool.conv)
+        assert np.array_equal(c_gpu, self.ref.conv), "conv windows differ"
+        err = max_rel_err(widen(s_gpu), widen(self.ref.ssm))
+        assert err <= tol, f"state max rel err {err}"
+        assert rsc.rsc_get_device_error(self.pool) == 0
+
+
+def _decode_steps(c, slots, steps):
+    slots_d = to_dev(slots, c.dev)
+    for _ in range(steps):
+        B = len(slots)
+        x = c.proj((B,))
+        g, beta = c.gates((B,))
+        o_ref = oracle.decode_step(c.ref, 0, slots, x, c.w, g, beta)
+        o = rsc.kda_decode_step(c.pool, 0, slots_d, to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev),
+                                to_dev(beta, c.dev))
+        err = max_rel_err(widen(to_np(o)), widen(o_ref))
+        assert err <= TOL[c.io], f"output max rel err {err}"
+    c.check_pool()
+
+
+def test_decode_kda_fp32_small_config(cuda_dev):
+    """1 KDA layer, fp32, 16-slot pool, 4 random distinct slots, H=4, K=V=64, 8 steps."""
+    c = Case(cuda_dev, 0, L=1, P=16, H=4, K=64, V=64, st=0, io=0, gate=rsc.KDA)
+    slots = inputs.distinct_slots(c.r, 4, 16)
+    _decode_steps(c, slots, 8)
+
+
+@pytest.mark.parametrize("st,io,gate,H,K,V,B", [
+    (1, 1, rsc.KDA, 3, 128, 128, 5),     # Kimi-shaped heads, ragged head count
+    (0, 1, rsc.GDN, 2, 128, 128, 3),     # GDN: fp32 state with bf16 io
+    (1, 1, rsc.GDN, 2, 64, 128, 1),      # K != V, single request
+    (0, 0, rsc.KDA, 1, 128, 64, 7),      # fp32, K != V
+    (1, 0, rsc.KDA, 2, 64, 64, 2),       # bf16 state with fp32 io
+])
+def test_decode_variants(cuda_dev, st, io, gate, H, K, V, B):
+    c = Case(cuda_dev, 1, L=2, P=9, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    slots = inputs.distinct_slots(c.r, B, 9)
+    _decode_steps(c, slots, 3)
+
+
+def test_decode_padding_slot_zero_is_legal(cuda_dev):
+    c = Case(cuda_dev, 2, L=1, P=4, H=2, K=64, V=64, st=1, io=1, gate=rsc.KDA)
+    _decode_steps(c, np.int32([0, 3]), 2)
+
+
+def test_decode_bad_slot_sets_flag_and_skips_row(cuda_dev):
+    c = Case(cuda_dev, 3, L=1, P=4, H=2, K=64, V=64, st=0, io=0, gate=rsc.KDA)
+    before_s, before_c = to_np(c.pool.ssm).copy(), to_np(c.pool.conv).copy()
+    slots = np.int32([2, 7])  # 7 > P
+    x = c.proj((2,))
+    g, beta = c.gates((2,))
+    rsc.kda_decode_step(c.pool, 0, to_dev(slots, c.dev), to_dev(x, c.dev), c.w_dev,
+                        to_dev(g, c.dev), to_dev(beta, c.dev))
+    assert rsc.rsc_get_device_error(c.pool) == rsc.binding.DEVERR_SLOT
+    assert rsc.rsc_get_device_error(c.pool) == 0  # read clears
+    # row 0 (slot 2) was processed; nothing else moved
+    s_now, c_now = to_np(c.pool.ssm), to_np(c.pool.conv)
+    others = [0, 1, 3, 4]
+    assert np.array_equal(s_now[0, others], before_s[0, others])
+    assert np.array_equal(c_now[0, others], before_c[0, others])
+    o_ref = oracle.decode_step(c.ref, 0, slots[:1], x[:1], c.w, g[:1], beta[:1])
+    assert np.array_equal(c_now[0, 2], c.ref.conv[0, 2])
+    assert max_rel_err(widen(s_now[0, 2]), widen(c.ref.ssm[0, 2])) <= TOL[0]
+
+
+# ------------------------------------------------------------------ slot copy
+
+@pytest.mark.parametrize("st,io,layer", [(1, 1, -1), (0, 1, 1), (0, 0, -1)])
+def test_slot_copy_bit_exact(cuda_dev, st, io, layer):
+    c = Case(cuda_dev, 4, L=3, P=12, H=2, K=128, V=64, st=st, io=io, gate=rsc.KDA)
+    perm = c.r.permutation(12) + 1
+    src, dst = perm[:4].astype(np.int32), perm[4:8].astype(np.int32)
+    mask = np.uint8([1, 0, 1, 1])
+    rsc.ssm_slot_copy(c.pool, layer, to_dev(src, c.dev), to_dev(dst, c.dev), to_dev(mask, c.dev))
+    oracle.slot_copy(c.ref, layer, src, dst, mask)
+    assert np.array_equal(to_np(c.pool.ssm), c.ref.ssm)
+    assert np.array_equal(to_np(c.pool.conv), c.ref.conv)
+
+
+def test_slot_copy_bad_slot_flags(cuda_dev):
+    c = Case(cuda_dev, 5, L=1, P=4, H=1, K=64, V=64, st=1, io=1, gate=rsc.KDA)
+    before = to_np(c.pool.ssm).copy()
+    rsc.ssm_slot_copy(c.pool, 0, to_dev(np.int32([1, 9]), c.dev), to_dev(np.int32([2, 3]), c.dev))
+    assert rsc.rsc_get_device_error(c.pool) == rsc.binding.DEVERR_SLOT
+    now = to_np(c.pool.ssm)
+    assert np.array_equal(now[0, 2], before[0, 1])
+    assert np.array_equal(now[0, 3], before[0, 3])
+
+
+# ------------------------------------------------------------------ spec verify / commit
+
+@pytest.mark.parametrize("st,io,gate,K,V", [(1, 1, rsc.KDA, 128, 128), (0, 0, rsc.KDA, 64, 64),
+                                            (0, 1, rsc.GDN, 128, 64)])
+def test_spec_verify_and_commit(cuda_dev, st, io, gate, K, V):
+    H, B, T, L = 2, 5, 8, 16
+    c = Case(cuda_dev, 6, L=1, P=10, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    slots = inputs.distinct_slots(c.r, B, 10)
+    x = c.proj((B, T))
+    g, beta = c.gates((B, T))
+    sS_ref, sC_ref, o_ref = oracle.spec_verify(c.ref, 0, slots, T, L, x, c.w, g, beta)
+    sdt = rsc.binding.TORCH_DTYPE[st]
+    spec_ssm = torch.zeros((B, L, H, V, K), dtype=sdt, device=c.dev)
+    spec_conv = torch.zeros((B, L, 3, c.D), dtype=c.pool.io_dtype, device=c.dev)
+    before = to_np(c.pool.ssm).copy(), to_np(c.pool.conv).copy()
+    slots_d = to_dev(slots, c.dev)
+    o = rsc.kda_spec_verify_commit(c.pool, 0, rsc.VERIFY, slots_d, T, L, spec_ssm, spec_conv,
+                                   to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev),
+                                   to_dev(beta, c.dev))
+    assert np.array_equal(to_np(c.pool.ssm), before[0]) and np.array_equal(to_np(c.pool.conv), before[1])
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= TOL[io]
+    assert np.array_equal(to_np(spec_conv)[:, :T], sC_ref[:, :T])
+    for t in range(T):
+        assert max_rel_err(widen(to_np(spec_ssm)[:, t]), widen(sS_ref[:, t])) <= TOL[st], t
+    accept = inputs.accept_counts(c.r, B, T)
+    rsc.kda_spec_verify_commit(c.pool, 0, rsc.COMMIT, slots_d, T, L, spec_ssm, spec_conv,
+                               accept=to_dev(accept, c.dev))
+    # commit is a byte gather of the device's own cache entries
+    gs, gc = to_np(spec_ssm), to_np(spec_conv)
+    now_s, now_c = to_np(c.pool.ssm), to_np(c.pool.conv)
+    for b, s in enumerate(slots):
+        assert np.array_equal(now_s[0, s], gs[b, accept[b]])
+        assert np.array_equal(now_c[0, s], gc[b, accept[b]])
+    oracle.spec_commit(c.ref, 0, slots, T, L, sS_ref, sC_ref, accept)
+    c.check_pool()
+
+
+def test_spec_commit_bad_accept_flags(cuda_dev):
+    c = Case(cuda_dev, 7, L=1, P=4, H=1, K=64, V=64, st=1, io=1, gate=rsc.KDA)
+    B, T, L = 2, 3, 4
+    spec_ssm = torch.ones((B, L, 1, 64, 64), dtype=torch.bfloat16, device=c.dev)
+    spec_conv = torch.ones((B, L, 3, c.D), dtype=torch.bfloat16, device=c.dev)
+    before = to_np(c.pool.ssm).copy()
+    rsc.kda_spec_verify_commit(c.pool, 0, rsc.COMMIT, to_dev(np.int32([1, 2]), c.dev), T, L,
+                               spec_ssm, spec_conv, accept=to_dev(np.int32([1, 3]), c.dev))
+    assert rsc.rsc_get_device_error(c.pool) == rsc.binding.DEVERR_ACCEPT
+    now = to_np(c.pool.ssm)
+    assert np.array_equal(now[0, 2], before[0, 2])
+    assert np.all(widen(now[0, 1]) == 1.0)
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("st,io,gate,K,V,lens,init", [
+    (0, 0, rsc.KDA, 64, 64, [1, 70, 2, 129], [1, 1, 0, 1]),
+    (0, 1, rsc.GDN, 128, 128, [200], [1]),
+    (1, 1, rsc.KDA, 128, 128, [64, 1, 131], [1, 0, 1]),
+    (1, 1, rsc.KDA, 128, 128, [300], [1]),
+])
+def test_prefill_parity(cuda_dev, st, io, gate, K, V, lens, init):
+    H = 2
+    c = Case(cuda_dev, 8, L=2, P=8, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    N = len(lens)
+    slots = inputs.distinct_slots(c.r, N, 8)
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    x = c.proj((T,))
+    g, beta = c.gates((T,))
+    hi = np.uint8(init)
+    o_ref = oracle.prefill(c.ref, 1, slots, cu, x, c.w, g, beta, has_init=hi)
+    o = rsc.kda_prefill_chunk(c.pool, 1, to_dev(slots, c.dev), to_dev(cu, c.dev),
+                              to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                              has_initial_state=to_dev(hi, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= TOL[io]
+    c.check_pool()
+
+
+def test_prefill_bad_cu_seqlens_flags(cuda_dev):
+    c = Case(cuda_dev, 9, L=1, P=4, H=1, K=64, V=64, st=0, io=0, gate=rsc.KDA)
+    x = c.proj((10,))
+    g, beta = c.gates((10,))
+    before = to_np(c.pool.ssm).copy()
+    rsc.kda_prefill_chunk(c.pool, 0, to_dev(np.int32([1]), c.dev), to_dev(np.int32([0, 12]), c.dev),
+                          to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
+    assert rsc.rsc_get_device_error(c.pool) & rsc.binding.DEVERR_SEQ
+    assert np.array_equal(to_np(c.pool.ssm), before)

@@ -1,12 +1,13 @@
 """Parity metric and tolerances shared by the tests.
 
 max relative error of a tensor = max_i |got_i - ref_i| / max_i |ref_i|  (infinity-norm
-relative error).  Bars: 1e-4 when the state is fp32, 2e-2 when the state is bf16.
+relative error).  Bars by the storage dtype of the compared tensor: 1e-4 for fp32,
+2e-2 for bf16 (a state by the state dtype, an output by the io dtype).
 Integer, index and byte results are compared bit for bit instead.
 """
 import numpy as np
 
-TOL = {0: 1e-4, 1: 2e-2}  # keyed by state dtype: 0 = fp32, 1 = bf16
+TOL = {0: 1e-4, 1: 2e-2}  # keyed by storage dtype: 0 = fp32, 1 = bf16
 
 
 def max_rel_err(got, ref) -> float:
