@@ -60,6 +60,7 @@ extern "C" {
 #define RSC_DEVERR_SLOT   1 /* a slot id outside [0, num_slots]                      */
 #define RSC_DEVERR_ACCEPT 2 /* an accept count outside [0, T-1]                      */
 #define RSC_DEVERR_SEQ    4 /* cu_seqlens not non-decreasing within [0, total]       */
+#define RSC_DEVERR_TIMEOUT 8 /* a bounded on-chip wait ran out; that tile was skipped  */
 
 typedef enum { RSC_F32 = 0, RSC_BF16 = 1 } rsc_dtype;
 typedef enum { RSC_GATE_KDA = 0, RSC_GATE_GDN = 1 } rsc_gate;

@@ -89,16 +89,20 @@ __device__ __forceinline__ float group_sum(float v) {
   return v;
 }
 
-// Sum three values over a 128-thread block; every thread gets the totals.
-// `red` is shared scratch of at least 12 floats; contains a __syncthreads pair.
-__device__ __forceinline__ void block3_sum_128(float &a, float &b, float &c, float *red) {
+// Sum three values over a block of NW warps; every thread gets the totals.
+// `red` is shared scratch of at least 3*NW floats; ends with a __syncthreads.
+template <int NW>
+__device__ __forceinline__ void block3_sum(float &a, float &b, float &c, float *red) {
   a = group_sum<32>(a); b = group_sum<32>(b); c = group_sum<32>(c);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) { red[warp] = a; red[4 + warp] = b; red[8 + warp] = c; }
+  if (lane == 0) { red[warp] = a; red[NW + warp] = b; red[2 * NW + warp] = c; }
   __syncthreads();
-  a = red[0] + red[1] + red[2] + red[3];
-  b = red[4] + red[5] + red[6] + red[7];
-  c = red[8] + red[9] + red[10] + red[11];
+  a = 0.f; b = 0.f; c = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) { a += red[w]; b += red[NW + w]; c += red[2 * NW + w]; }
+}
+__device__ __forceinline__ void block3_sum_128(float &a, float &b, float &c, float *red) {
+  block3_sum<4>(a, b, c, red);
 }
 
 // ------------------------------------------------------------------ bulk rows
@@ -132,6 +136,46 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// ------------------------------------------------------------------ TMA bulk + mbarrier
+// One-shot bulk copies global -> shared completed on an mbarrier (transaction count).
+// Every wait is bounded: a wait that runs out sets RSC_DEVERR_TIMEOUT in the pool's
+// error word and the caller skips its work instead of spinning forever.
+
+constexpr uint32_t kMbarSpinLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n"
+               " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(phase) : "memory");
+  return ok != 0;
+}
+// Bounded wait for phase `phase` of `bar`; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase) {
+  for (uint32_t i = 0; i < kMbarSpinLimit; ++i)
+    if (mbar_try_wait(bar, phase)) return true;
+  return false;
+}
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) into this CTA's
+// shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *smem, const void *gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
 
 // ------------------------------------------------------------------ clusters
 

@@ -12,12 +12,12 @@
 
 namespace rsc {
 
-template <typename ST, int K, int VT>
+template <typename ST, int K, int VT, int NW = 4>
 struct TileGeom {
   static constexpr int EPL = VecTraits<ST>::N;  // elements per 16-byte vector
   static constexpr int LPR = K / EPL;           // lanes per row
   static constexpr int RPW = 32 / LPR;          // rows per warp per pass
-  static constexpr int RPP = 4 * RPW;           // rows per CTA per pass
+  static constexpr int RPP = NW * RPW;          // rows per CTA per pass
   static constexpr int NP = VT / RPP;           // passes
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must fit a warp");
   static_assert(NP >= 1 && NP * RPP == VT, "tile rows must be whole passes");
@@ -43,7 +43,8 @@ __device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<S
   for (int p = 0; p < G::NP; ++p) st16(base + (size_t)G::row(p) * K + G::kofs(), pack16(s[p]));
 }
 
-// One token of the gated delta rule on the tile, for every row r of the tile:
+// One token of the gated delta rule on one row segment held by this lane (EPL elements
+// of row r; the LPR lanes of the row together hold the whole row):
 //   s <- s . alpha            (decay, S Diag(alpha))
 //   u  = s . k_hat ;  w = s . q_hat          (one pass, two row dots)
 //   d  = beta (v_r - u)
@@ -51,6 +52,26 @@ __device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<S
 //   o_r = w + d (k_hat . q_hat)
 // The last line is S_new q_hat written out: (S Diag(alpha) + d k^T) q = w + d (k.q), so
 // the output of the updated state costs no second pass over the row.
+template <int EPL, int LPR>
+__device__ __forceinline__ float delta_rule_row(float (&s)[EPL], const float (&qh)[EPL],
+                                                const float (&kh)[EPL], const float (&al)[EPL],
+                                                float beta, float kq, float v_r) {
+  float u = 0.f, w = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    s[e] *= al[e];
+    u = fmaf(s[e], kh[e], u);
+    w = fmaf(s[e], qh[e], w);
+  }
+  u = group_sum<LPR>(u);
+  w = group_sum<LPR>(w);
+  const float d = beta * (v_r - u);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) s[e] = fmaf(d, kh[e], s[e]);
+  return fmaf(d, kq, w);
+}
+
+// The same for every row of a register-held tile (rows G::row(p), p < NP).
 template <typename ST, int K, int VT>
 __device__ __forceinline__ void delta_rule_tile(
     float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL],
@@ -59,21 +80,8 @@ __device__ __forceinline__ void delta_rule_tile(
     float (&o)[TileGeom<ST, K, VT>::NP]) {
   using G = TileGeom<ST, K, VT>;
 #pragma unroll
-  for (int p = 0; p < G::NP; ++p) {
-    float u = 0.f, w = 0.f;
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) {
-      s[p][e] *= al[e];
-      u = fmaf(s[p][e], kh[e], u);
-      w = fmaf(s[p][e], qh[e], w);
-    }
-    u = group_sum<G::LPR>(u);
-    w = group_sum<G::LPR>(w);
-    const float d = beta * (v_rows[G::row(p)] - u);
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) s[p][e] = fmaf(d, kh[e], s[p][e]);
-    o[p] = fmaf(d, kq, w);
-  }
+  for (int p = 0; p < G::NP; ++p)
+    o[p] = delta_rule_row<G::EPL, G::LPR>(s[p], qh, kh, al, beta, kq, v_rows[G::row(p)]);
 }
 
 // The conv of one channel: taps 0..2 on the window rows (oldest first), tap 3 on x.
