@@ -141,6 +141,33 @@ int kda_prefill_chunk(rsc_pool *pool, int layer, const int32_t *slot_ids,
                       const float *conv_w, const float *g, const float *beta, void *out,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of the device scratch array behind kda_prefill_chunk_noalloc. */
+#define RSC_PREFILL_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* kda_prefill_chunk without a caller workspace.  The pages have no counterpart of this
+ * call: it exists for callers that cannot allocate device memory when they prefill --
+ * for example a serving engine that hands all of HBM to its own state and KV pools at
+ * start-up (a later cudaMalloc fails or fragments its pools), or a latency-bound host
+ * path that cannot afford cudaMalloc's implicit device synchronisation.
+ * Arguments and results are those of kda_prefill_chunk minus the workspace.  The
+ * scratch is a file-scope device array of RSC_PREFILL_STATIC_SCRATCH_BYTES (32 MiB)
+ * that every GPU loading the library holds until the process exits.
+ *   - The first call on a device looks up that device's address of the array
+ *     (cudaGetSymbolAddress, with the device current); make that first call before
+ *     any stream capture.
+ *   - A call whose workspace need (kda_prefill_workspace_size) exceeds the array
+ *     returns RSC_ENOSPACE before launching anything.
+ *   - All calls share the one array and it keeps the last call's contents; nothing in
+ *     it needs clearing (every byte a call reads was written earlier in that call).
+ *     Calls that may overlap on the GPU (different streams, different host threads)
+ *     race on the array: order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+int kda_prefill_chunk_noalloc(rsc_pool *pool, int layer, const int32_t *slot_ids,
+                              const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                              const uint8_t *has_initial_state, const void *qkv,
+                              const float *conv_w, const float *g, const float *beta,
+                              void *out, void *stream);
+
 /* Slot copy ([p1] masked track copy: conv[dst] = conv[src], ssm[dst] = ssm[src]).
  *   layer  >= 0 copies that layer, -1 copies every layer
  *   src, dst [n] device int32; dst distinct and disjoint from src

@@ -26,7 +26,8 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Every symbol include/rsc.h declares.
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
-           "kda_prefill_workspace_size", "kda_prefill_chunk", "ssm_slot_copy",
+           "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
+           "ssm_slot_copy",
            "kda_spec_verify_commit", "rsc_get_device_error", "rsc_status_string")
 
 
@@ -74,6 +75,8 @@ def lib():
         L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
         L.kda_prefill_chunk.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
                                         vp, sz, vp]
+        L.kda_prefill_chunk_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp,
+                                                vp, vp]
         L.ssm_slot_copy.argtypes = [vp, i32, vp, vp, vp, i32, vp]
         L.kda_spec_verify_commit.argtypes = [vp, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp,
                                              vp, vp, vp, vp, vp]
@@ -227,6 +230,33 @@ def kda_prefill_chunk(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, conv_w, 
                                    _p(has_initial_state), _p(qkv), _p(conv_w), _p(g), _p(beta),
                                    _p(out), _p(workspace), workspace.numel(), _stream(stream)),
            "kda_prefill_chunk")
+    return out
+
+
+def kda_prefill_chunk_noalloc(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, conv_w, g,
+                              beta, has_initial_state=None, out=None, stream=None):
+    """kda_prefill_chunk on the library's static device scratch, for callers that cannot
+    allocate device memory (all of HBM already given to their own pools, or no
+    tolerance for cudaMalloc's device synchronisation).  Allocates nothing besides
+    `out` when it is not given.  Calls share the scratch: keep them on one stream."""
+    N = slot_ids.shape[0]
+    T = qkv.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (T, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(g, "g", torch.float32, pool.gate_shape((T,)), dev)
+    _need(beta, "beta", torch.float32, (T, pool.H), dev)
+    if has_initial_state is not None:
+        _need(has_initial_state, "has_initial_state", torch.uint8, (N,), dev)
+    if out is None:
+        out = torch.empty((T, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (T, pool.H, pool.V), dev)
+    _check(lib().kda_prefill_chunk_noalloc(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N,
+                                           T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
+                                           _p(beta), _p(out), _stream(stream)),
+           "kda_prefill_chunk_noalloc")
     return out
 
 
