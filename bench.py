@@ -52,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=69,
+                    help="layers of the headline decode pool (69 = the Kimi-K3 shard; fewer "
+                         "only for small profiling captures)")
     return ap.parse_args(argv)
 
 
@@ -462,7 +465,7 @@ def main(argv=None):
     torch.cuda.set_stream(stream)
 
     # ---- headline: Kimi-K3 shard KDA decode, 69 layers, batch 64
-    wl = DecodeWorkload(dev, 69, 320, 64, 12, 128, 128, b.BF16, b.BF16, b.KDA, seed=0)
+    wl = DecodeWorkload(dev, args.layers, 320, 64, 12, 128, 128, b.BF16, b.BF16, b.KDA, seed=0)
     graph = graph_of(wl.step, stream)
     with ClockSampler(local) as clk:
         ms = timed(graph.replay, args.steps, args.warmup, stream, dist)
@@ -518,11 +521,13 @@ def main(argv=None):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "kda_decode_kimi_k3_tp8_shard", "layers": 69, "batch": 64,
+        "config": {"workload": "kda_decode_kimi_k3_tp8_shard" + ("" if args.layers == 69 else
+                                                                  f"_layers{args.layers}"),
+                   "layers": args.layers, "batch": 64,
                    "pool_slots": 320, "H": 12, "K": 128, "V": 128, "state_dtype": "bf16",
                    "io_dtype": "bf16", "tokens_per_request_per_step": 1,
                    "l2": "inputs larger than L2: 1.74 GB of state moved per step, no flush",
-                   "launch": "69 kda_decode_step launches per step replayed from a CUDA graph",
+                   "launch": f"{args.layers} kda_decode_step launches per step replayed from a CUDA graph",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -531,7 +536,7 @@ def main(argv=None):
         "e2e": {"value": round(sum_over_ranks(units, dist, dev) / (ms_e2e * 1e-3), 1),
                 "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 69 * args.steps,
+        "gpu_launches": args.layers * args.steps,
         "clocks": clocks,
         "legs": legs,
     }

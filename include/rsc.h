@@ -24,8 +24,8 @@
  *     caller; the library never allocates, frees or retains device memory, except where
  *     a call says otherwise.  Pointers documented "host" are read before the call returns.
  *   - Device arrays read or written with 16-byte vector accesses must be 16-byte
- *     aligned: pool bases, qkv, out, conv_w, spec caches, workspace, and g of a
- *     prefill.  Other arrays need their element alignment.  Otherwise RSC_EALIGN.
+ *     aligned: pool bases, qkv, out, conv_w, g, spec caches, workspace.  Other
+ *     arrays need their element alignment.  Otherwise RSC_EALIGN.
  *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  Host-side validation failures return a negative status before anything
  *     is launched.  A CUDA launch failure returns RSC_ECUDA.

@@ -7,27 +7,30 @@
 // "Conv state".
 //
 // One thread-block cluster per (request, head): NVT CTAs of NW warps, CTA j owning
-// rows [j*VT, (j+1)*VT) of the head's state S[V][K] (VT = V/NVT).  Data flow of a CTA:
-//   1. the slot id is bounds-checked and one elected thread starts a TMA bulk copy of
-//      the CTA's whole S tile (VT*K contiguous elements) into shared memory, completing
-//      on an mbarrier: the tile's HBM traffic is in flight while the rest of the
-//      prologue runs, and no registers are tied up holding it;
-//   2. every CTA of the cluster computes the conv of all 2K q/k channels of its head
-//      (redundantly, a few KB from L2) and of its own VT value channels;
+// rows [j*VT, (j+1)*VT) of the head's state S[V][K] (VT = V/NVT; NVT = 1 by default, a
+// whole head per CTA).  Data flow of a CTA:
+//   1. the small inputs are requested first -- qkv, conv taps, gate and beta before the
+//      slot id returns, the slot's window right after -- because the conv depends on
+//      them and, requested later, they would queue in DRAM behind the tile copies of
+//      every CTA on the GPU (measured: the conv then finished ~5 us into a 13 us launch);
+//   2. one elected thread starts TMA bulk copies of the CTA's S tile (VT*K contiguous
+//      elements) into shared memory in NCH row chunks, each completing on its own
+//      mbarrier: EARLY chunks at once, the rest as soon as the conv is computed;
 //   3. block reductions give |q|^2, |k|^2, q.k, hence q_hat, k_hat and k_hat.q_hat;
-//   4. a cluster barrier orders every CTA's window reads before any window write; each
-//      window channel is then rolled by exactly one thread of the cluster (q/k channels
-//      partitioned over the NVT CTAs, value channels by row tile), so the window update
-//      is a bit-exact shift with a single writer per byte;
-//   5. after a bounded wait on the mbarrier, each warp streams its rows out of shared
-//      memory pass by pass: delta rule on 16-byte row segments (rsc_step.cuh), the new
-//      state stored straight back to the slot with coalesced 16-byte stores.
+//   4. (clusters only) a cluster barrier orders every CTA's window reads before any
+//      window write; each window channel is rolled by exactly one thread of the cluster
+//      (q/k channels partitioned over the NVT CTAs, value channels by row tile), so the
+//      window update is a bit-exact shift with a single writer per byte;
+//   5. each warp streams its rows out of shared memory pass by pass, waiting (bounded)
+//      for a chunk only when it reaches it: delta rule on 16-byte row segments
+//      (rsc_step.cuh), the new state stored straight back to the slot with coalesced
+//      16-byte stores, so a CTA's writes overlap its own later reads.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
 namespace rsc {
 
-template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE>
 __global__ void __cluster_dims__(NVT, 1, 1) __launch_bounds__(NW * 32)
 kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                   const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -39,19 +42,65 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   constexpr int QK_T = (2 * K + NT - 1) / NT;  // q/k channels per thread
   constexpr int OWN = 2 * K / NVT;             // q/k channels rolled by each CTA
   constexpr uint32_t TILE_BYTES = VT * K * sizeof(ST);
+  constexpr uint32_t CHUNK_BYTES = TILE_BYTES / NCH;  // one bulk copy + mbarrier each
+  constexpr int PPC = G::NP / NCH;                    // passes per chunk
   static_assert(VT <= NT && K <= NT, "one value row and one key channel per thread");
-  static_assert(TILE_BYTES % 16 == 0, "bulk copy granularity");
+  static_assert(PPC * NCH == G::NP && CHUNK_BYTES % 16 == 0, "chunks of whole passes");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   ST *s_S = reinterpret_cast<ST *>(smem_raw);  // the VT x K tile
   __shared__ float s_qk[2 * K];                // conv outputs: q then k of this head
   __shared__ float s_v[VT];                    // conv outputs of this tile's value rows
   __shared__ float s_red[3 * NW];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_bar[NCH];
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int H = pv.H, D = pv.D;
+
+  grid_dep_wait();               // previous grid done and visible before any global access
+  grid_dep_launch_dependents();  // the next grid may be scheduled while this one drains
+
+  // 1. Small inputs first.  Their DRAM requests must not queue behind the tile copies of
+  //    every CTA on the GPU, because the conv (and with it every row update) waits on
+  //    them: slot-independent loads (qkv, taps, gate, beta) are issued before the slot id
+  //    returns, the window right after it, and only then the first chunk of the tile.
+  const IO *x = qkv + (size_t)b * D;
+  float4 wqk[QK_T];
+  IO xqk[QK_T];
+#pragma unroll
+  for (int u = 0; u < QK_T; ++u) {
+    const int i2 = tid + u * NT;
+    if (i2 < 2 * K) {
+      const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
+      wqk[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)c);
+      xqk[u] = x[c];
+    }
+  }
+  const int cv = 2 * H * K + h * V + j * VT + tid;
+  float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+  IO xv = from_f32<IO>(0.f);
+  if (tid < VT) {
+    wv = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cv);
+    xv = x[cv];
+  }
+  const int k0 = G::kofs();
+  float gl[G::EPL];  // the gate
+  if (GATE == RSC_GATE_KDA) {
+    float4 g4[G::EPL / 4];
+    const float4 *gg = reinterpret_cast<const float4 *>(g + ((size_t)b * H + h) * K + k0);
+#pragma unroll
+    for (int e = 0; e < G::EPL / 4; ++e) g4[e] = gg[e];
+#pragma unroll
+    for (int e = 0; e < G::EPL / 4; ++e) {
+      gl[4 * e] = g4[e].x; gl[4 * e + 1] = g4[e].y; gl[4 * e + 2] = g4[e].z; gl[4 * e + 3] = g4[e].w;
+    }
+  } else {
+    const float gh = g[(size_t)b * H + h];
+#pragma unroll
+    for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
+  }
+  const float bt = beta[(size_t)b * H + h];
 
   const int slot = slots[b];
   if (slot < 0 || slot > pv.P) {
@@ -60,39 +109,56 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   }
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
   ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
-
-  // 1. S tile -> shared memory, asynchronously.
-  if (tid == 0) mbar_init(&s_bar, 1);
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&s_bar, TILE_BYTES);
-    bulk_g2s(s_S, S, TILE_BYTES, &s_bar);
-  }
-
-  // 2. conv of the head's q/k channels and of this tile's value channels.
   IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
-  const IO *x = qkv + (size_t)b * D;
   IO keep[QK_T][3];
 #pragma unroll
   for (int u = 0; u < QK_T; ++u) {
     const int i2 = tid + u * NT;
     if (i2 < 2 * K) {
       const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
-      const float4 w = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)c);
-      const IO w0 = W[c], w1 = W[D + c], w2 = W[2 * D + c], xc = x[c];
-      s_qk[i2] = conv4(w, to_f32(w0), to_f32(w1), to_f32(w2), to_f32(xc));
-      keep[u][0] = w1; keep[u][1] = w2; keep[u][2] = xc;
+      keep[u][0] = W[c]; keep[u][1] = W[D + c]; keep[u][2] = W[2 * D + c];
     }
   }
   IO keepv[3];
-  const int cv = 2 * H * K + h * V + j * VT + tid;
-  if (tid < VT) {
-    const float4 w = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cv);
-    const IO w0 = W[cv], w1 = W[D + cv], w2 = W[2 * D + cv], xc = x[cv];
-    s_v[tid] = conv4(w, to_f32(w0), to_f32(w1), to_f32(w2), to_f32(xc));
-    keepv[0] = w1; keepv[1] = w2; keepv[2] = xc;
+  if (tid < VT) { keepv[0] = W[cv]; keepv[1] = W[D + cv]; keepv[2] = W[2 * D + cv]; }
+
+  // 2. The tile, in NCH row chunks on their own mbarriers (chunk c holds the rows of
+  //    passes [c*PPC, (c+1)*PPC)): EARLY chunks now, the rest once the conv is done.
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) mbar_init(&s_bar[c], 1);
   }
   __syncthreads();
+  auto issue_chunk = [&](int c) {
+    mbar_arrive_expect_tx(&s_bar[c], CHUNK_BYTES);
+    bulk_g2s(reinterpret_cast<char *>(s_S) + c * CHUNK_BYTES,
+             reinterpret_cast<const char *>(S) + c * CHUNK_BYTES, CHUNK_BYTES, &s_bar[c]);
+  };
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < EARLY; ++c) issue_chunk(c);
+  }
+
+  // conv of the head's q/k channels and of this tile's value channels; the window values
+  // each thread will roll are kept (keep[u] becomes rows 1, 2 and the input).
+#pragma unroll
+  for (int u = 0; u < QK_T; ++u) {
+    const int i2 = tid + u * NT;
+    if (i2 < 2 * K) {
+      s_qk[i2] = conv4(wqk[u], to_f32(keep[u][0]), to_f32(keep[u][1]), to_f32(keep[u][2]),
+                       to_f32(xqk[u]));
+      keep[u][0] = keep[u][1]; keep[u][1] = keep[u][2]; keep[u][2] = xqk[u];
+    }
+  }
+  if (tid < VT) {
+    s_v[tid] = conv4(wv, to_f32(keepv[0]), to_f32(keepv[1]), to_f32(keepv[2]), to_f32(xv));
+    keepv[0] = keepv[1]; keepv[1] = keepv[2]; keepv[2] = xv;
+  }
+  __syncthreads();
+  if (tid == 0) {
+#pragma unroll
+    for (int c = EARLY; c < NCH; ++c) issue_chunk(c);
+  }
 
   // 3. norms and k.q.
   float qq = 0.f, kk = 0.f, qk = 0.f;
@@ -106,22 +172,12 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   const float kq = qk * rq * rk;
 
   float qh[G::EPL], kh[G::EPL], al[G::EPL];
-  const int k0 = G::kofs();
 #pragma unroll
   for (int e = 0; e < G::EPL; ++e) {
     qh[e] = s_qk[k0 + e] * rq;
     kh[e] = s_qk[K + k0 + e] * rk;
+    al[e] = expf(gl[e]);
   }
-  if (GATE == RSC_GATE_KDA) {
-    const float *gg = g + ((size_t)b * H + h) * K + k0;
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) al[e] = expf(gg[e]);
-  } else {
-    const float a = expf(g[(size_t)b * H + h]);
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) al[e] = a;
-  }
-  const float bt = beta[(size_t)b * H + h];
 
   // 4. window roll: all reads of the cluster happen before any write.
   if (NVT > 1) cluster_sync_all();
@@ -136,14 +192,14 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   if (tid < VT) { W[cv] = keepv[0]; W[D + cv] = keepv[1]; W[2 * D + cv] = keepv[2]; }
 
   // 5. delta rule pass by pass out of shared memory; state back in place.
-  if (!mbar_wait(&s_bar, 0)) {
-    flag_error(pv.err, RSC_DEVERR_TIMEOUT);
-    mbar_wait(&s_bar, 0);  // give the copy one more bounded chance to land
-    return;
-  }
   IO *ob = out + ((size_t)b * H + h) * V + (size_t)j * VT;
 #pragma unroll 2
   for (int p = 0; p < G::NP; ++p) {
+    if (p % PPC == 0 && !mbar_wait(&s_bar[p / PPC], 0)) {
+      flag_error(pv.err, RSC_DEVERR_TIMEOUT);
+      for (int c = p / PPC; c < NCH; ++c) mbar_wait(&s_bar[c], 0);  // let copies land
+      return;
+    }
     const int r = G::row(p);
     float s[G::EPL];
     unpack16(*reinterpret_cast<const uint4 *>(s_S + (size_t)r * K + k0), s);
@@ -155,16 +211,29 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 
 // Tile shape per state dtype: rows per CTA (VT) and warps per CTA.
 #ifndef RSC_DECODE_ROWS_BF16
-#define RSC_DECODE_ROWS_BF16 32
+#define RSC_DECODE_ROWS_BF16 128
 #endif
 #ifndef RSC_DECODE_WARPS_BF16
 #define RSC_DECODE_WARPS_BF16 4
 #endif
 #ifndef RSC_DECODE_ROWS_F32
-#define RSC_DECODE_ROWS_F32 32
+#define RSC_DECODE_ROWS_F32 128
 #endif
 #ifndef RSC_DECODE_WARPS_F32
-#define RSC_DECODE_WARPS_F32 4
+#define RSC_DECODE_WARPS_F32 8
+#endif
+
+// Programmatic dependent launch of consecutive decode grids (see launch_pdl).  Off: on
+// GB300 the 69-layer graph ran slower with it (13.6 vs 12.7 us per layer).
+#ifndef RSC_DECODE_PDL
+#define RSC_DECODE_PDL 0
+#endif
+// Bulk copies (and mbarriers) per CTA tile, and how many of them start before the conv.
+#ifndef RSC_DECODE_CHUNKS
+#define RSC_DECODE_CHUNKS 4
+#endif
+#ifndef RSC_DECODE_EARLY_CHUNKS
+#define RSC_DECODE_EARLY_CHUNKS 2
 #endif
 
 template <typename ST> struct DecodeTile;
@@ -184,7 +253,10 @@ struct DecodeLaunch {
     constexpr int NVT = V / ROWS;
     constexpr int NW = DecodeTile<ST>::WARPS;
     constexpr size_t SMEM = (size_t)ROWS * K * sizeof(ST);
-    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, GATE>;
+    constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
+    constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
+    constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
+    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
@@ -193,9 +265,14 @@ struct DecodeLaunch {
       attr_set = true;
     }
     dim3 grid(NVT, a->pv.H, B);
+#if RSC_DECODE_PDL
+    return launch_pdl(kern, grid, dim3(NW * 32), SMEM, s, a->pv, a->layer, slots,
+                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out));
+#else
     kern<<<grid, NW * 32, SMEM, s>>>(a->pv, a->layer, slots, static_cast<const IO *>(qkv),
                                      conv_w, g, beta, static_cast<IO *>(out));
     return launch_status();
+#endif
   }
 };
 

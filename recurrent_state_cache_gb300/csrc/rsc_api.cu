@@ -95,7 +95,7 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
     return RSC_ERANGE;
   if (batch == 0) return RSC_OK;
   if (!slot_ids || !qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 4) ||
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
       !aligned(beta, 4) || !aligned(slot_ids, 4))
     return RSC_EALIGN;
   return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
@@ -171,7 +171,7 @@ int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *s
                                    as_stream(stream));
   }
   if (!qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 4) ||
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
       !aligned(beta, 4))
     return RSC_EALIGN;
   return rsc::launch_spec_verify(a, slot_ids, batch, T, L, spec_ssm, spec_conv, qkv, conv_w, g,

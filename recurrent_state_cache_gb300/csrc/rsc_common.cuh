@@ -177,6 +177,17 @@ __device__ __forceinline__ void bulk_g2s(void *smem, const void *gmem, uint32_t 
       ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Wait until the previous grid on the stream has completed and its writes are visible
+// (no-op when the grid was not launched as a programmatic dependent), then allow the next
+// grid to be scheduled early.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ void cluster_sync_all() {

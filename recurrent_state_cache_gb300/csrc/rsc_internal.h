@@ -44,6 +44,28 @@ inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? RSC_OK : RSC_ECUDA;
 }
 
+// Launch with programmatic stream serialization: the grid may be scheduled while the
+// previous kernel on the stream drains.  Kernels launched this way call grid_dep_wait()
+// before touching global memory, which waits for the previous grid to complete and its
+// writes to be visible, so stream-order semantics are unchanged; only the launch latency
+// and ramp of the new grid overlap the tail of the old one.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+               Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess ? RSC_OK
+                                                                                      : RSC_ECUDA;
+}
+
 // Compile-time dispatch over (state dtype, io dtype, K, V, gate) onto L<ST,IO,K,V,GATE>::run.
 template <template <typename, typename, int, int, int> class L, typename ST, typename IO,
           int K, int V, typename... A>

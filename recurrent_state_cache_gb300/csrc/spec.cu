@@ -6,8 +6,10 @@
 // per-step cache and the commit scatters the snapshot of the last accepted step into
 // the persistent state; the intermediate SSM cache does the same for S.
 //
-// VERIFY runs the decode body of decode.cu T times with the state tile held in
-// registers (fp32) across tokens; the slot is only read.  Each CTA keeps its own copy
+// VERIFY runs the decode body T times with the state tile held in registers (fp32)
+// across tokens; the slot is only read.  The per-token inputs (q/k channels of the head,
+// the tile's value channels, gate, beta) are staged into shared memory eight tokens at a
+// time with cp.async, one block ahead, so the token loop never waits on HBM.  Each CTA keeps its own copy
 // of the head's q/k windows plus its value rows' windows in registers and rolls them
 // token by token, so no CTA ever writes memory another one reads: no cluster needed.
 // Each window channel of a cache entry is written by exactly one CTA (q/k channels
@@ -29,7 +31,17 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   using G = TileGeom<ST, K, VT>;
   constexpr int QK_T = 2 * K / 128;
   constexpr int OWN = 2 * K / NVT;
+  constexpr int TS = 8;                       // tokens per staged block
+  constexpr int GW = GATE == RSC_GATE_KDA ? K : 1;
+  constexpr int XV = 16 / sizeof(IO);         // io elements per 16-byte copy
+  static_assert((2 * K) % XV == 0 && VT % XV == 0, "16-byte staging");
 
+  // Per-token inputs of TS tokens, double-buffered: this head's q/k channels, this tile's
+  // value channels, the gate and beta.  Staged with cp.async one block ahead.
+  __shared__ __align__(16) IO s_xqk[2][TS][2 * K];
+  __shared__ __align__(16) IO s_xv[2][TS][VT];
+  __shared__ __align__(16) float s_g[2][TS][GW];
+  __shared__ float s_b[2][TS];
   __shared__ float s_qk[2 * K];
   __shared__ float s_v[VT];
   __shared__ float s_red[12];
@@ -44,6 +56,31 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     return;
   }
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+
+  auto stage = [&](int buf, int t0) {
+    const int cnt = min(TS, T - t0);
+    for (int i = tid; i < cnt * (2 * K / XV); i += 128) {
+      const int tau = i / (2 * K / XV), c = (i % (2 * K / XV)) * XV;
+      const int src = c < K ? h * K + c : H * K + h * K + (c - K);
+      cp_async16(&s_xqk[buf][tau][c], qkv + ((size_t)b * T + t0 + tau) * D + src);
+    }
+    for (int i = tid; i < cnt * (VT / XV); i += 128) {
+      const int tau = i / (VT / XV), c = (i % (VT / XV)) * XV;
+      cp_async16(&s_xv[buf][tau][c],
+                 qkv + ((size_t)b * T + t0 + tau) * D + 2 * H * K + h * V + j * VT + c);
+    }
+    if (GATE == RSC_GATE_KDA) {
+      for (int i = tid; i < cnt * (K / 4); i += 128) {
+        const int tau = i / (K / 4), c = (i % (K / 4)) * 4;
+        cp_async16(&s_g[buf][tau][c], g + (((size_t)b * T + t0 + tau) * H + h) * K + c);
+      }
+    } else if (tid < cnt) {
+      cp_async4(&s_g[buf][tid][0], g + ((size_t)b * T + t0 + tid) * H + h);
+    }
+    if (tid < cnt) cp_async4(&s_b[buf][tid], beta + ((size_t)b * T + t0 + tid) * H + h);
+    cp_async_commit();
+  };
+  stage(0, 0);
 
   const ST *S = reinterpret_cast<const ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
   float s[G::NP][G::EPL];
@@ -70,68 +107,64 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   }
 
   const int k0 = G::kofs();
-  for (int t = 0; t < T; ++t) {
-    const size_t bt = (size_t)b * T + t;
-    const IO *x = qkv + bt * D;
-    IO *E = spec_conv + ((size_t)b * L + t) * 3 * (size_t)D;
-    if (t > 0) __syncthreads();  // previous token's readers of s_qk / s_v are done
+  int cur = 0;
+  for (int t0 = 0; t0 < T; t0 += TS) {
+    cp_async_wait_all();
+    __syncthreads();  // block `cur` landed; every reader of block cur^1 is done
+    if (t0 + TS < T) stage(cur ^ 1, t0 + TS);
+    const int cnt = min(TS, T - t0);
+    for (int tau = 0; tau < cnt; ++tau) {
+      const int t = t0 + tau;
+      const size_t bt = (size_t)b * T + t;
+      IO *E = spec_conv + ((size_t)b * L + t) * 3 * (size_t)D;
+      if (tau > 0) __syncthreads();  // previous token's readers of s_qk / s_v / s_red done
 #pragma unroll
-    for (int u = 0; u < QK_T; ++u) {
-      const IO xc = x[cqk[u]];
-      s_qk[tid + u * 128] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]),
-                                  to_f32(win[u][2]), to_f32(xc));
-      win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
-      const int i2 = tid + u * 128;
-      if (i2 >= j * OWN && i2 < (j + 1) * OWN) {
-        E[cqk[u]] = win[u][0]; E[D + cqk[u]] = win[u][1]; E[2 * D + cqk[u]] = win[u][2];
+      for (int u = 0; u < QK_T; ++u) {
+        const int i2 = tid + u * 128;
+        const IO xc = s_xqk[cur][tau][i2];
+        s_qk[i2] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
+                         to_f32(xc));
+        win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
+        if (i2 >= j * OWN && i2 < (j + 1) * OWN) {
+          E[cqk[u]] = win[u][0]; E[D + cqk[u]] = win[u][1]; E[2 * D + cqk[u]] = win[u][2];
+        }
+      }
+      if (tid < VT) {
+        const IO xc = s_xv[cur][tau][tid];
+        s_v[tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
+        winv[0] = winv[1]; winv[1] = winv[2]; winv[2] = xc;
+        E[cv] = winv[0]; E[D + cv] = winv[1]; E[2 * D + cv] = winv[2];
+      }
+      __syncthreads();
+
+      float qq = 0.f, kk = 0.f, qk = 0.f;
+      if (tid < K) {
+        const float a = s_qk[tid], c = s_qk[K + tid];
+        qq = a * a; kk = c * c; qk = a * c;
+      }
+      block3_sum_128(qq, kk, qk, s_red);
+      const float rq = 1.0f / sqrtf(qq + kNormEps);
+      const float rk = 1.0f / sqrtf(kk + kNormEps);
+      const float kq = qk * rq * rk;
+
+      float qh[G::EPL], kh[G::EPL], al[G::EPL];
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) {
+        qh[e] = s_qk[k0 + e] * rq;
+        kh[e] = s_qk[K + k0 + e] * rk;
+        al[e] = expf(GATE == RSC_GATE_KDA ? s_g[cur][tau][k0 + e] : s_g[cur][tau][0]);
+      }
+      float o[G::NP];
+      delta_rule_tile<ST, K, VT>(s, qh, kh, al, s_b[cur][tau], kq, s_v, o);
+      ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
+      tile_store<ST, K, VT>(Se, s);
+      if (k0 == 0) {
+        IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
+#pragma unroll
+        for (int p = 0; p < G::NP; ++p) ob[G::row(p)] = from_f32<IO>(o[p]);
       }
     }
-    if (tid < VT) {
-      const IO xc = x[cv];
-      s_v[tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
-      winv[0] = winv[1]; winv[1] = winv[2]; winv[2] = xc;
-      E[cv] = winv[0]; E[D + cv] = winv[1]; E[2 * D + cv] = winv[2];
-    }
-    __syncthreads();
-
-    float qq = 0.f, kk = 0.f, qk = 0.f;
-    if (tid < K) {
-      const float a = s_qk[tid], c = s_qk[K + tid];
-      qq = a * a; kk = c * c; qk = a * c;
-    }
-    block3_sum_128(qq, kk, qk, s_red);
-    const float rq = 1.0f / sqrtf(qq + kNormEps);
-    const float rk = 1.0f / sqrtf(kk + kNormEps);
-    const float kq = qk * rq * rk;
-
-    float qh[G::EPL], kh[G::EPL], al[G::EPL];
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) {
-      qh[e] = s_qk[k0 + e] * rq;
-      kh[e] = s_qk[K + k0 + e] * rk;
-    }
-    if (GATE == RSC_GATE_KDA) {
-      const float *gg = g + (bt * H + h) * K + k0;
-#pragma unroll
-      for (int e = 0; e < G::EPL; ++e) al[e] = expf(gg[e]);
-    } else {
-      const float a = expf(g[bt * H + h]);
-#pragma unroll
-      for (int e = 0; e < G::EPL; ++e) al[e] = a;
-    }
-    const float bta = beta[bt * H + h];
-
-    float o[G::NP];
-    delta_rule_tile<ST, K, VT>(s, qh, kh, al, bta, kq, s_v, o);
-    ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
-    tile_store<ST, K, VT>(Se, s);
-    if (k0 == 0) {
-      IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
-#pragma unroll
-      for (int p = 0; p < G::NP; ++p) ob[G::row(p)] = from_f32<IO>(o[p]);
-    }
-    // the block reduction scratch is rewritten next token only after the barrier at
-    // the top of the loop, which every thread reaches after its reads of s_red above
+    cur ^= 1;
   }
 }
 
@@ -158,13 +191,15 @@ int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, i
                                     spec_ssm, spec_conv, qkv, conv_w, g, beta, out, s);
 }
 
-// COMMIT: slot <- cache entry accept[b], for S (which == 0) or the window (which == 1).
-// Grid (chunks of kCopyChunk bytes, batch).  Bad slot or accept count: row skipped.
+// COMMIT: slot <- cache entry accept[b], the state rows (blockIdx.z == 0) and the window
+// rows (blockIdx.z == 1) in one launch.  Grid (chunks of kCopyChunk bytes of the longer
+// row, batch, 2).  A bad slot or accept count skips the row and sets the error word.
 __global__ void __launch_bounds__(128)
-kda_spec_commit_kernel(PoolView pv, int layer, size_t row_bytes, int which,
+kda_spec_commit_kernel(PoolView pv, int layer, size_t ssm_row_bytes, size_t conv_row_bytes,
                        const int32_t *__restrict__ slots, int T, int L,
-                       const char *__restrict__ cache, const int32_t *__restrict__ accept) {
-  const int b = blockIdx.y;
+                       const char *__restrict__ spec_ssm, const char *__restrict__ spec_conv,
+                       const int32_t *__restrict__ accept) {
+  const int b = blockIdx.y, which = blockIdx.z;
   const int slot = slots[b], a = accept[b];
   const bool bad_slot = slot < 0 || slot > pv.P, bad_acc = a < 0 || a >= T;
   if (bad_slot || bad_acc) {
@@ -172,11 +207,12 @@ kda_spec_commit_kernel(PoolView pv, int layer, size_t row_bytes, int which,
       flag_error(pv.err, (bad_slot ? RSC_DEVERR_SLOT : 0) | (bad_acc ? RSC_DEVERR_ACCEPT : 0));
     return;
   }
+  const size_t row_bytes = which == 0 ? ssm_row_bytes : conv_row_bytes;
   const size_t off = (size_t)blockIdx.x * kCopyChunk;
   if (off >= row_bytes) return;
   char *base = reinterpret_cast<char *>(which == 0 ? pv.ssm : pv.conv);
   char *dst = base + ((size_t)layer * (pv.P + 1) + slot) * row_bytes;
-  const char *src = cache + ((size_t)b * L + a) * row_bytes;
+  const char *src = (which == 0 ? spec_ssm : spec_conv) + ((size_t)b * L + a) * row_bytes;
   copy_chunk(dst, src, row_bytes, off);
 }
 
@@ -186,13 +222,11 @@ int launch_spec_commit(const LayerArgs &a, const int32_t *slots, int B, int T, i
   const size_t ssz = a.st == RSC_F32 ? 4 : 2, csz = a.io == RSC_F32 ? 4 : 2;
   const size_t sb = (size_t)a.pv.H * a.pv.V * a.pv.K * ssz;
   const size_t cb = (size_t)3 * a.pv.D * csz;
-  dim3 gs((unsigned)((sb + kCopyChunk - 1) / kCopyChunk), B);
-  kda_spec_commit_kernel<<<gs, 128, 0, s>>>(a.pv, a.layer, sb, 0, slots, T, L,
-                                            static_cast<const char *>(spec_ssm), accept);
-  if (launch_status() != RSC_OK) return RSC_ECUDA;
-  dim3 gc((unsigned)((cb + kCopyChunk - 1) / kCopyChunk), B);
-  kda_spec_commit_kernel<<<gc, 128, 0, s>>>(a.pv, a.layer, cb, 1, slots, T, L,
-                                            static_cast<const char *>(spec_conv), accept);
+  const size_t longest = sb > cb ? sb : cb;
+  dim3 grid((unsigned)((longest + kCopyChunk - 1) / kCopyChunk), B, 2);
+  kda_spec_commit_kernel<<<grid, 128, 0, s>>>(a.pv, a.layer, sb, cb, slots, T, L,
+                                              static_cast<const char *>(spec_ssm),
+                                              static_cast<const char *>(spec_conv), accept);
   return launch_status();
 }
 
