@@ -312,7 +312,7 @@ def leg_prefill(dev, peaks, stream):
            "tensor_frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 5),
            "io_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
            "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-           "path": "token-serial fp32 recurrence"}
+           "path": "chunkwise, tcgen05 tensor cores"}
     return res
 
 

@@ -20,7 +20,7 @@ VERIFY, COMMIT = 0, 1
 
 RSC_OK, RSC_EINVAL, RSC_ERANGE, RSC_EDTYPE, RSC_EALIGN, RSC_ECUDA, RSC_ENOSPACE = (
     0, -1, -2, -3, -4, -5, -6)
-DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ = 1, 2, 4
+DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ, DEVERR_TIMEOUT, DEVERR_GATE = 1, 2, 4, 8, 16
 
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 

@@ -25,11 +25,7 @@ namespace rsc {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-struct PrefillWs {
-  float *q, *k, *v, *kq;
-};
-
-static PrefillWs carve(void *ws, const PoolView &pv, int T) {
+PrefillWs prefill_carve(void *ws, const PoolView &pv, int T) {
   char *p = static_cast<char *>(ws);
   PrefillWs w;
   const size_t nq = align256((size_t)T * pv.H * pv.K * 4);
@@ -41,7 +37,7 @@ static PrefillWs carve(void *ws, const PoolView &pv, int T) {
   return w;
 }
 
-size_t prefill_serial_workspace_bytes(const PoolView &pv, int T) {
+size_t prefill_prep_bytes(const PoolView &pv, int T) {
   return 2 * align256((size_t)T * pv.H * pv.K * 4) + align256((size_t)T * pv.H * pv.V * 4) +
          align256((size_t)T * pv.H * 4);
 }
@@ -239,7 +235,7 @@ struct PrefillSerialLaunch {
                  const uint8_t *has_init, const void *qkv, const float *conv_w,
                  const float *g, const float *beta, void *out, void *ws, cudaStream_t s) {
     constexpr int NVT = V / 32;
-    const PrefillWs w = carve(ws, a->pv, T);
+    const PrefillWs w = prefill_carve(ws, a->pv, T);
     if (T > 0) {
       prefill_prep_kernel<IO, K, V><<<dim3(T, a->pv.H), 128, 0, s>>>(
           a->pv, a->layer, slots, cu, N, has_init, static_cast<const IO *>(qkv), conv_w, w);
@@ -262,9 +258,50 @@ int launch_prefill_serial(const LayerArgs &a, const int32_t *slots, const int32_
                                            N, T, has_init, qkv, conv_w, g, beta, out, ws, s);
 }
 
+int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                        int T, const uint8_t *has_init, const void *qkv, const float *conv_w,
+                        const PrefillWs &w, cudaStream_t s) {
+  if (T == 0) return RSC_OK;
+  const int K = a.pv.K, V = a.pv.V;
+  const dim3 grid(T, a.pv.H);
+#define RSC_PREP(IO_, K_, V_)                                                               \
+  prefill_prep_kernel<IO_, K_, V_><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, N, has_init, \
+                                                        static_cast<const IO_ *>(qkv), conv_w, w)
+  if (a.io == RSC_BF16) {
+    if (K == 128 && V == 128) RSC_PREP(bf16, 128, 128);
+    else if (K == 128) RSC_PREP(bf16, 128, 64);
+    else if (V == 128) RSC_PREP(bf16, 64, 128);
+    else RSC_PREP(bf16, 64, 64);
+  } else {
+    if (K == 128 && V == 128) RSC_PREP(float, 128, 128);
+    else if (K == 128) RSC_PREP(float, 128, 64);
+    else if (V == 128) RSC_PREP(float, 64, 128);
+    else RSC_PREP(float, 64, 64);
+  }
+#undef RSC_PREP
+  return launch_status();
+}
+
+int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                          int T, const uint8_t *has_init, const void *qkv, cudaStream_t s) {
+  const dim3 grid((a.pv.D + 127) / 128, N);
+  if (a.io == RSC_BF16)
+    prefill_window_kernel<bf16><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
+                                                     static_cast<const bf16 *>(qkv));
+  else
+    prefill_window_kernel<float><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
+                                                      static_cast<const float *>(qkv));
+  return launch_status();
+}
+
+static bool use_tc(const PoolView &pv, int st) { return st == RSC_BF16 && pv.K == 128; }
+
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T) {
-  (void)st; (void)N;
-  return prefill_serial_workspace_bytes(pv, T);
+  size_t b = prefill_prep_bytes(pv, T);
+  if (use_tc(pv, st))
+    b += align256((size_t)(N + 1) * 4) +
+         prefill_tc_chunk_capacity(N, T) * (size_t)pv.H * prefill_tc_block_bytes();
+  return b;
 }
 
 int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_seqlens,
@@ -272,8 +309,19 @@ int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_s
                    const float *conv_w, const float *g, const float *beta, void *out,
                    void *ws, size_t ws_bytes, cudaStream_t s) {
   if (ws_bytes < prefill_workspace_bytes(a.pv, a.st, N, T)) return RSC_ENOSPACE;
-  return launch_prefill_serial(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta,
-                               out, ws, s);
+  if (!use_tc(a.pv, a.st))
+    return launch_prefill_serial(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta,
+                                 out, ws, s);
+  const PrefillWs w = prefill_carve(ws, a.pv, T);
+  char *tail = static_cast<char *>(ws) + prefill_prep_bytes(a.pv, T);
+  int32_t *chunk_base = reinterpret_cast<int32_t *>(tail);
+  char *blocks = tail + align256((size_t)(N + 1) * 4);
+  int rc = launch_prefill_prep(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, w, s);
+  if (rc != RSC_OK) return rc;
+  rc = launch_prefill_tc(a, slots, cu_seqlens, N, T, has_init, w, g, beta, out, chunk_base,
+                         blocks, s);
+  if (rc != RSC_OK) return rc;
+  return launch_prefill_window(a, slots, cu_seqlens, N, T, has_init, qkv, s);
 }
 
 }  // namespace rsc

@@ -35,6 +35,26 @@ int launch_slot_copy(const PoolView &pv, int st, int io, int layer0, int nlayers
 
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T);
 
+// Per-token prefill operands written by the prep kernel (fp32): q_hat, k_hat [T][H][K],
+// conv'd v [T][H][V], k_hat . q_hat [T][H].
+struct PrefillWs {
+  float *q, *k, *v, *kq;
+};
+size_t prefill_prep_bytes(const PoolView &pv, int T);
+PrefillWs prefill_carve(void *ws, const PoolView &pv, int T);
+int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                        int T, const uint8_t *has_init, const void *qkv, const float *conv_w,
+                        const PrefillWs &w, cudaStream_t s);
+int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                          int T, const uint8_t *has_init, const void *qkv, cudaStream_t s);
+// Tensor-core chunkwise path (bf16 state, K = 128).
+size_t prefill_tc_chunk_capacity(int N, int T);
+size_t prefill_tc_block_bytes();
+int launch_prefill_tc(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
+                      const uint8_t *has_init, const PrefillWs &w, const float *g,
+                      const float *beta, void *out, int32_t *chunk_base, char *blocks,
+                      cudaStream_t s);
+
 int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_seqlens,
                    int N, int T, const uint8_t *has_init, const void *qkv,
                    const float *conv_w, const float *g, const float *beta, void *out,
