@@ -40,6 +40,12 @@ if ROOT not in sys.path:
 
 HEADLINE_METRIC = "decode tokens/s per layer and achieved HBM GB/s (% of peak); prefill tok/s"
 
+# DRAM bytes (read + write) per launch of the headline decode kernel in an ncu capture of the
+# same launch shape (64 requests; profiles/kda_decode_kimi_k3_b64.md), keyed by a hash of the
+# kernel's source files: reported only while the kernel is the one that was captured.
+DECODE_SOURCES = ("decode.cu", "rsc_step.cuh", "rsc_common.cuh")
+CAPTURED_DECODE_TRAFFIC = {"fd28ef45e5dd585d": 28_143_104}
+
 
 # --------------------------------------------------------------------------- plumbing
 
@@ -189,6 +195,15 @@ def graph_of(fn, stream):
             fn()
     torch.cuda.synchronize()
     return g
+
+
+def decode_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "recurrent_state_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------------------- workloads
@@ -531,7 +546,10 @@ def main(argv=None):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": None, "kernel": "kda_decode_kernel",
+                     "traffic": CAPTURED_DECODE_TRAFFIC.get(decode_source_hash()),
+                     "traffic_note": "ncu dram read+write of one launch; the in-place state "
+                                     "writes stay in L2 until later layers evict them",
+                     "kernel": "kda_decode_kernel",
                      "bytes_per_launch": bpl, "peak_source": peaks["source"]},
         "e2e": {"value": round(sum_over_ranks(units, dist, dev) / (ms_e2e * 1e-3), 1),
                 "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
