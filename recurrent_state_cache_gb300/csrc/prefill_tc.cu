@@ -156,8 +156,11 @@ prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
   char *blk = blocks + ((size_t)cid * H + h) * kBlockBytes;
   const int ch = tid;
 
+  if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+
   // cumulative gates and the per-channel reference point R (midpoint of G's range)
   float G = 0.f, gmin = 0.f, gmax = 0.f;
+#pragma unroll 8
   for (int r = 0; r < kC; ++r) {
     if (r < Lc) {
       const size_t th = (size_t)(t0 + r) * H + h;
@@ -171,18 +174,24 @@ prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
   const float R = 0.5f * (gmin + gmax);
   const float Glast = sG[(Lc - 1) * kK + ch];
   reinterpret_cast<float *>(blk + kOffGC)[ch] = expf(Glast);
-  if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+  __syncthreads();  // s_beta
 
-  // operands of A / P (shared memory) and the state-independent operands of the state
-  // pass (workspace): Q.Gamma rows of [W; Q.Gamma] and (K.Gamma_c/Gamma)^T
+  // operands of A / P (shared memory), the state-independent operands of the state pass
+  // (workspace): Q.Gamma rows of [W; Q.Gamma] and (K.Gamma_c/Gamma)^T, and the right-hand
+  // sides beta_r k_r Gamma_r, beta_r v_r of the forward substitution below (seeded into
+  // the rows it overwrites in place, so that loop touches no global memory)
+#pragma unroll 4
   for (int r = 0; r < kC; ++r) {
-    float kr = 0.f, qr = 0.f;
+    float kr = 0.f, qr = 0.f, vr = 0.f;
     if (r < Lc) {
       const size_t th = (size_t)(t0 + r) * H + h;
       kr = ws.k[th * kK + ch];
       qr = ws.q[th * kK + ch];
+      if (ch < V) vr = ws.v[th * V + ch];
     }
     const float Gr = sG[r * kK + ch];
+    sWh[r * kK + ch] = s_beta[r] * kr * expf(Gr);
+    if (ch < V) sUh[r * 128 + ch] = s_beta[r] * vr;
     const float ep = expf(Gr - R), en = expf(R - Gr);
     st_bf16(sX + tc::kmajor_offset(r, ch, kK), kr * ep);
     st_bf16(sX + tc::kmajor_offset(kC + r, ch, kK), qr * ep);
@@ -240,10 +249,8 @@ prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
   for (int r = 0; r < kC; ++r) {
     float w = 0.f, u = 0.f;
     if (r < Lc) {
-      const size_t th = (size_t)(t0 + r) * H + h;
-      const float br = s_beta[r];
-      w = br * ws.k[th * kK + ch] * expf(sG[r * kK + ch]);
-      if (ch < V) u = br * ws.v[th * V + ch];
+      w = sWh[r * kK + ch];
+      if (ch < V) u = sUh[r * 128 + ch];
       float w2 = 0.f, u2 = 0.f;  // two accumulators for instruction-level parallelism
       int j = 0;
       for (; j + 1 < r; j += 2) {
