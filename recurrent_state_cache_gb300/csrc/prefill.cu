@@ -297,11 +297,10 @@ int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_
 static bool use_tc(const PoolView &pv, int st) { return st == RSC_BF16 && pv.K == 128; }
 
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T) {
-  size_t b = prefill_prep_bytes(pv, T);
   if (use_tc(pv, st))
-    b += align256((size_t)(N + 1) * 4) +
-         prefill_tc_chunk_capacity(N, T) * (size_t)pv.H * prefill_tc_block_bytes();
-  return b;
+    return align256((size_t)(N + 1) * 4) +
+           prefill_tc_chunk_capacity(N, T) * (size_t)pv.H * prefill_tc_block_bytes();
+  return prefill_prep_bytes(pv, T);
 }
 
 int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_seqlens,
@@ -312,14 +311,10 @@ int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_s
   if (!use_tc(a.pv, a.st))
     return launch_prefill_serial(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta,
                                  out, ws, s);
-  const PrefillWs w = prefill_carve(ws, a.pv, T);
-  char *tail = static_cast<char *>(ws) + prefill_prep_bytes(a.pv, T);
-  int32_t *chunk_base = reinterpret_cast<int32_t *>(tail);
-  char *blocks = tail + align256((size_t)(N + 1) * 4);
-  int rc = launch_prefill_prep(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, w, s);
-  if (rc != RSC_OK) return rc;
-  rc = launch_prefill_tc(a, slots, cu_seqlens, N, T, has_init, w, g, beta, out, chunk_base,
-                         blocks, s);
+  int32_t *chunk_base = static_cast<int32_t *>(ws);
+  char *blocks = static_cast<char *>(ws) + align256((size_t)(N + 1) * 4);
+  int rc = launch_prefill_tc(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta, out,
+                             chunk_base, blocks, s);
   if (rc != RSC_OK) return rc;
   return launch_prefill_window(a, slots, cu_seqlens, N, T, has_init, qkv, s);
 }

@@ -16,22 +16,24 @@
 //   O  = (Q . Gamma) S0^T + P U
 //   S_c = S0 Diag(Gamma_c) + U^T (K . Gamma_c / Gamma)
 //
-// Launches (after the conv/norm prep kernel of prefill.cu):
+// Launches:
 //   chunk table  one warp: chunk_base[n] = chunks before sequence n (64-token chunks).
-//   intra        grid (chunk, head): the parts that do not depend on the state.  The
-//                products A and P are one 128x64x128 MMA ([K.e^(G-R); Q.e^(G-R)] times
-//                (K.e^(R-G))^T, R the per-channel midpoint of G over the chunk, so no
-//                factor exceeds e^(range/2)); W and U' by forward substitution in fp32.
-//                Writes per (chunk, head) a block of bf16 tensor-core operands already
-//                in the canonical shared-memory layout: [W; Q.Gamma] (128xK),
-//                (K.Gamma_c/Gamma)^T (Kx64), P (64x64), U' by 32-column tiles, Gamma_c.
+//   chunk        grid (chunk, head): everything that does not depend on the state, from
+//                the raw projections (conv, L2 norm, gates, the A/P products as one
+//                128x64x128 MMA with a per-channel midpoint reference R of the cumulative
+//                gate so no split factor exceeds e^(range/2), W and U' by blocked forward
+//                substitution).  Writes per (chunk, head) a block of bf16 tensor-core
+//                operands already in the canonical shared-memory layout: [W; Q.Gamma]
+//                (128xK), (K.Gamma_c/Gamma)^T (Kx64), P (64x64), U' by 32-column tiles,
+//                and Gamma_c.
 //   state        grid (32-row tile of S, head, sequence): walks the sequence's chunks in
 //                order with the tile's state in fp32 registers (thread k holds column k)
 //                and per chunk runs MMA1 = [W; Q.Gamma] S0^T (U correction and the
 //                inter-chunk output in one 128x32x128 MMA), then MMA2 = (K.Gamma_c/
 //                Gamma)^T U (state update) and MMA3 = [0; P] U (intra-chunk output).
 //                The next chunk's operand block is fetched by TMA bulk copies into the
-//                other half of a double buffer while the current chunk runs.
+//                other half of a double buffer; a chunk's output is written while the
+//                next chunk's first MMA runs.
 //   window       prefill.cu's window kernel.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
@@ -67,20 +69,17 @@ constexpr uint32_t kOffS = 2 * kBufBytes;            // S0 tile (bf16) as MMA1 o
 constexpr uint32_t kOffU = kOffS + kVT * kK * 2;     // U^T (bf16) as MMA2/3 operand: 32 x 64
 constexpr uint32_t kStateSmem = kOffU + kVT * kC * 2;
 
-// Shared memory of the intra kernel.
-constexpr uint32_t kIntraG = 0;                          // fp32 [64][K]   cumulative gates
-constexpr uint32_t kIntraA = kIntraG + kC * kK * 4;      // fp32 [64][64]  A
-constexpr uint32_t kIntraX = kIntraA + kC * kC * 4;      // bf16 128 x K   [K.e^(G-R); Q.e^(G-R)]
-constexpr uint32_t kIntraKi = kIntraX + 128 * kK * 2;    // bf16 64 x K    K.e^(R-G)
-constexpr uint32_t kIntraWh = kIntraKi + kC * kK * 2;    // fp32 [64][K]   rows of W
-constexpr uint32_t kIntraUh = kIntraWh + kC * kK * 4;    // fp32 [64][128] rows of U'
-constexpr uint32_t kIntraSmem = kIntraUh + kC * 128 * 4;
+// Shared memory of the fused chunk kernel (bytes).  sQ becomes the W history and sV the
+// U' history in place; sX becomes A once the MMA that reads it has completed.
+constexpr uint32_t kChQ = 0;                         // bf16 [64][K]  q_hat   -> W rows
+constexpr uint32_t kChK = kChQ + kC * kK * 2;        // bf16 [64][K]  k_hat
+constexpr uint32_t kChV = kChK + kC * kK * 2;        // bf16 [64][128] beta.v -> U' rows
+constexpr uint32_t kChX = kChV + kC * 128 * 2;       // bf16 128 x K  [K.e^(G-R); Q.e^(G-R)] -> fp32 A [64][64]
+constexpr uint32_t kChKi = kChX + 128 * kK * 2;      // bf16 64 x K   K.e^(R-G)
+constexpr uint32_t kChSmem = kChKi + kC * kK * 2;    // 96 KB: two CTAs per SM
 
 __device__ __forceinline__ void st_bf16(void *p, float x) {
   *reinterpret_cast<bf16 *>(p) = __float2bfloat16_rn(x);
-}
-__device__ __forceinline__ float ld_bf16(const void *p) {
-  return __bfloat162float(*reinterpret_cast<const bf16 *>(p));
 }
 
 // Last n in [0, N) with base[n] <= x.
@@ -128,79 +127,179 @@ __global__ void prefill_chunk_table_kernel(const int32_t *__restrict__ cu, int N
   }
 }
 
-// Intra-chunk work of one (chunk, head).  128 threads; thread `ch` owns key channel ch.
-// The gate g is [T][H][K] (KDA) or [T][H] (GDN, one value for every channel of a head).
-template <int V, int GATE>
-__global__ void __launch_bounds__(128)
-prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
-                        const int32_t *__restrict__ chunk_base, int N, PrefillWs ws,
-                        const float *__restrict__ g, const float *__restrict__ beta,
-                        char *__restrict__ blocks) {
+// Everything of one (chunk, head) that does not depend on the state, from the raw
+// projections: 256 threads.
+//   1. conv + L2 norm, one warp per token (8 tokens per warp), lane l owning channels
+//      4l..4l+3 of the head's q, k and v blocks; the three previous inputs come from the
+//      sequence, or for its first tokens from the slot's window (zeros for a fresh one).
+//      q_hat, k_hat and beta.v land in shared memory as bf16.
+//   2. cumulative gates in registers: thread t owns channel t % 128 for rows
+//      32 (t / 128) .. +31; the per-channel midpoint R of G's range, Gamma_c.
+//   3. operands: [K.e^(G-R); Q.e^(G-R)] and K.e^(R-G) for the A/P MMA (shared memory);
+//      Q.Gamma rows of [W; Q.Gamma] and (K.Gamma_c/Gamma)^T straight to the block;
+//      beta.k.Gamma (the right-hand side of W) over q_hat in place.
+//   4. A and P with one 128x64x128 MMA; A (x beta, strictly lower) to shared memory over
+//      the spent operand, P (lower incl. diagonal) to the block.
+//   5. W = (I+A)^-1 [beta.k.Gamma] and U' = (I+A)^-1 [beta.v] by blocked forward
+//      substitution: thread t owns one column (W for t < 128, U' above); per 16-row block
+//      the earlier blocks' contribution with 16 independent accumulators, then the
+//      triangular 16x16 solve.  Rows of earlier blocks are read back as bf16 (what the
+//      state pass consumes anyway).
+template <typename IO, int V, int GATE>
+__global__ void __launch_bounds__(256, 2)
+prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
+                        const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_base,
+                        int N, const uint8_t *__restrict__ has_init, const IO *__restrict__ qkv,
+                        const float *__restrict__ conv_w, const float *__restrict__ g,
+                        const float *__restrict__ beta, char *__restrict__ blocks) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  float *sG = reinterpret_cast<float *>(smem + kIntraG);
-  float *sA = reinterpret_cast<float *>(smem + kIntraA);
-  unsigned char *sX = smem + kIntraX;
-  unsigned char *sKi = smem + kIntraKi;
-  float *sWh = reinterpret_cast<float *>(smem + kIntraWh);
-  float *sUh = reinterpret_cast<float *>(smem + kIntraUh);
+  bf16 *sQ = reinterpret_cast<bf16 *>(smem + kChQ);
+  bf16 *sK = reinterpret_cast<bf16 *>(smem + kChK);
+  bf16 *sV = reinterpret_cast<bf16 *>(smem + kChV);
+  unsigned char *sX = smem + kChX;
+  unsigned char *sKi = smem + kChKi;
+  float *sA = reinterpret_cast<float *>(smem + kChX);
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_bar;
   __shared__ float s_beta[kC];
+  __shared__ float s_half[kK], s_min[kK], s_max[kK], s_glast[kK];
 
-  const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-  const int H = pv.H;
+  const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int H = pv.H, D = pv.D;
   if (cid >= chunk_base[N]) return;
   const int n = last_le(chunk_base, N, cid);
-  const int t0 = cu[n] + kC * (cid - chunk_base[n]);
+  const int seq0 = cu[n];
+  const int c_in_seq = cid - chunk_base[n];
+  const int t0 = seq0 + kC * c_in_seq;
   const int Lc = min(kC, cu[n + 1] - t0);
+  const int slot = slots[n];
+  if (slot < 0 || slot > pv.P) return;  // flagged by the state pass
+  const bool init = has_init == nullptr || has_init[n] != 0;
   char *blk = blocks + ((size_t)cid * H + h) * kBlockBytes;
-  const int ch = tid;
-
   if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+  __syncthreads();
 
-  // cumulative gates and the per-channel reference point R (midpoint of G's range)
-  float G = 0.f, gmin = 0.f, gmax = 0.f;
-#pragma unroll 8
-  for (int r = 0; r < kC; ++r) {
-    if (r < Lc) {
-      const size_t th = (size_t)(t0 + r) * H + h;
-      G += GATE == RSC_GATE_KDA ? g[th * kK + ch] : g[th];
+  // ---- 1. conv + L2 norm: warp per token, lane l owns channels 4l..4l+3 of q, k, v
+  {
+    const int cq = h * kK + 4 * lane, ck = H * kK + h * kK + 4 * lane;
+    const int cv = 2 * H * kK + h * V + 4 * lane;
+    const bool has_v = 4 * lane < V;
+    float4 wq[4], wk[4], wv[4];  // taps of the lane's 4 channels per block
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wq[e] = reinterpret_cast<const float4 *>(conv_w)[cq + e];
+      wk[e] = reinterpret_cast<const float4 *>(conv_w)[ck + e];
+      wv[e] = has_v ? reinterpret_cast<const float4 *>(conv_w)[cv + e] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    sG[r * kK + ch] = G;
-    if (r == 0) { gmin = G; gmax = G; }
-    else if (r < Lc) { gmin = fminf(gmin, G); gmax = fmaxf(gmax, G); }
+    const IO *W = reinterpret_cast<const IO *>(pv.conv) +
+                  ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
+    auto load4 = [&](int pos, int c, float (&x)[4]) {  // input of sequence position pos
+      if (pos >= 0) {
+        const IO *p = qkv + (size_t)(seq0 + pos) * D + c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = to_f32(p[e]);
+      } else if (init) {
+        const IO *p = W + (size_t)(3 + pos) * D + c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = to_f32(p[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = 0.f;
+      }
+    };
+    for (int r = warp; r < kC; r += 8) {
+      float yq[4] = {0.f, 0.f, 0.f, 0.f}, yk[4] = {0.f, 0.f, 0.f, 0.f}, yv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < Lc) {
+        const int pos = t0 - seq0 + r;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // tap i on position pos - 3 + i
+          float xq[4], xk[4], xv[4];
+          load4(pos - 3 + i, cq, xq);
+          load4(pos - 3 + i, ck, xk);
+          if (has_v) load4(pos - 3 + i, cv, xv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float tq = i == 0 ? wq[e].x : i == 1 ? wq[e].y : i == 2 ? wq[e].z : wq[e].w;
+            const float tk = i == 0 ? wk[e].x : i == 1 ? wk[e].y : i == 2 ? wk[e].z : wk[e].w;
+            const float tv = i == 0 ? wv[e].x : i == 1 ? wv[e].y : i == 2 ? wv[e].z : wv[e].w;
+            yq[e] = fmaf(tq, xq[e], yq[e]);
+            yk[e] = fmaf(tk, xk[e], yk[e]);
+            if (has_v) yv[e] = fmaf(tv, xv[e], yv[e]);
+          }
+        }
+      }
+      float qq = yq[0] * yq[0] + yq[1] * yq[1] + yq[2] * yq[2] + yq[3] * yq[3];
+      float kk = yk[0] * yk[0] + yk[1] * yk[1] + yk[2] * yk[2] + yk[3] * yk[3];
+      qq = group_sum<32>(qq);
+      kk = group_sum<32>(kk);
+      const float rq = 1.0f / sqrtf(qq + kNormEps), rk = 1.0f / sqrtf(kk + kNormEps);
+      const float br = s_beta[r];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sQ[r * kK + 4 * lane + e] = __float2bfloat16_rn(yq[e] * rq);
+        sK[r * kK + 4 * lane + e] = __float2bfloat16_rn(yk[e] * rk);
+        if (has_v) sV[r * 128 + 4 * lane + e] = __float2bfloat16_rn(br * yv[e]);
+      }
+    }
   }
-  if (gmax - gmin > kGateSpreadLimit) flag_error(pv.err, RSC_DEVERR_GATE);
-  const float R = 0.5f * (gmin + gmax);
-  const float Glast = sG[(Lc - 1) * kK + ch];
-  reinterpret_cast<float *>(blk + kOffGC)[ch] = expf(Glast);
-  __syncthreads();  // s_beta
 
-  // operands of A / P (shared memory), the state-independent operands of the state pass
-  // (workspace): Q.Gamma rows of [W; Q.Gamma] and (K.Gamma_c/Gamma)^T, and the right-hand
-  // sides beta_r k_r Gamma_r, beta_r v_r of the forward substitution below (seeded into
-  // the rows it overwrites in place, so that loop touches no global memory)
-#pragma unroll 4
-  for (int r = 0; r < kC; ++r) {
-    float kr = 0.f, qr = 0.f, vr = 0.f;
-    if (r < Lc) {
-      const size_t th = (size_t)(t0 + r) * H + h;
-      kr = ws.k[th * kK + ch];
-      qr = ws.q[th * kK + ch];
-      if (ch < V) vr = ws.v[th * V + ch];
-    }
-    const float Gr = sG[r * kK + ch];
-    sWh[r * kK + ch] = s_beta[r] * kr * expf(Gr);
-    if (ch < V) sUh[r * 128 + ch] = s_beta[r] * vr;
-    const float ep = expf(Gr - R), en = expf(R - Gr);
+  // ---- 2. cumulative gates (registers), reference point, Gamma_c
+  const int ch = tid & (kK - 1), half = tid >> 7, r0 = 32 * half;
+  float G[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = r0 + i;
+    const size_t th = (size_t)(t0 + r) * H + h;
+    G[i] = r < Lc ? (GATE == RSC_GATE_KDA ? g[th * kK + ch] : g[th]) : 0.f;
+  }
+#pragma unroll
+  for (int i = 1; i < 32; ++i) G[i] += G[i - 1];
+  if (half == 0) s_half[ch] = G[31];
+  __syncthreads();
+  if (half == 1) {
+    const float off = s_half[ch];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) G[i] += off;
+  }
+  float gmin = 3.0e38f, gmax = -3.0e38f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (r0 + i < Lc) { gmin = fminf(gmin, G[i]); gmax = fmaxf(gmax, G[i]); }
+  if (half == 1) { s_min[ch] = gmin; s_max[ch] = gmax; }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (r0 + i == Lc - 1) s_glast[ch] = G[i];
+  __syncthreads();
+  if (half == 0) {
+    gmin = fminf(gmin, s_min[ch]);
+    gmax = fmaxf(gmax, s_max[ch]);
+    s_min[ch] = gmin;
+    s_max[ch] = gmax;
+    if (gmax - gmin > kGateSpreadLimit) flag_error(pv.err, RSC_DEVERR_GATE);
+    reinterpret_cast<float *>(blk + kOffGC)[ch] = expf(s_glast[ch]);
+  }
+  __syncthreads();
+  const float R = 0.5f * (s_min[ch] + s_max[ch]);
+  const float Glast = s_glast[ch];
+
+  // ---- 3. operands
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = r0 + i;
+    const float kr = __bfloat162float(sK[r * kK + ch]);
+    const float qr = __bfloat162float(sQ[r * kK + ch]);
+    const float Gr = G[i];
+    const float ep = expf(Gr - R), en = expf(R - Gr), gam = expf(Gr);
     st_bf16(sX + tc::kmajor_offset(r, ch, kK), kr * ep);
     st_bf16(sX + tc::kmajor_offset(kC + r, ch, kK), qr * ep);
     st_bf16(sKi + tc::kmajor_offset(r, ch, kK), kr * en);
-    st_bf16(blk + kOffXW + tc::kmajor_offset(kC + r, ch, kK), qr * expf(Gr));
+    st_bf16(blk + kOffXW + tc::kmajor_offset(kC + r, ch, kK), qr * gam);
     st_bf16(blk + kOffBT + tc::kmajor_offset(ch, r, kC), r < Lc ? kr * expf(Glast - Gr) : 0.f);
+    sQ[r * kK + ch] = __float2bfloat16_rn(s_beta[r] * kr * gam);  // right-hand side of W
   }
 
-  // MMA: [K.e^(G-R); Q.e^(G-R)] (128 x K) times (K.e^(R-G))^T -> 128 x 64 in TMEM
+  // ---- 4. A and P: [K.e^(G-R); Q.e^(G-R)] (128 x K) times (K.e^(R-G))^T -> 128 x 64
   tc::fence_smem_to_async();
   if (tid == 0) mbar_init(&s_bar, 1);
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 64); tc::tmem_relinquish(); }
@@ -218,21 +317,31 @@ prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
   const bool ok = __syncthreads_and(mbar_wait(&s_bar, 0));
   tc::fence_after_sync();
   if (ok) {
-    // lane = row: rows 0..63 hold A' (warps 0, 1), rows 64..127 hold P' (warps 2, 3)
-    const int row = tid;
+    // warp w reads lanes 32 (w % 4) .. +31 (rows) and columns 32 (w / 4) .. +31
+    const int row = 32 * (warp & 3) + lane, cbase = 32 * (warp >> 2);
+    float d[32];
+    {
+      float d0[16], d1[16];
+      tc::tmem_ld16(tc::tmem_addr(taddr, 32 * (warp & 3), cbase), d0);
+      tc::tmem_ld16(tc::tmem_addr(taddr, 32 * (warp & 3), cbase + 16), d1);
 #pragma unroll
-    for (int q4 = 0; q4 < kC / 16; ++q4) {
-      float d[16];
-      tc::tmem_ld16(tc::tmem_addr(taddr, 32 * warp, 16 * q4), d);
+      for (int i = 0; i < 16; ++i) { d[i] = d0[i]; d[16 + i] = d1[i]; }
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // every read of sX by the MMA is over; A may overwrite it
+    if (row < kC) {
+      const float br = s_beta[row];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int j = 16 * q4 + i;
-        if (row < kC) {
-          sA[row * kC + j] = (j < row && row < Lc) ? s_beta[row] * d[i] : 0.f;
-        } else {
-          const int r = row - kC;
-          st_bf16(blk + kOffP + tc::kmajor_offset(r, j, kC), (j <= r && r < Lc) ? d[i] : 0.f);
-        }
+      for (int i = 0; i < 32; ++i) {
+        const int j = cbase + i;
+        sA[row * kC + j] = (j < row && row < Lc) ? br * d[i] : 0.f;
+      }
+    } else {
+      const int r = row - kC;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int j = cbase + i;
+        st_bf16(blk + kOffP + tc::kmajor_offset(r, j, kC), (j <= r && r < Lc) ? d[i] : 0.f);
       }
     }
   } else if (tid == 0) {
@@ -243,38 +352,34 @@ prefill_tc_intra_kernel(PoolView pv, const int32_t *__restrict__ cu,
   if (warp == 0) tc::tmem_dealloc(taddr, 64);
   if (!ok) return;
 
-  // W = (I+A)^-1 Diag(beta) (K.Gamma) and U' = (I+A)^-1 Diag(beta) V by forward
-  // substitution down the rows; thread ch owns column ch of both, so it only ever reads
-  // its own earlier rows (no barrier inside the loop).
-  for (int r = 0; r < kC; ++r) {
-    float w = 0.f, u = 0.f;
-    if (r < Lc) {
-      w = sWh[r * kK + ch];
-      if (ch < V) u = sUh[r * 128 + ch];
-      float w2 = 0.f, u2 = 0.f;  // two accumulators for instruction-level parallelism
-      int j = 0;
-      for (; j + 1 < r; j += 2) {
-        const float a0 = sA[r * kC + j], a1 = sA[r * kC + j + 1];
-        w = fmaf(-a0, sWh[j * kK + ch], w);
-        w2 = fmaf(-a1, sWh[(j + 1) * kK + ch], w2);
-        if (ch < V) {
-          u = fmaf(-a0, sUh[j * 128 + ch], u);
-          u2 = fmaf(-a1, sUh[(j + 1) * 128 + ch], u2);
-        }
-      }
-      if (j < r) {
-        const float a0 = sA[r * kC + j];
-        w = fmaf(-a0, sWh[j * kK + ch], w);
-        if (ch < V) u = fmaf(-a0, sUh[j * 128 + ch], u);
-      }
-      w += w2;
-      u += u2;
+  // ---- 5. blocked forward substitution, one column per thread
+  const bool is_w = tid < kK;
+  const int col = is_w ? tid : tid - kK;
+  if (!is_w && col >= V) return;
+  bf16 *hist = is_w ? sQ : sV;          // rows of W / U' (right-hand side until solved)
+  const int hstride = is_w ? kK : 128;
+#pragma unroll 1
+  for (int I = 0; I < kC / 16; ++I) {
+    float acc[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) acc[r] = __bfloat162float(hist[(16 * I + r) * hstride + col]);
+#pragma unroll 1
+    for (int j = 0; j < 16 * I; ++j) {  // earlier blocks, solved
+      const float xj = __bfloat162float(hist[j * hstride + col]);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) acc[r] = fmaf(-sA[(16 * I + r) * kC + j], xj, acc[r]);
     }
-    sWh[r * kK + ch] = w;
-    st_bf16(blk + kOffXW + tc::kmajor_offset(r, ch, kK), w);
-    if (ch < V) {
-      sUh[r * 128 + ch] = u;
-      st_bf16(blk + kOffUP + ((size_t)((ch / kVT) * kC + r) * kVT + (ch % kVT)) * 2, u);
+#pragma unroll
+    for (int r = 1; r < 16; ++r)  // the block's own triangle
+#pragma unroll
+      for (int j = 0; j < r; ++j) acc[r] = fmaf(-sA[(16 * I + r) * kC + 16 * I + j], acc[j], acc[r]);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int row = 16 * I + r;
+      const float x = row < Lc ? acc[r] : 0.f;
+      hist[row * hstride + col] = __float2bfloat16_rn(x);
+      if (is_w) st_bf16(blk + kOffXW + tc::kmajor_offset(row, col, kK), x);
+      else st_bf16(blk + kOffUP + ((size_t)((col / kVT) * kC + row) * kVT + (col % kVT)) * 2, x);
     }
   }
 }
@@ -341,37 +446,41 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     bulk_g2s(dst + kBufUP, blk + kOffUP + (size_t)vt * kC * kVT * 2, kC * kVT * 2, &s_lbar[b]);
     bulk_g2s(dst + kBufGC, blk + kOffGC, kK * 4, &s_lbar[b]);
   };
-  int issued = 0;  // loads issued (tid 0's count; the loop below consumes them in order)
-  if (tid == 0 && nch > 0) { issue_load(0, 0); }
-  issued = nch > 0 ? 1 : 0;
+  auto issue_mma1 = [&](int b) {  // tid 0: D1 = [W; Q.Gamma] S0^T
+    const unsigned char *buf = smem + b * kBufBytes;
+#pragma unroll
+    for (int ks = 0; ks < kK / 16; ++ks)
+      tc::mma_bf16(tD1, tc::kmajor_desc(buf + kBufXW, kK, ks), tc::kmajor_desc(sS, kK, ks),
+                   tc::idesc_bf16<128, kVT>(), ks > 0);
+    tc::mma_commit(&s_bar1);
+  };
+  auto write_s0 = [&]() {  // S0 (bf16) as MMA1's B operand: element (v, k)
+#pragma unroll
+    for (int v = 0; v < kVT; ++v) st_bf16(sS + tc::kmajor_offset(v, tid, kK), S[v]);
+  };
 
+  // Pipeline of one chunk c (buffer b = c & 1):
+  //   wait MMA1(c) -> U = U' - W S0^T into shared memory (rows 0..63), keep the inter-chunk
+  //   output (rows 64..127) -> MMA2 / MMA3(c), prefetch chunk c+1's operands -> wait ->
+  //   state update, S1 into shared memory -> MMA1(c+1) -> output of chunk c written while
+  //   MMA1(c+1) runs.
+  int issued = 0;  // operand blocks requested (tid 0 issues; every thread keeps the count)
   bool ok = true;
+  if (nch > 0) {
+    if (tid == 0) issue_load(0, 0);
+    issued = 1;
+    write_s0();
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    ok = __syncthreads_and(mbar_wait(&s_lbar[0], 0));
+    tc::fence_after_sync();
+    if (ok && tid == 0) issue_mma1(0);
+  }
   int c = 0;
-  for (; c < nch; ++c) {
+  for (; ok && c < nch; ++c) {
     const int b = c & 1;
     const unsigned char *buf = smem + b * kBufBytes;
     const int t0 = start + kC * c, Lc = min(kC, end - t0);
-    // S0 (bf16) as MMA1's B operand: element (v, k)
-#pragma unroll
-    for (int v = 0; v < kVT; ++v) st_bf16(sS + tc::kmajor_offset(v, tid, kK), S[v]);
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    ok = __syncthreads_and(mbar_wait(&s_lbar[b], (c >> 1) & 1));
-    if (!ok) break;
-    tc::fence_after_sync();
-    // Prefetch chunk c+1 into the other buffer.  Its last readers (chunk c-1's MMAs and
-    // every thread's reads of its U' tile and Gamma_c) are all behind the barrier above.
-    if (c + 1 < nch) {
-      if (tid == 0) issue_load(c + 1, b ^ 1);
-      issued = c + 2;
-    }
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < kK / 16; ++ks)
-        tc::mma_bf16(tD1, tc::kmajor_desc(buf + kBufXW, kK, ks), tc::kmajor_desc(sS, kK, ks),
-                     tc::idesc_bf16<128, kVT>(), ks > 0);
-      tc::mma_commit(&s_bar1);
-    }
     ok = __syncthreads_and(mbar_wait(&s_bar1, c & 1));
     if (!ok) break;
     tc::fence_after_sync();
@@ -386,17 +495,27 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     if (warp < 2) {
       // rows 0..63: U = U' - W S0^T, stored transposed (element (v, r)) for MMA2 / MMA3
       const int r = tid;
-      const unsigned char *up = buf + kBufUP + (size_t)r * kVT * 2;
+      const uint4 *up = reinterpret_cast<const uint4 *>(buf + kBufUP + (size_t)r * kVT * 2);
 #pragma unroll
-      for (int v = 0; v < kVT; ++v) {
-        const float u = r < Lc ? ld_bf16(up + v * 2) - d[v] : 0.f;
-        st_bf16(sU + tc::kmajor_offset(v, r, kC), u);
+      for (int q = 0; q < kVT / 8; ++q) {
+        float u8[8];
+        unpack16(up[q], u8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int v = 8 * q + e;
+          st_bf16(sU + tc::kmajor_offset(v, r, kC), r < Lc ? u8[e] - d[v] : 0.f);
+        }
       }
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    // Every thread is past chunk c-1, so the other buffer is free for chunk c+1.
+    if (c + 1 < nch) {
+      if (tid == 0) issue_load(c + 1, b ^ 1);
+      issued = c + 2;
+    }
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
@@ -411,21 +530,6 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     ok = __syncthreads_and(mbar_wait(&s_bar2, c & 1));
     if (!ok) break;
     tc::fence_after_sync();
-    if (warp >= 2) {
-      // rows 64..127: O = (Q.Gamma) S0^T + P U for token r of the chunk
-      const int r = tid - kC;
-      float d0[16], d1[16];
-      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 0), d0);
-      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 16), d1);
-      if (r < Lc) {
-        IO *o = out + ((size_t)(t0 + r) * H + h) * V + (size_t)vt * kVT;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          o[i] = from_f32<IO>(d[i] + d0[i]);
-          o[16 + i] = from_f32<IO>(d[16 + i] + d1[i]);
-        }
-      }
-    }
     {
       // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] + (K.Gamma_c/Gamma)^T U for this thread's k
       const float gc = reinterpret_cast<const float *>(buf + kBufGC)[tid];
@@ -438,7 +542,38 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
         S[16 + i] = fmaf(gc, S[16 + i], d1[i]);
       }
     }
+    float o[kVT];
+    if (warp >= 2) {
+      float d0[16], d1[16];
+      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 0), d0);
+      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 16), d1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { o[i] = d[i] + d0[i]; o[16 + i] = d[16 + i] + d1[i]; }
+    }
+    if (c + 1 < nch) {
+      write_s0();
+      tc::fence_smem_to_async();
+    }
     tc::fence_before_sync();
+    ok = __syncthreads_and(c + 1 < nch ? mbar_wait(&s_lbar[b ^ 1], ((c + 1) >> 1) & 1) : true);
+    if (!ok) break;
+    tc::fence_after_sync();
+    if (c + 1 < nch && tid == 0) issue_mma1(b ^ 1);
+    if (warp >= 2) {
+      // rows 64..127: O = (Q.Gamma) S0^T + P U of token r, written while MMA1(c+1) runs
+      const int r = tid - kC;
+      if (r < Lc) {
+        IO *op = out + ((size_t)(t0 + r) * H + h) * V + (size_t)vt * kVT;
+        constexpr int EPV = 16 / sizeof(IO);
+#pragma unroll
+        for (int q = 0; q < kVT / EPV; ++q) {
+          float x[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) x[e] = o[EPV * q + e];
+          st16(op + EPV * q, pack16(x));
+        }
+      }
+    }
   }
   if (!ok) {
     if (tid == 0) {
@@ -459,41 +594,44 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 
 template <typename IO, int V, int GATE>
 static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                       const uint8_t *has_init, const PrefillWs &w, const float *g,
-                       const float *beta, void *out, int32_t *chunk_base, char *blocks,
-                       cudaStream_t s) {
+                       const uint8_t *has_init, const void *qkv, const float *conv_w,
+                       const float *g, const float *beta, void *out, int32_t *chunk_base,
+                       char *blocks, cudaStream_t s) {
+  auto chunk_kernel = prefill_tc_chunk_kernel<IO, V, GATE>;
+  auto state_kernel = prefill_tc_state_kernel<IO, V>;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(prefill_tc_intra_kernel<V, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kIntraSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(prefill_tc_state_kernel<IO, V>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kChSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStateSmem) != cudaSuccess)
       return RSC_ECUDA;
     attr = true;
   }
   const unsigned cap = (unsigned)prefill_tc_chunk_capacity(N, T);
   if (cap > 0 && T > 0) {
-    prefill_tc_intra_kernel<V, GATE><<<dim3(cap, a.pv.H), 128, kIntraSmem, s>>>(a.pv, cu, chunk_base, N, w, g,
-                                                                          beta, blocks);
+    chunk_kernel<<<dim3(cap, a.pv.H), 256, kChSmem, s>>>(a.pv, a.layer, slots, cu, chunk_base, N,
+                                                          has_init, static_cast<const IO *>(qkv),
+                                                          conv_w, g, beta, blocks);
     if (launch_status() != RSC_OK) return RSC_ECUDA;
   }
-  prefill_tc_state_kernel<IO, V><<<dim3(V / kVT, a.pv.H, N), 128, kStateSmem, s>>>(
+  state_kernel<<<dim3(V / kVT, a.pv.H, N), 128, kStateSmem, s>>>(
       a.pv, a.layer, slots, cu, chunk_base, T, has_init, blocks, static_cast<IO *>(out));
   return launch_status();
 }
 
 int launch_prefill_tc(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                      const uint8_t *has_init, const PrefillWs &w, const float *g,
-                      const float *beta, void *out, int32_t *chunk_base, char *blocks,
-                      cudaStream_t s) {
+                      const uint8_t *has_init, const void *qkv, const float *conv_w,
+                      const float *g, const float *beta, void *out, int32_t *chunk_base,
+                      char *blocks, cudaStream_t s) {
   prefill_chunk_table_kernel<<<1, 32, 0, s>>>(cu, N, T, chunk_base, a.pv.err);
   if (launch_status() != RSC_OK) return RSC_ECUDA;
   const bool kda = a.gate == RSC_GATE_KDA;
 #define RSC_TC(IO_, V_)                                                                        \
-  (kda ? launch_tc_v<IO_, V_, RSC_GATE_KDA>(a, slots, cu, N, T, has_init, w, g, beta, out,      \
-                                            chunk_base, blocks, s)                             \
-       : launch_tc_v<IO_, V_, RSC_GATE_GDN>(a, slots, cu, N, T, has_init, w, g, beta, out,      \
-                                            chunk_base, blocks, s))
+  (kda ? launch_tc_v<IO_, V_, RSC_GATE_KDA>(a, slots, cu, N, T, has_init, qkv, conv_w, g, beta, \
+                                            out, chunk_base, blocks, s)                        \
+       : launch_tc_v<IO_, V_, RSC_GATE_GDN>(a, slots, cu, N, T, has_init, qkv, conv_w, g, beta, \
+                                            out, chunk_base, blocks, s))
   if (a.io == RSC_BF16) return a.pv.V == 128 ? RSC_TC(bf16, 128) : RSC_TC(bf16, 64);
   return a.pv.V == 128 ? RSC_TC(float, 128) : RSC_TC(float, 64);
 #undef RSC_TC

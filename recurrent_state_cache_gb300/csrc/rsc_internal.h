@@ -51,9 +51,9 @@ int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_
 size_t prefill_tc_chunk_capacity(int N, int T);
 size_t prefill_tc_block_bytes();
 int launch_prefill_tc(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                      const uint8_t *has_init, const PrefillWs &w, const float *g,
-                      const float *beta, void *out, int32_t *chunk_base, char *blocks,
-                      cudaStream_t s);
+                      const uint8_t *has_init, const void *qkv, const float *conv_w,
+                      const float *g, const float *beta, void *out, int32_t *chunk_base,
+                      char *blocks, cudaStream_t s);
 
 int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_seqlens,
                    int N, int T, const uint8_t *has_init, const void *qkv,
