@@ -65,8 +65,8 @@ constexpr uint32_t kBufP0 = kBufBT + kK * kC * 2;    // 49152: [64 zero rows | P
 constexpr uint32_t kBufUP = kBufP0 + 128 * kC * 2;   // 65536: U' tile 64 x 32
 constexpr uint32_t kBufGC = kBufUP + kC * kVT * 2;   // 69632
 constexpr uint32_t kBufBytes = ((kBufGC + kK * 4) + 1023) / 1024 * 1024;
-constexpr uint32_t kOffS = 2 * kBufBytes;            // S0 tile (bf16) as MMA1 operand: 32 x K
-constexpr uint32_t kOffU = kOffS + kVT * kK * 2;     // U^T (bf16) as MMA2/3 operand: 32 x 64
+constexpr uint32_t kOffS = 2 * kBufBytes;            // S0 tile (bf16), MMA1's B: 32 x K, MN-major
+constexpr uint32_t kOffU = kOffS + kVT * kK * 2;     // U (bf16), MMA2/3's B: 32 x 64, MN-major
 constexpr uint32_t kStateSmem = kOffU + kVT * kC * 2;
 
 // Shared memory of the fused chunk kernel (bytes).  sQ becomes the W history and sV the
@@ -74,9 +74,15 @@ constexpr uint32_t kStateSmem = kOffU + kVT * kC * 2;
 constexpr uint32_t kChQ = 0;                         // bf16 [64][K]  q_hat   -> W rows
 constexpr uint32_t kChK = kChQ + kC * kK * 2;        // bf16 [64][K]  k_hat
 constexpr uint32_t kChV = kChK + kC * kK * 2;        // bf16 [64][128] beta.v -> U' rows
-constexpr uint32_t kChX = kChV + kC * 128 * 2;       // bf16 128 x K  [K.e^(G-R); Q.e^(G-R)] -> fp32 A [64][64]
+constexpr uint32_t kChX = kChV + kC * 128 * 2;       // bf16 128 x K  [K.e^(G-R); Q.e^(G-R)] -> fp32 A^T [64][64]
 constexpr uint32_t kChKi = kChX + 128 * kK * 2;      // bf16 64 x K   K.e^(R-G)
-constexpr uint32_t kChSmem = kChKi + kC * kK * 2;    // 96 KB: two CTAs per SM
+// Before the operands exist, the same region stages the chunk's raw bf16 inputs: rows of
+// sequence positions t0-3 .. t0+63, channels [q (K) | k (K) | v (V)] of the head.
+constexpr int kStageRows = kC + 3;
+constexpr uint32_t kChStage = kChX;
+constexpr uint32_t kChStageBytes = kStageRows * (2 * kK + 128) * 2;
+constexpr uint32_t kChSmem = kChX + (kChStageBytes > 128 * kK * 2 + kC * kK * 2
+                                         ? kChStageBytes : 128 * kK * 2 + kC * kK * 2);  // ~100 KB: two CTAs per SM
 
 __device__ __forceinline__ void st_bf16(void *p, float x) {
   *reinterpret_cast<bf16 *>(p) = __float2bfloat16_rn(x);
@@ -180,8 +186,87 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
   __syncthreads();
 
-  // ---- 1. conv + L2 norm: warp per token, lane l owns channels 4l..4l+3 of q, k, v
-  {
+  // the gates of this thread's rows, requested now so their latency hides behind the conv
+  const int ch = tid & (kK - 1), half = tid >> 7, r0 = 32 * half;
+  float G[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = r0 + i;
+    const size_t th = (size_t)(t0 + r) * H + h;
+    G[i] = r < Lc ? (GATE == RSC_GATE_KDA ? g[th * kK + ch] : g[th]) : 0.f;
+  }
+
+  // ---- 1. conv + L2 norm
+  if constexpr (sizeof(IO) == 2) {
+    // bf16 inputs: the chunk's rows (3 before it, from the sequence or the slot's window,
+    // or zero for a fresh sequence) staged with cp.async, then a sliding window per
+    // channel and a warp-per-token norm pass.
+    constexpr int CH = 2 * kK + V;  // staged channels
+    bf16 *stg = reinterpret_cast<bf16 *>(smem + kChStage);
+    const IO *Wn = reinterpret_cast<const IO *>(pv.conv) +
+                   ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
+    const int p0 = t0 - seq0 - 3;   // sequence position of staged row 0
+    for (int i = tid; i < kStageRows * (CH / 8); i += 256) {
+      const int row = i / (CH / 8), c8 = (i % (CH / 8)) * 8;
+      const int pos = p0 + row;
+      const int src_c = c8 < kK ? h * kK + c8 : c8 < 2 * kK ? H * kK + h * kK + (c8 - kK)
+                                                            : 2 * H * kK + h * V + (c8 - 2 * kK);
+      bf16 *dst = stg + row * CH + c8;
+      if (row - 3 >= Lc) {
+        st16(dst, make_uint4(0, 0, 0, 0));
+      } else if (pos >= 0) {
+        cp_async16(dst, qkv + (size_t)(seq0 + pos) * D + src_c);
+      } else if (init) {
+        cp_async16(dst, Wn + (size_t)(3 + pos) * D + src_c);
+      } else {
+        st16(dst, make_uint4(0, 0, 0, 0));
+      }
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int c = tid; c < CH; c += 256) {
+      const int gc = c < kK ? h * kK + c : c < 2 * kK ? H * kK + h * kK + (c - kK)
+                                                     : 2 * H * kK + h * V + (c - 2 * kK);
+      const float4 w = reinterpret_cast<const float4 *>(conv_w)[gc];
+      float x0 = __bfloat162float(stg[c]), x1 = __bfloat162float(stg[CH + c]);
+      float x2 = __bfloat162float(stg[2 * CH + c]);
+      bf16 *dst = c < kK ? sQ + c : c < 2 * kK ? sK + (c - kK) : sV + (c - 2 * kK);
+      const int dstride = c < 2 * kK ? kK : 128;
+#pragma unroll 8
+      for (int r = 0; r < kC; ++r) {
+        const float x3 = __bfloat162float(stg[(r + 3) * CH + c]);
+        dst[r * dstride] = __float2bfloat16_rn(conv4(w, x0, x1, x2, x3));
+        x0 = x1; x1 = x2; x2 = x3;
+      }
+    }
+    __syncthreads();
+    for (int r = warp; r < kC; r += 8) {
+      float q[4], k[4], v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        q[e] = __bfloat162float(sQ[r * kK + 4 * lane + e]);
+        k[e] = __bfloat162float(sK[r * kK + 4 * lane + e]);
+        v[e] = 4 * lane < V ? __bfloat162float(sV[r * 128 + 4 * lane + e]) : 0.f;
+      }
+      float qq = q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3];
+      float kk = k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3];
+      qq = group_sum<32>(qq);
+      kk = group_sum<32>(kk);
+      const bool live = r < Lc;
+      const float rq = live ? 1.0f / sqrtf(qq + kNormEps) : 0.f;
+      const float rk = live ? 1.0f / sqrtf(kk + kNormEps) : 0.f;
+      const float br = s_beta[r];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sQ[r * kK + 4 * lane + e] = __float2bfloat16_rn(q[e] * rq);
+        sK[r * kK + 4 * lane + e] = __float2bfloat16_rn(k[e] * rk);
+        if (4 * lane < V) sV[r * 128 + 4 * lane + e] = __float2bfloat16_rn(live ? br * v[e] : 0.f);
+      }
+    }
+  } else {
+    // fp32 inputs: a warp per token straight from global memory (lane l owns channels
+    // 4l..4l+3 of q, k, v).
     const int cq = h * kK + 4 * lane, ck = H * kK + h * kK + 4 * lane;
     const int cv = 2 * H * kK + h * V + 4 * lane;
     const bool has_v = 4 * lane < V;
@@ -245,14 +330,6 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   }
 
   // ---- 2. cumulative gates (registers), reference point, Gamma_c
-  const int ch = tid & (kK - 1), half = tid >> 7, r0 = 32 * half;
-  float G[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int r = r0 + i;
-    const size_t th = (size_t)(t0 + r) * H + h;
-    G[i] = r < Lc ? (GATE == RSC_GATE_KDA ? g[th * kK + ch] : g[th]) : 0.f;
-  }
 #pragma unroll
   for (int i = 1; i < 32; ++i) G[i] += G[i - 1];
   if (half == 0) s_half[ch] = G[31];
@@ -334,7 +411,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int j = cbase + i;
-        sA[row * kC + j] = (j < row && row < Lc) ? br * d[i] : 0.f;
+        sA[j * kC + row] = (j < row && row < Lc) ? br * d[i] : 0.f;  // stored transposed
       }
     } else {
       const int r = row - kC;
@@ -363,16 +440,25 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     float acc[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) acc[r] = __bfloat162float(hist[(16 * I + r) * hstride + col]);
-#pragma unroll 1
-    for (int j = 0; j < 16 * I; ++j) {  // earlier blocks, solved
+#pragma unroll 2
+    for (int j = 0; j < 16 * I; ++j) {  // earlier blocks, solved; A^T row j = 16 coefficients
       const float xj = __bfloat162float(hist[j * hstride + col]);
+      const float4 *aj = reinterpret_cast<const float4 *>(sA + j * kC + 16 * I);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) acc[r] = fmaf(-sA[(16 * I + r) * kC + j], xj, acc[r]);
+      for (int q = 0; q < 4; ++q) {
+        const float4 a4 = aj[q];
+        acc[4 * q] = fmaf(-a4.x, xj, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(-a4.y, xj, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(-a4.z, xj, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(-a4.w, xj, acc[4 * q + 3]);
+      }
     }
 #pragma unroll
-    for (int r = 1; r < 16; ++r)  // the block's own triangle
+    for (int j = 0; j < 15; ++j) {  // the block's own triangle, column by column
+      const float *aj = sA + (16 * I + j) * kC + 16 * I;
 #pragma unroll
-      for (int j = 0; j < r; ++j) acc[r] = fmaf(-sA[(16 * I + r) * kC + 16 * I + j], acc[j], acc[r]);
+      for (int r = j + 1; r < 16; ++r) acc[r] = fmaf(-aj[r], acc[j], acc[r]);
+    }
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int row = 16 * I + r;
@@ -394,7 +480,8 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_lbar[2];
-  __shared__ __align__(8) uint64_t s_bar1, s_bar2;
+  __shared__ __align__(8) uint64_t s_bar1, s_bar2, s_bar3;
+  __shared__ volatile int s_fail;  // a bounded wait ran out somewhere; checked after barriers
   const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = pv.H;
@@ -426,6 +513,8 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     mbar_init(&s_lbar[1], 1);
     mbar_init(&s_bar1, 1);
     mbar_init(&s_bar2, 1);
+    mbar_init(&s_bar3, 1);
+    s_fail = 0;
   }
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 128); tc::tmem_relinquish(); }
   tc::fence_smem_to_async();
@@ -450,20 +539,30 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     const unsigned char *buf = smem + b * kBufBytes;
 #pragma unroll
     for (int ks = 0; ks < kK / 16; ++ks)
-      tc::mma_bf16(tD1, tc::kmajor_desc(buf + kBufXW, kK, ks), tc::kmajor_desc(sS, kK, ks),
-                   tc::idesc_bf16<128, kVT>(), ks > 0);
+      tc::mma_bf16(tD1, tc::kmajor_desc(buf + kBufXW, kK, ks), tc::mnmajor_desc(sS, kVT, ks),
+                   tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
     tc::mma_commit(&s_bar1);
   };
-  auto write_s0 = [&]() {  // S0 (bf16) as MMA1's B operand: element (v, k)
+  auto write_s0 = [&]() {  // S0 (bf16) as MMA1's MN-major B operand: element (v, k = tid)
 #pragma unroll
-    for (int v = 0; v < kVT; ++v) st_bf16(sS + tc::kmajor_offset(v, tid, kK), S[v]);
+    for (int q = 0; q < kVT / 8; ++q) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = S[8 * q + e];
+      st16(sS + tc::mnmajor_offset(8 * q, tid, kVT), pack16(x));
+    }
+  };
+  auto wait = [&](uint64_t *bar, uint32_t phase) {
+    if (!mbar_wait(bar, phase)) s_fail = 1;
   };
 
   // Pipeline of one chunk c (buffer b = c & 1):
   //   wait MMA1(c) -> U = U' - W S0^T into shared memory (rows 0..63), keep the inter-chunk
-  //   output (rows 64..127) -> MMA2 / MMA3(c), prefetch chunk c+1's operands -> wait ->
-  //   state update, S1 into shared memory -> MMA1(c+1) -> output of chunk c written while
-  //   MMA1(c+1) runs.
+  //   output (rows 64..127) -> barrier -> MMA2 (state) and MMA3 (intra-chunk output), each
+  //   with its own commit; prefetch chunk c+1's operands -> state update, S1 into shared
+  //   memory -> barrier -> MMA1(c+1) -> output of chunk c written while MMA1(c+1) runs.
+  //   Waits on mbarriers are per thread and bounded; a failed one sets s_fail, which
+  //   every thread reads after the next barrier, so all leave the loop together.
   int issued = 0;  // operand blocks requested (tid 0 issues; every thread keeps the count)
   bool ok = true;
   if (nch > 0) {
@@ -472,17 +571,19 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     write_s0();
     tc::fence_smem_to_async();
     tc::fence_before_sync();
-    ok = __syncthreads_and(mbar_wait(&s_lbar[0], 0));
+    __syncthreads();
     tc::fence_after_sync();
-    if (ok && tid == 0) issue_mma1(0);
+    if (tid == 0) {
+      wait(&s_lbar[0], 0);
+      if (!s_fail) issue_mma1(0);
+    }
   }
   int c = 0;
-  for (; ok && c < nch; ++c) {
+  for (; c < nch; ++c) {
     const int b = c & 1;
     const unsigned char *buf = smem + b * kBufBytes;
     const int t0 = start + kC * c, Lc = min(kC, end - t0);
-    ok = __syncthreads_and(mbar_wait(&s_bar1, c & 1));
-    if (!ok) break;
+    wait(&s_bar1, c & 1);
     tc::fence_after_sync();
     float d[kVT];
     {
@@ -492,8 +593,9 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 #pragma unroll
       for (int i = 0; i < 16; ++i) { d[i] = d0[i]; d[16 + i] = d1[i]; }
     }
+    wait(&s_lbar[b], (c >> 1) & 1);  // the operand block is visible to this thread
     if (warp < 2) {
-      // rows 0..63: U = U' - W S0^T, stored transposed (element (v, r)) for MMA2 / MMA3
+      // rows 0..63: U = U' - W S0^T as MMA2/3's MN-major B operand: element (v, r = tid)
       const int r = tid;
       const uint4 *up = reinterpret_cast<const uint4 *>(buf + kBufUP + (size_t)r * kVT * 2);
 #pragma unroll
@@ -501,15 +603,14 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
         float u8[8];
         unpack16(up[q], u8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int v = 8 * q + e;
-          st_bf16(sU + tc::kmajor_offset(v, r, kC), r < Lc ? u8[e] - d[v] : 0.f);
-        }
+        for (int e = 0; e < 8; ++e) u8[e] = r < Lc ? u8[e] - d[8 * q + e] : 0.f;
+        st16(sU + tc::mnmajor_offset(8 * q, r, kVT), pack16(u8));
       }
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
+    if (s_fail) { ok = false; break; }
     tc::fence_after_sync();
     // Every thread is past chunk c-1, so the other buffer is free for chunk c+1.
     if (c + 1 < nch) {
@@ -519,16 +620,16 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
-        tc::mma_bf16(tD2, tc::kmajor_desc(buf + kBufBT, kC, ks), tc::kmajor_desc(sU, kC, ks),
-                     tc::idesc_bf16<128, kVT>(), ks > 0);
+        tc::mma_bf16(tD2, tc::kmajor_desc(buf + kBufBT, kC, ks), tc::mnmajor_desc(sU, kVT, ks),
+                     tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
+      tc::mma_commit(&s_bar2);
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
-        tc::mma_bf16(tD3, tc::kmajor_desc(buf + kBufP0, kC, ks), tc::kmajor_desc(sU, kC, ks),
-                     tc::idesc_bf16<128, kVT>(), ks > 0);
-      tc::mma_commit(&s_bar2);
+        tc::mma_bf16(tD3, tc::kmajor_desc(buf + kBufP0, kC, ks), tc::mnmajor_desc(sU, kVT, ks),
+                     tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
+      tc::mma_commit(&s_bar3);
     }
-    ok = __syncthreads_and(mbar_wait(&s_bar2, c & 1));
-    if (!ok) break;
+    wait(&s_bar2, c & 1);
     tc::fence_after_sync();
     {
       // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] + (K.Gamma_c/Gamma)^T U for this thread's k
@@ -542,23 +643,28 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
         S[16 + i] = fmaf(gc, S[16 + i], d1[i]);
       }
     }
+    if (c + 1 < nch) {
+      write_s0();
+      tc::fence_smem_to_async();
+    }
     float o[kVT];
     if (warp >= 2) {
+      wait(&s_bar3, c & 1);
+      tc::fence_after_sync();
       float d0[16], d1[16];
       tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 0), d0);
       tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 16), d1);
 #pragma unroll
       for (int i = 0; i < 16; ++i) { o[i] = d[i] + d0[i]; o[16 + i] = d[16 + i] + d1[i]; }
     }
-    if (c + 1 < nch) {
-      write_s0();
-      tc::fence_smem_to_async();
-    }
     tc::fence_before_sync();
-    ok = __syncthreads_and(c + 1 < nch ? mbar_wait(&s_lbar[b ^ 1], ((c + 1) >> 1) & 1) : true);
-    if (!ok) break;
+    __syncthreads();
+    if (s_fail) { ok = false; break; }
     tc::fence_after_sync();
-    if (c + 1 < nch && tid == 0) issue_mma1(b ^ 1);
+    if (c + 1 < nch && tid == 0) {
+      wait(&s_lbar[b ^ 1], ((c + 1) >> 1) & 1);
+      if (!s_fail) issue_mma1(b ^ 1);  // a failure here surfaces after the next barrier
+    }
     if (warp >= 2) {
       // rows 64..127: O = (Q.Gamma) S0^T + P U of token r, written while MMA1(c+1) runs
       const int r = tid - kC;
@@ -575,6 +681,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       }
     }
   }
+  if (nch > 0 && s_fail) ok = false;
   if (!ok) {
     if (tid == 0) {
       flag_error(pv.err, RSC_DEVERR_TIMEOUT);

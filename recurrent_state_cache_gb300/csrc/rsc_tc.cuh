@@ -34,6 +34,20 @@ __device__ __forceinline__ uint64_t kmajor_desc(const void *base, int KD, int ks
   return smem_desc(static_cast<const char *>(base) + ks * 256, 128, (uint32_t)KD * 16);
 }
 
+// MN-major no-swizzle operand (used for B): element (n, kd) of an N x KD operand at
+//     ((kd/8) * (N/8) + n/8) * 128 + (kd%8) * 16 + (n%8) * 2
+// i.e. core matrices of 8 KD-rows of 16 bytes (8 consecutive n); core matrices adjacent
+// along N are 128 bytes apart, along KD N*16 bytes apart.  A thread holding one kd and
+// eight consecutive n writes one 16-byte vector.  Measured on GB300: for this form the
+// leading byte offset is the stride along KD and the stride byte offset the stride
+// along N (the assignment with the two swapped reads outside the operand).
+__device__ __forceinline__ uint32_t mnmajor_offset(int n, int kd, int N) {
+  return (uint32_t)((((kd >> 3) * (N >> 3) + (n >> 3)) << 7) + ((kd & 7) << 4) + ((n & 7) << 1));
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(const void *base, int N, int ks) {
+  return smem_desc(static_cast<const char *>(base) + ks * 2 * N * 16, (uint32_t)N * 16, 128);
+}
+
 // Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major, shape M x N.
 template <int M, int N>
 __host__ __device__ constexpr uint32_t idesc_bf16() {
@@ -41,6 +55,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N");
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with the B operand MN-major (transpose-B bit).
+template <int M, int N>
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn() {
+  return idesc_bf16<M, N>() | (1u << 16);
 }
 
 // ---------------------------------------------------------------- tensor memory
