@@ -479,7 +479,8 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
                         const char *__restrict__ blocks, IO *__restrict__ out) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ uint32_t s_taddr;
-  __shared__ __align__(8) uint64_t s_lbar[2];
+  __shared__ __align__(8) uint64_t s_xbar[2];  // [W; Q.Gamma] of a buffer landed
+  __shared__ __align__(8) uint64_t s_lbar[2];  // the rest of a buffer's block landed
   __shared__ __align__(8) uint64_t s_bar1, s_bar2, s_bar3;
   __shared__ volatile int s_fail;  // a bounded wait ran out somewhere; checked after barriers
   const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -509,6 +510,8 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     st16(smem + b * kBufBytes + kBufP0 + o * 16, make_uint4(0, 0, 0, 0));
   }
   if (tid == 0) {
+    mbar_init(&s_xbar[0], 1);
+    mbar_init(&s_xbar[1], 1);
     mbar_init(&s_lbar[0], 1);
     mbar_init(&s_lbar[1], 1);
     mbar_init(&s_bar1, 1);
@@ -525,11 +528,17 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   const uint32_t tD1 = tm, tD2 = tm + 32, tD3 = tm + 64;
   unsigned char *sS = smem + kOffS, *sU = smem + kOffU;
 
+  // [W; Q.Gamma] is all MMA1 needs: it is fetched two chunks ahead, into its buffer's
+  // region as soon as MMA1 of the chunk before has read it; the rest one chunk ahead.
+  auto issue_xw = [&](int c, int b) {
+    const char *blk = blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes;
+    mbar_arrive_expect_tx(&s_xbar[b], 128 * kK * 2);
+    bulk_g2s(smem + b * kBufBytes + kBufXW, blk + kOffXW, 128 * kK * 2, &s_xbar[b]);
+  };
   auto issue_load = [&](int c, int b) {
     const char *blk = blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes;
     unsigned char *dst = smem + b * kBufBytes;
-    mbar_arrive_expect_tx(&s_lbar[b], 128 * kK * 2 + kK * kC * 2 + kC * kC * 2 + kC * kVT * 2 + kK * 4);
-    bulk_g2s(dst + kBufXW, blk + kOffXW, 128 * kK * 2, &s_lbar[b]);
+    mbar_arrive_expect_tx(&s_lbar[b], kK * kC * 2 + kC * kC * 2 + kC * kVT * 2 + kK * 4);
     bulk_g2s(dst + kBufBT, blk + kOffBT, kK * kC * 2, &s_lbar[b]);
     bulk_g2s(dst + kBufP0 + kC * kC * 2, blk + kOffP, kC * kC * 2, &s_lbar[b]);
     bulk_g2s(dst + kBufUP, blk + kOffUP + (size_t)vt * kC * kVT * 2, kC * kVT * 2, &s_lbar[b]);
@@ -563,10 +572,17 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   //   memory -> barrier -> MMA1(c+1) -> output of chunk c written while MMA1(c+1) runs.
   //   Waits on mbarriers are per thread and bounded; a failed one sets s_fail, which
   //   every thread reads after the next barrier, so all leave the loop together.
-  int issued = 0;  // operand blocks requested (tid 0 issues; every thread keeps the count)
+  // counts of requested [W; Q.Gamma] parts and rest parts (tid 0 issues; every thread
+  // keeps the counts, which depend only on the loop position)
+  int issued_x = 0, issued = 0;
   bool ok = true;
   if (nch > 0) {
-    if (tid == 0) issue_load(0, 0);
+    if (tid == 0) {
+      issue_xw(0, 0);
+      if (nch > 1) issue_xw(1, 1);
+      issue_load(0, 0);
+    }
+    issued_x = nch > 1 ? 2 : 1;
     issued = 1;
     write_s0();
     tc::fence_smem_to_async();
@@ -574,7 +590,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) {
-      wait(&s_lbar[0], 0);
+      wait(&s_xbar[0], 0);
       if (!s_fail) issue_mma1(0);
     }
   }
@@ -585,6 +601,11 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     const int t0 = start + kC * c, Lc = min(kC, end - t0);
     wait(&s_bar1, c & 1);
     tc::fence_after_sync();
+    // MMA1(c) has read buffer b's [W; Q.Gamma]: refill it with chunk c+2's
+    if (c + 2 < nch) {
+      if (tid == 0) issue_xw(c + 2, b);
+      issued_x = c + 3;
+    }
     float d[kVT];
     {
       float d0[16], d1[16];
@@ -612,11 +633,6 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     __syncthreads();
     if (s_fail) { ok = false; break; }
     tc::fence_after_sync();
-    // Every thread is past chunk c-1, so the other buffer is free for chunk c+1.
-    if (c + 1 < nch) {
-      if (tid == 0) issue_load(c + 1, b ^ 1);
-      issued = c + 2;
-    }
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
@@ -628,6 +644,11 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
         tc::mma_bf16(tD3, tc::kmajor_desc(buf + kBufP0, kC, ks), tc::mnmajor_desc(sU, kVT, ks),
                      tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
       tc::mma_commit(&s_bar3);
+    }
+    // Every thread is past chunk c-1, so the rest of the other buffer is free for c+1.
+    if (c + 1 < nch) {
+      if (tid == 0) issue_load(c + 1, b ^ 1);
+      issued = c + 2;
     }
     wait(&s_bar2, c & 1);
     tc::fence_after_sync();
@@ -662,7 +683,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     if (s_fail) { ok = false; break; }
     tc::fence_after_sync();
     if (c + 1 < nch && tid == 0) {
-      wait(&s_lbar[b ^ 1], ((c + 1) >> 1) & 1);
+      wait(&s_xbar[b ^ 1], ((c + 1) >> 1) & 1);
       if (!s_fail) issue_mma1(b ^ 1);  // a failure here surfaces after the next barrier
     }
     if (warp >= 2) {
@@ -686,6 +707,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     if (tid == 0) {
       flag_error(pv.err, RSC_DEVERR_TIMEOUT);
       // let every issued bulk copy land before the shared memory is released
+      for (int k = c; k < issued_x; ++k) mbar_wait(&s_xbar[k & 1], (k >> 1) & 1);
       for (int k = c; k < issued; ++k) mbar_wait(&s_lbar[k & 1], (k >> 1) & 1);
     }
   } else {
