@@ -12,13 +12,13 @@
 
 namespace rsc {
 
-template <typename ST, int K, int VT, int NW = 4>
+template <typename ST, int K, int VT, int NW = 4, int VPL = 1>
 struct TileGeom {
-  static constexpr int EPL = VecTraits<ST>::N;  // elements per 16-byte vector
-  static constexpr int LPR = K / EPL;           // lanes per row
-  static constexpr int RPW = 32 / LPR;          // rows per warp per pass
-  static constexpr int RPP = NW * RPW;          // rows per CTA per pass
-  static constexpr int NP = VT / RPP;           // passes
+  static constexpr int EPL = VPL * VecTraits<ST>::N;  // elements per lane (VPL 16-byte vectors)
+  static constexpr int LPR = K / EPL;                 // lanes per row
+  static constexpr int RPW = 32 / LPR;                // rows per warp per pass
+  static constexpr int RPP = NW * RPW;                // rows per CTA per pass
+  static constexpr int NP = VT / RPP;                 // passes
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must fit a warp");
   static_assert(NP >= 1 && NP * RPP == VT, "tile rows must be whole passes");
   __device__ static __forceinline__ int row(int p) {
@@ -27,20 +27,36 @@ struct TileGeom {
   __device__ static __forceinline__ int kofs() { return ((threadIdx.x & 31) % LPR) * EPL; }
 };
 
-// Load / store this thread's part of the tile (rows base[row(p)*K + kofs()]).
-template <typename ST, int K, int VT>
-__device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL]) {
-  using G = TileGeom<ST, K, VT>;
+// Load / store this thread's part of the tile (rows base[row(p)*K + kofs()]): VPL
+// consecutive 16-byte vectors per lane and pass.
+template <typename ST, int K, int VT, int VPL = 1>
+__device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL]) {
+  using G = TileGeom<ST, K, VT, 4, VPL>;
+  constexpr int N16 = VecTraits<ST>::N;
 #pragma unroll
   for (int p = 0; p < G::NP; ++p)
-    unpack16(ld16_stream(base + (size_t)G::row(p) * K + G::kofs()), s[p]);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float x[N16];
+      unpack16(ld16_stream(base + (size_t)G::row(p) * K + G::kofs() + v * N16), x);
+#pragma unroll
+      for (int e = 0; e < N16; ++e) s[p][v * N16 + e] = x[e];
+    }
 }
 
-template <typename ST, int K, int VT>
-__device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL]) {
-  using G = TileGeom<ST, K, VT>;
+template <typename ST, int K, int VT, int VPL = 1>
+__device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL]) {
+  using G = TileGeom<ST, K, VT, 4, VPL>;
+  constexpr int N16 = VecTraits<ST>::N;
 #pragma unroll
-  for (int p = 0; p < G::NP; ++p) st16(base + (size_t)G::row(p) * K + G::kofs(), pack16(s[p]));
+  for (int p = 0; p < G::NP; ++p)
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float x[N16];
+#pragma unroll
+      for (int e = 0; e < N16; ++e) x[e] = s[p][v * N16 + e];
+      st16(base + (size_t)G::row(p) * K + G::kofs() + v * N16, pack16(x));
+    }
 }
 
 // One token of the gated delta rule on one row segment held by this lane (EPL elements
@@ -72,13 +88,14 @@ __device__ __forceinline__ float delta_rule_row(float (&s)[EPL], const float (&q
 }
 
 // The same for every row of a register-held tile (rows G::row(p), p < NP).
-template <typename ST, int K, int VT>
+template <typename ST, int K, int VT, int VPL = 1>
 __device__ __forceinline__ void delta_rule_tile(
-    float (&s)[TileGeom<ST, K, VT>::NP][TileGeom<ST, K, VT>::EPL],
-    const float (&qh)[TileGeom<ST, K, VT>::EPL], const float (&kh)[TileGeom<ST, K, VT>::EPL],
-    const float (&al)[TileGeom<ST, K, VT>::EPL], float beta, float kq, const float *v_rows,
-    float (&o)[TileGeom<ST, K, VT>::NP]) {
-  using G = TileGeom<ST, K, VT>;
+    float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL],
+    const float (&qh)[TileGeom<ST, K, VT, 4, VPL>::EPL],
+    const float (&kh)[TileGeom<ST, K, VT, 4, VPL>::EPL],
+    const float (&al)[TileGeom<ST, K, VT, 4, VPL>::EPL], float beta, float kq,
+    const float *v_rows, float (&o)[TileGeom<ST, K, VT, 4, VPL>::NP]) {
+  using G = TileGeom<ST, K, VT, 4, VPL>;
 #pragma unroll
   for (int p = 0; p < G::NP; ++p)
     o[p] = delta_rule_row<G::EPL, G::LPR>(s[p], qh, kh, al, beta, kq, v_rows[G::row(p)]);

@@ -6,10 +6,11 @@
 // per-step cache and the commit scatters the snapshot of the last accepted step into
 // the persistent state; the intermediate SSM cache does the same for S.
 //
-// VERIFY runs the decode body T times with the state tile held in registers (fp32)
-// across tokens; the slot is only read.  The per-token inputs (q/k channels of the head,
-// the tile's value channels, gate, beta) are staged into shared memory eight tokens at a
-// time with cp.async, one block ahead, so the token loop never waits on HBM.  Each CTA keeps its own copy
+// VERIFY runs the delta rule T times with the state tile held in registers (fp32) across
+// tokens; the slot is only read.  The per-token inputs (q/k channels of the head, the
+// tile's value channels, gate, beta) are staged into shared memory eight tokens at a
+// time with cp.async, one block ahead; conv, L2 norms and exp(g) of a whole block are
+// computed before its token loop, so that loop has no barrier and never waits on HBM.  Each CTA keeps its own copy
 // of the head's q/k windows plus its value rows' windows in registers and rolls them
 // token by token, so no CTA ever writes memory another one reads: no cluster needed.
 // Each window channel of a cache entry is written by exactly one CTA (q/k channels
@@ -28,7 +29,10 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
                        const float *__restrict__ g, const float *__restrict__ beta,
                        IO *__restrict__ out) {
   constexpr int VT = V / NVT;
-  using G = TileGeom<ST, K, VT>;
+  // one 16-byte vector per lane and pass (two were measured slower: 109 vs 66 us at the
+  // speculative workload)
+  constexpr int VPL = 1;
+  using G = TileGeom<ST, K, VT, 4, VPL>;
   constexpr int QK_T = 2 * K / 128;
   constexpr int OWN = 2 * K / NVT;
   constexpr int TS = 8;                       // tokens per staged block
@@ -42,12 +46,15 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   __shared__ __align__(16) IO s_xv[2][TS][VT];
   __shared__ __align__(16) float s_g[2][TS][GW];
   __shared__ float s_b[2][TS];
-  __shared__ float s_qk[2 * K];
-  __shared__ float s_v[VT];
-  __shared__ float s_red[12];
+  // Per-token operands of the current block, computed before its token loop: q_hat then
+  // k_hat (in place of the conv outputs), the value rows, alpha = exp(g), k_hat . q_hat.
+  __shared__ __align__(16) float s_qk[TS][2 * K];
+  __shared__ float s_v[TS][VT];
+  __shared__ __align__(16) float s_al[TS][GW];
+  __shared__ float s_kq[TS];
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = pv.H, D = pv.D;
 
   const int slot = slots[b];
@@ -84,7 +91,7 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
 
   const ST *S = reinterpret_cast<const ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
   float s[G::NP][G::EPL];
-  tile_load<ST, K, VT>(S, s);
+  tile_load<ST, K, VT, VPL>(S, s);
 
   // Window registers (raw io values, row 0 oldest) and taps of this thread's channels.
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
@@ -110,20 +117,20 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   int cur = 0;
   for (int t0 = 0; t0 < T; t0 += TS) {
     cp_async_wait_all();
-    __syncthreads();  // block `cur` landed; every reader of block cur^1 is done
+    __syncthreads();  // block `cur` landed; every reader of block cur^1 and of s_qk is done
     if (t0 + TS < T) stage(cur ^ 1, t0 + TS);
     const int cnt = min(TS, T - t0);
+
+    // conv of the block's tokens: each thread rolls its own channels' windows, writes the
+    // window after every token into the cache entry (channels it owns) and the conv output
     for (int tau = 0; tau < cnt; ++tau) {
-      const int t = t0 + tau;
-      const size_t bt = (size_t)b * T + t;
-      IO *E = spec_conv + ((size_t)b * L + t) * 3 * (size_t)D;
-      if (tau > 0) __syncthreads();  // previous token's readers of s_qk / s_v / s_red done
+      IO *E = spec_conv + ((size_t)b * L + t0 + tau) * 3 * (size_t)D;
 #pragma unroll
       for (int u = 0; u < QK_T; ++u) {
         const int i2 = tid + u * 128;
         const IO xc = s_xqk[cur][tau][i2];
-        s_qk[i2] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
-                         to_f32(xc));
+        s_qk[tau][i2] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
+                              to_f32(xc));
         win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
         if (i2 >= j * OWN && i2 < (j + 1) * OWN) {
           E[cqk[u]] = win[u][0]; E[D + cqk[u]] = win[u][1]; E[2 * D + cqk[u]] = win[u][2];
@@ -131,33 +138,51 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       }
       if (tid < VT) {
         const IO xc = s_xv[cur][tau][tid];
-        s_v[tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
+        s_v[tau][tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
         winv[0] = winv[1]; winv[1] = winv[2]; winv[2] = xc;
         E[cv] = winv[0]; E[D + cv] = winv[1]; E[2 * D + cv] = winv[2];
       }
-      __syncthreads();
-
+    }
+    if (GATE == RSC_GATE_KDA) {
+      for (int i = tid; i < cnt * K; i += 128) s_al[i / K][i % K] = expf(s_g[cur][i / K][i % K]);
+    } else if (tid < cnt) {
+      s_al[tid][0] = expf(s_g[cur][tid][0]);
+    }
+    __syncthreads();
+    // L2 norms, a warp per token: lane l holds channels l, l+32, ... of q and of k
+    for (int tau = warp; tau < cnt; tau += 4) {
       float qq = 0.f, kk = 0.f, qk = 0.f;
-      if (tid < K) {
-        const float a = s_qk[tid], c = s_qk[K + tid];
-        qq = a * a; kk = c * c; qk = a * c;
+#pragma unroll
+      for (int e = 0; e < K / 32; ++e) {
+        const float a = s_qk[tau][lane + 32 * e], c = s_qk[tau][K + lane + 32 * e];
+        qq = fmaf(a, a, qq); kk = fmaf(c, c, kk); qk = fmaf(a, c, qk);
       }
-      block3_sum_128(qq, kk, qk, s_red);
-      const float rq = 1.0f / sqrtf(qq + kNormEps);
-      const float rk = 1.0f / sqrtf(kk + kNormEps);
-      const float kq = qk * rq * rk;
+      qq = group_sum<32>(qq); kk = group_sum<32>(kk); qk = group_sum<32>(qk);
+      const float rq = 1.0f / sqrtf(qq + kNormEps), rk = 1.0f / sqrtf(kk + kNormEps);
+#pragma unroll
+      for (int e = 0; e < K / 32; ++e) {
+        s_qk[tau][lane + 32 * e] *= rq;
+        s_qk[tau][K + lane + 32 * e] *= rk;
+      }
+      if (lane == 0) s_kq[tau] = qk * rq * rk;
+    }
+    __syncthreads();
 
+    // the block's tokens: delta rule on the register tile, no barrier inside
+    for (int tau = 0; tau < cnt; ++tau) {
+      const int t = t0 + tau;
+      const size_t bt = (size_t)b * T + t;
       float qh[G::EPL], kh[G::EPL], al[G::EPL];
 #pragma unroll
       for (int e = 0; e < G::EPL; ++e) {
-        qh[e] = s_qk[k0 + e] * rq;
-        kh[e] = s_qk[K + k0 + e] * rk;
-        al[e] = expf(GATE == RSC_GATE_KDA ? s_g[cur][tau][k0 + e] : s_g[cur][tau][0]);
+        qh[e] = s_qk[tau][k0 + e];
+        kh[e] = s_qk[tau][K + k0 + e];
+        al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
       }
       float o[G::NP];
-      delta_rule_tile<ST, K, VT>(s, qh, kh, al, s_b[cur][tau], kq, s_v, o);
+      delta_rule_tile<ST, K, VT, VPL>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
       ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
-      tile_store<ST, K, VT>(Se, s);
+      tile_store<ST, K, VT, VPL>(Se, s);
       if (k0 == 0) {
         IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
 #pragma unroll
