@@ -29,9 +29,9 @@ struct TileGeom {
 
 // Load / store this thread's part of the tile (rows base[row(p)*K + kofs()]): VPL
 // consecutive 16-byte vectors per lane and pass.
-template <typename ST, int K, int VT, int VPL = 1>
-__device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL]) {
-  using G = TileGeom<ST, K, VT, 4, VPL>;
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
+__device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL]) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
   constexpr int N16 = VecTraits<ST>::N;
 #pragma unroll
   for (int p = 0; p < G::NP; ++p)
@@ -44,9 +44,9 @@ __device__ __forceinline__ void tile_load(const ST *base, float (&s)[TileGeom<ST
     }
 }
 
-template <typename ST, int K, int VT, int VPL = 1>
-__device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL]) {
-  using G = TileGeom<ST, K, VT, 4, VPL>;
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
+__device__ __forceinline__ void tile_store(ST *base, const float (&s)[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL]) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
   constexpr int N16 = VecTraits<ST>::N;
 #pragma unroll
   for (int p = 0; p < G::NP; ++p)
@@ -88,14 +88,14 @@ __device__ __forceinline__ float delta_rule_row(float (&s)[EPL], const float (&q
 }
 
 // The same for every row of a register-held tile (rows G::row(p), p < NP).
-template <typename ST, int K, int VT, int VPL = 1>
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
 __device__ __forceinline__ void delta_rule_tile(
-    float (&s)[TileGeom<ST, K, VT, 4, VPL>::NP][TileGeom<ST, K, VT, 4, VPL>::EPL],
-    const float (&qh)[TileGeom<ST, K, VT, 4, VPL>::EPL],
-    const float (&kh)[TileGeom<ST, K, VT, 4, VPL>::EPL],
-    const float (&al)[TileGeom<ST, K, VT, 4, VPL>::EPL], float beta, float kq,
-    const float *v_rows, float (&o)[TileGeom<ST, K, VT, 4, VPL>::NP]) {
-  using G = TileGeom<ST, K, VT, 4, VPL>;
+    float (&s)[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL],
+    const float (&qh)[TileGeom<ST, K, VT, NW, VPL>::EPL],
+    const float (&kh)[TileGeom<ST, K, VT, NW, VPL>::EPL],
+    const float (&al)[TileGeom<ST, K, VT, NW, VPL>::EPL], float beta, float kq,
+    const float *v_rows, float (&o)[TileGeom<ST, K, VT, NW, VPL>::NP]) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
 #pragma unroll
   for (int p = 0; p < G::NP; ++p)
     o[p] = delta_rule_row<G::EPL, G::LPR>(s[p], qh, kh, al, beta, kq, v_rows[G::row(p)]);

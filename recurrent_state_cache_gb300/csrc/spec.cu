@@ -21,8 +21,8 @@
 
 namespace rsc {
 
-template <typename ST, typename IO, int K, int V, int NVT, int GATE>
-__global__ void __launch_bounds__(128)
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
+__global__ void __launch_bounds__(NW * 32)
 kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
                        int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
                        const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -32,13 +32,15 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   // one 16-byte vector per lane and pass (two were measured slower: 109 vs 66 us at the
   // speculative workload)
   constexpr int VPL = 1;
-  using G = TileGeom<ST, K, VT, 4, VPL>;
-  constexpr int QK_T = 2 * K / 128;
+  constexpr int NT = NW * 32;
+  using G = TileGeom<ST, K, VT, NW, VPL>;
+  constexpr int QK_T = (2 * K + NT - 1) / NT;
   constexpr int OWN = 2 * K / NVT;
   constexpr int TS = 8;                       // tokens per staged block
   constexpr int GW = GATE == RSC_GATE_KDA ? K : 1;
   constexpr int XV = 16 / sizeof(IO);         // io elements per 16-byte copy
   static_assert((2 * K) % XV == 0 && VT % XV == 0, "16-byte staging");
+  static_assert(VT <= NT, "one value row per thread");
 
   // Per-token inputs of TS tokens, double-buffered: this head's q/k channels, this tile's
   // value channels, the gate and beta.  Staged with cp.async one block ahead.
@@ -66,18 +68,18 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
 
   auto stage = [&](int buf, int t0) {
     const int cnt = min(TS, T - t0);
-    for (int i = tid; i < cnt * (2 * K / XV); i += 128) {
+    for (int i = tid; i < cnt * (2 * K / XV); i += NT) {
       const int tau = i / (2 * K / XV), c = (i % (2 * K / XV)) * XV;
       const int src = c < K ? h * K + c : H * K + h * K + (c - K);
       cp_async16(&s_xqk[buf][tau][c], qkv + ((size_t)b * T + t0 + tau) * D + src);
     }
-    for (int i = tid; i < cnt * (VT / XV); i += 128) {
+    for (int i = tid; i < cnt * (VT / XV); i += NT) {
       const int tau = i / (VT / XV), c = (i % (VT / XV)) * XV;
       cp_async16(&s_xv[buf][tau][c],
                  qkv + ((size_t)b * T + t0 + tau) * D + 2 * H * K + h * V + j * VT + c);
     }
     if (GATE == RSC_GATE_KDA) {
-      for (int i = tid; i < cnt * (K / 4); i += 128) {
+      for (int i = tid; i < cnt * (K / 4); i += NT) {
         const int tau = i / (K / 4), c = (i % (K / 4)) * 4;
         cp_async16(&s_g[buf][tau][c], g + (((size_t)b * T + t0 + tau) * H + h) * K + c);
       }
@@ -91,7 +93,7 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
 
   const ST *S = reinterpret_cast<const ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
   float s[G::NP][G::EPL];
-  tile_load<ST, K, VT, VPL>(S, s);
+  tile_load<ST, K, VT, VPL, NW>(S, s);
 
   // Window registers (raw io values, row 0 oldest) and taps of this thread's channels.
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
@@ -100,10 +102,12 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   int cqk[QK_T];
 #pragma unroll
   for (int u = 0; u < QK_T; ++u) {
-    const int i2 = tid + u * 128;
+    const int i2 = tid + u * NT;
     cqk[u] = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
-    wt[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cqk[u]);
-    win[u][0] = W[cqk[u]]; win[u][1] = W[D + cqk[u]]; win[u][2] = W[2 * D + cqk[u]];
+    if (i2 < 2 * K) {
+      wt[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cqk[u]);
+      win[u][0] = W[cqk[u]]; win[u][1] = W[D + cqk[u]]; win[u][2] = W[2 * D + cqk[u]];
+    }
   }
   IO winv[3];
   float4 wtv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -127,7 +131,8 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       IO *E = spec_conv + ((size_t)b * L + t0 + tau) * 3 * (size_t)D;
 #pragma unroll
       for (int u = 0; u < QK_T; ++u) {
-        const int i2 = tid + u * 128;
+        const int i2 = tid + u * NT;
+        if (i2 >= 2 * K) continue;
         const IO xc = s_xqk[cur][tau][i2];
         s_qk[tau][i2] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
                               to_f32(xc));
@@ -144,13 +149,13 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       }
     }
     if (GATE == RSC_GATE_KDA) {
-      for (int i = tid; i < cnt * K; i += 128) s_al[i / K][i % K] = expf(s_g[cur][i / K][i % K]);
+      for (int i = tid; i < cnt * K; i += NT) s_al[i / K][i % K] = expf(s_g[cur][i / K][i % K]);
     } else if (tid < cnt) {
       s_al[tid][0] = expf(s_g[cur][tid][0]);
     }
     __syncthreads();
     // L2 norms, a warp per token: lane l holds channels l, l+32, ... of q and of k
-    for (int tau = warp; tau < cnt; tau += 4) {
+    for (int tau = warp; tau < cnt; tau += NW) {
       float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
       for (int e = 0; e < K / 32; ++e) {
@@ -180,9 +185,9 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
       }
       float o[G::NP];
-      delta_rule_tile<ST, K, VT, VPL>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
+      delta_rule_tile<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
       ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
-      tile_store<ST, K, VT, VPL>(Se, s);
+      tile_store<ST, K, VT, VPL, NW>(Se, s);
       if (k0 == 0) {
         IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
 #pragma unroll
@@ -193,14 +198,23 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   }
 }
 
+// State rows and warps per verify CTA.
+#ifndef RSC_VERIFY_ROWS
+#define RSC_VERIFY_ROWS 64
+#endif
+#ifndef RSC_VERIFY_WARPS
+#define RSC_VERIFY_WARPS 4
+#endif
+
 template <typename ST, typename IO, int K, int V, int GATE>
 struct VerifyLaunch {
   static int run(const LayerArgs *a, const int32_t *slots, int B, int T, int L,
                  void *spec_ssm, void *spec_conv, const void *qkv, const float *conv_w,
                  const float *g, const float *beta, void *out, cudaStream_t s) {
-    constexpr int NVT = V / 32;
+    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
+    constexpr int NW = RSC_VERIFY_WARPS;
     dim3 grid(NVT, a->pv.H, B);
-    kda_spec_verify_kernel<ST, IO, K, V, NVT, GATE><<<grid, 128, 0, s>>>(
+    kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE><<<grid, NW * 32, 0, s>>>(
         a->pv, a->layer, slots, T, L, static_cast<ST *>(spec_ssm),
         static_cast<IO *>(spec_conv), static_cast<const IO *>(qkv), conv_w, g, beta,
         static_cast<IO *>(out));
