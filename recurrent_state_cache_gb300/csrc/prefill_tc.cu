@@ -7,33 +7,36 @@
 // (ReplaySSM section).  The pages give no more than that; the algebra below is derived
 // from the recurrence and is checked against it by the oracle's own chunkwise form.
 //
-// For a chunk of c <= 64 tokens starting from state S0, with per-channel cumulative log
-// gates G_r = sum_{i<=r} g_i, Gamma_r = exp(G_r):
+// For a chunk of c <= 64 tokens starting from state S0 (V x K), with per-channel cumulative
+// log gates G_r = sum_{i<=r} g_i, Gamma_r = exp(G_r) and Gamma_c = Gamma of its last token:
 //   A[r][j]  = beta_r sum_k k_r[k] k_j[k] exp(G_r[k] - G_j[k])   (j < r)
 //   P[r][j]  =        sum_k q_r[k] k_j[k] exp(G_r[k] - G_j[k])   (j <= r)
 //   W  = (I + A)^-1 Diag(beta) (K . Gamma),   U' = (I + A)^-1 Diag(beta) V
 //   U  = U' - W S0^T              (row r of U is the delta d_r of token r)
 //   O  = (Q . Gamma) S0^T + P U
-//   S_c = S0 Diag(Gamma_c) + U^T (K . Gamma_c / Gamma)
+//   S_c = S0 Diag(Gamma_c) + U^T B,           B = K . Gamma_c / Gamma
+// Everything but S0 is known before the state is.  With
+//   Z = B^T W (K x K),   N^T = B^T U' (K x V),   E = Q . Gamma - P W (c x K),   F = P U' (c x V)
+// the two lines that involve the state become
+//   S_c^T = Diag(Gamma_c) S0^T - Z S0^T + N^T,      O = E S0^T + F,
+// so the sequential pass over chunks needs one tensor-core product per chunk.
 //
 // Launches:
 //   chunk table  one warp: chunk_base[n] = chunks before sequence n (64-token chunks).
-//   chunk        grid (chunk, head): everything that does not depend on the state, from
-//                the raw projections (conv, L2 norm, gates, the A/P products as one
-//                128x64x128 MMA with a per-channel midpoint reference R of the cumulative
-//                gate so no split factor exceeds e^(range/2), W and U' by blocked forward
-//                substitution).  Writes per (chunk, head) a block of bf16 tensor-core
-//                operands already in the canonical shared-memory layout: [W; Q.Gamma]
-//                (128xK), (K.Gamma_c/Gamma)^T (Kx64), P (64x64), U' by 32-column tiles,
-//                and Gamma_c.
+//   chunk        grid (chunk, head), 256 threads, two CTAs per SM: everything that does not
+//                depend on the state, from the raw projections.  Conv and L2 norm; the gate
+//                cumsum with a per-channel midpoint reference R (no split factor exceeds
+//                e^(range/2); a range beyond 160 sets an error bit); A and P as one
+//                128x64x128 MMA; (I + A)^-1 by 16x16 blocks in fp32; [W | U'] as one MMA of
+//                (I + A)^-1 Diag(beta) (split into bf16 high and low parts) with [K.Gamma | V];
+//                [Z | N^T] = B^T [W | U'] and [P W | F] = P [W | U'] as two more MMAs.  Writes
+//                per (chunk, head) a block of Z and E in the canonical K-major operand
+//                layout, N^T and F by 32-column tiles, and Gamma_c.
 //   state        grid (32-row tile of S, head, sequence): walks the sequence's chunks in
-//                order with the tile's state in fp32 registers (thread k holds column k)
-//                and per chunk runs MMA1 = [W; Q.Gamma] S0^T (U correction and the
-//                inter-chunk output in one 128x32x128 MMA), then MMA2 = (K.Gamma_c/
-//                Gamma)^T U (state update) and MMA3 = [0; P] U (intra-chunk output).
-//                The next chunk's operand block is fetched by TMA bulk copies into the
-//                other half of a double buffer; a chunk's output is written while the
-//                next chunk's first MMA runs.
+//                order with the tile's state in fp32 registers (thread k holds column k); per
+//                chunk one MMA pair Z S0^T, E S0^T, then the state update and the outputs.
+//                Operand blocks arrive by TMA bulk copies two chunks ahead; a chunk's outputs
+//                are written while the next chunk's MMAs run.
 //   window       prefill.cu's window kernel.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
@@ -43,46 +46,73 @@ namespace rsc {
 
 namespace {
 
-constexpr int kC = 64;     // chunk length
-constexpr int kK = 128;    // key dim of the tensor-core path
-constexpr int kVT = 32;    // state rows per state-pass CTA
+constexpr int kC = 64;      // chunk length
+constexpr int kK = 128;     // key dim of the tensor-core path
+constexpr int kVmax = 128;  // largest value dim
+constexpr int kVT = 32;     // state rows per state-pass CTA
 // Largest per-channel spread of the cumulative log gate inside one chunk for which the
 // split exponentials e^(+-(G - R)) stay far from the fp32 / bf16 range (e^80 ~ 5.5e34).
 constexpr float kGateSpreadLimit = 160.f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Per (chunk, head) operand block in the workspace (bytes).
-constexpr size_t kOffXW = 0;                         // [W; Q.Gamma]   128 x K   canonical, KD = K
-constexpr size_t kOffBT = kOffXW + 128 * kK * 2;     // (K.Gamma_c/Gamma)^T  K x 64  canonical, KD = 64
-constexpr size_t kOffP = kOffBT + kK * kC * 2;       // P  64 x 64  canonical, KD = 64
-constexpr size_t kOffUP = kOffP + kC * kC * 2;       // U' as [V/32][64][32] bf16 (room for V = 128)
-constexpr size_t kOffGC = kOffUP + 128 * kC * 2;     // Gamma_c [K] fp32
-constexpr size_t kBlockBytes = ((kOffGC + kK * 4) + 1023) / 1024 * 1024;
+constexpr size_t kOffZ = 0;                          // Z   128 x K  bf16, K-major (KD = K)
+constexpr size_t kOffE = kOffZ + kK * kK * 2;        // E   64 x K   bf16, K-major (KD = K)
+constexpr size_t kOffN = kOffE + kC * kK * 2;        // N^T as [V/32][K][32] bf16
+constexpr size_t kOffF = kOffN + kK * kVmax * 2;     // F   as [V/32][64][32] bf16
+constexpr size_t kOffGC = kOffF + kC * kVmax * 2;    // Gamma_c [K] fp32
+// S0 of the chunk (bf16, V x K), written by the state pass for the output kernel: the
+// MN-major B operand of E S0^T (n = v, contraction k), N = V.
+constexpr size_t kOffS0 = ((kOffGC + kK * 4) + 1023) / 1024 * 1024;
+constexpr size_t kBlockBytes = kOffS0 + kVmax * kK * 2;
 
-// Shared-memory buffer of the state pass (one per double-buffer half).
-constexpr uint32_t kBufXW = 0;
-constexpr uint32_t kBufBT = kBufXW + 128 * kK * 2;   // 32768
-constexpr uint32_t kBufP0 = kBufBT + kK * kC * 2;    // 49152: [64 zero rows | P] = 128 x 64
-constexpr uint32_t kBufUP = kBufP0 + 128 * kC * 2;   // 65536: U' tile 64 x 32
-constexpr uint32_t kBufGC = kBufUP + kC * kVT * 2;   // 69632
-constexpr uint32_t kBufBytes = ((kBufGC + kK * 4) + 1023) / 1024 * 1024;
-constexpr uint32_t kOffS = 2 * kBufBytes;            // S0 tile (bf16), MMA1's B: 32 x K, MN-major
-constexpr uint32_t kOffU = kOffS + kVT * kK * 2;     // U (bf16), MMA2/3's B: 32 x 64, MN-major
-constexpr uint32_t kStateSmem = kOffU + kVT * kC * 2;
-
-// Shared memory of the fused chunk kernel (bytes).  sQ becomes the W history and sV the
-// U' history in place; sX becomes A once the MMA that reads it has completed.
-constexpr uint32_t kChQ = 0;                         // bf16 [64][K]  q_hat   -> W rows
-constexpr uint32_t kChK = kChQ + kC * kK * 2;        // bf16 [64][K]  k_hat
-constexpr uint32_t kChV = kChK + kC * kK * 2;        // bf16 [64][128] beta.v -> U' rows
-constexpr uint32_t kChX = kChV + kC * 128 * 2;       // bf16 128 x K  [K.e^(G-R); Q.e^(G-R)] -> fp32 A^T [64][64]
-constexpr uint32_t kChKi = kChX + 128 * kK * 2;      // bf16 64 x K   K.e^(R-G)
-// Before the operands exist, the same region stages the chunk's raw bf16 inputs: rows of
-// sequence positions t0-3 .. t0+63, channels [q (K) | k (K) | v (V)] of the head.
+// ---- chunk kernel shared memory (bytes)
+// Phase 1: the chunk's raw rows (positions t0-3 .. t0+63, channels [q | k | v] of the
+// head) and the conv outputs of its 64 tokens (q_hat | k_hat after the norm), rows padded.
 constexpr int kStageRows = kC + 3;
-constexpr uint32_t kChStage = kChX;
-constexpr uint32_t kChStageBytes = kStageRows * (2 * kK + 128) * 2;
-constexpr uint32_t kChSmem = kChX + (kChStageBytes > 128 * kK * 2 + kC * kK * 2
-                                         ? kChStageBytes : 128 * kK * 2 + kC * kK * 2);  // ~100 KB: two CTAs per SM
+constexpr int kRowElems = (2 * kK + kVmax) + 8;           // 392 bf16 = 784 bytes per row
+constexpr uint32_t kChStg = 0;
+constexpr uint32_t kChY = 53248;                           // >= 67 * 784
+// Phase 2: tensor-core operands (overlaying phase 1; the V half of KV is written by the
+// norm pass, once the staged rows are dead).
+constexpr uint32_t kChKV = 0;        // [K.Gamma | V]        MN-major B, N = K + V, KD = 64
+constexpr uint32_t kChX = 32768;     // [K.e^(G-R); Q.e^(G-R)]  K-major 128 x K
+constexpr uint32_t kChKi = 65536;    // K.e^(R-G)              K-major 64 x K
+constexpr uint32_t kChBT = 81920;    // B^T                    K-major K x 64
+constexpr uint32_t kChPP = 98304;    // P                      K-major 64 x 64
+constexpr uint32_t kChSmem = 106496; // two CTAs per SM
+// Phase 3 (over X and Ki once the A/P product has completed).
+constexpr int kAS = 68;                                  // fp32 row stride of A
+constexpr uint32_t kChA = 32768;     // A, then (I + A)^-1 in place, fp32 [64][68]
+constexpr int kSS = 52;                                  // fp32 row stride of the partials
+constexpr uint32_t kChSt = kChA + kC * kAS * 4;          // block-row partial products [16][52]
+constexpr uint32_t kChTH = 54272;    // (I + A)^-1 Diag(beta), high bf16 part, K-major 64 x 64
+constexpr uint32_t kChTL = kChTH + kC * kC * 2;          // low part
+// Phase 4 (over phase 3 once the [W | U'] product has completed).
+constexpr uint32_t kChWU = 32768;    // [W | U']               MN-major B, N = K + V, KD = 64
+constexpr uint32_t kChQG = 0;        // Q.Gamma back from the block, K-major 64 x K (over KV)
+static_assert(kChY >= kStageRows * kRowElems * 2, "staging");
+static_assert(kChY + kC * kRowElems * 2 <= kChSmem, "conv outputs");
+static_assert(kChKV + kC * (kK + kVmax) * 2 <= kChY, "V half of KV beside the conv outputs");
+static_assert(kChSt + 16 * kSS * 4 <= kChTH && kChTL + kC * kC * 2 <= kChBT, "phase 3");
+static_assert(kChWU + kC * (kK + kVmax) * 2 <= kChBT, "phase 4");
+
+// ---- state pass shared memory (bytes): four operand buffers and two S0 buffers
+constexpr uint32_t kSbZ = 0;                          // Z        128 x K K-major
+constexpr uint32_t kSbN = kSbZ + kK * kK * 2;         // N^T tile [K][32]
+constexpr uint32_t kSbGC = kSbN + kK * kVT * 2;       // Gamma_c  [K] fp32
+constexpr uint32_t kSBuf = ((kSbGC + kK * 4) + 1023) / 1024 * 1024;
+constexpr int kNBuf = 4;                              // operands fetched 3 chunks ahead
+constexpr uint32_t kStS = kNBuf * kSBuf;              // S0 (bf16) x 2, MN-major B, N = 32, KD = K
+constexpr uint32_t kSBytes = kVT * kK * 2;
+constexpr uint32_t kStateSmem = kStS + 2 * kSBytes;
+constexpr uint32_t kLoadBytes = kK * kK * 2 + kK * kVT * 2 + kK * 4;
+
+// ---- output kernel shared memory (bytes)
+constexpr uint32_t kOuE = 0;                          // E   64 x K K-major
+constexpr uint32_t kOuS = kOuE + kC * kK * 2;         // S0  MN-major, N = V, KD = K
+constexpr uint32_t kOuF = kOuS + kVmax * kK * 2;      // F   [V/32][64][32]
+constexpr uint32_t kOutSmem = kOuF + kC * kVmax * 2;
 
 __device__ __forceinline__ void st_bf16(void *p, float x) {
   *reinterpret_cast<bf16 *>(p) = __float2bfloat16_rn(x);
@@ -96,6 +126,65 @@ __device__ __forceinline__ int last_le(const int32_t *base, int N, int x) {
     if (base[mid] <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
+  acc.x = fmaf(a, b.x, acc.x); acc.y = fmaf(a, b.y, acc.y);
+  acc.z = fmaf(a, b.z, acc.z); acc.w = fmaf(a, b.w, acc.w);
+}
+
+// Stage I of the blocked inverse: rows 16I .. 16I+15 of T = (I + A)^-1, columns below 16I.
+// sA holds T in its rows < 16I (zeros above the diagonal), T's diagonal 16x16 blocks, and
+// A in rows >= 16I.  The partials A[16I.., 0..16I) T[0..16I, 0..16I) go to sSt, then
+// T[16I.., c] = -T_II (partials).  Writes the T rows into sA and T Diag(beta) as bf16
+// high and low parts.
+template <int I>
+__device__ __forceinline__ void inverse_stage(float *sA, float *sSt, unsigned char *sTH,
+                                              unsigned char *sTL, const float *s_beta, int tid) {
+  constexpr int NQ = 4 * I;  // column quads per row
+  const bool busy = tid < 16 * NQ;
+  const int rr = tid / NQ, c = 4 * (tid % NQ);
+  if (busy) {
+    const float *arow = sA + (16 * I + rr) * kAS;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16 * I; m += 4) {
+      const float4 a = ld4(arow + m);
+      fma4(acc, a.x, ld4(sA + (m + 0) * kAS + c));
+      fma4(acc, a.y, ld4(sA + (m + 1) * kAS + c));
+      fma4(acc, a.z, ld4(sA + (m + 2) * kAS + c));
+      fma4(acc, a.w, ld4(sA + (m + 3) * kAS + c));
+    }
+    st4(sSt + rr * kSS + c, acc);
+  }
+  __syncthreads();
+  if (busy) {
+    const float *trow = sA + (16 * I + rr) * kAS + 16 * I;  // row rr of T_II
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; m += 4) {
+      const float4 a = ld4(trow + m);
+      fma4(acc, a.x, ld4(sSt + (m + 0) * kSS + c));
+      fma4(acc, a.y, ld4(sSt + (m + 1) * kSS + c));
+      fma4(acc, a.z, ld4(sSt + (m + 2) * kSS + c));
+      fma4(acc, a.w, ld4(sSt + (m + 3) * kSS + c));
+    }
+    const float t[4] = {-acc.x, -acc.y, -acc.z, -acc.w};
+    st4(sA + (16 * I + rr) * kAS + c, make_float4(t[0], t[1], t[2], t[3]));
+    float hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = t[e] * s_beta[c + e];
+      hi[e] = __bfloat162float(__float2bfloat16_rn(x));
+      lo[e] = x - hi[e];
+    }
+    const uint32_t off = tc::kmajor_offset(16 * I + rr, c, kC);  // 4 elements, 8 bytes
+    *reinterpret_cast<uint2 *>(sTH + off) = make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]));
+    *reinterpret_cast<uint2 *>(sTL + off) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+  }
+  __syncthreads();
 }
 
 }  // namespace
@@ -133,24 +222,17 @@ __global__ void prefill_chunk_table_kernel(const int32_t *__restrict__ cu, int N
   }
 }
 
-// Everything of one (chunk, head) that does not depend on the state, from the raw
-// projections: 256 threads.
-//   1. conv + L2 norm, one warp per token (8 tokens per warp), lane l owning channels
-//      4l..4l+3 of the head's q, k and v blocks; the three previous inputs come from the
-//      sequence, or for its first tokens from the slot's window (zeros for a fresh one).
-//      q_hat, k_hat and beta.v land in shared memory as bf16.
-//   2. cumulative gates in registers: thread t owns channel t % 128 for rows
-//      32 (t / 128) .. +31; the per-channel midpoint R of G's range, Gamma_c.
-//   3. operands: [K.e^(G-R); Q.e^(G-R)] and K.e^(R-G) for the A/P MMA (shared memory);
-//      Q.Gamma rows of [W; Q.Gamma] and (K.Gamma_c/Gamma)^T straight to the block;
-//      beta.k.Gamma (the right-hand side of W) over q_hat in place.
-//   4. A and P with one 128x64x128 MMA; A (x beta, strictly lower) to shared memory over
-//      the spent operand, P (lower incl. diagonal) to the block.
-//   5. W = (I+A)^-1 [beta.k.Gamma] and U' = (I+A)^-1 [beta.v] by blocked forward
-//      substitution: thread t owns one column (W for t < 128, U' above); per 16-row block
-//      the earlier blocks' contribution with 16 independent accumulators, then the
-//      triangular 16x16 solve.  Rows of earlier blocks are read back as bf16 (what the
-//      state pass consumes anyway).
+// Everything of one (chunk, head) that does not depend on the state: 256 threads.
+//   1. conv + L2 norm: q_hat | k_hat rows (bf16) in shared memory, v straight into the V
+//      half of the [K.Gamma | V] operand.
+//   2. gates, in the layout of step 3 (thread t: channels 8 (t / 16) .. +7, rows
+//      4 (t % 16) .. +3): cumsum by a 16-lane scan, per-channel midpoint R, Gamma_c.
+//   3. operands, 16-byte stores: [K.e^(G-R); Q.e^(G-R)] and K.e^(R-G) for the A/P MMA,
+//      K.Gamma for the W/U' MMA, B^T, and Q.Gamma (parked in the block's E slot).
+//   4. A and P with one 128x64x128 MMA; A (x beta, strictly lower) to fp32, P to bf16.
+//   5. T = (I + A)^-1 by 16x16 blocks; T Diag(beta) as bf16 high + low parts.
+//   6. [W | U'] = T Diag(beta) [K.Gamma | V] (two accumulating MMAs), to shared memory.
+//   7. [Z | N^T] = B^T [W | U'] -> block.   8. [P W | F] = P [W | U'] -> E = Q.Gamma - P W, F.
 template <typename IO, int V, int GATE>
 __global__ void __launch_bounds__(256, 2)
 prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
@@ -158,17 +240,18 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
                         int N, const uint8_t *__restrict__ has_init, const IO *__restrict__ qkv,
                         const float *__restrict__ conv_w, const float *__restrict__ g,
                         const float *__restrict__ beta, char *__restrict__ blocks) {
+  constexpr int NKV = kK + V;     // columns of [K.Gamma | V] and [W | U']
+  constexpr int CH = 2 * kK + V;  // channels of one head
   extern __shared__ __align__(1024) unsigned char smem[];
-  bf16 *sQ = reinterpret_cast<bf16 *>(smem + kChQ);
-  bf16 *sK = reinterpret_cast<bf16 *>(smem + kChK);
-  bf16 *sV = reinterpret_cast<bf16 *>(smem + kChV);
-  unsigned char *sX = smem + kChX;
-  unsigned char *sKi = smem + kChKi;
-  float *sA = reinterpret_cast<float *>(smem + kChX);
+  bf16 *Y = reinterpret_cast<bf16 *>(smem + kChY);
+  unsigned char *sKV = smem + kChKV, *sX = smem + kChX, *sKi = smem + kChKi;
+  unsigned char *sBT = smem + kChBT, *sPP = smem + kChPP, *sWU = smem + kChWU;
+  unsigned char *sTH = smem + kChTH, *sTL = smem + kChTL, *sQG = smem + kChQG;
+  float *sA = reinterpret_cast<float *>(smem + kChA);
+  float *sSt = reinterpret_cast<float *>(smem + kChSt);
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_bar;
   __shared__ float s_beta[kC];
-  __shared__ float s_half[kK], s_min[kK], s_max[kK], s_glast[kK];
 
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -184,34 +267,52 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   const bool init = has_init == nullptr || has_init[n] != 0;
   char *blk = blocks + ((size_t)cid * H + h) * kBlockBytes;
   if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-  __syncthreads();
+  // tensor memory and the MMA barrier, ready long before the first product
+  if (tid == 0) mbar_init(&s_bar, 1);
+  if (warp == 0) { tc::tmem_alloc(&s_taddr, 256); tc::tmem_relinquish(); }
 
-  // the gates of this thread's rows, requested now so their latency hides behind the conv
-  const int ch = tid & (kK - 1), half = tid >> 7, r0 = 32 * half;
-  float G[32];
+  // the gates of this thread's rows and channels, requested now so their latency hides
+  // behind the conv
+  const int kg = tid >> 4, rsub = tid & 15;
+  float G[4][8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int r = r0 + i;
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * rsub + i;
     const size_t th = (size_t)(t0 + r) * H + h;
-    G[i] = r < Lc ? (GATE == RSC_GATE_KDA ? g[th * kK + ch] : g[th]) : 0.f;
+    if (r < Lc) {
+      if constexpr (GATE == RSC_GATE_KDA) {
+        const float4 a = ld4(g + th * kK + 8 * kg), b = ld4(g + th * kK + 8 * kg + 4);
+        G[i][0] = a.x; G[i][1] = a.y; G[i][2] = a.z; G[i][3] = a.w;
+        G[i][4] = b.x; G[i][5] = b.y; G[i][6] = b.z; G[i][7] = b.w;
+      } else {
+        const float x = g[th];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) G[i][e] = x;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) G[i][e] = 0.f;
+    }
   }
 
-  // ---- 1. conv + L2 norm
+  // ---- 1. conv + L2 norm -> Y rows 0..63: q_hat | k_hat; v (zero beyond the chunk) -> KV
+  auto src_channel = [&](int c) {  // channel c of the head -> column of the projections
+    return c < kK ? h * kK + c : c < 2 * kK ? H * kK + h * kK + (c - kK)
+                                           : 2 * H * kK + h * V + (c - 2 * kK);
+  };
   if constexpr (sizeof(IO) == 2) {
     // bf16 inputs: the chunk's rows (3 before it, from the sequence or the slot's window,
     // or zero for a fresh sequence) staged with cp.async, then a sliding window per
-    // channel and a warp-per-token norm pass.
-    constexpr int CH = 2 * kK + V;  // staged channels
-    bf16 *stg = reinterpret_cast<bf16 *>(smem + kChStage);
+    // (channel, half of the rows).
+    bf16 *stg = reinterpret_cast<bf16 *>(smem + kChStg);
     const IO *Wn = reinterpret_cast<const IO *>(pv.conv) +
                    ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
     const int p0 = t0 - seq0 - 3;   // sequence position of staged row 0
     for (int i = tid; i < kStageRows * (CH / 8); i += 256) {
       const int row = i / (CH / 8), c8 = (i % (CH / 8)) * 8;
       const int pos = p0 + row;
-      const int src_c = c8 < kK ? h * kK + c8 : c8 < 2 * kK ? H * kK + h * kK + (c8 - kK)
-                                                            : 2 * H * kK + h * V + (c8 - 2 * kK);
-      bf16 *dst = stg + row * CH + c8;
+      const int src_c = src_channel(c8);
+      bf16 *dst = stg + row * kRowElems + c8;
       if (row - 3 >= Lc) {
         st16(dst, make_uint4(0, 0, 0, 0));
       } else if (pos >= 0) {
@@ -225,43 +326,56 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    for (int c = tid; c < CH; c += 256) {
-      const int gc = c < kK ? h * kK + c : c < 2 * kK ? H * kK + h * kK + (c - kK)
-                                                     : 2 * H * kK + h * V + (c - 2 * kK);
-      const float4 w = reinterpret_cast<const float4 *>(conv_w)[gc];
-      float x0 = __bfloat162float(stg[c]), x1 = __bfloat162float(stg[CH + c]);
-      float x2 = __bfloat162float(stg[2 * CH + c]);
-      bf16 *dst = c < kK ? sQ + c : c < 2 * kK ? sK + (c - kK) : sV + (c - 2 * kK);
-      const int dstride = c < 2 * kK ? kK : 128;
+    for (int it = tid; it < 2 * CH; it += 256) {
+      const int c = it % CH, r0 = (it / CH) * (kC / 2);
+      const float4 w = reinterpret_cast<const float4 *>(conv_w)[src_channel(c)];
+      float x0 = __bfloat162float(stg[r0 * kRowElems + c]);
+      float x1 = __bfloat162float(stg[(r0 + 1) * kRowElems + c]);
+      float x2 = __bfloat162float(stg[(r0 + 2) * kRowElems + c]);
 #pragma unroll 8
-      for (int r = 0; r < kC; ++r) {
-        const float x3 = __bfloat162float(stg[(r + 3) * CH + c]);
-        dst[r * dstride] = __float2bfloat16_rn(conv4(w, x0, x1, x2, x3));
+      for (int r = r0; r < r0 + kC / 2; ++r) {
+        const float x3 = __bfloat162float(stg[(r + 3) * kRowElems + c]);
+        Y[r * kRowElems + c] = __float2bfloat16_rn(conv4(w, x0, x1, x2, x3));
         x0 = x1; x1 = x2; x2 = x3;
       }
     }
-    __syncthreads();
-    for (int r = warp; r < kC; r += 8) {
-      float q[4], k[4], v[4];
+    __syncthreads();  // the staged rows are dead from here
+    // a warp per token, two tokens at a time: lane l owns channels 4l..4l+3
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        q[e] = __bfloat162float(sQ[r * kK + 4 * lane + e]);
-        k[e] = __bfloat162float(sK[r * kK + 4 * lane + e]);
-        v[e] = 4 * lane < V ? __bfloat162float(sV[r * 128 + 4 * lane + e]) : 0.f;
+    for (int r0 = warp; r0 < kC; r0 += 16) {
+      bf16 *yr[2] = {Y + r0 * kRowElems, Y + (r0 + 8) * kRowElems};
+      float q[2][4], k[2][4], qq[2], kk[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint2 qu = *reinterpret_cast<const uint2 *>(yr[u] + 4 * lane);
+        const uint2 ku = *reinterpret_cast<const uint2 *>(yr[u] + kK + 4 * lane);
+        q[u][0] = bf16lo(qu.x); q[u][1] = bf16hi(qu.x); q[u][2] = bf16lo(qu.y); q[u][3] = bf16hi(qu.y);
+        k[u][0] = bf16lo(ku.x); k[u][1] = bf16hi(ku.x); k[u][2] = bf16lo(ku.y); k[u][3] = bf16hi(ku.y);
+        qq[u] = q[u][0] * q[u][0] + q[u][1] * q[u][1] + q[u][2] * q[u][2] + q[u][3] * q[u][3];
+        kk[u] = k[u][0] * k[u][0] + k[u][1] * k[u][1] + k[u][2] * k[u][2] + k[u][3] * k[u][3];
       }
-      float qq = q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3];
-      float kk = k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3];
-      qq = group_sum<32>(qq);
-      kk = group_sum<32>(kk);
-      const bool live = r < Lc;
-      const float rq = live ? 1.0f / sqrtf(qq + kNormEps) : 0.f;
-      const float rk = live ? 1.0f / sqrtf(kk + kNormEps) : 0.f;
-      const float br = s_beta[r];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sQ[r * kK + 4 * lane + e] = __float2bfloat16_rn(q[e] * rq);
-        sK[r * kK + 4 * lane + e] = __float2bfloat16_rn(k[e] * rk);
-        if (4 * lane < V) sV[r * 128 + 4 * lane + e] = __float2bfloat16_rn(live ? br * v[e] : 0.f);
+      for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          qq[u] += __shfl_xor_sync(0xffffffffu, qq[u], o);
+          kk[u] += __shfl_xor_sync(0xffffffffu, kk[u], o);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = r0 + 8 * u;
+        const bool live = r < Lc;
+        const float rq = live ? rsqrtf(qq[u] + kNormEps) : 0.f;
+        const float rk = live ? rsqrtf(kk[u] + kNormEps) : 0.f;
+        *reinterpret_cast<uint2 *>(yr[u] + 4 * lane) =
+            make_uint2(pack_bf16x2(q[u][0] * rq, q[u][1] * rq), pack_bf16x2(q[u][2] * rq, q[u][3] * rq));
+        *reinterpret_cast<uint2 *>(yr[u] + kK + 4 * lane) =
+            make_uint2(pack_bf16x2(k[u][0] * rk, k[u][1] * rk), pack_bf16x2(k[u][2] * rk, k[u][3] * rk));
+        if (4 * lane < V) {
+          const uint2 vu = live ? *reinterpret_cast<const uint2 *>(yr[u] + 2 * kK + 4 * lane) : make_uint2(0, 0);
+          *reinterpret_cast<uint2 *>(sKV + tc::mnmajor_offset(kK + 4 * lane, r, NKV)) = vu;
+        }
       }
     }
   } else {
@@ -314,72 +428,131 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
           }
         }
       }
-      float qq = yq[0] * yq[0] + yq[1] * yq[1] + yq[2] * yq[2] + yq[3] * yq[3];
-      float kk = yk[0] * yk[0] + yk[1] * yk[1] + yk[2] * yk[2] + yk[3] * yk[3];
-      qq = group_sum<32>(qq);
-      kk = group_sum<32>(kk);
-      const float rq = 1.0f / sqrtf(qq + kNormEps), rk = 1.0f / sqrtf(kk + kNormEps);
-      const float br = s_beta[r];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sQ[r * kK + 4 * lane + e] = __float2bfloat16_rn(yq[e] * rq);
-        sK[r * kK + 4 * lane + e] = __float2bfloat16_rn(yk[e] * rk);
-        if (has_v) sV[r * 128 + 4 * lane + e] = __float2bfloat16_rn(br * yv[e]);
-      }
+      const float qq = group_sum<32>(yq[0] * yq[0] + yq[1] * yq[1] + yq[2] * yq[2] + yq[3] * yq[3]);
+      const float kk = group_sum<32>(yk[0] * yk[0] + yk[1] * yk[1] + yk[2] * yk[2] + yk[3] * yk[3]);
+      const bool live = r < Lc;
+      const float rq = live ? 1.0f / sqrtf(qq + kNormEps) : 0.f;
+      const float rk = live ? 1.0f / sqrtf(kk + kNormEps) : 0.f;
+      bf16 *yr = Y + r * kRowElems;
+      *reinterpret_cast<uint2 *>(yr + 4 * lane) =
+          make_uint2(pack_bf16x2(yq[0] * rq, yq[1] * rq), pack_bf16x2(yq[2] * rq, yq[3] * rq));
+      *reinterpret_cast<uint2 *>(yr + kK + 4 * lane) =
+          make_uint2(pack_bf16x2(yk[0] * rk, yk[1] * rk), pack_bf16x2(yk[2] * rk, yk[3] * rk));
+      if (has_v)
+        *reinterpret_cast<uint2 *>(sKV + tc::mnmajor_offset(kK + 4 * lane, r, NKV)) =
+            make_uint2(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]));
     }
   }
 
-  // ---- 2. cumulative gates (registers), reference point, Gamma_c
+  // ---- 2. cumulative gates: this thread's 4 rows by a local prefix, across the 16 lanes
+  // of its half-warp (rows 4 rsub .. 4 rsub + 3) by a scan
 #pragma unroll
-  for (int i = 1; i < 32; ++i) G[i] += G[i - 1];
-  if (half == 0) s_half[ch] = G[31];
-  __syncthreads();
-  if (half == 1) {
-    const float off = s_half[ch];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) G[i] += off;
+  for (int e = 0; e < 8; ++e) {
+    G[1][e] += G[0][e];
+    G[2][e] += G[1][e];
+    G[3][e] += G[2][e];
   }
-  float gmin = 3.0e38f, gmax = -3.0e38f;
+  {
+    float incl[8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (r0 + i < Lc) { gmin = fminf(gmin, G[i]); gmax = fmaxf(gmax, G[i]); }
-  if (half == 1) { s_min[ch] = gmin; s_max[ch] = gmax; }
+    for (int e = 0; e < 8; ++e) incl[e] = G[3][e];
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (r0 + i == Lc - 1) s_glast[ch] = G[i];
-  __syncthreads();
-  if (half == 0) {
-    gmin = fminf(gmin, s_min[ch]);
-    gmax = fmaxf(gmax, s_max[ch]);
-    s_min[ch] = gmin;
-    s_max[ch] = gmax;
-    if (gmax - gmin > kGateSpreadLimit) flag_error(pv.err, RSC_DEVERR_GATE);
-    reinterpret_cast<float *>(blk + kOffGC)[ch] = expf(s_glast[ch]);
+    for (int o = 1; o < 16; o <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float y = __shfl_up_sync(0xffffffffu, incl[e], o, 16);
+        if (rsub >= o) incl[e] += y;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float ex = __shfl_up_sync(0xffffffffu, incl[e], 1, 16);
+      if (rsub == 0) ex = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) G[i][e] += ex;
+    }
   }
-  __syncthreads();
-  const float R = 0.5f * (s_min[ch] + s_max[ch]);
-  const float Glast = s_glast[ch];
+  float R[8], Gl[8];
+  {
+    float mn[8], mx[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      mn[e] = 3.0e38f;
+      mx[e] = -3.0e38f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * rsub + i < Lc) { mn[e] = fminf(mn[e], G[i][e]); mx[e] = fmaxf(mx[e], G[i][e]); }
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], o, 16));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], o, 16));
+      }
+    }
+    const int last = Lc - 1, src = last >> 2, il = last & 3;
+    bool wide = false;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float gv = il == 0 ? G[0][e] : il == 1 ? G[1][e] : il == 2 ? G[2][e] : G[3][e];
+      Gl[e] = __shfl_sync(0xffffffffu, gv, src, 16);
+      R[e] = 0.5f * (mn[e] + mx[e]);
+      wide |= mx[e] - mn[e] > kGateSpreadLimit;
+    }
+    if (rsub == 0) {
+      if (wide) flag_error(pv.err, RSC_DEVERR_GATE);
+      float *gc = reinterpret_cast<float *>(blk + kOffGC) + 8 * kg;
+      st4(gc, make_float4(expf(Gl[0]), expf(Gl[1]), expf(Gl[2]), expf(Gl[3])));
+      st4(gc + 4, make_float4(expf(Gl[4]), expf(Gl[5]), expf(Gl[6]), expf(Gl[7])));
+    }
+  }
 
   // ---- 3. operands
+  __syncthreads();  // the norm pass is complete
+  uint4 qv[4], kv[4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int r = r0 + i;
-    const float kr = __bfloat162float(sK[r * kK + ch]);
-    const float qr = __bfloat162float(sQ[r * kK + ch]);
-    const float Gr = G[i];
-    const float ep = expf(Gr - R), en = expf(R - Gr), gam = expf(Gr);
-    st_bf16(sX + tc::kmajor_offset(r, ch, kK), kr * ep);
-    st_bf16(sX + tc::kmajor_offset(kC + r, ch, kK), qr * ep);
-    st_bf16(sKi + tc::kmajor_offset(r, ch, kK), kr * en);
-    st_bf16(blk + kOffXW + tc::kmajor_offset(kC + r, ch, kK), qr * gam);
-    st_bf16(blk + kOffBT + tc::kmajor_offset(ch, r, kC), r < Lc ? kr * expf(Glast - Gr) : 0.f);
-    sQ[r * kK + ch] = __float2bfloat16_rn(s_beta[r] * kr * gam);  // right-hand side of W
+  for (int i = 0; i < 4; ++i) {
+    const bf16 *yr = Y + (4 * rsub + i) * kRowElems;
+    qv[i] = ld16(yr + 8 * kg);
+    kv[i] = ld16(yr + kK + 8 * kg);
+  }
+  __syncthreads();  // Y is dead; the operands overlay it
+#pragma unroll
+  for (int ip = 0; ip < 4; ip += 2) {  // rows in pairs: B^T takes two rows per 4-byte store
+    float bt[8][2];
+#pragma unroll
+    for (int i = ip; i < ip + 2; ++i) {
+      const int r = 4 * rsub + i;
+      const bool live = r < Lc;
+      float q8[8], k8[8], xk[8], xq[8], ki[8], kgm[8], qgm[8];
+      unpack16(qv[i], q8);
+      unpack16(kv[i], k8);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = (G[i][e] - R[e]) * kLog2e;
+        const float ep = exp2f(d), en = exp2f(-d), gam = exp2f(G[i][e] * kLog2e);
+        xk[e] = k8[e] * ep;
+        xq[e] = q8[e] * ep;
+        ki[e] = k8[e] * en;
+        kgm[e] = k8[e] * gam;
+        qgm[e] = q8[e] * gam;
+        bt[e][i - ip] = live ? k8[e] * exp2f((Gl[e] - G[i][e]) * kLog2e) : 0.f;
+      }
+      st16(sX + tc::kmajor_offset(r, 8 * kg, kK), pack16(xk));
+      st16(sX + tc::kmajor_offset(kC + r, 8 * kg, kK), pack16(xq));
+      st16(sKi + tc::kmajor_offset(r, 8 * kg, kK), pack16(ki));
+      st16(sKV + tc::mnmajor_offset(8 * kg, r, NKV), pack16(kgm));
+      st16(blk + kOffE + tc::kmajor_offset(r, 8 * kg, kK), pack16(qgm));  // Q.Gamma, E later
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<uint32_t *>(sBT + tc::kmajor_offset(8 * kg + e, 4 * rsub + ip, kC)) =
+          pack_bf16x2(bt[e][0], bt[e][1]);
   }
 
   // ---- 4. A and P: [K.e^(G-R); Q.e^(G-R)] (128 x K) times (K.e^(R-G))^T -> 128 x 64
   tc::fence_smem_to_async();
-  if (tid == 0) mbar_init(&s_bar, 1);
-  if (warp == 0) { tc::tmem_alloc(&s_taddr, 64); tc::tmem_relinquish(); }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -391,34 +564,224 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
                    tc::idesc_bf16<128, kC>(), ks > 0);
     tc::mma_commit(&s_bar);
   }
-  const bool ok = __syncthreads_and(mbar_wait(&s_bar, 0));
+  const int q4 = warp & 3, half = warp >> 2;
+  bool ok = __syncthreads_and(mbar_wait(&s_bar, 0));
   tc::fence_after_sync();
   if (ok) {
     // warp w reads lanes 32 (w % 4) .. +31 (rows) and columns 32 (w / 4) .. +31
-    const int row = 32 * (warp & 3) + lane, cbase = 32 * (warp >> 2);
+    const int row = 32 * q4 + lane, cb = 32 * half;
     float d[32];
-    {
-      float d0[16], d1[16];
-      tc::tmem_ld16(tc::tmem_addr(taddr, 32 * (warp & 3), cbase), d0);
-      tc::tmem_ld16(tc::tmem_addr(taddr, 32 * (warp & 3), cbase + 16), d1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { d[i] = d0[i]; d[16 + i] = d1[i]; }
-    }
-    tc::fence_before_sync();
-    __syncthreads();  // every read of sX by the MMA is over; A may overwrite it
-    if (row < kC) {
+    tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, cb), d);
+    if (row < kC) {  // A (x beta, strictly lower) over the spent X operand
       const float br = s_beta[row];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int j = cbase + i;
-        sA[j * kC + row] = (j < row && row < Lc) ? br * d[i] : 0.f;  // stored transposed
+      for (int m = 0; m < 8; ++m) {
+        float a[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = cb + 4 * m + e < row ? br * d[4 * m + e] : 0.f;
+        st4(sA + row * kAS + cb + 4 * m, make_float4(a[0], a[1], a[2], a[3]));
       }
-    } else {
+    } else {         // P (lower incl. diagonal)
       const int r = row - kC;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int j = cbase + i;
-        st_bf16(blk + kOffP + tc::kmajor_offset(r, j, kC), (j <= r && r < Lc) ? d[i] : 0.f);
+      for (int m = 0; m < 4; ++m) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = (cb + 8 * m + e <= r && r < Lc) ? d[8 * m + e] : 0.f;
+        st16(sPP + tc::kmajor_offset(r, cb + 8 * m, kC), pack16(x));
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+
+  // ---- 5. T = (I + A)^-1 by 16x16 blocks.  Diagonal blocks: thread (I, c) < 64 solves
+  // column c of block I by forward substitution; the others zero T Diag(beta) above them.
+  float x[16];
+  if (ok) {
+    if (tid < 64) {
+      const int I = tid >> 4, c = tid & 15;
+      const float *ab = sA + 16 * I * kAS + 16 * I;
+      // right-looking: once x[m] is known, every later row takes its term at once, so
+      // the dependent chain is one FMA per row
+      float acc[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        x[m] = m == c ? 1.f : (m > c ? -acc[m] : 0.f);
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(ab[r * kAS + m], x[m], acc[r]);
+      }
+    } else {
+      // the 6 blocks (I, J > I) x 4 core matrices x 8 rows, in both parts
+      for (int idx = tid - 64; idx < 2 * 6 * 32; idx += 192) {
+        const int mat = idx / 192, rem = idx % 192, b6 = rem / 32, w = rem % 32;
+        const int I = b6 < 3 ? 0 : b6 < 5 ? 1 : 2;
+        const int J = b6 < 3 ? b6 + 1 : b6 < 5 ? b6 - 1 : 3;
+        const uint32_t off = ((2 * I + (w >> 4)) * 8 + 2 * J + ((w >> 3) & 1)) * 128 + (w & 7) * 16;
+        st16((mat ? sTL : sTH) + off, make_uint4(0, 0, 0, 0));
+      }
+    }
+  }
+  __syncthreads();
+  if (ok && tid < 64) {
+    const int I = tid >> 4, c = tid & 15;
+    const float bc = s_beta[16 * I + c];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      sA[(16 * I + r) * kAS + 16 * I + c] = x[r];
+      const float v = x[r] * bc;
+      const float hi = __bfloat162float(__float2bfloat16_rn(v));
+      const uint32_t off = tc::kmajor_offset(16 * I + r, 16 * I + c, kC);
+      st_bf16(sTH + off, hi);
+      st_bf16(sTL + off, v - hi);
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    inverse_stage<1>(sA, sSt, sTH, sTL, s_beta, tid);
+    inverse_stage<2>(sA, sSt, sTH, sTL, s_beta, tid);
+    inverse_stage<3>(sA, sSt, sTH, sTL, s_beta, tid);
+  }
+
+  // ---- 6. [W | U'] = T Diag(beta) [K.Gamma | V]   (M = 64: row r in lane r % 16 of
+  // quadrant r / 16)
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ok && tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(sTH, kC, ks), tc::mnmajor_desc(sKV, NKV, ks),
+                   tc::idesc_bf16_bmn<64, NKV>(), ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(sTL, kC, ks), tc::mnmajor_desc(sKV, NKV, ks),
+                   tc::idesc_bf16_bmn<64, NKV>(), true);
+    tc::mma_commit(&s_bar);
+  }
+  if (ok) ok = __syncthreads_and(mbar_wait(&s_bar, 1));
+  tc::fence_after_sync();
+  if (ok) {
+    const int r = 16 * q4 + lane;      // lanes 0..15 hold rows
+    const int c0 = half ? kK : 0, ncol = half ? V : kK;
+    for (int cc = 0; cc < ncol; cc += 32) {
+      float d[32];
+      tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, c0 + cc), d);
+      if (lane < 16) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a[e] = d[8 * q + e];
+          st16(sWU + tc::mnmajor_offset(c0 + cc + 8 * q, r, NKV), pack16(a));
+        }
+      }
+    }
+  }
+
+  // ---- 7. [Z | N^T] = B^T [W | U']   (M = 128: row k in lane k)
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  // Q.Gamma (parked in the block's E slot by step 3) back into shared memory over the
+  // spent [K.Gamma | V] operand, for step 8
+  if (ok) {
+#pragma unroll
+    for (int i = 0; i < kC * kK * 2 / 16 / 256; ++i) {
+      const int o = (tid + 256 * i) * 16;
+      cp_async16(sQG + o, blk + kOffE + o);
+    }
+    cp_async_commit();
+  }
+  if (ok && tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(sBT, kC, ks), tc::mnmajor_desc(sWU, NKV, ks),
+                   tc::idesc_bf16_bmn<128, NKV>(), ks > 0);
+    tc::mma_commit(&s_bar);
+  }
+  if (ok) ok = __syncthreads_and(mbar_wait(&s_bar, 0));
+  tc::fence_after_sync();
+  if (ok) {
+    const int k = 32 * q4 + lane;
+    if (half == 0) {
+      for (int cc = 0; cc < kK; cc += 32) {
+        float d[32];
+        tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, cc), d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a[e] = d[8 * q + e];
+          st16(blk + kOffZ + tc::kmajor_offset(k, cc + 8 * q, kK), pack16(a));
+        }
+      }
+    } else {
+      for (int cc = 0; cc < V; cc += 32) {
+        float d[32];
+        tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, kK + cc), d);
+        char *p = blk + kOffN + ((size_t)((cc / kVT) * kK + k) * kVT) * 2;  // one 32-column tile row
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a[e] = d[8 * q + e];
+          st16(p + 16 * q, pack16(a));
+        }
+      }
+    }
+  }
+  cp_async_wait_all();  // this thread's part of Q.Gamma; the barrier below publishes it
+
+  // ---- 8. [P W | F] = P [W | U'];  E = Q.Gamma - P W   (M = 64)
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ok && tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(sPP, kC, ks), tc::mnmajor_desc(sWU, NKV, ks),
+                   tc::idesc_bf16_bmn<64, NKV>(), ks > 0);
+    tc::mma_commit(&s_bar);
+  }
+  const int r = 16 * q4 + lane;
+  if (ok) ok = __syncthreads_and(mbar_wait(&s_bar, 1));
+  tc::fence_after_sync();
+  if (ok) {
+    if (half == 0) {
+      for (int cc = 0; cc < kK; cc += 32) {
+        float d[32];
+        tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, cc), d);
+        if (lane < 16) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t off = tc::kmajor_offset(r, cc + 8 * q, kK);
+            float a[8];
+            unpack16(ld16(sQG + off), a);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] -= d[8 * q + e];
+            st16(blk + kOffE + off, pack16(a));
+          }
+        }
+      }
+    } else {
+      for (int cc = 0; cc < V; cc += 32) {
+        float d[32];
+        tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, kK + cc), d);
+        if (lane < 16) {
+          char *p = blk + kOffF + ((size_t)((cc / kVT) * kC + r) * kVT) * 2;  // one 32-column tile row
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] = d[8 * q + e];
+            st16(p + 16 * q, pack16(a));
+          }
+        }
       }
     }
   } else if (tid == 0) {
@@ -426,62 +789,21 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(taddr, 64);
-  if (!ok) return;
-
-  // ---- 5. blocked forward substitution, one column per thread
-  const bool is_w = tid < kK;
-  const int col = is_w ? tid : tid - kK;
-  if (!is_w && col >= V) return;
-  bf16 *hist = is_w ? sQ : sV;          // rows of W / U' (right-hand side until solved)
-  const int hstride = is_w ? kK : 128;
-#pragma unroll 1
-  for (int I = 0; I < kC / 16; ++I) {
-    float acc[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) acc[r] = __bfloat162float(hist[(16 * I + r) * hstride + col]);
-#pragma unroll 2
-    for (int j = 0; j < 16 * I; ++j) {  // earlier blocks, solved; A^T row j = 16 coefficients
-      const float xj = __bfloat162float(hist[j * hstride + col]);
-      const float4 *aj = reinterpret_cast<const float4 *>(sA + j * kC + 16 * I);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 a4 = aj[q];
-        acc[4 * q] = fmaf(-a4.x, xj, acc[4 * q]);
-        acc[4 * q + 1] = fmaf(-a4.y, xj, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(-a4.z, xj, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(-a4.w, xj, acc[4 * q + 3]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 15; ++j) {  // the block's own triangle, column by column
-      const float *aj = sA + (16 * I + j) * kC + 16 * I;
-#pragma unroll
-      for (int r = j + 1; r < 16; ++r) acc[r] = fmaf(-aj[r], acc[j], acc[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int row = 16 * I + r;
-      const float x = row < Lc ? acc[r] : 0.f;
-      hist[row * hstride + col] = __float2bfloat16_rn(x);
-      if (is_w) st_bf16(blk + kOffXW + tc::kmajor_offset(row, col, kK), x);
-      else st_bf16(blk + kOffUP + ((size_t)((col / kVT) * kC + row) * kVT + (col % kVT)) * 2, x);
-    }
-  }
+  if (warp == 0) tc::tmem_dealloc(taddr, 256);
 }
 
-// Sequential state pass of one (32-row tile, head, sequence).
+// Sequential state pass of one (32-row tile, head, sequence): per chunk S1^T = Gamma_c S0^T
+// - Z S0^T + N^T, one 128x32x128 product on the path; S0 of every chunk also goes to the
+// chunk's block for the output kernel.
 template <typename IO, int V>
 __global__ void __launch_bounds__(128)
 prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                         const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_base,
-                        int T, const uint8_t *__restrict__ has_init,
-                        const char *__restrict__ blocks, IO *__restrict__ out) {
+                        int T, const uint8_t *__restrict__ has_init, char *__restrict__ blocks) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ uint32_t s_taddr;
-  __shared__ __align__(8) uint64_t s_xbar[2];  // [W; Q.Gamma] of a buffer landed
-  __shared__ __align__(8) uint64_t s_lbar[2];  // the rest of a buffer's block landed
-  __shared__ __align__(8) uint64_t s_bar1, s_bar2, s_bar3;
+  __shared__ __align__(8) uint64_t s_lbar[kNBuf];  // a buffer's operand block landed
+  __shared__ __align__(8) uint64_t s_barz;         // Z S0^T of a chunk done
   __shared__ volatile int s_fail;  // a bounded wait ran out somewhere; checked after barriers
   const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -498,217 +820,122 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   const bool init = has_init == nullptr || has_init[n] != 0;
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
   bf16 *Sg = reinterpret_cast<bf16 *>(pv.ssm) + ((prow * H + h) * V + (size_t)vt * kVT) * kK;
+  auto block = [&](int c) { return blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes; };
 
   // state tile in registers, transposed: thread k holds S[v][k] for the tile's 32 rows v
   float S[kVT];
 #pragma unroll
   for (int v = 0; v < kVT; ++v) S[v] = init ? __bfloat162float(Sg[(size_t)v * kK + tid]) : 0.f;
 
-  // zero rows 0..63 of both [0; P] operands (the TMA fills rows 64..127)
-  for (int i = tid; i < 2 * (kC * kC * 2 / 16); i += 128) {
-    const int b = i / (kC * kC * 2 / 16), o = i % (kC * kC * 2 / 16);
-    st16(smem + b * kBufBytes + kBufP0 + o * 16, make_uint4(0, 0, 0, 0));
-  }
   if (tid == 0) {
-    mbar_init(&s_xbar[0], 1);
-    mbar_init(&s_xbar[1], 1);
-    mbar_init(&s_lbar[0], 1);
-    mbar_init(&s_lbar[1], 1);
-    mbar_init(&s_bar1, 1);
-    mbar_init(&s_bar2, 1);
-    mbar_init(&s_bar3, 1);
+    for (int b = 0; b < kNBuf; ++b) mbar_init(&s_lbar[b], 1);
+    mbar_init(&s_barz, 1);
     s_fail = 0;
   }
-  if (warp == 0) { tc::tmem_alloc(&s_taddr, 128); tc::tmem_relinquish(); }
-  tc::fence_smem_to_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tm = s_taddr;
-  const uint32_t tD1 = tm, tD2 = tm + 32, tD3 = tm + 64;
-  unsigned char *sS = smem + kOffS, *sU = smem + kOffU;
-
-  // [W; Q.Gamma] is all MMA1 needs: it is fetched two chunks ahead, into its buffer's
-  // region as soon as MMA1 of the chunk before has read it; the rest one chunk ahead.
-  auto issue_xw = [&](int c, int b) {
-    const char *blk = blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes;
-    mbar_arrive_expect_tx(&s_xbar[b], 128 * kK * 2);
-    bulk_g2s(smem + b * kBufBytes + kBufXW, blk + kOffXW, 128 * kK * 2, &s_xbar[b]);
-  };
-  auto issue_load = [&](int c, int b) {
-    const char *blk = blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes;
-    unsigned char *dst = smem + b * kBufBytes;
-    mbar_arrive_expect_tx(&s_lbar[b], kK * kC * 2 + kC * kC * 2 + kC * kVT * 2 + kK * 4);
-    bulk_g2s(dst + kBufBT, blk + kOffBT, kK * kC * 2, &s_lbar[b]);
-    bulk_g2s(dst + kBufP0 + kC * kC * 2, blk + kOffP, kC * kC * 2, &s_lbar[b]);
-    bulk_g2s(dst + kBufUP, blk + kOffUP + (size_t)vt * kC * kVT * 2, kC * kVT * 2, &s_lbar[b]);
-    bulk_g2s(dst + kBufGC, blk + kOffGC, kK * 4, &s_lbar[b]);
-  };
-  auto issue_mma1 = [&](int b) {  // tid 0: D1 = [W; Q.Gamma] S0^T
-    const unsigned char *buf = smem + b * kBufBytes;
-#pragma unroll
-    for (int ks = 0; ks < kK / 16; ++ks)
-      tc::mma_bf16(tD1, tc::kmajor_desc(buf + kBufXW, kK, ks), tc::mnmajor_desc(sS, kVT, ks),
-                   tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
-    tc::mma_commit(&s_bar1);
-  };
-  auto write_s0 = [&]() {  // S0 (bf16) as MMA1's MN-major B operand: element (v, k = tid)
+  if (warp == 0) { tc::tmem_alloc(&s_taddr, 32); tc::tmem_relinquish(); }
+  // S0 of chunk c (bf16): into S buffer c & 1 as the MN-major B operand (element (v, k = tid))
+  // and into chunk c's block, rows 32 vt .. +31 of the N = V operand there
+  auto write_s0 = [&](int c) {
+    unsigned char *sS = smem + kStS + (c & 1) * kSBytes;
+    char *g = block(c) + kOffS0;
 #pragma unroll
     for (int q = 0; q < kVT / 8; ++q) {
       float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = S[8 * q + e];
-      st16(sS + tc::mnmajor_offset(8 * q, tid, kVT), pack16(x));
+      const uint4 u = pack16(x);
+      st16(sS + tc::mnmajor_offset(8 * q, tid, kVT), u);
+      st16(g + tc::mnmajor_offset(kVT * vt + 8 * q, tid, V), u);
     }
   };
-  auto wait = [&](uint64_t *bar, uint32_t phase) {
-    if (!mbar_wait(bar, phase)) s_fail = 1;
-  };
+  if (nch > 0) write_s0(0);
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tDZ = s_taddr;  // Z S0^T: 32 columns
 
-  // Pipeline of one chunk c (buffer b = c & 1):
-  //   wait MMA1(c) -> U = U' - W S0^T into shared memory (rows 0..63), keep the inter-chunk
-  //   output (rows 64..127) -> barrier -> MMA2 (state) and MMA3 (intra-chunk output), each
-  //   with its own commit; prefetch chunk c+1's operands -> state update, S1 into shared
-  //   memory -> barrier -> MMA1(c+1) -> output of chunk c written while MMA1(c+1) runs.
-  //   Waits on mbarriers are per thread and bounded; a failed one sets s_fail, which
-  //   every thread reads after the next barrier, so all leave the loop together.
-  // counts of requested [W; Q.Gamma] parts and rest parts (tid 0 issues; every thread
-  // keeps the counts, which depend only on the loop position)
-  int issued_x = 0, issued = 0;
+  auto issue_load = [&](int c) {
+    const int b = c % kNBuf;
+    const char *blk = block(c);
+    unsigned char *dst = smem + b * kSBuf;
+    mbar_arrive_expect_tx(&s_lbar[b], kLoadBytes);
+    bulk_g2s(dst + kSbZ, blk + kOffZ, kK * kK * 2, &s_lbar[b]);
+    bulk_g2s(dst + kSbN, blk + kOffN + (size_t)vt * kK * kVT * 2, kK * kVT * 2, &s_lbar[b]);
+    bulk_g2s(dst + kSbGC, blk + kOffGC, kK * 4, &s_lbar[b]);
+  };
+  // Shared-memory descriptors of buffer 0 / S buffer 0; the loop moves them by fixed
+  // offsets (one add per MMA instead of a descriptor built from the address).
+  const uint64_t dZ0 = tc::kmajor_desc(smem + kSbZ, kK, 0);
+  const uint64_t dS0 = tc::mnmajor_desc(smem + kStS, kVT, 0);
+  constexpr uint32_t kIdZ = tc::idesc_bf16_bmn<128, kVT>();
+
+  // Chunk c (operand buffer c % 4, S0 in S buffer c & 1):
+  //   tid 0 issues Z S0^T and commits it, then fetches chunk c+3 into the buffer chunk c-1
+  //   used (its product is done: every thread waited for it before the last barrier)
+  //   -> every thread reads N^T and Gamma_c of its column -> wait Z S0^T -> state update,
+  //   S1 into the other S buffer (its last reader, chunk c-1's product, is done) and into
+  //   chunk c+1's block -> barrier.  Waits on mbarriers are per thread and bounded; a
+  //   failed one sets s_fail, which every thread reads after the next barrier, so all
+  //   leave the loop together.
+  int issued = 0;  // chunks whose operand copies were requested (every thread keeps it)
   bool ok = true;
   if (nch > 0) {
-    if (tid == 0) {
-      issue_xw(0, 0);
-      if (nch > 1) issue_xw(1, 1);
-      issue_load(0, 0);
-    }
-    issued_x = nch > 1 ? 2 : 1;
-    issued = 1;
-    write_s0();
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (tid == 0) {
-      wait(&s_xbar[0], 0);
-      if (!s_fail) issue_mma1(0);
-    }
+    if (tid == 0)
+      for (int k = 0; k < nch && k < kNBuf - 1; ++k) issue_load(k);
+    issued = nch < kNBuf - 1 ? nch : kNBuf - 1;
   }
   int c = 0;
   for (; c < nch; ++c) {
-    const int b = c & 1;
-    const unsigned char *buf = smem + b * kBufBytes;
-    const int t0 = start + kC * c, Lc = min(kC, end - t0);
-    wait(&s_bar1, c & 1);
-    tc::fence_after_sync();
-    // MMA1(c) has read buffer b's [W; Q.Gamma]: refill it with chunk c+2's
-    if (c + 2 < nch) {
-      if (tid == 0) issue_xw(c + 2, b);
-      issued_x = c + 3;
-    }
-    float d[kVT];
-    {
-      float d0[16], d1[16];
-      tc::tmem_ld16(tc::tmem_addr(tD1, 32 * warp, 0), d0);
-      tc::tmem_ld16(tc::tmem_addr(tD1, 32 * warp, 16), d1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { d[i] = d0[i]; d[16 + i] = d1[i]; }
-    }
-    wait(&s_lbar[b], (c >> 1) & 1);  // the operand block is visible to this thread
-    if (warp < 2) {
-      // rows 0..63: U = U' - W S0^T as MMA2/3's MN-major B operand: element (v, r = tid)
-      const int r = tid;
-      const uint4 *up = reinterpret_cast<const uint4 *>(buf + kBufUP + (size_t)r * kVT * 2);
-#pragma unroll
-      for (int q = 0; q < kVT / 8; ++q) {
-        float u8[8];
-        unpack16(up[q], u8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u8[e] = r < Lc ? u8[e] - d[8 * q + e] : 0.f;
-        st16(sU + tc::mnmajor_offset(8 * q, r, kVT), pack16(u8));
-      }
-    }
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (s_fail) { ok = false; break; }
-    tc::fence_after_sync();
+    const int b = c % kNBuf;
+    const unsigned char *buf = smem + b * kSBuf;
     if (tid == 0) {
+      if (!mbar_wait(&s_lbar[b], (c / kNBuf) & 1)) {
+        s_fail = 1;
+      } else {
+        const uint64_t dz = tc::desc_add(dZ0, b * kSBuf);
+        const uint64_t ds = tc::desc_add(dS0, (c & 1) * kSBytes);
 #pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        tc::mma_bf16(tD2, tc::kmajor_desc(buf + kBufBT, kC, ks), tc::mnmajor_desc(sU, kVT, ks),
-                     tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
-      tc::mma_commit(&s_bar2);
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        tc::mma_bf16(tD3, tc::kmajor_desc(buf + kBufP0, kC, ks), tc::mnmajor_desc(sU, kVT, ks),
-                     tc::idesc_bf16_bmn<128, kVT>(), ks > 0);
-      tc::mma_commit(&s_bar3);
-    }
-    // Every thread is past chunk c-1, so the rest of the other buffer is free for c+1.
-    if (c + 1 < nch) {
-      if (tid == 0) issue_load(c + 1, b ^ 1);
-      issued = c + 2;
-    }
-    wait(&s_bar2, c & 1);
-    tc::fence_after_sync();
-    {
-      // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] + (K.Gamma_c/Gamma)^T U for this thread's k
-      const float gc = reinterpret_cast<const float *>(buf + kBufGC)[tid];
-      float d0[16], d1[16];
-      tc::tmem_ld16(tc::tmem_addr(tD2, 32 * warp, 0), d0);
-      tc::tmem_ld16(tc::tmem_addr(tD2, 32 * warp, 16), d1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        S[i] = fmaf(gc, S[i], d0[i]);
-        S[16 + i] = fmaf(gc, S[16 + i], d1[i]);
+        for (int ks = 0; ks < kK / 16; ++ks)
+          tc::mma_bf16(tDZ, tc::desc_add(dz, ks * 256), tc::desc_add(ds, ks * 2 * kVT * 16), kIdZ, ks > 0);
+        tc::mma_commit(&s_barz);
+        if (c + kNBuf - 1 < nch) issue_load(c + kNBuf - 1);
       }
     }
+    if (c + kNBuf - 1 < nch) issued = c + kNBuf;
+    if (!mbar_wait(&s_lbar[b], (c / kNBuf) & 1)) s_fail = 1;  // visible to this thread
+    float nt[kVT];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+      unpack16(ld16(buf + kSbN + tid * kVT * 2 + 16 * q), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nt[8 * q + e] = f[e];
+    }
+    const float gc = reinterpret_cast<const float *>(buf + kSbGC)[tid];
+    if (!mbar_wait(&s_barz, c & 1)) s_fail = 1;
+    tc::fence_after_sync();
+    {
+      // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] - (Z S0^T)[k][:] + N^T[k][:] for this thread's k
+      float d[kVT];
+      tc::tmem_ld32(tc::tmem_addr(tDZ, 32 * warp, 0), d);
+#pragma unroll
+      for (int i = 0; i < kVT; ++i) S[i] = fmaf(gc, S[i], nt[i] - d[i]);
+    }
     if (c + 1 < nch) {
-      write_s0();
+      write_s0(c + 1);
       tc::fence_smem_to_async();
     }
-    float o[kVT];
-    if (warp >= 2) {
-      wait(&s_bar3, c & 1);
-      tc::fence_after_sync();
-      float d0[16], d1[16];
-      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 0), d0);
-      tc::tmem_ld16(tc::tmem_addr(tD3, 32 * warp, 16), d1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { o[i] = d[i] + d0[i]; o[16 + i] = d[16 + i] + d1[i]; }
-    }
     tc::fence_before_sync();
     __syncthreads();
     if (s_fail) { ok = false; break; }
     tc::fence_after_sync();
-    if (c + 1 < nch && tid == 0) {
-      wait(&s_xbar[b ^ 1], ((c + 1) >> 1) & 1);
-      if (!s_fail) issue_mma1(b ^ 1);  // a failure here surfaces after the next barrier
-    }
-    if (warp >= 2) {
-      // rows 64..127: O = (Q.Gamma) S0^T + P U of token r, written while MMA1(c+1) runs
-      const int r = tid - kC;
-      if (r < Lc) {
-        IO *op = out + ((size_t)(t0 + r) * H + h) * V + (size_t)vt * kVT;
-        constexpr int EPV = 16 / sizeof(IO);
-#pragma unroll
-        for (int q = 0; q < kVT / EPV; ++q) {
-          float x[EPV];
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) x[e] = o[EPV * q + e];
-          st16(op + EPV * q, pack16(x));
-        }
-      }
-    }
   }
-  if (nch > 0 && s_fail) ok = false;
   if (!ok) {
     if (tid == 0) {
       flag_error(pv.err, RSC_DEVERR_TIMEOUT);
-      // let every issued bulk copy land before the shared memory is released
-      for (int k = c; k < issued_x; ++k) mbar_wait(&s_xbar[k & 1], (k >> 1) & 1);
-      for (int k = c; k < issued; ++k) mbar_wait(&s_lbar[k & 1], (k >> 1) & 1);
+      // let every requested bulk copy land before the shared memory is released
+      for (int k = c; k < issued; ++k) mbar_wait(&s_lbar[k % kNBuf], (k / kNBuf) & 1);
     }
   } else {
 #pragma unroll
@@ -716,7 +943,86 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tm, 128);
+  if (warp == 0) tc::tmem_dealloc(tDZ, 32);
+}
+
+// Outputs of one (chunk, head): O = E S0^T + F, one 64 x V x 128 product from the block
+// (E, F from the chunk kernel, S0 from the state pass).  128 threads; token r of the
+// chunk is lane r % 16 of warp r / 16.
+template <typename IO, int V>
+__global__ void __launch_bounds__(128)
+prefill_tc_out_kernel(PoolView pv, const int32_t *__restrict__ slots,
+                      const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_base,
+                      int N, const char *__restrict__ blocks, IO *__restrict__ out) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ uint32_t s_taddr;
+  __shared__ __align__(8) uint64_t s_lbar, s_bar;
+  const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int H = pv.H;
+  if (cid >= chunk_base[N]) return;
+  const int n = last_le(chunk_base, N, cid);
+  if (slots[n] < 0 || slots[n] > pv.P) return;  // flagged by the state pass
+  const int t0 = cu[n] + kC * (cid - chunk_base[n]);
+  const int Lc = min(kC, cu[n + 1] - t0);
+  const char *blk = blocks + ((size_t)cid * H + h) * kBlockBytes;
+  if (tid == 0) {
+    mbar_init(&s_lbar, 1);
+    mbar_init(&s_bar, 1);
+    mbar_arrive_expect_tx(&s_lbar, kC * kK * 2 + V * kK * 2 + kC * V * 2);
+    bulk_g2s(smem + kOuE, blk + kOffE, kC * kK * 2, &s_lbar);
+    bulk_g2s(smem + kOuS, blk + kOffS0, V * kK * 2, &s_lbar);
+    bulk_g2s(smem + kOuF, blk + kOffF, kC * V * 2, &s_lbar);
+  }
+  if (warp == 0) { tc::tmem_alloc(&s_taddr, V); tc::tmem_relinquish(); }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t taddr = s_taddr;
+  bool ok = mbar_wait(&s_lbar, 0);  // the operands are visible to this thread
+  if (tid == 0 && ok) {
+#pragma unroll
+    for (int ks = 0; ks < kK / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(smem + kOuE, kK, ks), tc::mnmajor_desc(smem + kOuS, V, ks),
+                   tc::idesc_bf16_bmn<64, V>(), ks > 0);
+    tc::mma_commit(&s_bar);
+  }
+  ok = __syncthreads_and(ok && mbar_wait(&s_bar, 0));
+  tc::fence_after_sync();
+  if (ok) {
+    const int r = 16 * warp + lane;
+#pragma unroll
+    for (int cc = 0; cc < V; cc += 32) {
+      float d[32];
+      tc::tmem_ld32(tc::tmem_addr(taddr, 32 * warp, cc), d);
+      if (lane < 16 && r < Lc) {
+        const unsigned char *fr = smem + kOuF + ((size_t)((cc / kVT) * kC + r) * kVT) * 2;
+        float o[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
+          unpack16(ld16(fr + 16 * q), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[8 * q + e] = d[8 * q + e] + f[e];
+        }
+        IO *op = out + ((size_t)(t0 + r) * H + h) * V + cc;
+        constexpr int EPV = 16 / sizeof(IO);
+#pragma unroll
+        for (int q = 0; q < 32 / EPV; ++q) {
+          float y[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) y[e] = o[EPV * q + e];
+          st16(op + EPV * q, pack16(y));
+        }
+      }
+    }
+  } else if (tid == 0) {
+    flag_error(pv.err, RSC_DEVERR_TIMEOUT);
+    mbar_wait(&s_lbar, 0);  // let the copies land before the shared memory is released
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(taddr, V);
 }
 
 // ---------------------------------------------------------------------------- launch
@@ -728,12 +1034,15 @@ static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *
                        char *blocks, cudaStream_t s) {
   auto chunk_kernel = prefill_tc_chunk_kernel<IO, V, GATE>;
   auto state_kernel = prefill_tc_state_kernel<IO, V>;
+  auto out_kernel = prefill_tc_out_kernel<IO, V>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kChSmem) != cudaSuccess ||
         cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStateSmem) != cudaSuccess)
+                             (int)kStateSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kOutSmem) != cudaSuccess)
       return RSC_ECUDA;
     attr = true;
   }
@@ -744,8 +1053,12 @@ static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *
                                                           conv_w, g, beta, blocks);
     if (launch_status() != RSC_OK) return RSC_ECUDA;
   }
-  state_kernel<<<dim3(V / kVT, a.pv.H, N), 128, kStateSmem, s>>>(
-      a.pv, a.layer, slots, cu, chunk_base, T, has_init, blocks, static_cast<IO *>(out));
+  state_kernel<<<dim3(V / kVT, a.pv.H, N), 128, kStateSmem, s>>>(a.pv, a.layer, slots, cu,
+                                                                   chunk_base, T, has_init, blocks);
+  if (launch_status() != RSC_OK) return RSC_ECUDA;
+  if (cap > 0 && T > 0)
+    out_kernel<<<dim3(cap, a.pv.H), 128, kOutSmem, s>>>(a.pv, slots, cu, chunk_base, N, blocks,
+                                                         static_cast<IO *>(out));
   return launch_status();
 }
 
