@@ -16,6 +16,8 @@ Pinning status (what the tests check each function against, besides itself):
   chunkwise_head     equals recurrent_head (two independent derivations)
   decode/prefill     split order and L2 norm pinned through closed-form special cases
   slot_copy/commit   byte equality
+  replay_verify/     commit(a) equals the snapshot path's commit(a) (fp32 records); the
+  replay_commit      records rebuild the state by the pages' closed form; ring wrap-around
   pool_bytes         every logged pool size printed on the pages (tests/golden)
   bf16_round         torch's float32 -> bfloat16 conversion (round to nearest even)
 """
@@ -50,6 +52,14 @@ def build(force: bool = False) -> str:
         )
         os.replace(tmp, _SO)
     return _SO
+
+
+class _Rings(ctypes.Structure):
+    _fields_ = [
+        ("depth", ctypes.c_int32),
+        ("d", ctypes.c_void_p), ("k", ctypes.c_void_p), ("rawv", ctypes.c_void_p),
+        ("rawk", ctypes.c_void_p), ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+    ]
 
 
 class _Pool(ctypes.Structure):
@@ -88,6 +98,11 @@ def _load():
         lib.orc_spec_verify.restype = i32
         lib.orc_spec_commit.argtypes = [pp, i32, vp, i32, i32, i32, vp, vp, vp]
         lib.orc_spec_commit.restype = i32
+        rp = ctypes.POINTER(_Rings)
+        lib.orc_replay_verify.argtypes = [pp, rp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.orc_replay_verify.restype = i32
+        lib.orc_replay_commit.argtypes = [pp, rp, i32, vp, vp, i32, i32, i32, vp, vp]
+        lib.orc_replay_commit.restype = i32
         _lib = lib
     return _lib
 
@@ -246,6 +261,57 @@ def spec_commit(pool: Pool, layer, slots, T, Lc, spec_ssm, spec_conv, accept):
     st = pool._struct()
     _check(_load().orc_spec_commit(ctypes.byref(st), layer, _ptr(slots), slots.shape[0], T,
                                    Lc, _ptr(ss), _ptr(sc), _ptr(acc)), "spec_commit")
+
+
+class Rings:
+    """ReplaySSM rings of a pool (numpy, mutated in place): per layer, pool row, head and
+    entry: d [V], k [K], rawv [V], rawk [K] in the state dtype; g [K] (KDA) or [1] (GDN) and
+    beta in fp32.  Shapes [layers][P+1][H][depth][n]."""
+
+    def __init__(self, pool: "Pool", depth: int):
+        L, R, H, K, V = pool.num_layers, pool.num_slots + 1, pool.H, pool.K, pool.V
+        sd = storage_np_dtype(pool.state_dtype)
+        gn = K if pool.gate == KDA else 1
+        self.depth = depth
+        self.d = np.zeros((L, R, H, depth, V), sd)
+        self.k = np.zeros((L, R, H, depth, K), sd)
+        self.rawv = np.zeros((L, R, H, depth, V), sd)
+        self.rawk = np.zeros((L, R, H, depth, K), sd)
+        self.g = np.zeros((L, R, H, depth, gn), np.float32)
+        self.beta = np.zeros((L, R, H, depth), np.float32)
+
+    def _struct(self):
+        return _Rings(self.depth, _ptr(self.d), _ptr(self.k), _ptr(self.rawv), _ptr(self.rawk),
+                      _ptr(self.g), _ptr(self.beta))
+
+
+def replay_verify(pool: Pool, rings: Rings, layer, slots, pos, T, Lc, qkv, conv_w, g, beta):
+    """ReplaySSM verify: records of token t go to ring entry (pos[b] + t) mod depth; the slot
+    is not modified.  Returns (spec_conv [B][Lc][3][D], out [B][T][H][V])."""
+    slots, pos = _c(slots, np.int32), _c(pos, np.int32)
+    B = slots.shape[0]
+    qkv = _c(qkv, pool.io_np()).reshape(B, T, pool.D)
+    g = _gate_arr(pool, g, (B, T))
+    beta = _c(beta, np.float32).reshape(B, T, pool.H)
+    w = _c(conv_w, np.float32).reshape(pool.D, 4)
+    spec_conv = np.zeros((B, Lc, 3, pool.D), pool.io_np())
+    out = np.zeros((B, T, pool.H, pool.V), pool.io_np())
+    st, rs = pool._struct(), rings._struct()
+    _check(_load().orc_replay_verify(ctypes.byref(st), ctypes.byref(rs), layer, _ptr(slots),
+                                     _ptr(pos), B, T, Lc, _ptr(spec_conv), _ptr(qkv), _ptr(w),
+                                     _ptr(g), _ptr(beta), _ptr(out)), "replay_verify")
+    return spec_conv, out
+
+
+def replay_commit(pool: Pool, rings: Rings, layer, slots, pos, T, Lc, spec_conv, accept):
+    """ReplaySSM commit: replay tokens 0..accept[b] from the slot state out of the rings,
+    store the state into the slot and the window snapshot spec_conv[b][accept[b]]."""
+    slots, pos, acc = _c(slots, np.int32), _c(pos, np.int32), _c(accept, np.int32)
+    sc = _c(spec_conv, pool.io_np())
+    st, rs = pool._struct(), rings._struct()
+    _check(_load().orc_replay_commit(ctypes.byref(st), ctypes.byref(rs), layer, _ptr(slots),
+                                     _ptr(pos), slots.shape[0], T, Lc, _ptr(sc), _ptr(acc)),
+           "replay_commit")
 
 
 # ----------------------------------------------------------------------------- pieces

@@ -483,6 +483,147 @@ int orc_spec_commit(const orc_pool *p, int layer, const int32_t *slots, int B, i
   return 0;
 }
 
+/* ---------------------------------------------------------------- ReplaySSM */
+
+/* ReplaySSM rings ("SGLang Qwen3/kimi-k3 Hybrid Linear Mamba KV cache管理", ReplaySSM
+ * section; "Kimi K3 ... KV cache", §4 replay buffers): per pool row (slot) and head, `depth`
+ * entries, each the records of one token:
+ *   d     the delta beta (v - S k) the token wrote (length V)
+ *   k     its L2-normalised key (K)
+ *   g     its log-decay (K for KDA, one value for GDN)
+ *   rawv  the value entering the delta rule, before v - S k (V)
+ *   rawk  the key before its L2 norm (K)
+ *   beta  its beta.
+ * d, k, rawv, rawk are stored in the pool's state dtype (bf16 in the pages' deployment), g
+ * and beta in fp32.  Layout [layers][P+1][H][depth][n].  Token t of a verify call for a
+ * request whose ring position is pos goes to entry (pos + t) mod depth. */
+typedef struct {
+  int32_t depth;
+  void *d, *k, *rawv, *rawk;
+  float *g, *beta;
+} orc_rings;
+
+static size_t ring_at(const orc_pool *p, const orc_rings *R, int layer, int slot, int h, int e,
+                      size_t n) {
+  return ((((size_t)layer * (p->num_slots + 1) + slot) * p->H + h) * (size_t)R->depth + e) * n;
+}
+
+static int replay_args_ok(const orc_pool *p, const orc_rings *R, int layer, const int32_t *slots,
+                          const int32_t *pos, int B, int T, int Lc) {
+  if (layer < 0 || layer >= p->num_layers || T < 1 || T > Lc) return 0;
+  if (R->depth < 1 || (R->depth & (R->depth - 1)) != 0 || 2 * T > R->depth) return 0;
+  for (int b = 0; b < B; ++b)
+    if (!check_slot(p, slots[b]) || pos[b] < 0 || pos[b] >= R->depth) return 0;
+  return 1;
+}
+
+/* ReplaySSM verify: for each request run T tokens from the slot state (which is not
+ * modified), as the snapshot verify does, but instead of storing S_t record the token's
+ * (d, k, g, rawv, rawk, beta) in the rings at entry (pos[b] + t) mod depth.  The window
+ * after token t goes to spec_conv[b][t] and the outputs to out, as in orc_spec_verify. */
+int orc_replay_verify(const orc_pool *p, const orc_rings *R, int layer, const int32_t *slots,
+                      const int32_t *pos, int B, int T, int Lc, void *spec_conv, const void *qkv,
+                      const float *conv_w, const float *g, const float *beta, void *out) {
+  if (!replay_args_ok(p, R, layer, slots, pos, B, T, Lc)) return -1;
+  layer_ws w;
+  if (ws_init(&w, p)) return -2;
+  const int D = w.D, H = p->H, K = p->K, V = p->V, st_dt = p->state_dtype;
+  const size_t nS = ssm_row_elems(p), nW = conv_row_elems(p), ng = gate_elems(p);
+  const size_t gn = p->gate == ORC_GATE_KDA ? (size_t)K : 1;
+  double *S = malloc(sizeof(double) * nS), *win = malloc(sizeof(double) * nW);
+  double *x = malloc(sizeof(double) * (size_t)D), *o = malloc(sizeof(double) * (size_t)H * V);
+  for (int b = 0; b < B; ++b) {
+    size_t sr = ssm_row(p, layer, slots[b]), cr = conv_row(p, layer, slots[b]);
+    for (size_t i = 0; i < nS; ++i) S[i] = ld(p->ssm, sr + i, st_dt);
+    for (size_t i = 0; i < nW; ++i) win[i] = ld(p->conv, cr + i, p->conv_dtype);
+    for (int t = 0; t < T; ++t) {
+      const size_t bt = (size_t)b * T + t;
+      const int e = (pos[b] + t) & (R->depth - 1);
+      for (int c = 0; c < D; ++c) x[c] = ld(qkv, bt * D + c, p->conv_dtype);
+      orc_conv_token(D, win, x, conv_w, w.y);
+      for (int h = 0; h < H; ++h) {
+        const double *q = w.y + (size_t)h * K;
+        const double *k = w.y + (size_t)H * K + (size_t)h * K;
+        const double *v = w.y + (size_t)2 * H * K + (size_t)h * V;
+        const float *gt = g + bt * ng + (p->gate == ORC_GATE_KDA ? (size_t)h * K : (size_t)h);
+        const float bh = beta[bt * H + h];
+        l2norm(K, q, w.qn);
+        l2norm(K, k, w.kn);
+        for (int c = 0; c < K; ++c) w.alpha[c] = exp((double)gt[p->gate == ORC_GATE_KDA ? c : 0]);
+        head_token(K, V, S + (size_t)h * V * K, w.qn, w.kn, v, w.alpha, (double)bh,
+                   o + (size_t)h * V, w.d);
+        const size_t rk = ring_at(p, R, layer, slots[b], h, e, (size_t)K);
+        const size_t rv = ring_at(p, R, layer, slots[b], h, e, (size_t)V);
+        for (int c = 0; c < K; ++c) {
+          st(R->k, rk + c, st_dt, w.kn[c]);
+          st(R->rawk, rk + c, st_dt, k[c]);
+        }
+        for (int r = 0; r < V; ++r) {
+          st(R->d, rv + r, st_dt, w.d[r]);
+          st(R->rawv, rv + r, st_dt, v[r]);
+        }
+        memcpy(R->g + ring_at(p, R, layer, slots[b], h, e, gn), gt, sizeof(float) * gn);
+        R->beta[ring_at(p, R, layer, slots[b], h, e, 1)] = bh;
+      }
+      for (size_t i = 0; i < nW; ++i) st(spec_conv, ((size_t)b * Lc + t) * nW + i, p->conv_dtype, win[i]);
+      for (int i = 0; i < H * V; ++i) st(out, bt * H * V + i, p->conv_dtype, o[i]);
+    }
+  }
+  free(S); free(win); free(x); free(o);
+  ws_free(&w);
+  return 0;
+}
+
+/* ReplaySSM commit ([p3] exact commit of accepted tokens): from the slot state replay tokens
+ * 0..accept[b] in order from the rings,
+ *   k = rawk / sqrt(|rawk|^2 + eps),  alpha = exp(g),  S <- S Diag(alpha),
+ *   d = beta (rawv - S k),  S <- S + d k^T,
+ * in fp64, then store S (rounded to the state dtype) into the slot; the window becomes the
+ * snapshot spec_conv[b][accept[b]]. */
+int orc_replay_commit(const orc_pool *p, const orc_rings *R, int layer, const int32_t *slots,
+                      const int32_t *pos, int B, int T, int Lc, const void *spec_conv,
+                      const int32_t *accept) {
+  if (!replay_args_ok(p, R, layer, slots, pos, B, T, Lc)) return -1;
+  for (int b = 0; b < B; ++b)
+    if (accept[b] < 0 || accept[b] >= T) return -1;
+  const int H = p->H, K = p->K, V = p->V, st_dt = p->state_dtype;
+  const size_t nS = ssm_row_elems(p), nW = conv_row_elems(p);
+  const size_t gn = p->gate == ORC_GATE_KDA ? (size_t)K : 1;
+  double *S = malloc(sizeof(double) * nS), *raw = malloc(sizeof(double) * (size_t)K);
+  double *kn = malloc(sizeof(double) * (size_t)K);
+  for (int b = 0; b < B; ++b) {
+    const size_t sr = ssm_row(p, layer, slots[b]);
+    for (size_t i = 0; i < nS; ++i) S[i] = ld(p->ssm, sr + i, st_dt);
+    for (int t = 0; t <= accept[b]; ++t) {
+      const int e = (pos[b] + t) & (R->depth - 1);
+      for (int h = 0; h < H; ++h) {
+        const size_t rk = ring_at(p, R, layer, slots[b], h, e, (size_t)K);
+        const size_t rv = ring_at(p, R, layer, slots[b], h, e, (size_t)V);
+        const float *gt = R->g + ring_at(p, R, layer, slots[b], h, e, gn);
+        const double bh = R->beta[ring_at(p, R, layer, slots[b], h, e, 1)];
+        for (int c = 0; c < K; ++c) raw[c] = ld(R->rawk, rk + c, st_dt);
+        l2norm(K, raw, kn);
+        double *Sh = S + (size_t)h * V * K;
+        for (int r = 0; r < V; ++r) {
+          double u = 0.0;
+          for (int c = 0; c < K; ++c) {
+            Sh[(size_t)r * K + c] *= exp((double)gt[gn == 1 ? 0 : c]);
+            u += Sh[(size_t)r * K + c] * kn[c];
+          }
+          const double d = bh * (ld(R->rawv, rv + r, st_dt) - u);
+          for (int c = 0; c < K; ++c) Sh[(size_t)r * K + c] += d * kn[c];
+        }
+      }
+    }
+    for (size_t i = 0; i < nS; ++i) st(p->ssm, sr + i, st_dt, S[i]);
+    memcpy((char *)p->conv + conv_row(p, layer, slots[b]) * dsize(p->conv_dtype),
+           (const char *)spec_conv + ((size_t)b * Lc + accept[b]) * nW * dsize(p->conv_dtype),
+           nW * dsize(p->conv_dtype));
+  }
+  free(S); free(raw); free(kn);
+  return 0;
+}
+
 /* Array helper for the Python wrapper: round n doubles to bf16 bit patterns. */
 void orc_bf16_round_array(const double *x, uint16_t *out, size_t n) {
   for (size_t i = 0; i < n; ++i) out[i] = orc_bf16_round(x[i]);

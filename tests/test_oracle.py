@@ -344,6 +344,129 @@ def test_spec_commit_equals_accepted_decode_steps(st):
         assert np.max(np.abs(a - e)) <= tol * np.max(np.abs(e))
 
 
+# ----------------------------------------------------------------------- ReplaySSM
+
+def _replay_case(seed, st, gate=oracle.KDA, depth=16):
+    H, K, V, T, Lc = 2, 8, 6, 5, 8
+    r, pool, w = _pool_case(seed, H=H, K=K, V=V, st=st, io=st, gate=gate)
+    B = 3
+    slots = np.int32([5, 2, 4])
+    x = inputs.projections(r, (B, T), H, K, V, st)
+    g, beta = inputs.gates(r, (B, T), H, K, gate)
+    return dict(H=H, K=K, V=V, T=T, Lc=Lc, B=B, pool=pool, w=w, slots=slots, x=x, g=g, beta=beta,
+                depth=depth, st=st, gate=gate)
+
+
+@pytest.mark.parametrize("gate", [oracle.KDA, oracle.GDN])
+def test_replay_commit_equals_snapshot_commit(gate):
+    """ReplaySSM commit(a) replays tokens 0..a from the slot out of the rings; with fp32 records
+    it lands where the snapshot path's commit(a) does (cache entry a), windows bit-exact, and
+    verify leaves the slot untouched and gives the snapshot verify's outputs bit for bit."""
+    c = _replay_case(21, oracle.F32, gate)
+    pool, st = c["pool"], c["st"]
+    snap = oracle.Pool(1, 5, c["H"], c["K"], c["V"], st, st, gate, pool.ssm.copy(), pool.conv.copy())
+    before = pool.ssm.copy(), pool.conv.copy()
+    rings = oracle.Rings(pool, c["depth"])
+    pos = np.int32([0, 3, 14])  # the last request wraps around the ring
+    accept = np.int32([0, 4, 2])
+    sC, out = oracle.replay_verify(pool, rings, 0, c["slots"], pos, c["T"], c["Lc"], c["x"], c["w"],
+                                   c["g"], c["beta"])
+    assert np.array_equal(pool.ssm, before[0]) and np.array_equal(pool.conv, before[1])
+    sS2, sC2, out2 = oracle.spec_verify(snap, 0, c["slots"], c["T"], c["Lc"], c["x"], c["w"],
+                                        c["g"], c["beta"])
+    assert np.array_equal(out, out2) and np.array_equal(sC, sC2)
+    oracle.replay_commit(pool, rings, 0, c["slots"], pos, c["T"], c["Lc"], sC, accept)
+    oracle.spec_commit(snap, 0, c["slots"], c["T"], c["Lc"], sS2, sC2, accept)
+    assert np.array_equal(pool.conv, snap.conv)
+    a, e = oracle.to_f64(pool.ssm, st), oracle.to_f64(snap.ssm, st)
+    assert np.max(np.abs(a - e)) <= 1e-6 * np.max(np.abs(e))
+
+
+def test_replay_records_rebuild_state_by_closed_form():
+    """The pages' closed form from the checkpoint and the (d, k, g) records,
+    S_m = S_0 Diag(prod_i alpha_i) + sum_j d_j (k_j . prod_{i>j} alpha_i)^T,
+    gives the state the snapshot verify stored after m tokens (fp32 records)."""
+    c = _replay_case(22, oracle.F32)
+    pool, st, H, K, V, T = c["pool"], c["st"], c["H"], c["K"], c["V"], c["T"]
+    snap = oracle.Pool(1, 5, H, K, V, st, st, oracle.KDA, pool.ssm.copy(), pool.conv.copy())
+    rings = oracle.Rings(pool, c["depth"])
+    pos = np.int32([7, 12, 1])
+    oracle.replay_verify(pool, rings, 0, c["slots"], pos, T, c["Lc"], c["x"], c["w"], c["g"], c["beta"])
+    sS, _, _ = oracle.spec_verify(snap, 0, c["slots"], T, c["Lc"], c["x"], c["w"], c["g"], c["beta"])
+    L = c["depth"]
+    for b, s in enumerate(c["slots"]):
+        S0 = oracle.to_f64(pool.ssm[0, s], st)
+        ent = [(pos[b] + t) % L for t in range(T)]
+        for m in range(1, T + 1):
+            for h in range(H):
+                al = np.exp(rings.g[0, s, h, ent[:m]].astype(np.float64))  # [m][K]
+                Sm = S0[h] * np.prod(al, axis=0)[None, :]
+                for j in range(m):
+                    later = np.prod(al[j + 1:], axis=0) if j + 1 < m else np.ones(K)
+                    kj = rings.k[0, s, h, ent[j]].astype(np.float64)
+                    dj = rings.d[0, s, h, ent[j]].astype(np.float64)
+                    Sm = Sm + np.outer(dj, kj * later)
+                ref = oracle.to_f64(sS[b, m - 1, h], st)
+                assert np.max(np.abs(Sm - ref)) <= 1e-5 * np.max(np.abs(ref)), (b, m, h)
+
+
+def test_replay_rawk_rawv_are_pre_norm_key_and_conv_value():
+    """rawk is the key before its L2 norm (k = rawk / sqrt(|rawk|^2 + eps)), rawv the conv'd
+    value channel of the head, g and beta the inputs as given."""
+    c = _replay_case(23, oracle.F32)
+    pool, H, K, V, T = c["pool"], c["H"], c["K"], c["V"], c["T"]
+    rings = oracle.Rings(pool, c["depth"])
+    pos = np.int32([2, 2, 2])
+    oracle.replay_verify(pool, rings, 0, c["slots"], pos, T, c["Lc"], c["x"], c["w"], c["g"], c["beta"])
+    D = pool.D
+    for b, s in enumerate(c["slots"]):
+        win = oracle.to_f64(pool.conv[0, s], oracle.F32).reshape(3, D)
+        _, y = oracle.conv_sequence(win, oracle.to_f64(c["x"][b], oracle.F32), c["w"])
+        for t in range(T):
+            e = (2 + t) % c["depth"]
+            for h in range(H):
+                rk = rings.rawk[0, s, h, e].astype(np.float64)
+                np.testing.assert_allclose(rk, y[t, H * K + h * K: H * K + (h + 1) * K], rtol=1e-6, atol=1e-7)
+                np.testing.assert_allclose(rings.rawv[0, s, h, e], y[t, 2 * H * K + h * V: 2 * H * K + (h + 1) * V],
+                                           rtol=1e-6, atol=1e-7)
+                kn = rk / np.sqrt(np.sum(rk * rk) + 1e-6)
+                np.testing.assert_allclose(rings.k[0, s, h, e], kn, rtol=1e-5, atol=1e-7)
+                assert np.array_equal(rings.g[0, s, h, e], c["g"][b, t, h])
+                assert rings.beta[0, s, h, e] == c["beta"][b, t, h]
+
+
+def test_replay_bf16_records_commit_within_tolerance():
+    """bf16 records (the pages' storage): commit(a) stays within the bf16 bar of the snapshot
+    path's commit(a)."""
+    c = _replay_case(24, oracle.BF16)
+    pool, st = c["pool"], c["st"]
+    snap = oracle.Pool(1, 5, c["H"], c["K"], c["V"], st, st, oracle.KDA, pool.ssm.copy(), pool.conv.copy())
+    rings = oracle.Rings(pool, c["depth"])
+    pos = np.int32([9, 0, 15])
+    accept = np.int32([4, 1, 3])
+    sC, _ = oracle.replay_verify(pool, rings, 0, c["slots"], pos, c["T"], c["Lc"], c["x"], c["w"],
+                                 c["g"], c["beta"])
+    oracle.replay_commit(pool, rings, 0, c["slots"], pos, c["T"], c["Lc"], sC, accept)
+    sS2, sC2, _ = oracle.spec_verify(snap, 0, c["slots"], c["T"], c["Lc"], c["x"], c["w"], c["g"], c["beta"])
+    oracle.spec_commit(snap, 0, c["slots"], c["T"], c["Lc"], sS2, sC2, accept)
+    assert np.array_equal(pool.conv, snap.conv)
+    a, e = oracle.to_f64(pool.ssm, st), oracle.to_f64(snap.ssm, st)
+    assert np.max(np.abs(a - e)) <= 2e-2 * np.max(np.abs(e))
+
+
+def test_replay_rejects_short_ring_and_bad_position():
+    c = _replay_case(25, oracle.F32, depth=8)  # 2 T = 10 > 8
+    rings = oracle.Rings(c["pool"], 8)
+    with pytest.raises(ValueError):
+        oracle.replay_verify(c["pool"], rings, 0, c["slots"], np.int32([0, 0, 0]), c["T"], c["Lc"],
+                             c["x"], c["w"], c["g"], c["beta"])
+    c = _replay_case(25, oracle.F32)
+    rings = oracle.Rings(c["pool"], 16)
+    with pytest.raises(ValueError):
+        oracle.replay_verify(c["pool"], rings, 0, c["slots"], np.int32([0, 16, 0]), c["T"], c["Lc"],
+                             c["x"], c["w"], c["g"], c["beta"])
+
+
 # ----------------------------------------------------------------------- pool layout
 
 def test_pool_bytes_reproduce_logged_sizes():
