@@ -55,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec or all/none")
+    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=69,
@@ -415,6 +415,52 @@ def leg_spec(dev, peaks, stream):
             "commit_frac": round(cb / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
+def leg_replay(dev, peaks, stream):
+    """ReplaySSM verify / commit on the speculative workload of leg_spec: verify writes ring
+    records (d, k, rawv, rawk, g, beta) instead of 8 states per request; commit replays the
+    accepted tokens from the slot state."""
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    from recurrent_state_cache_gb300 import binding as b, inputs
+    H, K, V, B, T, L, P = 12, 128, 128, 64, 8, 16, 320
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    D = H * (2 * K + V)
+    ssm = torch.empty((1, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    conv = torch.empty((1, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    pool = rsc.SlotPool(1, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
+    rings = rsc.ReplayRings(pool, L)
+    r = inputs.rng(4)
+    slots = torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev)
+    accept_np = inputs.accept_counts(r, B, T)
+    accept = torch.from_numpy(accept_np).to(dev)
+    pos = torch.from_numpy(inputs.rng(5).integers(0, L, B).astype("int32")).to(dev)
+    qkv = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((B, T, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((B, T, H), device=dev).normal_(0, 1, generator=gen))
+    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
+    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    spec_conv = torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev)
+    verify = lambda: rsc.kda_replay_verify_commit(pool, rings, 0, rsc.VERIFY, slots, pos, T, spec_conv,
+                                                  qkv, w, g, beta, out)
+    commit = lambda: rsc.kda_replay_verify_commit(pool, rings, 0, rsc.COMMIT, slots, pos, T, spec_conv,
+                                                  accept=accept)
+    ms_v = timed(verify, 10, 3, stream)
+    ms_c = timed(commit, 10, 3, stream)
+    S, Wb = H * V * K * 2, 3 * D * 2
+    rec = H * (2 * V * 2 + 2 * K * 2 + K * 4 + 4)   # one token's records over the heads
+    rep_ = H * (V * 2 + K * 2 + K * 4 + 4)          # what commit reads of one token's records
+    vb = B * (S + T * rec + Wb + T * Wb + T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2 + 8)
+    cb = int(2 * B * S + 2 * B * Wb + int(accept_np.astype("int64").sum() + B) * rep_ + 12 * B)
+    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), ring depth 16",
+            "verify_ms": round(ms_v, 4), "verify_bytes": vb,
+            "verify_gbs": round(vb / (ms_v * 1e-3) / 1e9, 1),
+            "verify_frac": round(vb / (ms_v * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "commit_ms": round(ms_c, 4), "commit_bytes": cb,
+            "commit_gbs": round(cb / (ms_c * 1e-3) / 1e9, 1),
+            "commit_frac": round(cb / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
 # --------------------------------------------------------------------------- oracle timing
 
 class OracleDecodeSample:
@@ -542,13 +588,15 @@ def main(argv=None):
     d2h = h_out.numel() * h_out.element_size()
 
     legs = {}
-    want = set(["gdn", "prefill", "copy", "spec"] if args.legs == "all" else
+    want = set(["gdn", "prefill", "copy", "spec", "replay"] if args.legs == "all" else
                ([] if args.legs == "none" else args.legs.split(",")))
     if "copy" in want:
         legs["slot_copy"] = leg_copy(dev, peaks, stream, wl)
     del graph
     if "spec" in want:
         legs["spec"] = leg_spec(dev, peaks, stream)
+    if "replay" in want:
+        legs["replay_spec"] = leg_replay(dev, peaks, stream)
     if "prefill" in want:
         legs["prefill"] = leg_prefill(dev, peaks, stream)
     del wl

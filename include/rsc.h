@@ -65,6 +65,7 @@ extern "C" {
                                 gate spans more than 160 in some channel; its split
                                 exponentials lose range and that chunk's result is not
                                 reliable (the gate must decay, g <= 0)                */
+#define RSC_DEVERR_RING   32 /* a ReplaySSM ring position outside [0, depth)            */
 
 typedef enum { RSC_F32 = 0, RSC_BF16 = 1 } rsc_dtype;
 typedef enum { RSC_GATE_KDA = 0, RSC_GATE_GDN = 1 } rsc_gate;
@@ -201,6 +202,44 @@ int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *s
                            const void *qkv, const float *conv_w, const float *g,
                            const float *beta, void *out, const int32_t *accept,
                            void *stream);
+
+/* ReplaySSM rings of a pool ([p1] ReplaySSM section: the (d, k, g) records rebuild the
+ * state from a checkpoint by the unrolled closed form, the (rawv, rawk, g, beta) records
+ * replay accepted tokens exactly; [p4] §4 replay buffer table: six ring buffers per KDA
+ * layer, depth L a power of two, L >= 2 x the tokens of one verify).  All device, owned by
+ * the caller, indexed like the pool by [layer][slot (P+1 rows)][head][entry 0..depth-1]:
+ *   d     [..][V]  state dtype   the delta beta (v - S k) the token wrote
+ *   k     [..][K]  state dtype   its L2-normalised key
+ *   rawv  [..][V]  state dtype   the value entering the delta rule (conv'd, before v - S k)
+ *   rawk  [..][K]  state dtype   the conv'd key before its L2 norm
+ *   g     [..][K] (KDA) or [..] (GDN)  fp32   its log-decay as given to the call
+ *   beta  [..]     fp32          its beta
+ * d, k, rawv, rawk, g must be 16-byte aligned, beta 4-byte aligned. */
+typedef struct {
+  int depth;
+  void *d, *k, *rawv, *rawk;
+  float *g, *beta;
+} rsc_replay_rings;
+
+/* ReplaySSM speculative verify / commit: the same contract as kda_spec_verify_commit, but
+ * verify keeps no per-token states.
+ *   VERIFY: for each request b run T tokens from its slot state (not modified); the records
+ *     of token t go to entry (ring_pos[b] + t) mod depth of the slot's rings; the window
+ *     after token t goes to spec_conv[b][t]; out[b][t] = o_t.  accept is ignored.
+ *   COMMIT: from the slot state replay tokens 0..accept[b] out of the rings in fp32
+ *     (k = rawk / sqrt(|rawk|^2 + eps), S <- S Diag(exp(g)), d = beta (rawv - S k),
+ *     S <- S + d k^T), store the state into the slot and the window snapshot
+ *     spec_conv[b][accept[b]].  qkv, conv_w, g, beta, out are ignored.
+ *   ring_pos  [batch] device int32 in [0, depth), the entry of each request's token 0;
+ *             advancing it between rounds is the caller's (RSC_DEVERR_RING if outside)
+ *   spec_conv [batch][depth][3][D] device, conv dtype;  other arrays as in
+ *   kda_spec_verify_commit;  1 <= T, 2 T <= depth, depth a power of two <= 4096.
+ * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ECUDA. */
+int kda_replay_verify_commit(rsc_pool *pool, const rsc_replay_rings *rings, int layer, int mode,
+                             const int32_t *slot_ids, const int32_t *ring_pos, int batch, int T,
+                             void *spec_conv, const void *qkv, const float *conv_w,
+                             const float *g, const float *beta, void *out,
+                             const int32_t *accept, void *stream);
 
 /* Read the pool's device error word into *code and clear it.  Synchronises `stream`.
  * Errors: RSC_EINVAL, RSC_ECUDA. */

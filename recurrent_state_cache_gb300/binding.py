@@ -20,7 +20,7 @@ VERIFY, COMMIT = 0, 1
 
 RSC_OK, RSC_EINVAL, RSC_ERANGE, RSC_EDTYPE, RSC_EALIGN, RSC_ECUDA, RSC_ENOSPACE = (
     0, -1, -2, -3, -4, -5, -6)
-DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ, DEVERR_TIMEOUT, DEVERR_GATE = 1, 2, 4, 8, 16
+DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ, DEVERR_TIMEOUT, DEVERR_GATE, DEVERR_RING = 1, 2, 4, 8, 16, 32
 
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -28,7 +28,8 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
-           "kda_spec_verify_commit", "rsc_get_device_error", "rsc_status_string")
+           "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
+           "rsc_status_string")
 
 
 class RscError(RuntimeError):
@@ -46,6 +47,14 @@ class PoolDesc(ctypes.Structure):
         ("gate", ctypes.c_int32),
         ("ssm_base", ctypes.c_void_p), ("conv_base", ctypes.c_void_p),
         ("dev_error", ctypes.c_void_p),
+    ]
+
+
+class ReplayRingsDesc(ctypes.Structure):
+    _fields_ = [
+        ("depth", ctypes.c_int32),
+        ("d", ctypes.c_void_p), ("k", ctypes.c_void_p), ("rawv", ctypes.c_void_p),
+        ("rawk", ctypes.c_void_p), ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
     ]
 
 
@@ -80,6 +89,8 @@ def lib():
         L.ssm_slot_copy.argtypes = [vp, i32, vp, vp, vp, i32, vp]
         L.kda_spec_verify_commit.argtypes = [vp, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp,
                                              vp, vp, vp, vp, vp]
+        L.kda_replay_verify_commit.argtypes = [vp, ctypes.POINTER(ReplayRingsDesc), i32, i32,
+                                               vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.rsc_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         L.rsc_status_string.argtypes = [i32]
         L.rsc_status_string.restype = ctypes.c_char_p
@@ -293,6 +304,56 @@ def kda_spec_verify_commit(pool: SlotPool, layer, mode, slot_ids, T, L, spec_ssm
                                         _p(spec_ssm), _p(spec_conv), _p(qkv), _p(conv_w), _p(g),
                                         _p(beta), _p(out), _p(accept), _stream(stream)),
            "kda_spec_verify_commit")
+    return out
+
+
+class ReplayRings:
+    """ReplaySSM rings of a pool, allocated by torch ([layers][slots+1][H][depth][n]):
+    d, rawv [..][V] and k, rawk [..][K] in the state dtype; g [..][K] (KDA) or [..] (GDN)
+    and beta [..] in fp32."""
+
+    def __init__(self, pool: SlotPool, depth: int):
+        L, R, H, K, V = pool.num_layers, pool.num_slots + 1, pool.H, pool.K, pool.V
+        sd, dev = TORCH_DTYPE[pool.state_dtype], pool.device
+        self.depth = depth
+        self.d = torch.zeros((L, R, H, depth, V), dtype=sd, device=dev)
+        self.k = torch.zeros((L, R, H, depth, K), dtype=sd, device=dev)
+        self.rawv = torch.zeros((L, R, H, depth, V), dtype=sd, device=dev)
+        self.rawk = torch.zeros((L, R, H, depth, K), dtype=sd, device=dev)
+        gshape = (L, R, H, depth, K) if pool.gate == KDA else (L, R, H, depth)
+        self.g = torch.zeros(gshape, dtype=torch.float32, device=dev)
+        self.beta = torch.zeros((L, R, H, depth), dtype=torch.float32, device=dev)
+
+    def desc(self) -> ReplayRingsDesc:
+        return ReplayRingsDesc(self.depth, self.d.data_ptr(), self.k.data_ptr(),
+                               self.rawv.data_ptr(), self.rawk.data_ptr(), self.g.data_ptr(),
+                               self.beta.data_ptr())
+
+
+def kda_replay_verify_commit(pool: SlotPool, rings: ReplayRings, layer, mode, slot_ids, ring_pos,
+                             T, spec_conv, qkv=None, conv_w=None, g=None, beta=None, out=None,
+                             accept=None, stream=None):
+    B = slot_ids.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(ring_pos, "ring_pos", torch.int32, (B,), dev)
+    _need(spec_conv, "spec_conv", pool.io_dtype, (B, rings.depth, 3, pool.D), dev)
+    if mode == VERIFY:
+        _need(qkv, "qkv", pool.io_dtype, (B, T, pool.D), dev)
+        _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+        _need(g, "g", torch.float32, pool.gate_shape((B, T)), dev)
+        _need(beta, "beta", torch.float32, (B, T, pool.H), dev)
+        if out is None:
+            out = torch.empty((B, T, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+        _need(out, "out", pool.io_dtype, (B, T, pool.H, pool.V), dev)
+    else:
+        _need(accept, "accept", torch.int32, (B,), dev)
+    d = rings.desc()
+    _check(lib().kda_replay_verify_commit(pool.handle, ctypes.byref(d), layer, mode,
+                                          _p(slot_ids), _p(ring_pos), B, T, _p(spec_conv),
+                                          _p(qkv), _p(conv_w), _p(g), _p(beta), _p(out),
+                                          _p(accept), _stream(stream)),
+           "kda_replay_verify_commit")
     return out
 
 

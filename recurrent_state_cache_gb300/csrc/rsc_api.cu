@@ -178,6 +178,41 @@ int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *s
                                  beta, out, as_stream(stream));
 }
 
+int kda_replay_verify_commit(rsc_pool *pool, const rsc_replay_rings *rings, int layer, int mode,
+                             const int32_t *slot_ids, const int32_t *ring_pos, int batch, int T,
+                             void *spec_conv, const void *qkv, const float *conv_w,
+                             const float *g, const float *beta, void *out,
+                             const int32_t *accept, void *stream) {
+  if (!pool || !rings) return RSC_EINVAL;
+  if (mode != RSC_SPEC_VERIFY && mode != RSC_SPEC_COMMIT) return RSC_EINVAL;
+  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
+    return RSC_ERANGE;
+  const int L = rings->depth;
+  if (L < 2 || L > 4096 || (L & (L - 1)) != 0 || T < 1 || 2 * T > L) return RSC_ERANGE;
+  if (batch == 0) return RSC_OK;
+  if (!slot_ids || !ring_pos || !spec_conv || !rings->d || !rings->k || !rings->rawv ||
+      !rings->rawk || !rings->g || !rings->beta)
+    return RSC_EINVAL;
+  if (!aligned(spec_conv, 16) || !aligned(slot_ids, 4) || !aligned(ring_pos, 4) ||
+      !aligned(rings->d, 16) || !aligned(rings->k, 16) || !aligned(rings->rawv, 16) ||
+      !aligned(rings->rawk, 16) || !aligned(rings->g, 16) || !aligned(rings->beta, 4))
+    return RSC_EALIGN;
+  const rsc::LayerArgs a = layer_args(pool, layer);
+  const rsc::RingView rv{rings->d, rings->k, rings->rawv, rings->rawk, rings->g, rings->beta, L};
+  if (mode == RSC_SPEC_COMMIT) {
+    if (!accept) return RSC_EINVAL;
+    if (!aligned(accept, 4)) return RSC_EALIGN;
+    return rsc::launch_replay_commit(a, rv, slot_ids, ring_pos, batch, T, spec_conv, accept,
+                                     as_stream(stream));
+  }
+  if (!qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
+      !aligned(beta, 4))
+    return RSC_EALIGN;
+  return rsc::launch_replay_verify(a, rv, slot_ids, ring_pos, batch, T, spec_conv, qkv, conv_w,
+                                   g, beta, out, as_stream(stream));
+}
+
 int rsc_get_device_error(rsc_pool *pool, int32_t *code, void *stream) {
   if (!pool || !code) return RSC_EINVAL;
   cudaStream_t s = as_stream(stream);

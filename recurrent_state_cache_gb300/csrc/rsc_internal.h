@@ -29,6 +29,20 @@ int launch_spec_commit(const LayerArgs &a, const int32_t *slots, int B, int T, i
                        const void *spec_ssm, const void *spec_conv, const int32_t *accept,
                        cudaStream_t s);
 
+// ReplaySSM rings of the pool ([layer][P+1][H][depth][n]); see rsc_replay_rings.
+struct RingView {
+  void *d, *k, *rawv, *rawk;  // state dtype
+  float *g, *beta;
+  int depth;
+};
+int launch_replay_verify(const LayerArgs &a, const RingView &rv, const int32_t *slots,
+                         const int32_t *pos, int B, int T, void *spec_conv, const void *qkv,
+                         const float *conv_w, const float *g, const float *beta, void *out,
+                         cudaStream_t s);
+int launch_replay_commit(const LayerArgs &a, const RingView &rv, const int32_t *slots,
+                         const int32_t *pos, int B, int T, const void *spec_conv,
+                         const int32_t *accept, cudaStream_t s);
+
 int launch_slot_copy(const PoolView &pv, int st, int io, int layer0, int nlayers,
                      const int32_t *src, const int32_t *dst, const uint8_t *mask, int n,
                      cudaStream_t s);

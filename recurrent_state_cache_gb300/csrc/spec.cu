@@ -16,18 +16,24 @@
 // Each window channel of a cache entry is written by exactly one CTA (q/k channels
 // partitioned over the NVT tiles of the head, value channels by tile), each S entry
 // tile by its owner.
+//
+// REPLAY (ReplaySSM, same page, ReplaySSM section): the same pass, but instead of S_t each
+// token leaves its records in the slot's rings at entry (pos + t) mod depth: the delta d
+// (rows of the tile, by their owner), the normalised key, the pre-norm key (the CTA owning
+// the key channels' windows), the log-decay and beta (tile 0).  COMMIT of the replay path
+// replays the accepted tokens from the slot state out of those records.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
 namespace rsc {
 
-template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE, bool REPLAY>
 __global__ void __launch_bounds__(NW * 32)
 kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
                        int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
                        const IO *__restrict__ qkv, const float *__restrict__ conv_w,
                        const float *__restrict__ g, const float *__restrict__ beta,
-                       IO *__restrict__ out) {
+                       IO *__restrict__ out, RingView rv, const int32_t *__restrict__ pos) {
   constexpr int VT = V / NVT;
   // one 16-byte vector per lane and pass (two were measured slower: 109 vs 66 us at the
   // speculative workload)
@@ -65,6 +71,16 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     return;
   }
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+  int p0 = 0;  // ring entry of token 0 (replay)
+  if constexpr (REPLAY) {
+    p0 = pos[b];
+    if (p0 < 0 || p0 >= rv.depth) {
+      if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_RING);
+      return;
+    }
+  }
+  // ring entry of token t of this (layer, slot, head)
+  auto ent = [&](int t) { return (prow * H + h) * (size_t)rv.depth + ((p0 + t) & (rv.depth - 1)); };
 
   auto stage = [&](int buf, int t0) {
     const int cnt = min(TS, T - t0);
@@ -134,18 +150,24 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         const int i2 = tid + u * NT;
         if (i2 >= 2 * K) continue;
         const IO xc = s_xqk[cur][tau][i2];
-        s_qk[tau][i2] = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
+        const float y = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]),
                               to_f32(xc));
+        s_qk[tau][i2] = y;
         win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
         if (i2 >= j * OWN && i2 < (j + 1) * OWN) {
           E[cqk[u]] = win[u][0]; E[D + cqk[u]] = win[u][1]; E[2 * D + cqk[u]] = win[u][2];
+          if constexpr (REPLAY)
+            if (i2 >= K) static_cast<ST *>(rv.rawk)[ent(t0 + tau) * K + (i2 - K)] = from_f32<ST>(y);
         }
       }
       if (tid < VT) {
         const IO xc = s_xv[cur][tau][tid];
-        s_v[tau][tid] = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
+        const float y = conv4(wtv, to_f32(winv[0]), to_f32(winv[1]), to_f32(winv[2]), to_f32(xc));
+        s_v[tau][tid] = y;
         winv[0] = winv[1]; winv[1] = winv[2]; winv[2] = xc;
         E[cv] = winv[0]; E[D + cv] = winv[1]; E[2 * D + cv] = winv[2];
+        if constexpr (REPLAY)
+          static_cast<ST *>(rv.rawv)[ent(t0 + tau) * V + (size_t)j * VT + tid] = from_f32<ST>(y);
       }
     }
     if (GATE == RSC_GATE_KDA) {
@@ -172,6 +194,19 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       if (lane == 0) s_kq[tau] = qk * rq * rk;
     }
     __syncthreads();
+    if constexpr (REPLAY) {
+      // the block's normalised keys (owner of the key channels), log-decays and betas (tile 0)
+      for (int i = tid; i < cnt * 2 * K; i += NT) {
+        const int tau = i / (2 * K), i2 = i % (2 * K);
+        if (i2 >= K && i2 >= j * OWN && i2 < (j + 1) * OWN)
+          static_cast<ST *>(rv.k)[ent(t0 + tau) * K + (i2 - K)] = from_f32<ST>(s_qk[tau][i2]);
+      }
+      if (j == 0) {
+        for (int i = tid; i < cnt * GW; i += NT)
+          rv.g[ent(t0 + i / GW) * GW + i % GW] = s_g[cur][i / GW][i % GW];
+        if (tid < cnt) rv.beta[ent(t0 + tid)] = s_b[cur][tid];
+      }
+    }
 
     // the block's tokens: delta rule on the register tile, no barrier inside
     for (int tau = 0; tau < cnt; ++tau) {
@@ -185,9 +220,19 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
       }
       float o[G::NP];
-      delta_rule_tile<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
-      ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
-      tile_store<ST, K, VT, VPL, NW>(Se, s);
+      if constexpr (REPLAY) {
+        float dd[G::NP];
+        delta_rule_tile_d<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, dd);
+        if (k0 == 0) {
+          ST *dr = static_cast<ST *>(rv.d) + ent(t) * V + (size_t)j * VT;
+#pragma unroll
+          for (int p = 0; p < G::NP; ++p) dr[G::row(p)] = from_f32<ST>(dd[p]);
+        }
+      } else {
+        delta_rule_tile<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
+        ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
+        tile_store<ST, K, VT, VPL, NW>(Se, s);
+      }
       if (k0 == 0) {
         IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
 #pragma unroll
@@ -214,10 +259,10 @@ struct VerifyLaunch {
     constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
     constexpr int NW = RSC_VERIFY_WARPS;
     dim3 grid(NVT, a->pv.H, B);
-    kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE><<<grid, NW * 32, 0, s>>>(
+    kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE, false><<<grid, NW * 32, 0, s>>>(
         a->pv, a->layer, slots, T, L, static_cast<ST *>(spec_ssm),
         static_cast<IO *>(spec_conv), static_cast<const IO *>(qkv), conv_w, g, beta,
-        static_cast<IO *>(out));
+        static_cast<IO *>(out), RingView{}, nullptr);
     return launch_status();
   }
 };
@@ -228,6 +273,165 @@ int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, i
                        cudaStream_t s) {
   return dispatch_all<VerifyLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, T, L,
                                     spec_ssm, spec_conv, qkv, conv_w, g, beta, out, s);
+}
+
+template <typename ST, typename IO, int K, int V, int GATE>
+struct ReplayVerifyLaunch {
+  static int run(const LayerArgs *a, const RingView *rv, const int32_t *slots, const int32_t *pos,
+                 int B, int T, void *spec_conv, const void *qkv, const float *conv_w,
+                 const float *g, const float *beta, void *out, cudaStream_t s) {
+    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
+    constexpr int NW = RSC_VERIFY_WARPS;
+    dim3 grid(NVT, a->pv.H, B);
+    kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE, true><<<grid, NW * 32, 0, s>>>(
+        a->pv, a->layer, slots, T, rv->depth, nullptr, static_cast<IO *>(spec_conv),
+        static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), *rv, pos);
+    return launch_status();
+  }
+};
+
+int launch_replay_verify(const LayerArgs &a, const RingView &rv, const int32_t *slots,
+                         const int32_t *pos, int B, int T, void *spec_conv, const void *qkv,
+                         const float *conv_w, const float *g, const float *beta, void *out,
+                         cudaStream_t s) {
+  return dispatch_all<ReplayVerifyLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, &rv, slots,
+                                          pos, B, T, spec_conv, qkv, conv_w, g, beta, out, s);
+}
+
+// ReplaySSM COMMIT: one CTA per (row tile, head, request).  The tile of the slot's state is
+// loaded into registers, tokens 0..accept[b] are replayed from the rings eight at a time
+// (their pre-norm keys, log-decays, this tile's value rows and betas staged by cp.async; the
+// key norms and exp(g) of the block computed before its token loop), and the tile is stored
+// back.  The CTA also restores its share of the window from snapshot accept[b] (the same
+// channel ownership as the verify pass), so every byte of the slot has one writer.
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
+__global__ void __launch_bounds__(NW * 32)
+kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__restrict__ slots,
+                         const int32_t *__restrict__ pos, int T, const IO *__restrict__ spec_conv,
+                         const int32_t *__restrict__ accept) {
+  constexpr int VT = V / NVT;
+  constexpr int VPL = 1;
+  constexpr int NT = NW * 32;
+  using G = TileGeom<ST, K, VT, NW, VPL>;
+  constexpr int OWN = 2 * K / NVT;
+  constexpr int TS = 8;
+  constexpr int GW = GATE == RSC_GATE_KDA ? K : 1;
+  constexpr int XS = 16 / sizeof(ST);  // state-dtype elements per 16-byte copy
+  static_assert(K % XS == 0 && VT % XS == 0, "16-byte staging");
+  __shared__ __align__(16) ST s_rk[TS][K];
+  __shared__ __align__(16) ST s_rv[TS][VT];
+  __shared__ __align__(16) float s_g[TS][GW];
+  __shared__ float s_b[TS];
+  __shared__ __align__(16) float s_kh[TS][K];
+  __shared__ float s_v[TS][VT];
+  __shared__ __align__(16) float s_al[TS][GW];
+
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = pv.H, D = pv.D;
+  const int slot = slots[b], acc = accept[b], p0 = pos[b];
+  const bool bad_slot = slot < 0 || slot > pv.P, bad_acc = acc < 0 || acc >= T;
+  const bool bad_pos = p0 < 0 || p0 >= rv.depth;
+  if (bad_slot || bad_acc || bad_pos) {
+    if (tid == 0 && j == 0 && h == 0)
+      flag_error(pv.err, (bad_slot ? RSC_DEVERR_SLOT : 0) | (bad_acc ? RSC_DEVERR_ACCEPT : 0) |
+                             (bad_pos ? RSC_DEVERR_RING : 0));
+    return;
+  }
+  const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+  auto ent = [&](int t) { return (prow * H + h) * (size_t)rv.depth + ((p0 + t) & (rv.depth - 1)); };
+  const int n = acc + 1;  // tokens to replay
+
+  ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
+  float s[G::NP][G::EPL];
+  tile_load<ST, K, VT, VPL, NW>(S, s);
+  const int k0 = G::kofs();
+
+  for (int t0 = 0; t0 < n; t0 += TS) {
+    const int cnt = min(TS, n - t0);
+    __syncthreads();  // the previous block's readers are done
+    for (int i = tid; i < cnt * (K / XS); i += NT) {
+      const int tau = i / (K / XS), c = (i % (K / XS)) * XS;
+      cp_async16(&s_rk[tau][c], static_cast<const ST *>(rv.rawk) + ent(t0 + tau) * K + c);
+    }
+    for (int i = tid; i < cnt * (VT / XS); i += NT) {
+      const int tau = i / (VT / XS), c = (i % (VT / XS)) * XS;
+      cp_async16(&s_rv[tau][c], static_cast<const ST *>(rv.rawv) + ent(t0 + tau) * V + (size_t)j * VT + c);
+    }
+    if (GATE == RSC_GATE_KDA) {
+      for (int i = tid; i < cnt * (K / 4); i += NT) {
+        const int tau = i / (K / 4), c = (i % (K / 4)) * 4;
+        cp_async16(&s_g[tau][c], rv.g + ent(t0 + tau) * K + c);
+      }
+    } else if (tid < cnt) {
+      cp_async4(&s_g[tid][0], rv.g + ent(t0 + tid));
+    }
+    if (tid < cnt) cp_async4(&s_b[tid], rv.beta + ent(t0 + tid));
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // normalised keys (a warp per token), alpha = exp(g), value rows to fp32
+    for (int tau = warp; tau < cnt; tau += NW) {
+      float kk = 0.f;
+#pragma unroll
+      for (int e = 0; e < K / 32; ++e) {
+        const float x = to_f32(s_rk[tau][lane + 32 * e]);
+        kk = fmaf(x, x, kk);
+      }
+      kk = group_sum<32>(kk);
+      const float rk = 1.0f / sqrtf(kk + kNormEps);
+#pragma unroll
+      for (int e = 0; e < K / 32; ++e) s_kh[tau][lane + 32 * e] = to_f32(s_rk[tau][lane + 32 * e]) * rk;
+    }
+    if (GATE == RSC_GATE_KDA) {
+      for (int i = tid; i < cnt * K; i += NT) s_al[i / K][i % K] = expf(s_g[i / K][i % K]);
+    } else if (tid < cnt) {
+      s_al[tid][0] = expf(s_g[tid][0]);
+    }
+    for (int i = tid; i < cnt * VT; i += NT) s_v[i / VT][i % VT] = to_f32(s_rv[i / VT][i % VT]);
+    __syncthreads();
+    for (int tau = 0; tau < cnt; ++tau) {
+      float kh[G::EPL], al[G::EPL];
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) {
+        kh[e] = s_kh[tau][k0 + e];
+        al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
+      }
+      delta_rule_tile_replay<ST, K, VT, VPL, NW>(s, kh, al, s_b[tau], s_v[tau]);
+    }
+  }
+  tile_store<ST, K, VT, VPL, NW>(S, s);
+
+  // window <- snapshot acc: this CTA's q/k channels of the head and its value channels
+  const IO *E = spec_conv + ((size_t)b * rv.depth + acc) * 3 * (size_t)D;
+  IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
+  for (int i = tid; i < 3 * (OWN + VT); i += NT) {
+    const int row = i / (OWN + VT), c = i % (OWN + VT);
+    const int i2 = j * OWN + c;
+    const int ch = c < OWN ? (i2 < K ? h * K + i2 : H * K + h * K + (i2 - K))
+                           : 2 * H * K + h * V + j * VT + (c - OWN);
+    W[(size_t)row * D + ch] = E[(size_t)row * D + ch];
+  }
+}
+
+template <typename ST, typename IO, int K, int V, int GATE>
+struct ReplayCommitLaunch {
+  static int run(const LayerArgs *a, const RingView *rv, const int32_t *slots, const int32_t *pos,
+                 int B, int T, const void *spec_conv, const int32_t *accept, cudaStream_t s) {
+    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
+    constexpr int NW = RSC_VERIFY_WARPS;
+    dim3 grid(NVT, a->pv.H, B);
+    kda_replay_commit_kernel<ST, IO, K, V, NVT, NW, GATE><<<grid, NW * 32, 0, s>>>(
+        a->pv, *rv, a->layer, slots, pos, T, static_cast<const IO *>(spec_conv), accept);
+    return launch_status();
+  }
+};
+
+int launch_replay_commit(const LayerArgs &a, const RingView &rv, const int32_t *slots,
+                         const int32_t *pos, int B, int T, const void *spec_conv,
+                         const int32_t *accept, cudaStream_t s) {
+  return dispatch_all<ReplayCommitLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, &rv, slots,
+                                          pos, B, T, spec_conv, accept, s);
 }
 
 // COMMIT: slot <- cache entry accept[b], the state rows (blockIdx.z == 0) and the window

@@ -86,6 +86,24 @@ def test_calls_reject_bad_arguments_before_launch(rsc):
                                         None) == rsc.RSC_EINVAL
         assert L.kda_spec_verify_commit(h, 0, 1, p, 1, 2, 8, p, p, None, None, None, None,
                                         None, None, None) == rsc.RSC_EINVAL  # no accept
+        # replay: ring too short for T (2 T > depth), depth not a power of two, no rings,
+        # misaligned ring array, no ring positions
+        R = rsc.ReplayRingsDesc(16, 0x50000, 0x50000, 0x50000, 0x50000, 0x50000, 0x50000)
+        rr = ctypes.byref(R)
+        assert L.kda_replay_verify_commit(h, rr, 0, 0, p, p, 1, 9, p, p, p, p, p, p, None,
+                                          None) == rsc.RSC_ERANGE
+        R12 = rsc.ReplayRingsDesc(12, 0x50000, 0x50000, 0x50000, 0x50000, 0x50000, 0x50000)
+        assert L.kda_replay_verify_commit(h, ctypes.byref(R12), 0, 0, p, p, 1, 2, p, p, p, p, p,
+                                          p, None, None) == rsc.RSC_ERANGE
+        assert L.kda_replay_verify_commit(h, None, 0, 0, p, p, 1, 2, p, p, p, p, p, p, None,
+                                          None) == rsc.RSC_EINVAL
+        Rm = rsc.ReplayRingsDesc(16, 0x50008, 0x50000, 0x50000, 0x50000, 0x50000, 0x50000)
+        assert L.kda_replay_verify_commit(h, ctypes.byref(Rm), 0, 0, p, p, 1, 2, p, p, p, p, p,
+                                          p, None, None) == rsc.RSC_EALIGN
+        assert L.kda_replay_verify_commit(h, rr, 0, 0, p, None, 1, 2, p, p, p, p, p, p, None,
+                                          None) == rsc.RSC_EINVAL
+        assert L.kda_replay_verify_commit(h, rr, 0, 1, p, p, 1, 2, p, None, None, None, None,
+                                          None, None, None) == rsc.RSC_EINVAL  # no accept
         # copy: layer below -1
         assert L.ssm_slot_copy(h, -2, p, p, None, 1, None) == rsc.RSC_ERANGE
         assert L.ssm_slot_copy(h, -1, None, None, None, 0, None) == 0

@@ -180,6 +180,91 @@ def test_spec_commit_bad_accept_flags(cuda_dev):
     assert np.all(widen(now[0, 1]) == 1.0)
 
 
+# ------------------------------------------------------------------ ReplaySSM
+
+def _rings_np(rings):
+    return {n: to_np(getattr(rings, n)) for n in ("d", "k", "rawv", "rawk", "g", "beta")}
+
+
+@pytest.mark.parametrize("st,io,gate,K,V", [
+    (0, 0, rsc.KDA, 64, 64), (1, 1, rsc.KDA, 128, 128), (1, 1, rsc.GDN, 128, 128),
+    (0, 1, rsc.KDA, 128, 64), (1, 0, rsc.KDA, 64, 128),
+])
+def test_replay_verify_commit_parity(cuda_dev, st, io, gate, K, V):
+    """Verify: outputs and ring records match the oracle, windows bit-exact, slot untouched;
+    commit: the replayed state matches the oracle's replay, windows bit-exact."""
+    H, B, T, depth = 2, 3, 5, 16
+    c = Case(cuda_dev, 31, L=2, P=6, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    slots = np.int32([5, 2, 4])
+    pos = np.int32([0, 9, 14])  # the last request wraps around its ring
+    x = c.proj((B, T))
+    g, beta = c.gates((B, T))
+    rings_ref = oracle.Rings(c.ref, depth)
+    sC_ref, o_ref = oracle.replay_verify(c.ref, rings_ref, 1, slots, pos, T, depth, x, c.w, g, beta)
+    rings = rsc.ReplayRings(c.pool, depth)
+    spec_conv = torch.zeros((B, depth, 3, c.D), dtype=c.pool.io_dtype, device=c.dev)
+    before = to_np(c.pool.ssm).copy(), to_np(c.pool.conv).copy()
+    slots_d, pos_d = to_dev(slots, c.dev), to_dev(pos, c.dev)
+    o = rsc.kda_replay_verify_commit(c.pool, rings, 1, rsc.VERIFY, slots_d, pos_d, T, spec_conv,
+                                     to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
+    assert np.array_equal(to_np(c.pool.ssm), before[0]) and np.array_equal(to_np(c.pool.conv), before[1])
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(st, io)
+    assert np.array_equal(to_np(spec_conv)[:, :T], sC_ref[:, :T])
+    got = _rings_np(rings)
+    for name in ("d", "k", "rawv", "rawk"):
+        assert max_rel_err(widen(got[name]), widen(getattr(rings_ref, name))) <= TOL[st], name
+    g_ref = rings_ref.g if gate == rsc.KDA else rings_ref.g[..., 0]
+    assert np.array_equal(got["g"], g_ref) and np.array_equal(got["beta"], rings_ref.beta)
+    assert rsc.rsc_get_device_error(c.pool) == 0
+    accept = np.int32([0, 4, 2])
+    rsc.kda_replay_verify_commit(c.pool, rings, 1, rsc.COMMIT, slots_d, pos_d, T, spec_conv,
+                                 accept=to_dev(accept, c.dev))
+    oracle.replay_commit(c.ref, rings_ref, 1, slots, pos, T, depth, sC_ref, accept)
+    c.check_pool()
+
+
+@pytest.mark.parametrize("st", [0, 1])
+def test_replay_commit_lands_on_the_snapshot_commit(cuda_dev, st):
+    """On the GPU, the replay path's commit(a) and the snapshot path's commit(a) agree (both
+    from the same slot state and inputs): to fp32 rounding with fp32 records, to the bf16 bar
+    with bf16 records; windows bit-exact."""
+    H, K, V, B, T, depth = 2, 128, 128, 4, 8, 16
+    c = Case(cuda_dev, 32, L=1, P=8, H=H, K=K, V=V, st=st, io=st, gate=rsc.KDA)
+    c2 = Case(cuda_dev, 32, L=1, P=8, H=H, K=K, V=V, st=st, io=st, gate=rsc.KDA)  # same seed
+    slots = to_dev(np.int32([7, 1, 3, 5]), c.dev)
+    pos = to_dev(np.int32([3, 8, 15, 0]), c.dev)
+    x = c.proj((B, T))
+    g, beta = c.gates((B, T))
+    accept = to_dev(np.int32([7, 0, 3, 5]), c.dev)
+    args = (to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
+    rings = rsc.ReplayRings(c.pool, depth)
+    sc1 = torch.zeros((B, depth, 3, c.D), dtype=c.pool.io_dtype, device=c.dev)
+    rsc.kda_replay_verify_commit(c.pool, rings, 0, rsc.VERIFY, slots, pos, T, sc1, *args)
+    rsc.kda_replay_verify_commit(c.pool, rings, 0, rsc.COMMIT, slots, pos, T, sc1, accept=accept)
+    ss2 = torch.zeros((B, depth, H, V, K), dtype=c2.pool.ssm.dtype, device=c.dev)
+    sc2 = torch.zeros((B, depth, 3, c.D), dtype=c2.pool.io_dtype, device=c.dev)
+    rsc.kda_spec_verify_commit(c2.pool, 0, rsc.VERIFY, slots, T, depth, ss2, sc2, *args)
+    rsc.kda_spec_verify_commit(c2.pool, 0, rsc.COMMIT, slots, T, depth, ss2, sc2, accept=accept)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(c.pool.conv), to_np(c2.pool.conv))
+    bar = 1e-5 if st == 0 else TOL[1]
+    assert max_rel_err(widen(to_np(c.pool.ssm)), widen(to_np(c2.pool.ssm))) <= bar
+    assert rsc.rsc_get_device_error(c.pool) == 0 and rsc.rsc_get_device_error(c2.pool) == 0
+
+
+def test_replay_bad_ring_position_flags(cuda_dev):
+    c = Case(cuda_dev, 33, L=1, P=4, H=1, K=64, V=64, st=1, io=1, gate=rsc.KDA)
+    B, T, depth = 2, 3, 8
+    rings = rsc.ReplayRings(c.pool, depth)
+    spec_conv = torch.zeros((B, depth, 3, c.D), dtype=c.pool.io_dtype, device=c.dev)
+    before = to_np(c.pool.ssm).copy()
+    slots = to_dev(np.int32([1, 2]), c.dev)
+    rsc.kda_replay_verify_commit(c.pool, rings, 0, rsc.COMMIT, slots, to_dev(np.int32([0, depth]), c.dev),
+                                 T, spec_conv, accept=to_dev(np.int32([1, 1]), c.dev))
+    assert rsc.rsc_get_device_error(c.pool) == rsc.binding.DEVERR_RING
+    assert np.array_equal(to_np(c.pool.ssm)[0, 2], before[0, 2])
+
+
 # ------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("st,io,gate,K,V,lens,init", [
