@@ -153,6 +153,73 @@ __device__ __forceinline__ void delta_rule_tile_replay(
   }
 }
 
+// ---- the same on a tile held as fp32 pairs: each lane's EPL elements of a row as EPL/2
+// float2, updated with the packed fp32 instructions (two lanes of arithmetic per issue).
+template <typename ST, int K, int VT, int NW = 4, int VPL = 1>
+using Tile2 = float2[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL / 2];
+
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
+__device__ __forceinline__ void tile_load2(const ST *base, Tile2<ST, K, VT, NW, VPL> &s) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
+  constexpr int N16 = VecTraits<ST>::N;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p)
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float x[N16];
+      unpack16(ld16_stream(base + (size_t)G::row(p) * K + G::kofs() + v * N16), x);
+#pragma unroll
+      for (int e = 0; e < N16 / 2; ++e) s[p][v * N16 / 2 + e] = make_float2(x[2 * e], x[2 * e + 1]);
+    }
+}
+
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
+__device__ __forceinline__ void tile_store2(ST *base, const Tile2<ST, K, VT, NW, VPL> &s) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
+  constexpr int N16 = VecTraits<ST>::N;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p)
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float x[N16];
+#pragma unroll
+      for (int e = 0; e < N16 / 2; ++e) {
+        x[2 * e] = s[p][v * N16 / 2 + e].x;
+        x[2 * e + 1] = s[p][v * N16 / 2 + e].y;
+      }
+      st16(base + (size_t)G::row(p) * K + G::kofs() + v * N16, pack16(x));
+    }
+}
+
+// One token on every row of a pair tile.  Returns o (row outputs, S_new q_hat) and, when
+// dd is given, each row's delta.  qh/kh/al are this lane's EPL/2 pairs of q_hat, k_hat, alpha.
+template <typename ST, int K, int VT, int VPL = 1, int NW = 4, bool WITH_Q = true>
+__device__ __forceinline__ void delta_rule_tile2(
+    Tile2<ST, K, VT, NW, VPL> &s, const float2 (&qh)[TileGeom<ST, K, VT, NW, VPL>::EPL / 2],
+    const float2 (&kh)[TileGeom<ST, K, VT, NW, VPL>::EPL / 2],
+    const float2 (&al)[TileGeom<ST, K, VT, NW, VPL>::EPL / 2], float beta, float kq,
+    const float *v_rows, float *o, float *dd) {
+  using G = TileGeom<ST, K, VT, NW, VPL>;
+  constexpr int E2 = G::EPL / 2;
+#pragma unroll
+  for (int p = 0; p < G::NP; ++p) {
+    float2 u2 = make_float2(0.f, 0.f), w2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < E2; ++e) {
+      s[p][e] = __fmul2_rn(s[p][e], al[e]);
+      u2 = __ffma2_rn(s[p][e], kh[e], u2);
+      if (WITH_Q) w2 = __ffma2_rn(s[p][e], qh[e], w2);
+    }
+    const float u = group_sum<G::LPR>(u2.x + u2.y);
+    const float d = beta * (v_rows[G::row(p)] - u);
+    const float2 d2 = make_float2(d, d);
+#pragma unroll
+    for (int e = 0; e < E2; ++e) s[p][e] = __ffma2_rn(d2, kh[e], s[p][e]);
+    if (WITH_Q) o[p] = fmaf(d, kq, group_sum<G::LPR>(w2.x + w2.y));
+    if (dd) dd[p] = d;
+  }
+}
+
 // The conv of one channel: taps 0..2 on the window rows (oldest first), tap 3 on x.
 __device__ __forceinline__ float conv4(const float4 &w, float w0, float w1, float w2, float x) {
   return fmaf(w.w, x, fmaf(w.z, w2, fmaf(w.y, w1, w.x * w0)));

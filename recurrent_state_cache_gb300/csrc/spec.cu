@@ -27,8 +27,14 @@
 
 namespace rsc {
 
+// Minimum resident CTAs per SM the record-mode verify and the replay commit are compiled
+// for (4: 128 registers; the snapshot verify keeps its unbounded register budget).
+#ifndef RSC_VERIFY_MINB
+#define RSC_VERIFY_MINB 4
+#endif
+
 template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE, bool REPLAY>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, REPLAY ? RSC_VERIFY_MINB : 1)
 kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
                        int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
                        const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -108,8 +114,8 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   stage(0, 0);
 
   const ST *S = reinterpret_cast<const ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
-  float s[G::NP][G::EPL];
-  tile_load<ST, K, VT, VPL, NW>(S, s);
+  Tile2<ST, K, VT, NW, VPL> s;
+  tile_load2<ST, K, VT, VPL, NW>(S, s);
 
   // Window registers (raw io values, row 0 oldest) and taps of this thread's channels.
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
@@ -212,26 +218,27 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     for (int tau = 0; tau < cnt; ++tau) {
       const int t = t0 + tau;
       const size_t bt = (size_t)b * T + t;
-      float qh[G::EPL], kh[G::EPL], al[G::EPL];
+      float2 qh[G::EPL / 2], kh[G::EPL / 2], al[G::EPL / 2];
 #pragma unroll
-      for (int e = 0; e < G::EPL; ++e) {
-        qh[e] = s_qk[tau][k0 + e];
-        kh[e] = s_qk[tau][K + k0 + e];
-        al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
+      for (int e = 0; e < G::EPL / 2; ++e) {
+        qh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][k0 + 2 * e]);
+        kh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][K + k0 + 2 * e]);
+        al[e] = GATE == RSC_GATE_KDA ? *reinterpret_cast<const float2 *>(&s_al[tau][k0 + 2 * e])
+                                     : make_float2(s_al[tau][0], s_al[tau][0]);
       }
       float o[G::NP];
       if constexpr (REPLAY) {
         float dd[G::NP];
-        delta_rule_tile_d<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, dd);
+        delta_rule_tile2<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, dd);
         if (k0 == 0) {
           ST *dr = static_cast<ST *>(rv.d) + ent(t) * V + (size_t)j * VT;
 #pragma unroll
           for (int p = 0; p < G::NP; ++p) dr[G::row(p)] = from_f32<ST>(dd[p]);
         }
       } else {
-        delta_rule_tile<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o);
+        delta_rule_tile2<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, nullptr);
         ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
-        tile_store<ST, K, VT, VPL, NW>(Se, s);
+        tile_store2<ST, K, VT, VPL, NW>(Se, s);
       }
       if (k0 == 0) {
         IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
@@ -305,7 +312,7 @@ int launch_replay_verify(const LayerArgs &a, const RingView &rv, const int32_t *
 // back.  The CTA also restores its share of the window from snapshot accept[b] (the same
 // channel ownership as the verify pass), so every byte of the slot has one writer.
 template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, RSC_VERIFY_MINB)
 kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__restrict__ slots,
                          const int32_t *__restrict__ pos, int T, const IO *__restrict__ spec_conv,
                          const int32_t *__restrict__ accept) {
@@ -343,8 +350,8 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
   const int n = acc + 1;  // tokens to replay
 
   ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
-  float s[G::NP][G::EPL];
-  tile_load<ST, K, VT, VPL, NW>(S, s);
+  Tile2<ST, K, VT, NW, VPL> s;
+  tile_load2<ST, K, VT, VPL, NW>(S, s);
   const int k0 = G::kofs();
 
   for (int t0 = 0; t0 < n; t0 += TS) {
@@ -391,16 +398,17 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
     for (int i = tid; i < cnt * VT; i += NT) s_v[i / VT][i % VT] = to_f32(s_rv[i / VT][i % VT]);
     __syncthreads();
     for (int tau = 0; tau < cnt; ++tau) {
-      float kh[G::EPL], al[G::EPL];
+      float2 kh[G::EPL / 2], al[G::EPL / 2];
 #pragma unroll
-      for (int e = 0; e < G::EPL; ++e) {
-        kh[e] = s_kh[tau][k0 + e];
-        al[e] = GATE == RSC_GATE_KDA ? s_al[tau][k0 + e] : s_al[tau][0];
+      for (int e = 0; e < G::EPL / 2; ++e) {
+        kh[e] = *reinterpret_cast<const float2 *>(&s_kh[tau][k0 + 2 * e]);
+        al[e] = GATE == RSC_GATE_KDA ? *reinterpret_cast<const float2 *>(&s_al[tau][k0 + 2 * e])
+                                     : make_float2(s_al[tau][0], s_al[tau][0]);
       }
-      delta_rule_tile_replay<ST, K, VT, VPL, NW>(s, kh, al, s_b[tau], s_v[tau]);
+      delta_rule_tile2<ST, K, VT, VPL, NW, false>(s, kh, kh, al, s_b[tau], 0.f, s_v[tau], nullptr, nullptr);
     }
   }
-  tile_store<ST, K, VT, VPL, NW>(S, s);
+  tile_store2<ST, K, VT, VPL, NW>(S, s);
 
   // window <- snapshot acc: this CTA's q/k channels of the head and its value channels
   const IO *E = spec_conv + ((size_t)b * rv.depth + acc) * 3 * (size_t)D;
