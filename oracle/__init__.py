@@ -16,6 +16,7 @@ Pinning status (what the tests check each function against, besides itself):
   chunkwise_head     equals recurrent_head (two independent derivations)
   decode/prefill     split order and L2 norm pinned through closed-form special cases
   slot_copy/commit   byte equality
+  softplus/sigmoid   values at 0, asymptotes, symmetry; fused-gate decode = decode with them
   replay_verify/     commit(a) equals the snapshot path's commit(a) (fp32 records); the
   replay_commit      records rebuild the state by the pages' closed form; ring wrap-around
   pool_bytes         every logged pool size printed on the pages (tests/golden)
@@ -98,6 +99,15 @@ def _load():
         lib.orc_spec_verify.restype = i32
         lib.orc_spec_commit.argtypes = [pp, i32, vp, i32, i32, i32, vp, vp, vp]
         lib.orc_spec_commit.restype = i32
+        dbl = ctypes.c_double
+        lib.orc_softplus.argtypes = [dbl]
+        lib.orc_softplus.restype = dbl
+        lib.orc_sigmoid.argtypes = [dbl]
+        lib.orc_sigmoid.restype = dbl
+        lib.orc_gates_from_raw.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.orc_gates_from_raw.restype = None
+        lib.orc_decode_step_gated.argtypes = [pp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_decode_step_gated.restype = i32
         rp = ctypes.POINTER(_Rings)
         lib.orc_replay_verify.argtypes = [pp, rp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.orc_replay_verify.restype = i32
@@ -261,6 +271,50 @@ def spec_commit(pool: Pool, layer, slots, T, Lc, spec_ssm, spec_conv, accept):
     st = pool._struct()
     _check(_load().orc_spec_commit(ctypes.byref(st), layer, _ptr(slots), slots.shape[0], T,
                                    Lc, _ptr(ss), _ptr(sc), _ptr(acc)), "spec_commit")
+
+
+def softplus(x: float) -> float:
+    return _load().orc_softplus(float(x))
+
+
+def sigmoid(x: float) -> float:
+    return _load().orc_sigmoid(float(x))
+
+
+def gates_from_raw(pool: "Pool", a, b, A_log, dt_bias):
+    """(g, beta) of a batch from the raw projections (the gating reading of the C file)."""
+    b = _c(b, np.float32)
+    lead = b.shape[:-1]
+    B = int(np.prod(lead)) if lead else 1
+    n = pool.K if pool.gate == KDA else 1
+    a = _c(a, np.float32).reshape(B, pool.H, n)
+    A_log = _c(A_log, np.float32).reshape(pool.H)
+    dt_bias = _c(dt_bias, np.float32).reshape(pool.H, n)
+    g = np.empty((B, pool.H, n), np.float32)
+    beta = np.empty((B, pool.H), np.float32)
+    _load().orc_gates_from_raw(B, pool.H, pool.K, pool.gate, _ptr(a), _ptr(b.reshape(B, pool.H)),
+                               _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta))
+    gshape = lead + ((pool.H, pool.K) if pool.gate == KDA else (pool.H,))
+    return g.reshape(gshape), beta.reshape(lead + (pool.H,))
+
+
+def decode_step_gated(pool: "Pool", layer, slots, qkv, conv_w, a, b, A_log, dt_bias):
+    """Decode with the gates computed from raw projections; returns out [B][H][V]."""
+    slots = _c(slots, np.int32)
+    B = slots.shape[0]
+    n = pool.K if pool.gate == KDA else 1
+    qkv = _c(qkv, pool.io_np()).reshape(B, pool.D)
+    w = _c(conv_w, np.float32).reshape(pool.D, 4)
+    a = _c(a, np.float32).reshape(B, pool.H, n)
+    b = _c(b, np.float32).reshape(B, pool.H)
+    A_log = _c(A_log, np.float32).reshape(pool.H)
+    dt_bias = _c(dt_bias, np.float32).reshape(pool.H, n)
+    out = np.zeros((B, pool.H, pool.V), pool.io_np())
+    st = pool._struct()
+    _check(_load().orc_decode_step_gated(ctypes.byref(st), layer, _ptr(slots), B, _ptr(qkv), _ptr(w),
+                                         _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(out)),
+           "decode_step_gated")
+    return out
 
 
 class Rings:

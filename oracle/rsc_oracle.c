@@ -369,6 +369,52 @@ int orc_decode_step(const orc_pool *p, int layer, const int32_t *slots, int B,
   return 0;
 }
 
+/* Gates from the raw projections ([p2] §8.5 forward_decode takes the raw a, b of the layer;
+ * "SGLang之KV Cache内存池机制" §10 names the fused sigmoid-gating decode kernel).  The pages
+ * give no formula; the reading taken here (the usual KDA / GDN gating):
+ *   beta = sigmoid(b) = 1 / (1 + e^-b)
+ *   g    = -exp(A_log[h]) * softplus(a + dt_bias),  softplus(x) = log(1 + e^x)
+ * with a and dt_bias per key channel (KDA: a [H][K], dt_bias [H][K]) or per head (GDN: a [H],
+ * dt_bias [H]); A_log [H].  Written in forms that neither overflow nor lose small values:
+ * softplus(x) = max(x, 0) + log1p(e^-|x|), sigmoid(x) = 1/(1 + e^-x) for x >= 0 and
+ * e^x / (1 + e^x) otherwise. */
+double orc_softplus(double x) { return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x))); }
+double orc_sigmoid(double x) {
+  if (x >= 0.0) return 1.0 / (1.0 + exp(-x));
+  double e = exp(x);
+  return e / (1.0 + e);
+}
+
+/* Gates of one token batch: a [B][H][K] (KDA) or [B][H] (GDN), b [B][H] -> g (same shape as
+ * a), beta [B][H], as fp32 (the type the layer step takes them in). */
+void orc_gates_from_raw(int B, int H, int K, int gate, const float *a, const float *b,
+                        const float *A_log, const float *dt_bias, float *g, float *beta) {
+  const int n = gate == ORC_GATE_KDA ? K : 1;
+  for (int i = 0; i < B; ++i)
+    for (int h = 0; h < H; ++h) {
+      const double scale = exp((double)A_log[h]);
+      for (int c = 0; c < n; ++c) {
+        const size_t e = ((size_t)i * H + h) * n + c;
+        g[e] = (float)(-scale * orc_softplus((double)a[e] + (double)dt_bias[(size_t)h * n + c]));
+      }
+      beta[(size_t)i * H + h] = (float)orc_sigmoid((double)b[(size_t)i * H + h]);
+    }
+}
+
+/* Decode with fused gating: the gates of the batch from the raw projections, then the
+ * decode step. */
+int orc_decode_step_gated(const orc_pool *p, int layer, const int32_t *slots, int B,
+                          const void *qkv, const float *conv_w, const float *a, const float *b,
+                          const float *A_log, const float *dt_bias, void *out) {
+  const size_t ng = gate_elems(p);
+  float *g = malloc(sizeof(float) * ng * (size_t)(B > 0 ? B : 1));
+  float *beta = malloc(sizeof(float) * (size_t)p->H * (size_t)(B > 0 ? B : 1));
+  orc_gates_from_raw(B, p->H, p->K, p->gate, a, b, A_log, dt_bias, g, beta);
+  int rc = orc_decode_step(p, layer, slots, B, qkv, conv_w, g, beta, out);
+  free(g); free(beta);
+  return rc;
+}
+
 /* Prefill of N sequences packed along tokens (cu_seqlens [N+1]); sequence n starts from
  * its slot's state (or from zero when has_init is given and has_init[n] == 0), runs the
  * recurrence token by token and writes the final state back to the slot ([p2] §8.5

@@ -344,6 +344,75 @@ def test_spec_commit_equals_accepted_decode_steps(st):
         assert np.max(np.abs(a - e)) <= tol * np.max(np.abs(e))
 
 
+# ----------------------------------------------------------------------- fused gating
+
+def test_softplus_and_sigmoid_closed_forms():
+    """softplus(0) = ln 2, softplus(x) - softplus(-x) = x, softplus(x) -> x and -> e^x at the
+    ends; sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, sigmoid(x) + sigmoid(-x) = 1; and softplus'
+    = sigmoid (central difference)."""
+    assert abs(oracle.softplus(0.0) - np.log(2.0)) < 1e-15
+    for x in [-30.0, -3.5, -0.25, 0.7, 4.0, 31.0]:
+        assert abs(oracle.softplus(x) - oracle.softplus(-x) - x) < 1e-12 * max(1.0, abs(x))
+        assert abs(oracle.sigmoid(x) + oracle.sigmoid(-x) - 1.0) < 1e-15
+        h = 1e-5
+        slope = (oracle.softplus(x + h) - oracle.softplus(x - h)) / (2 * h)
+        assert abs(slope - oracle.sigmoid(x)) < 1e-8
+    assert abs(oracle.softplus(60.0) - 60.0) <= 1e-14
+    assert abs(oracle.softplus(-60.0) / np.exp(-60.0) - 1.0) < 1e-12
+    assert oracle.sigmoid(0.0) == 0.5
+    assert abs(oracle.sigmoid(np.log(3.0)) - 0.75) < 1e-15
+    assert oracle.sigmoid(-800.0) == 0.0 and oracle.sigmoid(800.0) == 1.0
+
+
+@pytest.mark.parametrize("gate", [oracle.KDA, oracle.GDN])
+def test_gates_from_raw_closed_forms(gate):
+    """With a = -dt_bias the softplus argument is 0: g = -exp(A_log) ln 2, so A_log = 0 gives
+    alpha = 1/2 and A_log = ln 2 gives alpha = 1/4; b = 0 gives beta = 1/2, b = ln 3 beta = 3/4.
+    Each channel's own dt_bias is used (KDA)."""
+    H, K = 3, 8
+    pool = oracle.Pool(1, 1, H, K, 4, oracle.F32, oracle.F32, gate,
+                       np.zeros((1, 2, H, 4, K), np.float32), np.zeros((1, 2, 3, H * (2 * K + 4)), np.float32))
+    n = K if gate == oracle.KDA else 1
+    r = np.random.default_rng(26)
+    dt = r.normal(size=(H, n)).astype(np.float32)
+    A_log = np.float32([0.0, np.log(2.0), 0.0])
+    a = -dt[None]
+    b = np.float32([[0.0, np.log(3.0), -2.0]])
+    g, beta = oracle.gates_from_raw(pool, a, b, A_log, dt)
+    g = g.reshape(1, H, n)
+    np.testing.assert_allclose(np.exp(g[0, 0]), 0.5, rtol=1e-6)
+    np.testing.assert_allclose(np.exp(g[0, 1]), 0.25, rtol=1e-6)
+    assert abs(beta[0, 0] - 0.5) < 1e-7 and abs(beta[0, 1] - 0.75) < 1e-7
+    assert abs(beta[0, 2] - 1.0 / (1.0 + np.exp(2.0))) < 1e-7
+    # one channel moved off zero: only its gate changes, by the pinned softplus
+    a2 = a.copy()
+    a2[0, 2, n - 1] += 1.5
+    g2, _ = oracle.gates_from_raw(pool, a2, b, A_log, dt)
+    g2 = g2.reshape(1, H, n)
+    assert np.array_equal(np.delete(g2.ravel(), 2 * n + n - 1), np.delete(g.ravel(), 2 * n + n - 1))
+    assert abs(g2[0, 2, n - 1] - (-oracle.softplus(1.5))) < 1e-6
+
+
+@pytest.mark.parametrize("gate", [oracle.KDA, oracle.GDN])
+def test_gated_decode_is_decode_with_those_gates(gate):
+    r, pool, w = _pool_case(27, gate=gate)
+    ref = oracle.Pool(1, 5, pool.H, pool.K, pool.V, pool.state_dtype, pool.conv_dtype, gate,
+                      pool.ssm.copy(), pool.conv.copy())
+    H, K = pool.H, pool.K
+    n = K if gate == oracle.KDA else 1
+    B = 3
+    slots = np.int32([4, 1, 5])
+    x = inputs.projections(r, (B,), H, K, pool.V, oracle.F32)
+    a = r.normal(size=(B, H, n)).astype(np.float32)
+    b = r.normal(size=(B, H)).astype(np.float32)
+    A_log = r.normal(size=(H,)).astype(np.float32)
+    dt = r.normal(size=(H, n)).astype(np.float32)
+    o = oracle.decode_step_gated(pool, 0, slots, x, w, a, b, A_log, dt)
+    g, beta = oracle.gates_from_raw(ref, a, b, A_log, dt)
+    o2 = oracle.decode_step(ref, 0, slots, x, w, g, beta)
+    assert np.array_equal(o, o2) and np.array_equal(pool.ssm, ref.ssm) and np.array_equal(pool.conv, ref.conv)
+
+
 # ----------------------------------------------------------------------- ReplaySSM
 
 def _replay_case(seed, st, gate=oracle.KDA, depth=16):
