@@ -55,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay or all/none")
+    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay,gated or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=69,
@@ -415,6 +415,32 @@ def leg_spec(dev, peaks, stream):
             "commit_frac": round(cb / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
+def leg_gated(dev, peaks, stream, wl):
+    """The headline decode step with the gates formed in the kernel from raw projections
+    (a [B][H][K], b [B][H], per-head A_log and per-channel dt_bias) instead of given g, beta:
+    the same 69-layer graph, the raw projections in place of g and beta."""
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6)
+    H, K = wl.H, wl.K
+    A_log = torch.empty((wl.layers, H), device=dev).normal_(0, 0.5, generator=gen)
+    dt = torch.empty((wl.layers, H, K), device=dev).normal_(0, 1, generator=gen)
+
+    def step():
+        for l in range(wl.layers):
+            rsc.kda_decode_step_gated(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
+                                      A_log[l], dt[l], out=wl.out[l])
+    graph = graph_of(step, stream)
+    ms = timed(graph.replay, 50, 5, stream)
+    tok = wl.B / (ms * 1e-3 / wl.layers)
+    bytes_layer = wl.bytes_per_launch() + H * 4 + H * K * 4
+    return {"config": "headline decode workload, gates from raw projections in the kernel",
+            "ms_per_step": round(ms, 4), "tokens_per_s_per_layer": round(tok, 1),
+            "hbm_gbs": round(bytes_layer * wl.layers / (ms * 1e-3) / 1e9, 1),
+            "frac": round(bytes_layer * wl.layers / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
 def leg_replay(dev, peaks, stream):
     """ReplaySSM verify / commit on the speculative workload of leg_spec: verify writes ring
     records (d, k, rawv, rawk, g, beta) instead of 8 states per request; commit replays the
@@ -588,7 +614,7 @@ def main(argv=None):
     d2h = h_out.numel() * h_out.element_size()
 
     legs = {}
-    want = set(["gdn", "prefill", "copy", "spec", "replay"] if args.legs == "all" else
+    want = set(["gdn", "prefill", "copy", "spec", "replay", "gated"] if args.legs == "all" else
                ([] if args.legs == "none" else args.legs.split(",")))
     if "copy" in want:
         legs["slot_copy"] = leg_copy(dev, peaks, stream, wl)
@@ -597,6 +623,8 @@ def main(argv=None):
         legs["spec"] = leg_spec(dev, peaks, stream)
     if "replay" in want:
         legs["replay_spec"] = leg_replay(dev, peaks, stream)
+    if "gated" in want:
+        legs["decode_gated"] = leg_gated(dev, peaks, stream, wl)
     if "prefill" in want:
         legs["prefill"] = leg_prefill(dev, peaks, stream)
     del wl

@@ -122,6 +122,20 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
                     const void *qkv, const float *conv_w, const float *g,
                     const float *beta, void *out, void *stream);
 
+/* Decode with fused gating ([p2] §8.5: forward_decode(layer, mixed_qkv, a, b) hands the
+ * layer's raw gate projections to the fused sigmoid-gating decode kernel named in §10).  The
+ * pages give no gating formula; the reading implemented (the usual KDA / GDN gating):
+ *   beta = sigmoid(b),   g = -exp(A_log[h]) * softplus(a + dt_bias),   alpha = exp(g)
+ *   a        [batch][H][K] (KDA) or [batch][H] (GDN)  device fp32: raw decay projection
+ *   b        [batch][H]   device fp32: raw beta projection
+ *   A_log    [H]          device fp32
+ *   dt_bias  [H][K] (KDA) or [H] (GDN)  device fp32
+ * Otherwise exactly kda_decode_step.  a and dt_bias must be 16-byte aligned.
+ * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ECUDA. */
+int kda_decode_step_gated(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                          const void *qkv, const float *conv_w, const float *a, const float *b,
+                          const float *A_log, const float *dt_bias, void *out, void *stream);
+
 /* Workspace bytes kda_prefill_chunk needs for num_seqs sequences of total_tokens
  * tokens (host only). */
 int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tokens,

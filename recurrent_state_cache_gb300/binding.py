@@ -26,6 +26,7 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Every symbol include/rsc.h declares.
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
+           "kda_decode_step_gated",
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
            "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
@@ -81,6 +82,7 @@ def lib():
         L.ssm_pool_bytes.argtypes = [pd, ctypes.POINTER(ctypes.c_uint64),
                                      ctypes.POINTER(ctypes.c_uint64)]
         L.kda_decode_step.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kda_decode_step_gated.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
         L.kda_prefill_chunk.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
                                         vp, sz, vp]
@@ -268,6 +270,29 @@ def kda_prefill_chunk_noalloc(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, 
                                            T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
                                            _p(beta), _p(out), _stream(stream)),
            "kda_prefill_chunk_noalloc")
+    return out
+
+
+def kda_decode_step_gated(pool: SlotPool, layer, slot_ids, qkv, conv_w, a, b, A_log, dt_bias,
+                          out=None, stream=None):
+    """Decode with the gates formed in the kernel from the raw projections a, b (see the
+    header for the gating reading)."""
+    B = slot_ids.shape[0]
+    dev = pool.device
+    n = pool.K if pool.gate == KDA else 1
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (B, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(a, "a", torch.float32, pool.gate_shape((B,)), dev)
+    _need(b, "b", torch.float32, (B, pool.H), dev)
+    _need(A_log, "A_log", torch.float32, (pool.H,), dev)
+    _need(dt_bias, "dt_bias", torch.float32, (pool.H, n) if n > 1 else (pool.H,), dev)
+    if out is None:
+        out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
+    _check(lib().kda_decode_step_gated(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                       _p(a), _p(b), _p(A_log), _p(dt_bias), _p(out),
+                                       _stream(stream)), "kda_decode_step_gated")
     return out
 
 

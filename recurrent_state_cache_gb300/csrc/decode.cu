@@ -25,17 +25,33 @@
 //      for a chunk only when it reaches it: delta rule on 16-byte row segments
 //      (rsc_step.cuh), the new state stored straight back to the slot with coalesced
 //      16-byte stores, so a CTA's writes overlap its own later reads.
+//
+// RAW (kda_decode_step_gated): `g` and `beta` carry the layer's raw gate projections a, b and
+// the gates are formed in the kernel (reading of the fused sigmoid-gating decode named by
+// "SGLang之KV Cache内存池机制" §10; the pages give no formula):
+//   beta = sigmoid(b),  g = -exp(A_log[h]) * softplus(a + dt_bias)
+// per key channel (KDA) or per head (GDN).
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
 namespace rsc {
 
-template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE>
+__device__ __forceinline__ float softplus_f(float x) {
+  return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_f(float x) {
+  if (x >= 0.f) return 1.f / (1.f + expf(-x));
+  const float e = expf(x);
+  return e / (1.f + e);
+}
+
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE,
+          bool RAW = false>
 __global__ void __cluster_dims__(NVT, 1, 1) __launch_bounds__(NW * 32)
 kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                   const IO *__restrict__ qkv, const float *__restrict__ conv_w,
                   const float *__restrict__ g, const float *__restrict__ beta,
-                  IO *__restrict__ out) {
+                  IO *__restrict__ out, RawGates rg) {
   constexpr int NT = NW * 32;
   constexpr int VT = V / NVT;
   using G = TileGeom<ST, K, VT, NW>;
@@ -86,7 +102,14 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   }
   const int k0 = G::kofs();
   float gl[G::EPL];  // the gate
-  if (GATE == RSC_GATE_KDA) {
+  // fused gating, KDA: each key channel's gate once per CTA (thread t, channel t), read by
+  // the lanes after the barrier below
+  __shared__ float s_gate[RAW && GATE == RSC_GATE_KDA ? K : 1];
+  if constexpr (RAW && GATE == RSC_GATE_KDA) {
+    if (tid < K)
+      s_gate[tid] = -expf(rg.A_log[h]) *
+                    softplus_f(g[((size_t)b * H + h) * K + tid] + rg.dt_bias[(size_t)h * K + tid]);
+  } else if (GATE == RSC_GATE_KDA) {
     float4 g4[G::EPL / 4];
     const float4 *gg = reinterpret_cast<const float4 *>(g + ((size_t)b * H + h) * K + k0);
 #pragma unroll
@@ -100,7 +123,15 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #pragma unroll
     for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
   }
-  const float bt = beta[(size_t)b * H + h];
+  float bt = beta[(size_t)b * H + h];
+  if constexpr (RAW) {  // gates from the raw projections (b in bt; GDN: a in gl)
+    if (GATE != RSC_GATE_KDA) {
+      const float gh = -expf(rg.A_log[h]) * softplus_f(gl[0] + rg.dt_bias[h]);
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
+    }
+    bt = sigmoid_f(bt);
+  }
 
   const int slot = slots[b];
   if (slot < 0 || slot > pv.P) {
@@ -129,6 +160,10 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     for (int c = 0; c < NCH; ++c) mbar_init(&s_bar[c], 1);
   }
   __syncthreads();
+  if constexpr (RAW && GATE == RSC_GATE_KDA) {
+#pragma unroll
+    for (int e = 0; e < G::EPL; ++e) gl[e] = s_gate[k0 + e];
+  }
   auto issue_chunk = [&](int c) {
     mbar_arrive_expect_tx(&s_bar[c], CHUNK_BYTES);
     bulk_g2s(reinterpret_cast<char *>(s_S) + c * CHUNK_BYTES,
@@ -244,11 +279,11 @@ template <> struct DecodeTile<float> {
   static constexpr int ROWS = RSC_DECODE_ROWS_F32, WARPS = RSC_DECODE_WARPS_F32;
 };
 
-template <typename ST, typename IO, int K, int V, int GATE>
-struct DecodeLaunch {
+template <typename ST, typename IO, int K, int V, int GATE, bool RAW>
+struct DecodeLaunchT {
   static int run(const LayerArgs *a, const int32_t *slots, int B, const void *qkv,
                  const float *conv_w, const float *g, const float *beta, void *out,
-                 cudaStream_t s) {
+                 RawGates rg, cudaStream_t s) {
     constexpr int ROWS = DecodeTile<ST>::ROWS < V ? DecodeTile<ST>::ROWS : V;
     constexpr int NVT = V / ROWS;
     constexpr int NW = DecodeTile<ST>::WARPS;
@@ -256,7 +291,7 @@ struct DecodeLaunch {
     constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
     constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
     constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
-    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE>;
+    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE, RAW>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
@@ -267,20 +302,31 @@ struct DecodeLaunch {
     dim3 grid(NVT, a->pv.H, B);
 #if RSC_DECODE_PDL
     return launch_pdl(kern, grid, dim3(NW * 32), SMEM, s, a->pv, a->layer, slots,
-                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out));
+                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), rg);
 #else
     kern<<<grid, NW * 32, SMEM, s>>>(a->pv, a->layer, slots, static_cast<const IO *>(qkv),
-                                     conv_w, g, beta, static_cast<IO *>(out));
+                                     conv_w, g, beta, static_cast<IO *>(out), rg);
     return launch_status();
 #endif
   }
 };
+template <typename ST, typename IO, int K, int V, int GATE>
+struct DecodeLaunch : DecodeLaunchT<ST, IO, K, V, GATE, false> {};
+template <typename ST, typename IO, int K, int V, int GATE>
+struct DecodeGatedLaunch : DecodeLaunchT<ST, IO, K, V, GATE, true> {};
 
 int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
                   const float *conv_w, const float *g, const float *beta, void *out,
                   cudaStream_t s) {
   return dispatch_all<DecodeLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, qkv,
-                                    conv_w, g, beta, out, s);
+                                    conv_w, g, beta, out, RawGates{}, s);
+}
+
+int launch_decode_gated(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
+                        const float *conv_w, const float *a_raw, const float *b_raw,
+                        const float *A_log, const float *dt_bias, void *out, cudaStream_t s) {
+  return dispatch_all<DecodeGatedLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, qkv,
+                                         conv_w, a_raw, b_raw, out, RawGates{A_log, dt_bias}, s);
 }
 
 }  // namespace rsc

@@ -102,6 +102,21 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
                             as_stream(stream));
 }
 
+int kda_decode_step_gated(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                          const void *qkv, const float *conv_w, const float *a, const float *b,
+                          const float *A_log, const float *dt_bias, void *out, void *stream) {
+  if (!pool) return RSC_EINVAL;
+  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
+    return RSC_ERANGE;
+  if (batch == 0) return RSC_OK;
+  if (!slot_ids || !qkv || !conv_w || !a || !b || !A_log || !dt_bias || !out) return RSC_EINVAL;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(a, 16) ||
+      !aligned(dt_bias, 16) || !aligned(b, 4) || !aligned(A_log, 4) || !aligned(slot_ids, 4))
+    return RSC_EALIGN;
+  return rsc::launch_decode_gated(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, a, b,
+                                  A_log, dt_bias, out, as_stream(stream));
+}
+
 int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tokens,
                                size_t *bytes) {
   if (!pool || !bytes) return RSC_EINVAL;

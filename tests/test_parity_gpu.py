@@ -180,6 +180,34 @@ def test_spec_commit_bad_accept_flags(cuda_dev):
     assert np.all(widen(now[0, 1]) == 1.0)
 
 
+# ------------------------------------------------------------------ fused gating
+
+@pytest.mark.parametrize("st,io,gate,K,V", [
+    (0, 0, rsc.KDA, 64, 64), (1, 1, rsc.KDA, 128, 128), (0, 1, rsc.GDN, 128, 128),
+    (1, 0, rsc.GDN, 64, 128), (1, 1, rsc.KDA, 64, 128),
+])
+def test_decode_gated_parity(cuda_dev, st, io, gate, K, V):
+    """Gates formed in the kernel from raw projections: outputs, states and windows match the
+    oracle's gating followed by its decode step, over two steps."""
+    H, B = 3, 5
+    c = Case(cuda_dev, 34, L=2, P=9, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    n = K if gate == rsc.KDA else 1
+    slots = inputs.distinct_slots(c.r, B, 9)
+    A_log = c.r.normal(0, 0.5, size=(H,)).astype(np.float32)
+    dt = c.r.normal(0, 1, size=(H, n)).astype(np.float32)
+    dt_dev = to_dev(dt if n > 1 else dt[:, 0].copy(), c.dev)
+    for _ in range(2):
+        x = c.proj((B,))
+        a = c.r.normal(0, 2, size=(B, H, n)).astype(np.float32)
+        b = c.r.normal(0, 2, size=(B, H)).astype(np.float32)
+        o_ref = oracle.decode_step_gated(c.ref, 1, slots, x, c.w, a, b, A_log, dt)
+        a_dev = to_dev(a if n > 1 else a[:, :, 0].copy(), c.dev)
+        o = rsc.kda_decode_step_gated(c.pool, 1, to_dev(slots, c.dev), to_dev(x, c.dev), c.w_dev,
+                                      a_dev, to_dev(b, c.dev), to_dev(A_log, c.dev), dt_dev)
+        assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(st, io)
+    c.check_pool()
+
+
 # ------------------------------------------------------------------ ReplaySSM
 
 def _rings_np(rings):
