@@ -55,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay,gated or all/none")
+    ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay,gated,track or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=69,
@@ -441,6 +441,37 @@ def leg_gated(dev, peaks, stream, wl):
             "frac": round(bytes_layer * wl.layers / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
+def leg_track(dev, peaks, stream, wl):
+    """The headline decode step with every request tracked (the worst case of the pages'
+    mamba_track_interval copy): the track copy fused into decode against decode followed by
+    the masked slot copy of each layer."""
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    used = set(wl.slots.cpu().tolist())
+    free = [s for s in range(1, wl.P + 1) if s not in used][:wl.B]
+    track = torch.tensor(free, dtype=torch.int32, device=dev)
+    mask = torch.ones(wl.B, dtype=torch.uint8, device=dev)
+
+    def fused():
+        for l in range(wl.layers):
+            rsc.kda_decode_step_track(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
+                                      mask, track, out=wl.out[l])
+
+    def separate():
+        for l in range(wl.layers):
+            rsc.kda_decode_step(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l], wl.out[l])
+            rsc.ssm_slot_copy(wl.pool, l, wl.slots, track, mask)
+    ms_f = timed(graph_of(fused, stream).replay, 30, 5, stream)
+    ms_s = timed(graph_of(separate, stream).replay, 30, 5, stream)
+    row = wl.H * wl.V * wl.K * 2 + 3 * wl.D * 2          # one slot row of a layer (bf16)
+    bytes_f = (wl.bytes_per_launch() + wl.B * row) * wl.layers  # the track rows written once more
+    return {"config": "headline decode workload, all 64 requests tracked every step",
+            "fused_ms_per_step": round(ms_f, 4), "separate_ms_per_step": round(ms_s, 4),
+            "fused_tokens_per_s_per_layer": round(wl.B / (ms_f * 1e-3 / wl.layers), 1),
+            "fused_hbm_gbs": round(bytes_f / (ms_f * 1e-3) / 1e9, 1),
+            "fused_frac": round(bytes_f / (ms_f * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
 def leg_replay(dev, peaks, stream):
     """ReplaySSM verify / commit on the speculative workload of leg_spec: verify writes ring
     records (d, k, rawv, rawk, g, beta) instead of 8 states per request; commit replays the
@@ -614,7 +645,7 @@ def main(argv=None):
     d2h = h_out.numel() * h_out.element_size()
 
     legs = {}
-    want = set(["gdn", "prefill", "copy", "spec", "replay", "gated"] if args.legs == "all" else
+    want = set(["gdn", "prefill", "copy", "spec", "replay", "gated", "track"] if args.legs == "all" else
                ([] if args.legs == "none" else args.legs.split(",")))
     if "copy" in want:
         legs["slot_copy"] = leg_copy(dev, peaks, stream, wl)
@@ -625,6 +656,8 @@ def main(argv=None):
         legs["replay_spec"] = leg_replay(dev, peaks, stream)
     if "gated" in want:
         legs["decode_gated"] = leg_gated(dev, peaks, stream, wl)
+    if "track" in want:
+        legs["decode_track"] = leg_track(dev, peaks, stream, wl)
     if "prefill" in want:
         legs["prefill"] = leg_prefill(dev, peaks, stream)
     del wl

@@ -122,6 +122,21 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
                     const void *qkv, const float *conv_w, const float *g,
                     const float *beta, void *out, void *stream);
 
+/* Decode with the track copy fused in ([p1] mamba_track_interval: when a request's length
+ * reaches the tracking interval its mamba_track_mask is set and, after the forward step,
+ * conv and ssm state of its active slot are copied into its tracking slot).  Exactly
+ * kda_decode_step, and for every b with track_mask[b] != 0 the updated state and window of
+ * slot_ids[b] are also written, byte for byte, into slot track_slots[b] (from the kernel's
+ * registers: nothing is read back).
+ *   track_mask  [batch] device uint8;  track_slots [batch] device int32 in [0, num_slots],
+ *               distinct from every slot id of the call and from each other where the mask is
+ *               set (caller precondition); out of range: RSC_DEVERR_SLOT and no track write.
+ * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ECUDA. */
+int kda_decode_step_track(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                          const void *qkv, const float *conv_w, const float *g, const float *beta,
+                          void *out, const uint8_t *track_mask, const int32_t *track_slots,
+                          void *stream);
+
 /* Decode with fused gating ([p2] §8.5: forward_decode(layer, mixed_qkv, a, b) hands the
  * layer's raw gate projections to the fused sigmoid-gating decode kernel named in §10).  The
  * pages give no gating formula; the reading implemented (the usual KDA / GDN gating):

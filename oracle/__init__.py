@@ -108,6 +108,8 @@ def _load():
         lib.orc_gates_from_raw.restype = None
         lib.orc_decode_step_gated.argtypes = [pp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_decode_step_gated.restype = i32
+        lib.orc_decode_step_track.argtypes = [pp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_decode_step_track.restype = i32
         rp = ctypes.POINTER(_Rings)
         lib.orc_replay_verify.argtypes = [pp, rp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.orc_replay_verify.restype = i32
@@ -296,6 +298,23 @@ def gates_from_raw(pool: "Pool", a, b, A_log, dt_bias):
                                _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta))
     gshape = lead + ((pool.H, pool.K) if pool.gate == KDA else (pool.H,))
     return g.reshape(gshape), beta.reshape(lead + (pool.H,))
+
+
+def decode_step_track(pool: "Pool", layer, slots, qkv, conv_w, g, beta, mask, track_slots):
+    """Decode, then the masked track copy of the updated rows; returns out [B][H][V]."""
+    slots, ts = _c(slots, np.int32), _c(track_slots, np.int32)
+    mask = _c(mask, np.uint8)
+    B = slots.shape[0]
+    qkv = _c(qkv, pool.io_np()).reshape(B, pool.D)
+    g = _gate_arr(pool, g, (B,))
+    beta = _c(beta, np.float32).reshape(B, pool.H)
+    w = _c(conv_w, np.float32).reshape(pool.D, 4)
+    out = np.zeros((B, pool.H, pool.V), pool.io_np())
+    st = pool._struct()
+    _check(_load().orc_decode_step_track(ctypes.byref(st), layer, _ptr(slots), B, _ptr(qkv), _ptr(w),
+                                         _ptr(g), _ptr(beta), _ptr(out), _ptr(mask), _ptr(ts)),
+           "decode_step_track")
+    return out
 
 
 def decode_step_gated(pool: "Pool", layer, slots, qkv, conv_w, a, b, A_log, dt_bias):

@@ -369,6 +369,20 @@ int orc_decode_step(const orc_pool *p, int layer, const int32_t *slots, int B,
   return 0;
 }
 
+/* Decode with the track copy ([p1] mamba_track_interval / track_mamba_states_if_needed: after
+ * the forward step, if mask[b] then conv[track] = conv[active] and ssm[track] = ssm[active]):
+ * the decode step, then the masked copy of this layer's rows. */
+int orc_slot_copy(const orc_pool *p, int layer, const int32_t *src, const int32_t *dst,
+                  const uint8_t *mask, int n);
+
+int orc_decode_step_track(const orc_pool *p, int layer, const int32_t *slots, int B,
+                          const void *qkv, const float *conv_w, const float *g, const float *beta,
+                          void *out, const uint8_t *mask, const int32_t *track_slots) {
+  int rc = orc_decode_step(p, layer, slots, B, qkv, conv_w, g, beta, out);
+  if (rc) return rc;
+  return orc_slot_copy(p, layer, slots, track_slots, mask, B);
+}
+
 /* Gates from the raw projections ([p2] §8.5 forward_decode takes the raw a, b of the layer;
  * "SGLang之KV Cache内存池机制" §10 names the fused sigmoid-gating decode kernel).  The pages
  * give no formula; the reading taken here (the usual KDA / GDN gating):

@@ -26,7 +26,7 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Every symbol include/rsc.h declares.
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
-           "kda_decode_step_gated",
+           "kda_decode_step_gated", "kda_decode_step_track",
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
            "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
@@ -82,6 +82,7 @@ def lib():
         L.ssm_pool_bytes.argtypes = [pd, ctypes.POINTER(ctypes.c_uint64),
                                      ctypes.POINTER(ctypes.c_uint64)]
         L.kda_decode_step.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kda_decode_step_track.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_gated.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
         L.kda_prefill_chunk.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
@@ -270,6 +271,28 @@ def kda_prefill_chunk_noalloc(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, 
                                            T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
                                            _p(beta), _p(out), _stream(stream)),
            "kda_prefill_chunk_noalloc")
+    return out
+
+
+def kda_decode_step_track(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, track_mask,
+                          track_slots, out=None, stream=None):
+    """Decode, and for requests with track_mask set the updated state and window written
+    into track_slots as well (the masked track copy, fused)."""
+    B = slot_ids.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (B, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(g, "g", torch.float32, pool.gate_shape((B,)), dev)
+    _need(beta, "beta", torch.float32, (B, pool.H), dev)
+    _need(track_mask, "track_mask", torch.uint8, (B,), dev)
+    _need(track_slots, "track_slots", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
+    _check(lib().kda_decode_step_track(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                       _p(g), _p(beta), _p(out), _p(track_mask), _p(track_slots),
+                                       _stream(stream)), "kda_decode_step_track")
     return out
 
 

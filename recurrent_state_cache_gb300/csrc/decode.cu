@@ -26,11 +26,16 @@
 //      (rsc_step.cuh), the new state stored straight back to the slot with coalesced
 //      16-byte stores, so a CTA's writes overlap its own later reads.
 //
-// RAW (kda_decode_step_gated): `g` and `beta` carry the layer's raw gate projections a, b and
-// the gates are formed in the kernel (reading of the fused sigmoid-gating decode named by
-// "SGLang之KV Cache内存池机制" §10; the pages give no formula):
-//   beta = sigmoid(b),  g = -exp(A_log[h]) * softplus(a + dt_bias)
-// per key channel (KDA) or per head (GDN).
+// Extras, chosen per call (uniform branches, one kernel):
+//   fused gating (kda_decode_step_gated, ex.A_log set): `g` and `beta` carry the layer's raw
+//     gate projections a, b and the gates are formed in the kernel (reading of the fused
+//     sigmoid-gating decode named by "SGLang之KV Cache内存池机制" §10; the pages give no
+//     formula): beta = sigmoid(b), g = -exp(A_log[h]) * softplus(a + dt_bias), per key
+//     channel (KDA) or per head (GDN);
+//   tracking (kda_decode_step_track, ex.track_mask set): "SGLang Qwen3/kimi-k3 Hybrid Linear
+//     Mamba KV cache管理", mamba_track_interval: when track_mask[b] is set, the updated state
+//     and window of the request also go to slot track_slots[b] (the masked track copy of the
+//     pages, written from registers instead of re-read from the active slot).
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
@@ -45,13 +50,12 @@ __device__ __forceinline__ float sigmoid_f(float x) {
   return e / (1.f + e);
 }
 
-template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE,
-          bool RAW = false>
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE>
 __global__ void __cluster_dims__(NVT, 1, 1) __launch_bounds__(NW * 32)
 kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                   const IO *__restrict__ qkv, const float *__restrict__ conv_w,
                   const float *__restrict__ g, const float *__restrict__ beta,
-                  IO *__restrict__ out, RawGates rg) {
+                  IO *__restrict__ out, DecodeExtras ex) {
   constexpr int NT = NW * 32;
   constexpr int VT = V / NVT;
   using G = TileGeom<ST, K, VT, NW>;
@@ -101,14 +105,18 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     xv = x[cv];
   }
   const int k0 = G::kofs();
+  const bool raw = ex.A_log != nullptr;
   float gl[G::EPL];  // the gate
   // fused gating, KDA: each key channel's gate once per CTA (thread t, channel t), read by
   // the lanes after the barrier below
-  __shared__ float s_gate[RAW && GATE == RSC_GATE_KDA ? K : 1];
-  if constexpr (RAW && GATE == RSC_GATE_KDA) {
-    if (tid < K)
-      s_gate[tid] = -expf(rg.A_log[h]) *
-                    softplus_f(g[((size_t)b * H + h) * K + tid] + rg.dt_bias[(size_t)h * K + tid]);
+  __shared__ float s_gate[GATE == RSC_GATE_KDA ? K : 1];
+  float a_raw = 0.f, d_raw = 0.f, s_raw = 0.f;  // raw gate inputs, loaded now, used below
+  if (GATE == RSC_GATE_KDA && raw) {
+    if (tid < K) {
+      a_raw = g[((size_t)b * H + h) * K + tid];
+      d_raw = ex.dt_bias[(size_t)h * K + tid];
+      s_raw = ex.A_log[h];
+    }
   } else if (GATE == RSC_GATE_KDA) {
     float4 g4[G::EPL / 4];
     const float4 *gg = reinterpret_cast<const float4 *>(g + ((size_t)b * H + h) * K + k0);
@@ -124,13 +132,9 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
   }
   float bt = beta[(size_t)b * H + h];
-  if constexpr (RAW) {  // gates from the raw projections (b in bt; GDN: a in gl)
-    if (GATE != RSC_GATE_KDA) {
-      const float gh = -expf(rg.A_log[h]) * softplus_f(gl[0] + rg.dt_bias[h]);
-#pragma unroll
-      for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
-    }
-    bt = sigmoid_f(bt);
+  if (raw && GATE != RSC_GATE_KDA) {
+    d_raw = ex.dt_bias[h];
+    s_raw = ex.A_log[h];
   }
 
   const int slot = slots[b];
@@ -141,6 +145,19 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
   ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
   IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
+  // tracking: the same tile and window channels of the track slot (null when not tracked)
+  ST *St = nullptr;
+  IO *Wt = nullptr;
+  if (ex.track_mask != nullptr && ex.track_mask[b]) {
+    const int ts = ex.track_slots[b];
+    if (ts < 0 || ts > pv.P) {
+      if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
+    } else {
+      const size_t trow = (size_t)layer * (pv.P + 1) + ts;
+      St = reinterpret_cast<ST *>(pv.ssm) + ((trow * H + h) * V + (size_t)j * VT) * K;
+      Wt = reinterpret_cast<IO *>(pv.conv) + trow * 3 * (size_t)D;
+    }
+  }
   IO keep[QK_T][3];
 #pragma unroll
   for (int u = 0; u < QK_T; ++u) {
@@ -155,12 +172,24 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 
   // 2. The tile, in NCH row chunks on their own mbarriers (chunk c holds the rows of
   //    passes [c*PPC, (c+1)*PPC)): EARLY chunks now, the rest once the conv is done.
+  // fused gating, formed only now so that waiting for its inputs does not hold back the
+  // requests above (b in bt; GDN: a in gl)
+  if (raw) {
+    if (GATE == RSC_GATE_KDA) {
+      if (tid < K) s_gate[tid] = -expf(s_raw) * softplus_f(a_raw + d_raw);
+    } else {
+      const float gh = -expf(s_raw) * softplus_f(gl[0] + d_raw);
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
+    }
+    bt = sigmoid_f(bt);
+  }
   if (tid == 0) {
 #pragma unroll
     for (int c = 0; c < NCH; ++c) mbar_init(&s_bar[c], 1);
   }
   __syncthreads();
-  if constexpr (RAW && GATE == RSC_GATE_KDA) {
+  if (GATE == RSC_GATE_KDA && raw) {
 #pragma unroll
     for (int e = 0; e < G::EPL; ++e) gl[e] = s_gate[k0 + e];
   }
@@ -222,9 +251,13 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     if (i2 < 2 * K && i2 >= j * OWN && i2 < (j + 1) * OWN) {
       const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
       W[c] = keep[u][0]; W[D + c] = keep[u][1]; W[2 * D + c] = keep[u][2];
+      if (Wt) { Wt[c] = keep[u][0]; Wt[D + c] = keep[u][1]; Wt[2 * D + c] = keep[u][2]; }
     }
   }
-  if (tid < VT) { W[cv] = keepv[0]; W[D + cv] = keepv[1]; W[2 * D + cv] = keepv[2]; }
+  if (tid < VT) {
+    W[cv] = keepv[0]; W[D + cv] = keepv[1]; W[2 * D + cv] = keepv[2];
+    if (Wt) { Wt[cv] = keepv[0]; Wt[D + cv] = keepv[1]; Wt[2 * D + cv] = keepv[2]; }
+  }
 
   // 5. delta rule pass by pass out of shared memory; state back in place.
   IO *ob = out + ((size_t)b * H + h) * V + (size_t)j * VT;
@@ -239,7 +272,9 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     float s[G::EPL];
     unpack16(*reinterpret_cast<const uint4 *>(s_S + (size_t)r * K + k0), s);
     const float o = delta_rule_row<G::EPL, G::LPR>(s, qh, kh, al, bt, kq, s_v[r]);
-    st16(S + (size_t)r * K + k0, pack16(s));
+    const uint4 packed = pack16(s);
+    st16(S + (size_t)r * K + k0, packed);
+    if (St) st16(St + (size_t)r * K + k0, packed);
     if (k0 == 0) ob[r] = from_f32<IO>(o);
   }
 }
@@ -279,11 +314,11 @@ template <> struct DecodeTile<float> {
   static constexpr int ROWS = RSC_DECODE_ROWS_F32, WARPS = RSC_DECODE_WARPS_F32;
 };
 
-template <typename ST, typename IO, int K, int V, int GATE, bool RAW>
-struct DecodeLaunchT {
+template <typename ST, typename IO, int K, int V, int GATE>
+struct DecodeLaunch {
   static int run(const LayerArgs *a, const int32_t *slots, int B, const void *qkv,
                  const float *conv_w, const float *g, const float *beta, void *out,
-                 RawGates rg, cudaStream_t s) {
+                 DecodeExtras ex, cudaStream_t s) {
     constexpr int ROWS = DecodeTile<ST>::ROWS < V ? DecodeTile<ST>::ROWS : V;
     constexpr int NVT = V / ROWS;
     constexpr int NW = DecodeTile<ST>::WARPS;
@@ -291,7 +326,7 @@ struct DecodeLaunchT {
     constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
     constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
     constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
-    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE, RAW>;
+    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
@@ -302,31 +337,19 @@ struct DecodeLaunchT {
     dim3 grid(NVT, a->pv.H, B);
 #if RSC_DECODE_PDL
     return launch_pdl(kern, grid, dim3(NW * 32), SMEM, s, a->pv, a->layer, slots,
-                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), rg);
+                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), ex);
 #else
     kern<<<grid, NW * 32, SMEM, s>>>(a->pv, a->layer, slots, static_cast<const IO *>(qkv),
-                                     conv_w, g, beta, static_cast<IO *>(out), rg);
+                                     conv_w, g, beta, static_cast<IO *>(out), ex);
     return launch_status();
 #endif
   }
 };
-template <typename ST, typename IO, int K, int V, int GATE>
-struct DecodeLaunch : DecodeLaunchT<ST, IO, K, V, GATE, false> {};
-template <typename ST, typename IO, int K, int V, int GATE>
-struct DecodeGatedLaunch : DecodeLaunchT<ST, IO, K, V, GATE, true> {};
-
 int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
                   const float *conv_w, const float *g, const float *beta, void *out,
-                  cudaStream_t s) {
+                  const DecodeExtras &ex, cudaStream_t s) {
   return dispatch_all<DecodeLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, qkv,
-                                    conv_w, g, beta, out, RawGates{}, s);
-}
-
-int launch_decode_gated(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
-                        const float *conv_w, const float *a_raw, const float *b_raw,
-                        const float *A_log, const float *dt_bias, void *out, cudaStream_t s) {
-  return dispatch_all<DecodeGatedLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, B, qkv,
-                                         conv_w, a_raw, b_raw, out, RawGates{A_log, dt_bias}, s);
+                                    conv_w, g, beta, out, ex, s);
 }
 
 }  // namespace rsc

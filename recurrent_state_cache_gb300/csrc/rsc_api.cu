@@ -99,7 +99,27 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
       !aligned(beta, 4) || !aligned(slot_ids, 4))
     return RSC_EALIGN;
   return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
-                            as_stream(stream));
+                            rsc::DecodeExtras{}, as_stream(stream));
+}
+
+int kda_decode_step_track(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                          const void *qkv, const float *conv_w, const float *g, const float *beta,
+                          void *out, const uint8_t *track_mask, const int32_t *track_slots,
+                          void *stream) {
+  if (!pool) return RSC_EINVAL;
+  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
+    return RSC_ERANGE;
+  if (batch == 0) return RSC_OK;
+  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out || !track_mask || !track_slots)
+    return RSC_EINVAL;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
+      !aligned(beta, 4) || !aligned(slot_ids, 4) || !aligned(track_slots, 4))
+    return RSC_EALIGN;
+  rsc::DecodeExtras ex;
+  ex.track_mask = track_mask;
+  ex.track_slots = track_slots;
+  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
+                            ex, as_stream(stream));
 }
 
 int kda_decode_step_gated(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
@@ -113,8 +133,11 @@ int kda_decode_step_gated(rsc_pool *pool, int layer, const int32_t *slot_ids, in
   if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(a, 16) ||
       !aligned(dt_bias, 16) || !aligned(b, 4) || !aligned(A_log, 4) || !aligned(slot_ids, 4))
     return RSC_EALIGN;
-  return rsc::launch_decode_gated(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, a, b,
-                                  A_log, dt_bias, out, as_stream(stream));
+  rsc::DecodeExtras ex;
+  ex.A_log = A_log;
+  ex.dt_bias = dt_bias;
+  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, a, b, out, ex,
+                            as_stream(stream));
 }
 
 int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tokens,

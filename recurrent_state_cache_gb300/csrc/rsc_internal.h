@@ -16,16 +16,15 @@ struct LayerArgs {
   int layer;
 };
 
+// Per-call extras of the decode kernel (all null: the plain step).
+struct DecodeExtras {
+  const float *A_log = nullptr, *dt_bias = nullptr;  // fused gating: A_log [H], dt_bias [H][K] / [H]
+  const uint8_t *track_mask = nullptr;               // tracking: [B]
+  const int32_t *track_slots = nullptr;              // [B]
+};
 int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
                   const float *conv_w, const float *g, const float *beta, void *out,
-                  cudaStream_t s);
-// Per-head gate parameters of the fused-gate decode: A_log [H], dt_bias [H][K] (KDA) or [H].
-struct RawGates {
-  const float *A_log = nullptr, *dt_bias = nullptr;
-};
-int launch_decode_gated(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
-                        const float *conv_w, const float *a_raw, const float *b_raw,
-                        const float *A_log, const float *dt_bias, void *out, cudaStream_t s);
+                  const DecodeExtras &ex, cudaStream_t s);
 
 int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, int L,
                        void *spec_ssm, void *spec_conv, const void *qkv,

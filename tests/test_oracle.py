@@ -413,6 +413,26 @@ def test_gated_decode_is_decode_with_those_gates(gate):
     assert np.array_equal(o, o2) and np.array_equal(pool.ssm, ref.ssm) and np.array_equal(pool.conv, ref.conv)
 
 
+def test_tracked_decode_copies_updated_rows_only_where_masked():
+    """The track copy after a decode step ([p1] mamba_track_interval): masked requests' track
+    slots hold the updated state and window byte for byte; unmasked track slots and every other
+    row are untouched; the step itself equals the plain decode."""
+    r, pool, w = _pool_case(28)
+    ref = oracle.Pool(1, 5, pool.H, pool.K, pool.V, pool.state_dtype, pool.conv_dtype, oracle.KDA,
+                      pool.ssm.copy(), pool.conv.copy())
+    before = pool.ssm.copy(), pool.conv.copy()
+    slots, track, mask = np.int32([1, 3]), np.int32([4, 5]), np.uint8([1, 0])
+    x = inputs.projections(r, (2,), pool.H, pool.K, pool.V, oracle.F32)
+    g, beta = inputs.gates(r, (2,), pool.H, pool.K, oracle.KDA)
+    o = oracle.decode_step_track(pool, 0, slots, x, w, g, beta, mask, track)
+    o2 = oracle.decode_step(ref, 0, slots, x, w, g, beta)
+    assert np.array_equal(o, o2)
+    assert np.array_equal(pool.ssm[0, 4], pool.ssm[0, 1]) and np.array_equal(pool.conv[0, 4], pool.conv[0, 1])
+    assert np.array_equal(pool.ssm[0, 5], before[0][0, 5]) and np.array_equal(pool.conv[0, 5], before[1][0, 5])
+    for s in (0, 1, 2, 3):
+        assert np.array_equal(pool.ssm[0, s], ref.ssm[0, s]) and np.array_equal(pool.conv[0, s], ref.conv[0, s])
+
+
 # ----------------------------------------------------------------------- ReplaySSM
 
 def _replay_case(seed, st, gate=oracle.KDA, depth=16):

@@ -208,6 +208,31 @@ def test_decode_gated_parity(cuda_dev, st, io, gate, K, V):
     c.check_pool()
 
 
+@pytest.mark.parametrize("st,io,K,V", [(0, 0, 64, 64), (1, 1, 128, 128), (0, 1, 128, 64)])
+def test_decode_track_parity(cuda_dev, st, io, K, V):
+    """Tracking fused into decode: masked requests' track slots receive the updated state and
+    window bit for bit (the same bytes as the active slot), unmasked track slots and all other
+    rows match the oracle's decode followed by its masked copy."""
+    H, B = 2, 4
+    c = Case(cuda_dev, 35, L=2, P=12, H=H, K=K, V=V, st=st, io=io, gate=rsc.KDA)
+    slots = np.int32([2, 5, 7, 9])
+    track = np.int32([11, 1, 12, 3])
+    mask = np.uint8([1, 0, 1, 1])
+    x = c.proj((B,))
+    g, beta = c.gates((B,))
+    o_ref = oracle.decode_step_track(c.ref, 1, slots, x, c.w, g, beta, mask, track)
+    o = rsc.kda_decode_step_track(c.pool, 1, to_dev(slots, c.dev), to_dev(x, c.dev), c.w_dev,
+                                  to_dev(g, c.dev), to_dev(beta, c.dev), to_dev(mask, c.dev),
+                                  to_dev(track, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(st, io)
+    ssm, conv = to_np(c.pool.ssm), to_np(c.pool.conv)
+    for b in range(B):
+        if mask[b]:
+            assert np.array_equal(ssm[1, track[b]], ssm[1, slots[b]])
+            assert np.array_equal(conv[1, track[b]], conv[1, slots[b]])
+    c.check_pool()
+
+
 # ------------------------------------------------------------------ ReplaySSM
 
 def _rings_np(rings):
