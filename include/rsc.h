@@ -270,6 +270,36 @@ int kda_replay_verify_commit(rsc_pool *pool, const rsc_replay_rings *rings, int 
                              const float *g, const float *beta, void *out,
                              const int32_t *accept, void *stream);
 
+/* ------------------------------------------------------------------ host slot management
+ * ([p2] §8.3 MambaPool.alloc: a state slot per request from the pool's free list; [p1] the
+ * concurrency cap of the mamba state pool and the mamba_track_interval ping-pong track
+ * slots).  Host only: no CUDA call, callable without a GPU. */
+typedef struct rsc_slot_alloc rsc_slot_alloc;
+
+/* An allocator over slots 1..num_slots (row 0, the padding row, is never handed out); slot 1
+ * is handed out first.  Thread-safe.  Errors: RSC_EINVAL, RSC_ERANGE, RSC_ENOSPACE. */
+int rsc_slot_alloc_create(int num_slots, rsc_slot_alloc **out);
+int rsc_slot_alloc_destroy(rsc_slot_alloc *alloc);
+int rsc_slot_alloc_free_count(rsc_slot_alloc *alloc, int *count);
+/* n distinct free slots into slots[0..n) (host), or RSC_ENOSPACE and nothing taken. */
+int rsc_slot_alloc_acquire(rsc_slot_alloc *alloc, int n, int32_t *slots);
+/* Give n held slots back; a slot out of range (RSC_ERANGE), not held or repeated (RSC_EINVAL)
+ * rejects the whole call and frees nothing. */
+int rsc_slot_alloc_release(rsc_slot_alloc *alloc, int n, const int32_t *slots);
+
+/* Requests a pool of num_slots can run at once: each reserves 3 slots, 2 more with the
+ * overlap scheduler (its ping-pong track slots), 1 fewer with the decode-lock skip; the pages'
+ * example: 80 slots at 5 per request cap the running requests at 16.  Host only. */
+int rsc_max_running_requests(int num_slots, int overlap, int skip_decode_lock, int *out);
+
+/* Track plan of one decode step (host arrays): request b is tracked when seq_lens[b] is a
+ * positive multiple of interval; then mask[b] = 1, track_slots[b] =
+ * track_pairs[b][next_idx[b]] and next_idx[b] moves to the other of its ntrack (1 or 2) track
+ * slots (ping-pong); otherwise mask[b] = 0 and track_slots[b] = 0.  The outputs feed
+ * kda_decode_step_track.  Errors: RSC_EINVAL, RSC_ERANGE. */
+int rsc_track_plan(int batch, const int32_t *seq_lens, int interval, const int32_t *track_pairs,
+                   int ntrack, int32_t *next_idx, uint8_t *mask, int32_t *track_slots);
+
 /* Read the pool's device error word into *code and clear it.  Synchronises `stream`.
  * Errors: RSC_EINVAL, RSC_ECUDA. */
 int rsc_get_device_error(rsc_pool *pool, int32_t *code, void *stream);

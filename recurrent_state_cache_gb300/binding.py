@@ -30,7 +30,9 @@ EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
            "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
-           "rsc_status_string")
+           "rsc_status_string", "rsc_slot_alloc_create", "rsc_slot_alloc_destroy",
+           "rsc_slot_alloc_free_count", "rsc_slot_alloc_acquire", "rsc_slot_alloc_release",
+           "rsc_max_running_requests", "rsc_track_plan")
 
 
 class RscError(RuntimeError):
@@ -95,6 +97,14 @@ def lib():
         L.kda_replay_verify_commit.argtypes = [vp, ctypes.POINTER(ReplayRingsDesc), i32, i32,
                                                vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.rsc_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.rsc_slot_alloc_create.argtypes = [i32, ctypes.POINTER(vp)]
+        L.rsc_slot_alloc_destroy.argtypes = [vp]
+        L.rsc_slot_alloc_free_count.argtypes = [vp, ip]
+        L.rsc_slot_alloc_acquire.argtypes = [vp, i32, vp]
+        L.rsc_slot_alloc_release.argtypes = [vp, i32, vp]
+        L.rsc_max_running_requests.argtypes = [i32, i32, i32, ip]
+        L.rsc_track_plan.argtypes = [i32, vp, i32, vp, i32, vp, vp, vp]
         L.rsc_status_string.argtypes = [i32]
         L.rsc_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -403,6 +413,66 @@ def kda_replay_verify_commit(pool: SlotPool, rings: ReplayRings, layer, mode, sl
                                           _p(accept), _stream(stream)),
            "kda_replay_verify_commit")
     return out
+
+
+class SlotAllocator:
+    """Host slot allocator of a pool (rsc_slot_alloc): slots 1..num_slots, row 0 never handed
+    out.  acquire / release take and give back numpy int32 arrays of slot ids."""
+
+    def __init__(self, num_slots: int):
+        import numpy as np
+        self._np = np
+        h = ctypes.c_void_p()
+        _check(lib().rsc_slot_alloc_create(num_slots, ctypes.byref(h)), "rsc_slot_alloc_create")
+        self.handle = h
+        self.num_slots = num_slots
+
+    def free_count(self) -> int:
+        c = ctypes.c_int()
+        _check(lib().rsc_slot_alloc_free_count(self.handle, ctypes.byref(c)), "rsc_slot_alloc_free_count")
+        return c.value
+
+    def acquire(self, n: int):
+        out = self._np.zeros(n, self._np.int32)
+        _check(lib().rsc_slot_alloc_acquire(self.handle, n, out.ctypes.data_as(ctypes.c_void_p)),
+               "rsc_slot_alloc_acquire")
+        return out
+
+    def release(self, slots):
+        a = self._np.ascontiguousarray(slots, self._np.int32)
+        _check(lib().rsc_slot_alloc_release(self.handle, a.size, a.ctypes.data_as(ctypes.c_void_p)),
+               "rsc_slot_alloc_release")
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.rsc_slot_alloc_destroy(h)
+            self.handle = None
+
+
+def max_running_requests(num_slots: int, overlap: bool = True, skip_decode_lock: bool = False) -> int:
+    c = ctypes.c_int()
+    _check(lib().rsc_max_running_requests(num_slots, int(overlap), int(skip_decode_lock),
+                                          ctypes.byref(c)), "rsc_max_running_requests")
+    return c.value
+
+
+def track_plan(seq_lens, interval: int, track_pairs, next_idx):
+    """(mask uint8 [B], track_slots int32 [B]) of one decode step; next_idx (int32 [B], numpy) is
+    advanced in place for the tracked requests."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    tp = np.ascontiguousarray(track_pairs, np.int32)
+    B = sl.size
+    ntrack = tp.size // max(B, 1)
+    assert next_idx.dtype == np.int32 and next_idx.flags["C_CONTIGUOUS"] and next_idx.size == B
+    mask = np.zeros(B, np.uint8)
+    ts = np.zeros(B, np.int32)
+    vp = ctypes.c_void_p
+    _check(lib().rsc_track_plan(B, sl.ctypes.data_as(vp), interval, tp.ctypes.data_as(vp), ntrack,
+                                next_idx.ctypes.data_as(vp), mask.ctypes.data_as(vp),
+                                ts.ctypes.data_as(vp)), "rsc_track_plan")
+    return mask, ts
 
 
 def rsc_get_device_error(pool: SlotPool, stream=None) -> int:

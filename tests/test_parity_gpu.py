@@ -233,6 +233,39 @@ def test_decode_track_parity(cuda_dev, st, io, K, V):
     c.check_pool()
 
 
+def test_allocator_track_plan_and_fused_track_copy(cuda_dev):
+    """Host slot management driving the fused track copy: live and ping-pong track slots from
+    the allocator, the plan of two steps (lengths crossing the interval), each tracked
+    request's snapshot landing in the track slot the plan chose, bit for bit."""
+    from recurrent_state_cache_gb300 import binding
+    H, K, V, B, P = 2, 64, 64, 3, 16
+    c = Case(cuda_dev, 36, L=1, P=P, H=H, K=K, V=V, st=1, io=1, gate=rsc.KDA)
+    alloc = binding.SlotAllocator(P)
+    live = alloc.acquire(B)
+    pairs = alloc.acquire(2 * B).reshape(B, 2)
+    nxt = np.zeros(B, np.int32)
+    lens = np.int32([255, 256, 511])
+    for step in range(2):
+        lens = lens + 1  # the token of this step
+        mask, track = binding.track_plan(lens, 256, pairs, nxt)
+        x = c.proj((B,))
+        g, beta = c.gates((B,))
+        oracle.decode_step_track(c.ref, 0, live, x, c.w, g, beta, mask, track)
+        rsc.kda_decode_step_track(c.pool, 0, to_dev(live, c.dev), to_dev(x, c.dev), c.w_dev,
+                                  to_dev(g, c.dev), to_dev(beta, c.dev), to_dev(mask, c.dev),
+                                  to_dev(track, c.dev))
+        ssm, conv = to_np(c.pool.ssm), to_np(c.pool.conv)
+        for bb in range(B):
+            if mask[bb]:
+                assert np.array_equal(ssm[0, track[bb]], ssm[0, live[bb]])
+                assert np.array_equal(conv[0, track[bb]], conv[0, live[bb]])
+    # lengths 256 (step 0: request 0) and 512 (step 0: request 2; step 1: none) were tracked
+    assert nxt.tolist() == [1, 0, 1]
+    c.check_pool()
+    alloc.release(np.concatenate([live, pairs.ravel()]))
+    assert alloc.free_count() == P
+
+
 # ------------------------------------------------------------------ ReplaySSM
 
 def _rings_np(rings):
