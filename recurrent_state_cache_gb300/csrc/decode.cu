@@ -235,12 +235,13 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   const float rk = 1.0f / sqrtf(kk + kNormEps);
   const float kq = qk * rq * rk;
 
-  float qh[G::EPL], kh[G::EPL], al[G::EPL];
+  constexpr int E2 = G::EPL / 2;
+  float2 qh[E2], kh[E2], al[E2];
 #pragma unroll
-  for (int e = 0; e < G::EPL; ++e) {
-    qh[e] = s_qk[k0 + e] * rq;
-    kh[e] = s_qk[K + k0 + e] * rk;
-    al[e] = expf(gl[e]);
+  for (int e = 0; e < E2; ++e) {
+    qh[e] = make_float2(s_qk[k0 + 2 * e] * rq, s_qk[k0 + 2 * e + 1] * rq);
+    kh[e] = make_float2(s_qk[K + k0 + 2 * e] * rk, s_qk[K + k0 + 2 * e + 1] * rk);
+    al[e] = make_float2(expf(gl[2 * e]), expf(gl[2 * e + 1]));
   }
 
   // 4. window roll: all reads of the cluster happen before any write.
@@ -269,10 +270,15 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       return;
     }
     const int r = G::row(p);
-    float s[G::EPL];
-    unpack16(*reinterpret_cast<const uint4 *>(s_S + (size_t)r * K + k0), s);
-    const float o = delta_rule_row<G::EPL, G::LPR>(s, qh, kh, al, bt, kq, s_v[r]);
-    const uint4 packed = pack16(s);
+    float sf[G::EPL];
+    unpack16(*reinterpret_cast<const uint4 *>(s_S + (size_t)r * K + k0), sf);
+    float2 s[E2];
+#pragma unroll
+    for (int e = 0; e < E2; ++e) s[e] = make_float2(sf[2 * e], sf[2 * e + 1]);
+    const float o = delta_rule_row2<E2, G::LPR>(s, qh, kh, al, bt, kq, s_v[r]);
+#pragma unroll
+    for (int e = 0; e < E2; ++e) { sf[2 * e] = s[e].x; sf[2 * e + 1] = s[e].y; }
+    const uint4 packed = pack16(sf);
     st16(S + (size_t)r * K + k0, packed);
     if (St) st16(St + (size_t)r * K + k0, packed);
     if (k0 == 0) ob[r] = from_f32<IO>(o);

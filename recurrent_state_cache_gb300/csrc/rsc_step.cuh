@@ -87,6 +87,28 @@ __device__ __forceinline__ float delta_rule_row(float (&s)[EPL], const float (&q
   return fmaf(d, kq, w);
 }
 
+// delta_rule_row on fp32 pairs (the packed fp32 instructions: two lanes of arithmetic per
+// issue); the same update, the sums taken pairwise.
+template <int E2, int LPR>
+__device__ __forceinline__ float delta_rule_row2(float2 (&s)[E2], const float2 (&qh)[E2],
+                                                 const float2 (&kh)[E2], const float2 (&al)[E2],
+                                                 float beta, float kq, float v_r) {
+  float2 u2 = make_float2(0.f, 0.f), w2 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < E2; ++e) {
+    s[e] = __fmul2_rn(s[e], al[e]);
+    u2 = __ffma2_rn(s[e], kh[e], u2);
+    w2 = __ffma2_rn(s[e], qh[e], w2);
+  }
+  const float u = group_sum<LPR>(u2.x + u2.y);
+  const float w = group_sum<LPR>(w2.x + w2.y);
+  const float d = beta * (v_r - u);
+  const float2 d2 = make_float2(d, d);
+#pragma unroll
+  for (int e = 0; e < E2; ++e) s[e] = __ffma2_rn(d2, kh[e], s[e]);
+  return fmaf(d, kq, w);
+}
+
 // The same for every row of a register-held tile (rows G::row(p), p < NP).
 template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
 __device__ __forceinline__ void delta_rule_tile(
