@@ -794,7 +794,10 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 
 // Sequential state pass of one (32-row tile, head, sequence): per chunk S1^T = Gamma_c S0^T
 // - Z S0^T + N^T, one 128x32x128 product on the path; S0 of every chunk also goes to the
-// chunk's block for the output kernel.
+// chunk's block for the output kernel.  Z is the product's A operand in tensor memory (two
+// buffers): while chunk c's product runs, the threads move chunk c+1's Z from its operand
+// buffer into the other one (thread k: row k), so the product itself reads only the 8 KB
+// S0 operand from shared memory.
 template <typename IO, int V>
 __global__ void __launch_bounds__(128)
 prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
@@ -832,7 +835,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     mbar_init(&s_barz, 1);
     s_fail = 0;
   }
-  if (warp == 0) { tc::tmem_alloc(&s_taddr, 32); tc::tmem_relinquish(); }
+  if (warp == 0) { tc::tmem_alloc(&s_taddr, 256); tc::tmem_relinquish(); }
   // S0 of chunk c (bf16): into S buffer c & 1 as the MN-major B operand (element (v, k = tid))
   // and into chunk c's block, rows 32 vt .. +31 of the N = V operand there
   auto write_s0 = [&](int c) {
@@ -853,7 +856,8 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tDZ = s_taddr;  // Z S0^T: 32 columns
+  const uint32_t tDZ = s_taddr;  // Z S0^T: columns 0..31; Z of chunk c: columns 64 + 64 (c & 1) ..
+  auto tA = [&](int c) { return tDZ + 64 + 64 * (uint32_t)(c & 1); };
 
   auto issue_load = [&](int c) {
     const int b = c % kNBuf;
@@ -864,9 +868,24 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     bulk_g2s(dst + kSbN, blk + kOffN + (size_t)vt * kK * kVT * 2, kK * kVT * 2, &s_lbar[b]);
     bulk_g2s(dst + kSbGC, blk + kOffGC, kK * 4, &s_lbar[b]);
   };
-  // Shared-memory descriptors of buffer 0 / S buffer 0; the loop moves them by fixed
-  // offsets (one add per MMA instead of a descriptor built from the address).
-  const uint64_t dZ0 = tc::kmajor_desc(smem + kSbZ, kK, 0);
+  // Z of chunk c (operand buffer c % 4, K-major rows) into tensor-memory buffer c & 1: row k
+  // (thread k) as 64 columns of bf16 pairs, four 16-byte reads per 16 columns.
+  auto stage_z = [&](int c) {
+    if (!mbar_wait(&s_lbar[c % kNBuf], (c / kNBuf) & 1)) { s_fail = 1; return; }
+    const unsigned char *zb = smem + (c % kNBuf) * kSBuf + kSbZ;
+#pragma unroll
+    for (int j0 = 0; j0 < kK / 8; j0 += 4) {
+      uint32_t r[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ld16(zb + tc::kmajor_offset(tid, 8 * (j0 + q), kK));
+        r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+      }
+      tc::tmem_st16(tc::tmem_addr(tA(c), 32 * warp, 4 * j0), r);
+    }
+    tc::tmem_wait_st();
+  };
+  // Shared-memory descriptor of S buffer 0; the loop moves it by fixed offsets.
   const uint64_t dS0 = tc::mnmajor_desc(smem + kStS, kVT, 0);
   constexpr uint32_t kIdZ = tc::idesc_bf16_bmn<128, kVT>();
 
@@ -884,27 +903,30 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     if (tid == 0)
       for (int k = 0; k < nch && k < kNBuf - 1; ++k) issue_load(k);
     issued = nch < kNBuf - 1 ? nch : kNBuf - 1;
+    stage_z(0);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (s_fail) ok = false;
+    tc::fence_after_sync();
   }
   int c = 0;
-  for (; c < nch; ++c) {
+  for (; ok && c < nch; ++c) {
     const int b = c % kNBuf;
     const unsigned char *buf = smem + b * kSBuf;
     if (tid == 0) {
-      if (!mbar_wait(&s_lbar[b], (c / kNBuf) & 1)) {
-        s_fail = 1;
-      } else {
-        const uint64_t dz = tc::desc_add(dZ0, b * kSBuf);
-        const uint64_t ds = tc::desc_add(dS0, (c & 1) * kSBytes);
+      // chunk c's Z is in tensor memory (staged and fenced before the last barrier)
+      const uint64_t ds = tc::desc_add(dS0, (c & 1) * kSBytes);
 #pragma unroll
-        for (int ks = 0; ks < kK / 16; ++ks)
-          tc::mma_bf16(tDZ, tc::desc_add(dz, ks * 256), tc::desc_add(ds, ks * 2 * kVT * 16), kIdZ, ks > 0);
-        tc::mma_commit(&s_barz);
-        if (c + kNBuf - 1 < nch) issue_load(c + kNBuf - 1);
-      }
+      for (int ks = 0; ks < kK / 16; ++ks)
+        tc::mma_bf16_ta(tDZ, tA(c) + 8 * ks, tc::desc_add(ds, ks * 2 * kVT * 16), kIdZ, ks > 0);
+      tc::mma_commit(&s_barz);
+      if (c + kNBuf - 1 < nch) issue_load(c + kNBuf - 1);
     }
     if (c + kNBuf - 1 < nch) issued = c + kNBuf;
-    if (!mbar_wait(&s_lbar[b], (c / kNBuf) & 1)) s_fail = 1;  // visible to this thread
-    float nt[kVT];
+    // the next chunk's Z into the other tensor-memory buffer (its last reader, chunk c-1's
+    // product, is done) while this chunk's product runs
+    if (c + 1 < nch) stage_z(c + 1);
+    float nt[kVT];  // operand buffer b is visible: this thread waited for it when staging
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       float f[8];
@@ -943,7 +965,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tDZ, 32);
+  if (warp == 0) tc::tmem_dealloc(tDZ, 256);
 }
 
 // Outputs of one (chunk, head): O = E S0^T + F, one 64 x V x 128 product from the block
