@@ -4,8 +4,10 @@
 Headline (one JSON line on stdout): KDA decode over a Kimi-K3 TP8-shard pool -- 69
 layers, H=12 heads, K=V=128, bf16 state and io, 320 usable slots, 64 requests with
 distinct random slots, one token per request per step.  A step runs all 69 layer
-launches (replayed from a CUDA graph); value = decode tokens/s per layer =
-batch * layers / step time.  The per-step state working set (64 x 69 x 786 KB moved)
+launches (replayed from a CUDA graph) through kda_decode_step_overlap, each layer's decode
+a programmatic dependent of the previous layer's (its state reads overlap that layer's
+tail; the plain kda_decode_step is timed beside it as the decode_plain leg); value =
+decode tokens/s per layer = batch * layers / step time.  The per-step state working set (64 x 69 x 786 KB moved)
 is ~14x the 129 MB L2, so no flush is needed between steps.
 
 Legs reported in the same line (each timed separately with CUDA events):
@@ -242,12 +244,14 @@ class DecodeWorkload:
         self.beta = torch.sigmoid(torch.empty((layers, B, H), device=dev).normal_(0, 1, generator=gen))
         self.w = torch.empty((layers, D, 4), device=dev).normal_(0, 0.5, generator=gen)
         self.out = torch.empty((layers, B, H, V), dtype=idt, device=dev)
+        # consecutive calls are different layers, so the overlapped launch's precondition holds
+        self.overlap = True
 
     def step(self):
         rsc = self.rsc
         for l in range(self.layers):
             rsc.kda_decode_step(self.pool, l, self.slots, self.qkv[l], self.w[l], self.g[l],
-                                self.beta[l], self.out[l])
+                                self.beta[l], self.out[l], overlap=self.overlap)
 
     def bytes_per_launch(self):
         """Algorithmic bytes of one layer launch: per request the state read + written,
@@ -657,7 +661,7 @@ def main(argv=None):
             cur.wait_event(ev_in[i])
             for l in range(a, z):
                 wl.rsc.kda_decode_step(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l],
-                                       wl.beta[l], wl.out[l])
+                                       wl.beta[l], wl.out[l], overlap=True)
             ev_out[i].record(cur)
             cout.wait_event(ev_out[i])
             with torch.cuda.stream(cout):
@@ -679,6 +683,17 @@ def main(argv=None):
     d2h = h_out.numel() * h_out.element_size()
 
     legs = {}
+    # the plain launch (kda_decode_step) of the same workload
+    wl.overlap = False
+    ms_plain = timed(graph_of(wl.step, stream).replay, max(10, min(args.steps, 300)),
+                     args.warmup, stream)
+    wl.overlap = True
+    gbs_plain = bpl / (ms_plain * 1e-3 / wl.layers) / 1e9
+    legs["decode_plain"] = {"config": "the headline workload through kda_decode_step (no overlap)",
+                            "us_per_layer": round(ms_plain * 1e3 / wl.layers, 3),
+                            "tokens_per_s_per_layer": round(wl.B * wl.layers / (ms_plain * 1e-3), 1),
+                            "hbm_gbs": round(gbs_plain, 1),
+                            "frac": round(gbs_plain / peaks["hbm_gbs"], 4)}
     want = set(["gdn", "prefill", "copy", "spec", "replay", "gated", "track"] if args.legs == "all" else
                ([] if args.legs == "none" else args.legs.split(",")))
     if "copy" in want:
@@ -717,7 +732,7 @@ def main(argv=None):
                    "pool_slots": 320, "H": 12, "K": 128, "V": 128, "state_dtype": "bf16",
                    "io_dtype": "bf16", "tokens_per_request_per_step": 1,
                    "l2": "inputs larger than L2: 1.74 GB of state moved per step, no flush",
-                   "launch": f"{args.layers} kda_decode_step launches per step replayed from a CUDA graph",
+                   "launch": f"{args.layers} kda_decode_step_overlap launches per step replayed from a CUDA graph",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -730,7 +745,7 @@ def main(argv=None):
                 "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "per step: pinned host->device copies of every layer's qkv, g, beta, "
-                       "the kda_decode_step calls, device->host copies of every layer's output, "
+                       "the kda_decode_step_overlap calls, device->host copies of every layer's output, "
                        "overlapped layer by layer on a copy-in, a compute and a copy-out stream; "
                        "captured once in a CUDA graph and replayed"},
         "gpu_launches": args.layers * args.steps,

@@ -26,7 +26,7 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Every symbol include/rsc.h declares.
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
-           "kda_decode_step_gated", "kda_decode_step_track",
+           "kda_decode_step_overlap", "kda_decode_step_gated", "kda_decode_step_track",
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
            "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
@@ -84,6 +84,7 @@ def lib():
         L.ssm_pool_bytes.argtypes = [pd, ctypes.POINTER(ctypes.c_uint64),
                                      ctypes.POINTER(ctypes.c_uint64)]
         L.kda_decode_step.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kda_decode_step_overlap.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_track.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_gated.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
@@ -205,7 +206,11 @@ def ssm_pool_bytes(num_layers, num_slots, H, K, V, state_dtype, conv_dtype, gate
 
 
 def kda_decode_step(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, out=None,
-                    stream=None):
+                    stream=None, overlap=False):
+    """One decode step of layer `layer` for the requests in slot_ids.  overlap=True calls
+    kda_decode_step_overlap: the kernel reads slot_ids and this layer's state and window
+    rows of those slots before the earlier kernels on the stream finish, so none of them
+    may write those (see include/rsc.h)."""
     B = slot_ids.shape[0]
     dev = pool.device
     _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
@@ -216,9 +221,10 @@ def kda_decode_step(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, out=N
     if out is None:
         out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
     _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
-    _check(lib().kda_decode_step(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
-                                 _p(g), _p(beta), _p(out), _stream(stream)),
-           "kda_decode_step")
+    fn = lib().kda_decode_step_overlap if overlap else lib().kda_decode_step
+    _check(fn(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w), _p(g), _p(beta),
+              _p(out), _stream(stream)),
+           "kda_decode_step_overlap" if overlap else "kda_decode_step")
     return out
 
 

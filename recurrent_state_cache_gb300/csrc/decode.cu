@@ -9,10 +9,14 @@
 // One thread-block cluster per (request, head): NVT CTAs of NW warps, CTA j owning
 // rows [j*VT, (j+1)*VT) of the head's state S[V][K] (VT = V/NVT; NVT = 1 by default, a
 // whole head per CTA).  Data flow of a CTA:
-//   1. the small inputs are requested first -- qkv, conv taps, gate and beta before the
-//      slot id returns, the slot's window right after -- because the conv depends on
-//      them and, requested later, they would queue in DRAM behind the tile copies of
-//      every CTA on the GPU (measured: the conv then finished ~5 us into a 13 us launch);
+//   1. plain launch: the small inputs are requested first -- qkv, conv taps, gate and beta
+//      before the slot id returns, the slot's window right after -- because the conv
+//      depends on them and, requested later, they would queue in DRAM behind the tile
+//      copies of every CTA on the GPU (measured: the conv then finished ~5 us into a 13 us
+//      launch).  Overlapped launch (kda_decode_step_overlap, a programmatic dependent of
+//      the previous kernel on the stream): the slot id, the window and the first tile
+//      chunks are requested while that kernel still runs, and only the call's own inputs
+//      wait for it (measured on the 69-layer graph: 9.1 instead of 11.3 us per layer);
 //   2. one elected thread starts TMA bulk copies of the CTA's S tile (VT*K contiguous
 //      elements) into shared memory in NCH row chunks, each completing on its own
 //      mbarrier: EARLY chunks at once, the rest as soon as the conv is computed;
@@ -50,7 +54,8 @@ __device__ __forceinline__ float sigmoid_f(float x) {
   return e / (1.f + e);
 }
 
-template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE>
+template <typename ST, typename IO, int K, int V, int NVT, int NW, int NCH, int EARLY, int GATE,
+          bool OVL>
 __global__ void __cluster_dims__(NVT, 1, 1) __launch_bounds__(NW * 32)
 kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                   const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -73,78 +78,124 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   __shared__ float s_v[VT];                    // conv outputs of this tile's value rows
   __shared__ float s_red[3 * NW];
   __shared__ __align__(8) uint64_t s_bar[NCH];
+  // fused gating, KDA: each key channel's gate once per CTA (thread t, channel t)
+  __shared__ float s_gate[GATE == RSC_GATE_KDA ? K : 1];
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int H = pv.H, D = pv.D;
+  const int cv = 2 * H * K + h * V + j * VT + tid;  // value channel of thread tid < VT
+  const int k0 = G::kofs();
+  const bool raw = ex.A_log != nullptr;
 
-  grid_dep_wait();               // previous grid done and visible before any global access
-  grid_dep_launch_dependents();  // the next grid may be scheduled while this one drains
-
-  // 1. Small inputs first.  Their DRAM requests must not queue behind the tile copies of
-  //    every CTA on the GPU, because the conv (and with it every row update) waits on
-  //    them: slot-independent loads (qkv, taps, gate, beta) are issued before the slot id
-  //    returns, the window right after it, and only then the first chunk of the tile.
+  // The call's own inputs: qkv, conv taps, gate and beta, into registers.
   const IO *x = qkv + (size_t)b * D;
   float4 wqk[QK_T];
   IO xqk[QK_T];
-#pragma unroll
-  for (int u = 0; u < QK_T; ++u) {
-    const int i2 = tid + u * NT;
-    if (i2 < 2 * K) {
-      const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
-      wqk[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)c);
-      xqk[u] = x[c];
-    }
-  }
-  const int cv = 2 * H * K + h * V + j * VT + tid;
   float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
   IO xv = from_f32<IO>(0.f);
-  if (tid < VT) {
-    wv = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cv);
-    xv = x[cv];
-  }
-  const int k0 = G::kofs();
-  const bool raw = ex.A_log != nullptr;
   float gl[G::EPL];  // the gate
-  // fused gating, KDA: each key channel's gate once per CTA (thread t, channel t), read by
-  // the lanes after the barrier below
-  __shared__ float s_gate[GATE == RSC_GATE_KDA ? K : 1];
-  float a_raw = 0.f, d_raw = 0.f, s_raw = 0.f;  // raw gate inputs, loaded now, used below
-  if (GATE == RSC_GATE_KDA && raw) {
-    if (tid < K) {
-      a_raw = g[((size_t)b * H + h) * K + tid];
-      d_raw = ex.dt_bias[(size_t)h * K + tid];
+  float a_raw = 0.f, d_raw = 0.f, s_raw = 0.f;  // raw gate inputs, used once the tile is requested
+  float bt = 0.f;
+  auto load_inputs = [&]() {
+#pragma unroll
+    for (int u = 0; u < QK_T; ++u) {
+      const int i2 = tid + u * NT;
+      if (i2 < 2 * K) {
+        const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
+        wqk[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)c);
+        xqk[u] = x[c];
+      }
+    }
+    if (tid < VT) {
+      wv = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cv);
+      xv = x[cv];
+    }
+    if (GATE == RSC_GATE_KDA && raw) {
+      if (tid < K) {
+        a_raw = g[((size_t)b * H + h) * K + tid];
+        d_raw = ex.dt_bias[(size_t)h * K + tid];
+        s_raw = ex.A_log[h];
+      }
+    } else if (GATE == RSC_GATE_KDA) {
+      float4 g4[G::EPL / 4];
+      const float4 *gg = reinterpret_cast<const float4 *>(g + ((size_t)b * H + h) * K + k0);
+#pragma unroll
+      for (int e = 0; e < G::EPL / 4; ++e) g4[e] = gg[e];
+#pragma unroll
+      for (int e = 0; e < G::EPL / 4; ++e) {
+        gl[4 * e] = g4[e].x; gl[4 * e + 1] = g4[e].y; gl[4 * e + 2] = g4[e].z; gl[4 * e + 3] = g4[e].w;
+      }
+    } else {
+      const float gh = g[(size_t)b * H + h];
+#pragma unroll
+      for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
+    }
+    bt = beta[(size_t)b * H + h];
+    if (raw && GATE != RSC_GATE_KDA) {
+      d_raw = ex.dt_bias[h];
       s_raw = ex.A_log[h];
     }
-  } else if (GATE == RSC_GATE_KDA) {
-    float4 g4[G::EPL / 4];
-    const float4 *gg = reinterpret_cast<const float4 *>(g + ((size_t)b * H + h) * K + k0);
-#pragma unroll
-    for (int e = 0; e < G::EPL / 4; ++e) g4[e] = gg[e];
-#pragma unroll
-    for (int e = 0; e < G::EPL / 4; ++e) {
-      gl[4 * e] = g4[e].x; gl[4 * e + 1] = g4[e].y; gl[4 * e + 2] = g4[e].z; gl[4 * e + 3] = g4[e].w;
-    }
-  } else {
-    const float gh = g[(size_t)b * H + h];
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
-  }
-  float bt = beta[(size_t)b * H + h];
-  if (raw && GATE != RSC_GATE_KDA) {
-    d_raw = ex.dt_bias[h];
-    s_raw = ex.A_log[h];
-  }
+  };
 
-  const int slot = slots[b];
-  if (slot < 0 || slot > pv.P) {
-    if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
-    return;  // uniform over the cluster: every CTA of it sees the same slot
+  // The slot's rows: its state tile S and conv window W; the window channels this thread
+  // rolls go to registers, the tile to shared memory in NCH row chunks on their own
+  // mbarriers (chunk c holds the rows of passes [c*PPC, (c+1)*PPC)), EARLY of them now.
+  ST *S = nullptr;
+  IO *W = nullptr;
+  IO keep[QK_T][3];
+  IO keepv[3];
+  auto issue_chunk = [&](int c) {
+    mbar_arrive_expect_tx(&s_bar[c], CHUNK_BYTES);
+    bulk_g2s(reinterpret_cast<char *>(s_S) + c * CHUNK_BYTES,
+             reinterpret_cast<const char *>(S) + c * CHUNK_BYTES, CHUNK_BYTES, &s_bar[c]);
+  };
+  auto load_slot = [&]() -> bool {
+    const int slot = slots[b];
+    if (slot < 0 || slot > pv.P) {
+      if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
+      return false;  // uniform over the cluster: every CTA of it sees the same slot
+    }
+    const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+    S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
+    W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
+#pragma unroll
+    for (int u = 0; u < QK_T; ++u) {
+      const int i2 = tid + u * NT;
+      if (i2 < 2 * K) {
+        const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
+        keep[u][0] = W[c]; keep[u][1] = W[D + c]; keep[u][2] = W[2 * D + c];
+      }
+    }
+    if (tid < VT) { keepv[0] = W[cv]; keepv[1] = W[D + cv]; keepv[2] = W[2 * D + cv]; }
+    if (tid == 0) {
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) mbar_init(&s_bar[c], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int c = 0; c < EARLY; ++c) issue_chunk(c);
+    }
+    return true;
+  };
+
+  // 1. Request order.  Plain launch: the call's inputs first, then the slot id, the window
+  //    and the first tile chunks -- the conv (and with it every row update) waits on the
+  //    small inputs, and requested after the tiles of every CTA on the GPU they would queue
+  //    behind them in DRAM (measured: the conv then finished ~5 us into a 13 us launch).
+  //    Overlapped launch (programmatic dependent of the previous kernel on the stream): the
+  //    slot's rows are requested while that kernel still runs, and only the call's inputs,
+  //    which it may produce, wait for its completion.
+  if constexpr (OVL) {
+    grid_dep_launch_dependents();
+    if (!load_slot()) return;
+    grid_dep_wait();
+    load_inputs();
+  } else {
+    load_inputs();
+    if (!load_slot()) return;
   }
-  const size_t prow = (size_t)layer * (pv.P + 1) + slot;
-  ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
-  IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
   // tracking: the same tile and window channels of the track slot (null when not tracked)
   ST *St = nullptr;
   IO *Wt = nullptr;
@@ -158,22 +209,8 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       Wt = reinterpret_cast<IO *>(pv.conv) + trow * 3 * (size_t)D;
     }
   }
-  IO keep[QK_T][3];
-#pragma unroll
-  for (int u = 0; u < QK_T; ++u) {
-    const int i2 = tid + u * NT;
-    if (i2 < 2 * K) {
-      const int c = i2 < K ? h * K + i2 : H * K + h * K + (i2 - K);
-      keep[u][0] = W[c]; keep[u][1] = W[D + c]; keep[u][2] = W[2 * D + c];
-    }
-  }
-  IO keepv[3];
-  if (tid < VT) { keepv[0] = W[cv]; keepv[1] = W[D + cv]; keepv[2] = W[2 * D + cv]; }
-
-  // 2. The tile, in NCH row chunks on their own mbarriers (chunk c holds the rows of
-  //    passes [c*PPC, (c+1)*PPC)): EARLY chunks now, the rest once the conv is done.
-  // fused gating, formed only now so that waiting for its inputs does not hold back the
-  // requests above (b in bt; GDN: a in gl)
+  // fused gating, formed only now so that waiting for its inputs holds back no request
+  // (b in bt; GDN: a in gl)
   if (raw) {
     if (GATE == RSC_GATE_KDA) {
       if (tid < K) s_gate[tid] = -expf(s_raw) * softplus_f(a_raw + d_raw);
@@ -183,27 +220,14 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       for (int e = 0; e < G::EPL; ++e) gl[e] = gh;
     }
     bt = sigmoid_f(bt);
-  }
-  if (tid == 0) {
+    __syncthreads();  // uniform: raw is a kernel argument
+    if (GATE == RSC_GATE_KDA) {
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) mbar_init(&s_bar[c], 1);
-  }
-  __syncthreads();
-  if (GATE == RSC_GATE_KDA && raw) {
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) gl[e] = s_gate[k0 + e];
-  }
-  auto issue_chunk = [&](int c) {
-    mbar_arrive_expect_tx(&s_bar[c], CHUNK_BYTES);
-    bulk_g2s(reinterpret_cast<char *>(s_S) + c * CHUNK_BYTES,
-             reinterpret_cast<const char *>(S) + c * CHUNK_BYTES, CHUNK_BYTES, &s_bar[c]);
-  };
-  if (tid == 0) {
-#pragma unroll
-    for (int c = 0; c < EARLY; ++c) issue_chunk(c);
+      for (int e = 0; e < G::EPL; ++e) gl[e] = s_gate[k0 + e];
+    }
   }
 
-  // conv of the head's q/k channels and of this tile's value channels; the window values
+  // 2. conv of the head's q/k channels and of this tile's value channels; the window values
   // each thread will roll are kept (keep[u] becomes rows 1, 2 and the input).
 #pragma unroll
   for (int u = 0; u < QK_T; ++u) {
@@ -299,17 +323,17 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #define RSC_DECODE_WARPS_F32 8
 #endif
 
-// Programmatic dependent launch of consecutive decode grids (see launch_pdl).  Off: on
-// GB300 the 69-layer graph ran slower with it (13.6 vs 12.7 us per layer).
-#ifndef RSC_DECODE_PDL
-#define RSC_DECODE_PDL 0
-#endif
 // Bulk copies (and mbarriers) per CTA tile, and how many of them start before the conv.
 #ifndef RSC_DECODE_CHUNKS
 #define RSC_DECODE_CHUNKS 4
 #endif
 #ifndef RSC_DECODE_EARLY_CHUNKS
 #define RSC_DECODE_EARLY_CHUNKS 2
+#endif
+// The same for the overlapped launch, where the early chunks are requested before the wait
+// for the previous kernel.
+#ifndef RSC_DECODE_OVL_EARLY_CHUNKS
+#define RSC_DECODE_OVL_EARLY_CHUNKS 2
 #endif
 
 template <typename ST> struct DecodeTile;
@@ -332,23 +356,25 @@ struct DecodeLaunch {
     constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
     constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
     constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
-    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE>;
+    constexpr int OEARLY = RSC_DECODE_OVL_EARLY_CHUNKS < NCH ? RSC_DECODE_OVL_EARLY_CHUNKS : NCH;
+    auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE, false>;
+    auto kern_ovl = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, OEARLY, GATE, true>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
-          cudaSuccess)
+              cudaSuccess ||
+          cudaFuncSetAttribute(kern_ovl, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SMEM) != cudaSuccess)
         return RSC_ECUDA;
       attr_set = true;
     }
     dim3 grid(NVT, a->pv.H, B);
-#if RSC_DECODE_PDL
-    return launch_pdl(kern, grid, dim3(NW * 32), SMEM, s, a->pv, a->layer, slots,
-                      static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), ex);
-#else
+    if (ex.overlap)
+      return launch_pdl(kern_ovl, grid, dim3(NW * 32), SMEM, s, a->pv, a->layer, slots,
+                        static_cast<const IO *>(qkv), conv_w, g, beta, static_cast<IO *>(out), ex);
     kern<<<grid, NW * 32, SMEM, s>>>(a->pv, a->layer, slots, static_cast<const IO *>(qkv),
                                      conv_w, g, beta, static_cast<IO *>(out), ex);
     return launch_status();
-#endif
   }
 };
 int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,

@@ -797,9 +797,11 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 // chunk's block for the output kernel.  Z is the product's A operand in tensor memory (two
 // buffers): while chunk c's product runs, the threads move chunk c+1's Z from its operand
 // buffer into the other one (thread k: row k), so the product itself reads only the 8 KB
-// S0 operand from shared memory.
+// S0 operand from shared memory.  Warps 0-3 own the state (thread k: column k); warp 4
+// only issues the products and the operand copies, so neither waits behind the other.
+constexpr int kStateThreads = kK + 32;
 template <typename IO, int V>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kStateThreads)
 prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                         const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_base,
                         int T, const uint8_t *__restrict__ has_init, char *__restrict__ blocks) {
@@ -825,10 +827,12 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   bf16 *Sg = reinterpret_cast<bf16 *>(pv.ssm) + ((prow * H + h) * V + (size_t)vt * kVT) * kK;
   auto block = [&](int c) { return blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes; };
 
+  const bool owner = tid < kK;      // warps 0-3: thread k holds column k of the state tile
+  const bool issuer = tid == kK;    // warp 4, lane 0: products and operand copies
   // state tile in registers, transposed: thread k holds S[v][k] for the tile's 32 rows v
   float S[kVT];
 #pragma unroll
-  for (int v = 0; v < kVT; ++v) S[v] = init ? __bfloat162float(Sg[(size_t)v * kK + tid]) : 0.f;
+  for (int v = 0; v < kVT; ++v) S[v] = init && owner ? __bfloat162float(Sg[(size_t)v * kK + tid]) : 0.f;
 
   if (tid == 0) {
     for (int b = 0; b < kNBuf; ++b) mbar_init(&s_lbar[b], 1);
@@ -851,7 +855,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       st16(g + tc::mnmajor_offset(kVT * vt + 8 * q, tid, V), u);
     }
   };
-  if (nch > 0) write_s0(0);
+  if (nch > 0 && owner) write_s0(0);
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -890,20 +894,20 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   constexpr uint32_t kIdZ = tc::idesc_bf16_bmn<128, kVT>();
 
   // Chunk c (operand buffer c % 4, S0 in S buffer c & 1):
-  //   tid 0 issues Z S0^T and commits it, then fetches chunk c+3 into the buffer chunk c-1
-  //   used (its product is done: every thread waited for it before the last barrier)
-  //   -> every thread reads N^T and Gamma_c of its column -> wait Z S0^T -> state update,
-  //   S1 into the other S buffer (its last reader, chunk c-1's product, is done) and into
-  //   chunk c+1's block -> barrier.  Waits on mbarriers are per thread and bounded; a
-  //   failed one sets s_fail, which every thread reads after the next barrier, so all
-  //   leave the loop together.
+  //   the issuer starts Z S0^T and commits it, then fetches chunk c+3 into the buffer chunk
+  //   c-1 used (its last readers finished before the last barrier); meanwhile warps 0-3
+  //   stage chunk c+1's Z, read N^T and Gamma_c of their column, wait for Z S0^T, update
+  //   the state and write S1 into the other S buffer (its last reader, chunk c-1's product,
+  //   is done) and into chunk c+1's block -> barrier.  Waits on mbarriers are per thread and
+  //   bounded; a failed one sets s_fail, which every thread reads after the next barrier, so
+  //   all leave the loop together.
   int issued = 0;  // chunks whose operand copies were requested (every thread keeps it)
   bool ok = true;
   if (nch > 0) {
-    if (tid == 0)
+    if (issuer)
       for (int k = 0; k < nch && k < kNBuf - 1; ++k) issue_load(k);
     issued = nch < kNBuf - 1 ? nch : kNBuf - 1;
-    stage_z(0);
+    if (owner) stage_z(0);
     tc::fence_before_sync();
     __syncthreads();
     if (s_fail) ok = false;
@@ -913,7 +917,7 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   for (; ok && c < nch; ++c) {
     const int b = c % kNBuf;
     const unsigned char *buf = smem + b * kSBuf;
-    if (tid == 0) {
+    if (issuer) {
       // chunk c's Z is in tensor memory (staged and fenced before the last barrier)
       const uint64_t ds = tc::desc_add(dS0, (c & 1) * kSBytes);
 #pragma unroll
@@ -923,30 +927,32 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       if (c + kNBuf - 1 < nch) issue_load(c + kNBuf - 1);
     }
     if (c + kNBuf - 1 < nch) issued = c + kNBuf;
-    // the next chunk's Z into the other tensor-memory buffer (its last reader, chunk c-1's
-    // product, is done) while this chunk's product runs
-    if (c + 1 < nch) stage_z(c + 1);
-    float nt[kVT];  // operand buffer b is visible: this thread waited for it when staging
+    if (owner) {
+      // the next chunk's Z into the other tensor-memory buffer (its last reader, chunk c-1's
+      // product, is done) while this chunk's product runs
+      if (c + 1 < nch) stage_z(c + 1);
+      float nt[kVT];  // operand buffer b is visible: this thread waited for it when staging
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float f[8];
-      unpack16(ld16(buf + kSbN + tid * kVT * 2 + 16 * q), f);
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+        unpack16(ld16(buf + kSbN + tid * kVT * 2 + 16 * q), f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) nt[8 * q + e] = f[e];
-    }
-    const float gc = reinterpret_cast<const float *>(buf + kSbGC)[tid];
-    if (!mbar_wait(&s_barz, c & 1)) s_fail = 1;
-    tc::fence_after_sync();
-    {
-      // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] - (Z S0^T)[k][:] + N^T[k][:] for this thread's k
-      float d[kVT];
-      tc::tmem_ld32(tc::tmem_addr(tDZ, 32 * warp, 0), d);
+        for (int e = 0; e < 8; ++e) nt[8 * q + e] = f[e];
+      }
+      const float gc = reinterpret_cast<const float *>(buf + kSbGC)[tid];
+      if (!mbar_wait(&s_barz, c & 1)) s_fail = 1;
+      tc::fence_after_sync();
+      {
+        // S_c^T[k][:] = Gamma_c[k] S0^T[k][:] - (Z S0^T)[k][:] + N^T[k][:] for this thread's k
+        float d[kVT];
+        tc::tmem_ld32(tc::tmem_addr(tDZ, 32 * warp, 0), d);
 #pragma unroll
-      for (int i = 0; i < kVT; ++i) S[i] = fmaf(gc, S[i], nt[i] - d[i]);
-    }
-    if (c + 1 < nch) {
-      write_s0(c + 1);
-      tc::fence_smem_to_async();
+        for (int i = 0; i < kVT; ++i) S[i] = fmaf(gc, S[i], nt[i] - d[i]);
+      }
+      if (c + 1 < nch) {
+        write_s0(c + 1);
+        tc::fence_smem_to_async();
+      }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -954,12 +960,12 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     tc::fence_after_sync();
   }
   if (!ok) {
-    if (tid == 0) {
+    if (issuer) {
       flag_error(pv.err, RSC_DEVERR_TIMEOUT);
       // let every requested bulk copy land before the shared memory is released
       for (int k = c; k < issued; ++k) mbar_wait(&s_lbar[k % kNBuf], (k / kNBuf) & 1);
     }
-  } else {
+  } else if (owner) {
 #pragma unroll
     for (int v = 0; v < kVT; ++v) Sg[(size_t)v * kK + tid] = __float2bfloat16_rn(S[v]);
   }
@@ -1075,7 +1081,7 @@ static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *
                                                           conv_w, g, beta, blocks);
     if (launch_status() != RSC_OK) return RSC_ECUDA;
   }
-  state_kernel<<<dim3(V / kVT, a.pv.H, N), 128, kStateSmem, s>>>(a.pv, a.layer, slots, cu,
+  state_kernel<<<dim3(V / kVT, a.pv.H, N), kStateThreads, kStateSmem, s>>>(a.pv, a.layer, slots, cu,
                                                                    chunk_base, T, has_init, blocks);
   if (launch_status() != RSC_OK) return RSC_ECUDA;
   if (cap > 0 && T > 0)

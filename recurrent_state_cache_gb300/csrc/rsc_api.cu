@@ -102,6 +102,23 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
                             rsc::DecodeExtras{}, as_stream(stream));
 }
 
+int kda_decode_step_overlap(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                            const void *qkv, const float *conv_w, const float *g,
+                            const float *beta, void *out, void *stream) {
+  if (!pool) return RSC_EINVAL;
+  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
+    return RSC_ERANGE;
+  if (batch == 0) return RSC_OK;
+  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
+      !aligned(beta, 4) || !aligned(slot_ids, 4))
+    return RSC_EALIGN;
+  rsc::DecodeExtras ex;
+  ex.overlap = true;
+  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
+                            ex, as_stream(stream));
+}
+
 int kda_decode_step_track(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                           const void *qkv, const float *conv_w, const float *g, const float *beta,
                           void *out, const uint8_t *track_mask, const int32_t *track_slots,

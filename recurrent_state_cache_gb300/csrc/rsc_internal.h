@@ -21,6 +21,7 @@ struct DecodeExtras {
   const float *A_log = nullptr, *dt_bias = nullptr;  // fused gating: A_log [H], dt_bias [H][K] / [H]
   const uint8_t *track_mask = nullptr;               // tracking: [B]
   const int32_t *track_slots = nullptr;              // [B]
+  bool overlap = false;  // programmatic dependent launch; the slot's rows read before the wait
 };
 int launch_decode(const LayerArgs &a, const int32_t *slots, int B, const void *qkv,
                   const float *conv_w, const float *g, const float *beta, void *out,
@@ -86,9 +87,8 @@ inline int launch_status() {
 
 // Launch with programmatic stream serialization: the grid may be scheduled while the
 // previous kernel on the stream drains.  Kernels launched this way call grid_dep_wait()
-// before touching global memory, which waits for the previous grid to complete and its
-// writes to be visible, so stream-order semantics are unchanged; only the launch latency
-// and ramp of the new grid overlap the tail of the old one.
+// before they touch anything that kernel may write, which waits for it to complete and its
+// writes to be visible; what they read before the wait is the caller's contract.
 template <typename... KArgs, typename... Args>
 int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                Args... args) {

@@ -77,6 +77,12 @@ def test_calls_reject_bad_arguments_before_launch(rsc):
         assert L.kda_decode_step(h, 0, p, 1, None, p, p, p, p, None) == rsc.RSC_EINVAL
         assert L.kda_decode_step(h, 0, p, 1, ctypes.c_void_p(0x40008), p, p, p, p,
                                  None) == rsc.RSC_EALIGN
+        # the overlapped form validates the same way
+        assert L.kda_decode_step_overlap(h, 2, p, 1, p, p, p, p, p, None) == rsc.RSC_ERANGE
+        assert L.kda_decode_step_overlap(h, 0, None, 0, None, None, None, None, None, None) == 0
+        assert L.kda_decode_step_overlap(h, 0, p, 1, p, p, None, p, p, None) == rsc.RSC_EINVAL
+        assert L.kda_decode_step_overlap(h, 0, p, 1, p, p, p, p, ctypes.c_void_p(0x40004),
+                                         None) == rsc.RSC_EALIGN
         # spec: L not a power of two, T > L, bad mode
         assert L.kda_spec_verify_commit(h, 0, 0, p, 1, 3, 6, p, p, p, p, p, p, p, None,
                                         None) == rsc.RSC_ERANGE

@@ -105,6 +105,48 @@ def test_decode_bad_slot_sets_flag_and_skips_row(cuda_dev):
     assert max_rel_err(widen(s_now[0, 2]), widen(c.ref.ssm[0, 2])) <= TOL[0]
 
 
+@pytest.mark.parametrize("st,io,gate,H,K,V,B", [
+    (1, 1, rsc.KDA, 3, 128, 128, 5),
+    (0, 1, rsc.GDN, 2, 128, 128, 3),
+])
+def test_decode_overlap_layer_chain(cuda_dev, st, io, gate, H, K, V, B):
+    """kda_decode_step_overlap over a chain of layers on one stream, no synchronisation
+    between calls: each layer's qkv is produced by a torch kernel launched right before its
+    decode (the input the kernel must wait for), the other layers' decodes are the pending
+    work its early state reads overlap.  Against the oracle, and bit-identical to the plain
+    launch on a copy of the pool."""
+    L, P, steps = 4, 9, 2
+    c = Case(cuda_dev, 7, L=L, P=P, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    plain = rsc.SlotPool(L, P, H, K, V, st, io, gate, cuda_dev, ssm=c.pool.ssm.clone(),
+                         conv=c.pool.conv.clone())
+    slots = inputs.distinct_slots(c.r, B, P)
+    slots_d = to_dev(slots, c.dev)
+    for _ in range(steps):
+        xs = [c.proj((B,)) for _ in range(L)]
+        gb = [c.gates((B,)) for _ in range(L)]
+        src = [to_dev(x, c.dev) for x in xs]
+        gd = [(to_dev(g, c.dev), to_dev(b, c.dev)) for g, b in gb]
+        torch.cuda.synchronize()
+        outs, outs_plain = [], []
+        for l in range(L):
+            x = torch.zeros_like(src[l])
+            torch.mul(src[l], 1, out=x)  # produced by a kernel just before the decode
+            outs.append(rsc.kda_decode_step(c.pool, l, slots_d, x, c.w_dev, gd[l][0], gd[l][1],
+                                            overlap=True))
+        for l in range(L):
+            outs_plain.append(rsc.kda_decode_step(plain, l, slots_d, src[l], c.w_dev, gd[l][0],
+                                                  gd[l][1]))
+        torch.cuda.synchronize()
+        for l in range(L):
+            o_ref = oracle.decode_step(c.ref, l, slots, xs[l], c.w, gb[l][0], gb[l][1])
+            err = max_rel_err(widen(to_np(outs[l])), widen(o_ref))
+            assert err <= tol(c.st, c.io), f"layer {l}: output max rel err {err}"
+            assert torch.equal(outs[l], outs_plain[l]), f"layer {l}: overlap != plain"
+    c.check_pool()
+    assert torch.equal(c.pool.ssm, plain.ssm) and torch.equal(c.pool.conv, plain.conv)
+    assert rsc.rsc_get_device_error(plain) == 0
+
+
 # ------------------------------------------------------------------ slot copy
 
 @pytest.mark.parametrize("st,io,layer", [(1, 1, -1), (0, 1, 1), (0, 0, -1)])
