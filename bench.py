@@ -434,18 +434,20 @@ def leg_gated(dev, peaks, stream, wl):
     A_log = torch.empty((wl.layers, H), device=dev).normal_(0, 0.5, generator=gen)
     dt = torch.empty((wl.layers, H, K), device=dev).normal_(0, 1, generator=gen)
 
-    def step():
+    def step(overlap):
         for l in range(wl.layers):
-            rsc.kda_decode_step_gated(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
-                                      A_log[l], dt[l], out=wl.out[l])
-    graph = graph_of(step, stream)
-    ms = timed(graph.replay, 50, 5, stream)
+            rsc.kda_decode_step_ex(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
+                                   out=wl.out[l], A_log=A_log[l], dt_bias=dt[l], overlap=overlap)
+    ms = timed(graph_of(lambda: step(True), stream).replay, 50, 5, stream)
+    ms_plain = timed(graph_of(lambda: step(False), stream).replay, 50, 5, stream)
     tok = wl.B / (ms * 1e-3 / wl.layers)
     bytes_layer = wl.bytes_per_launch() + H * 4 + H * K * 4
-    return {"config": "headline decode workload, gates from raw projections in the kernel",
+    gbs = bytes_layer * wl.layers / (ms * 1e-3) / 1e9
+    return {"config": "headline decode workload, gates from raw projections in the kernel "
+                      "(kda_decode_step_ex, overlapped launch)",
             "ms_per_step": round(ms, 4), "tokens_per_s_per_layer": round(tok, 1),
-            "hbm_gbs": round(bytes_layer * wl.layers / (ms * 1e-3) / 1e9, 1),
-            "frac": round(bytes_layer * wl.layers / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+            "hbm_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "plain_launch_ms_per_step": round(ms_plain, 4)}
 
 
 def leg_track(dev, peaks, stream, wl):
@@ -459,21 +461,27 @@ def leg_track(dev, peaks, stream, wl):
     track = torch.tensor(free, dtype=torch.int32, device=dev)
     mask = torch.ones(wl.B, dtype=torch.uint8, device=dev)
 
-    def fused():
+    def fused(overlap=True):
         for l in range(wl.layers):
-            rsc.kda_decode_step_track(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
-                                      mask, track, out=wl.out[l])
+            rsc.kda_decode_step_ex(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
+                                   out=wl.out[l], track_mask=mask, track_slots=track,
+                                   overlap=overlap)
 
     def separate():
         for l in range(wl.layers):
-            rsc.kda_decode_step(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l], wl.out[l])
+            rsc.kda_decode_step(wl.pool, l, wl.slots, wl.qkv[l], wl.w[l], wl.g[l], wl.beta[l],
+                                wl.out[l], overlap=True)
             rsc.ssm_slot_copy(wl.pool, l, wl.slots, track, mask)
     ms_f = timed(graph_of(fused, stream).replay, 30, 5, stream)
+    ms_fp = timed(graph_of(lambda: fused(False), stream).replay, 30, 5, stream)
     ms_s = timed(graph_of(separate, stream).replay, 30, 5, stream)
     row = wl.H * wl.V * wl.K * 2 + 3 * wl.D * 2          # one slot row of a layer (bf16)
     bytes_f = (wl.bytes_per_launch() + wl.B * row) * wl.layers  # the track rows written once more
-    return {"config": "headline decode workload, all 64 requests tracked every step",
+    return {"config": "headline decode workload, all 64 requests tracked every step "
+                      "(kda_decode_step_ex, overlapped launch; separate = overlapped decode then "
+                      "ssm_slot_copy per layer)",
             "fused_ms_per_step": round(ms_f, 4), "separate_ms_per_step": round(ms_s, 4),
+            "fused_plain_launch_ms_per_step": round(ms_fp, 4),
             "fused_tokens_per_s_per_layer": round(wl.B / (ms_f * 1e-3 / wl.layers), 1),
             "fused_hbm_gbs": round(bytes_f / (ms_f * 1e-3) / 1e9, 1),
             "fused_frac": round(bytes_f / (ms_f * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}

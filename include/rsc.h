@@ -122,6 +122,26 @@ int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batc
                     const void *qkv, const float *conv_w, const float *g,
                     const float *beta, void *out, void *stream);
 
+/* Options of kda_decode_step_ex; zero-initialise and set what is wanted. */
+#define RSC_DECODE_OVERLAP 1 /* launch as kda_decode_step_overlap does (same precondition) */
+typedef struct rsc_decode_opts {
+  const float *A_log;          /* fused gating (see kda_decode_step_gated) when non-NULL:  */
+  const float *dt_bias;        /*   g and beta then carry the raw projections a and b     */
+  const uint8_t *track_mask;   /* fused track copy (see kda_decode_step_track) when       */
+  const int32_t *track_slots;  /*   non-NULL                                               */
+  int flags;                   /* RSC_DECODE_OVERLAP or 0                                  */
+} rsc_decode_opts;
+
+/* The general decode call: kda_decode_step with any combination of fused gating, the fused
+ * track copy and the overlapped launch; opts NULL is kda_decode_step.  Each option keeps the
+ * layouts, alignment and preconditions of the entry point that has it alone; with gating and
+ * tracking together the track slot receives the state updated with the formed gates.
+ * Errors: as kda_decode_step; RSC_EINVAL also for an unknown flag, or for A_log without
+ * dt_bias or track_mask without track_slots (or the reverse). */
+int kda_decode_step_ex(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                       const void *qkv, const float *conv_w, const float *g, const float *beta,
+                       void *out, const rsc_decode_opts *opts, void *stream);
+
 /* kda_decode_step as a programmatic dependent launch of the previous kernel on `stream`, so
  * that this layer's state reads overlap the tail of the work before it.  The kernel may
  * start while earlier kernels on the stream still run; BEFORE waiting for them it reads

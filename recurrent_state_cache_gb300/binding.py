@@ -26,7 +26,8 @@ TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Every symbol include/rsc.h declares.
 EXPORTS = ("ssm_pool_create", "ssm_pool_destroy", "ssm_pool_bytes", "kda_decode_step",
-           "kda_decode_step_overlap", "kda_decode_step_gated", "kda_decode_step_track",
+           "kda_decode_step_overlap", "kda_decode_step_ex", "kda_decode_step_gated",
+           "kda_decode_step_track",
            "kda_prefill_workspace_size", "kda_prefill_chunk", "kda_prefill_chunk_noalloc",
            "ssm_slot_copy",
            "kda_spec_verify_commit", "kda_replay_verify_commit", "rsc_get_device_error",
@@ -51,6 +52,18 @@ class PoolDesc(ctypes.Structure):
         ("ssm_base", ctypes.c_void_p), ("conv_base", ctypes.c_void_p),
         ("dev_error", ctypes.c_void_p),
     ]
+
+
+class DecodeOpts(ctypes.Structure):
+    """rsc_decode_opts of include/rsc.h."""
+    _fields_ = [
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("track_mask", ctypes.c_void_p), ("track_slots", ctypes.c_void_p),
+        ("flags", ctypes.c_int32),
+    ]
+
+
+DECODE_OVERLAP = 1
 
 
 class ReplayRingsDesc(ctypes.Structure):
@@ -85,6 +98,7 @@ def lib():
                                      ctypes.POINTER(ctypes.c_uint64)]
         L.kda_decode_step.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_overlap.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kda_decode_step_ex.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_track.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step_gated.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
@@ -287,6 +301,38 @@ def kda_prefill_chunk_noalloc(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, 
                                            T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
                                            _p(beta), _p(out), _stream(stream)),
            "kda_prefill_chunk_noalloc")
+    return out
+
+
+def kda_decode_step_ex(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, out=None,
+                       A_log=None, dt_bias=None, track_mask=None, track_slots=None,
+                       overlap=False, stream=None):
+    """The general decode call (kda_decode_step_ex): any combination of fused gating (A_log,
+    dt_bias given; g and beta are then the raw projections a and b), the fused track copy
+    (track_mask, track_slots given) and the overlapped launch."""
+    B = slot_ids.shape[0]
+    dev = pool.device
+    _need(slot_ids, "slot_ids", torch.int32, (B,), dev)
+    _need(qkv, "qkv", pool.io_dtype, (B, pool.D), dev)
+    _need(conv_w, "conv_w", torch.float32, (pool.D, 4), dev)
+    _need(g, "g", torch.float32, pool.gate_shape((B,)), dev)
+    _need(beta, "beta", torch.float32, (B, pool.H), dev)
+    if A_log is not None or dt_bias is not None:
+        n = pool.K if pool.gate == KDA else 1
+        _need(A_log, "A_log", torch.float32, (pool.H,), dev)
+        _need(dt_bias, "dt_bias", torch.float32, (pool.H, n) if n > 1 else (pool.H,), dev)
+    if track_mask is not None or track_slots is not None:
+        _need(track_mask, "track_mask", torch.uint8, (B,), dev)
+        _need(track_slots, "track_slots", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
+    _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
+    addr = lambda t: None if t is None else t.data_ptr()
+    opts = DecodeOpts(addr(A_log), addr(dt_bias), addr(track_mask), addr(track_slots),
+                      DECODE_OVERLAP if overlap else 0)
+    _check(lib().kda_decode_step_ex(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                    _p(g), _p(beta), _p(out), ctypes.byref(opts),
+                                    _stream(stream)), "kda_decode_step_ex")
     return out
 
 

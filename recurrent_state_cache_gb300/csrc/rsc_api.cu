@@ -44,6 +44,27 @@ rsc::LayerArgs layer_args(const rsc_pool *p, int layer) {
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// Shared checks and launch of every decode entry point; need_track / need_gate: the entry
+// point's own option pointers are required.
+int decode_impl(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch, const void *qkv,
+                const float *conv_w, const float *g, const float *beta, void *out,
+                const rsc::DecodeExtras &ex, bool need_track, bool need_gate, void *stream) {
+  if (!pool) return RSC_EINVAL;
+  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
+    return RSC_ERANGE;
+  if (batch == 0) return RSC_OK;
+  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
+  if (need_track && (!ex.track_mask || !ex.track_slots)) return RSC_EINVAL;
+  if (need_gate && (!ex.A_log || !ex.dt_bias)) return RSC_EINVAL;
+  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
+      !aligned(beta, 4) || !aligned(slot_ids, 4))
+    return RSC_EALIGN;
+  if (ex.A_log && (!aligned(ex.dt_bias, 16) || !aligned(ex.A_log, 4))) return RSC_EALIGN;
+  if (ex.track_slots && !aligned(ex.track_slots, 4)) return RSC_EALIGN;
+  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
+                            ex, as_stream(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -87,74 +108,59 @@ int ssm_pool_destroy(rsc_pool *pool) {
   return RSC_OK;
 }
 
+int kda_decode_step_ex(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
+                       const void *qkv, const float *conv_w, const float *g, const float *beta,
+                       void *out, const rsc_decode_opts *opts, void *stream) {
+  rsc::DecodeExtras ex;
+  if (opts) {
+    if ((opts->flags & ~RSC_DECODE_OVERLAP) != 0) return RSC_EINVAL;
+    if ((opts->A_log == nullptr) != (opts->dt_bias == nullptr)) return RSC_EINVAL;
+    if ((opts->track_mask == nullptr) != (opts->track_slots == nullptr)) return RSC_EINVAL;
+    ex.A_log = opts->A_log;
+    ex.dt_bias = opts->dt_bias;
+    ex.track_mask = opts->track_mask;
+    ex.track_slots = opts->track_slots;
+    ex.overlap = (opts->flags & RSC_DECODE_OVERLAP) != 0;
+  }
+  return decode_impl(pool, layer, slot_ids, batch, qkv, conv_w, g, beta, out, ex, false, false,
+                     stream);
+}
+
 int kda_decode_step(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                     const void *qkv, const float *conv_w, const float *g, const float *beta,
                     void *out, void *stream) {
-  if (!pool) return RSC_EINVAL;
-  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
-    return RSC_ERANGE;
-  if (batch == 0) return RSC_OK;
-  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
-      !aligned(beta, 4) || !aligned(slot_ids, 4))
-    return RSC_EALIGN;
-  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
-                            rsc::DecodeExtras{}, as_stream(stream));
+  return decode_impl(pool, layer, slot_ids, batch, qkv, conv_w, g, beta, out,
+                     rsc::DecodeExtras{}, false, false, stream);
 }
 
 int kda_decode_step_overlap(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                             const void *qkv, const float *conv_w, const float *g,
                             const float *beta, void *out, void *stream) {
-  if (!pool) return RSC_EINVAL;
-  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
-    return RSC_ERANGE;
-  if (batch == 0) return RSC_OK;
-  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out) return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
-      !aligned(beta, 4) || !aligned(slot_ids, 4))
-    return RSC_EALIGN;
   rsc::DecodeExtras ex;
   ex.overlap = true;
-  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
-                            ex, as_stream(stream));
+  return decode_impl(pool, layer, slot_ids, batch, qkv, conv_w, g, beta, out, ex, false, false,
+                     stream);
 }
 
 int kda_decode_step_track(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                           const void *qkv, const float *conv_w, const float *g, const float *beta,
                           void *out, const uint8_t *track_mask, const int32_t *track_slots,
                           void *stream) {
-  if (!pool) return RSC_EINVAL;
-  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
-    return RSC_ERANGE;
-  if (batch == 0) return RSC_OK;
-  if (!slot_ids || !qkv || !conv_w || !g || !beta || !out || !track_mask || !track_slots)
-    return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
-      !aligned(beta, 4) || !aligned(slot_ids, 4) || !aligned(track_slots, 4))
-    return RSC_EALIGN;
   rsc::DecodeExtras ex;
   ex.track_mask = track_mask;
   ex.track_slots = track_slots;
-  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
-                            ex, as_stream(stream));
+  return decode_impl(pool, layer, slot_ids, batch, qkv, conv_w, g, beta, out, ex, true, false,
+                     stream);
 }
 
 int kda_decode_step_gated(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                           const void *qkv, const float *conv_w, const float *a, const float *b,
                           const float *A_log, const float *dt_bias, void *out, void *stream) {
-  if (!pool) return RSC_EINVAL;
-  if (layer < 0 || layer >= pool->d.num_layers || batch < 0 || batch > kMaxGrid)
-    return RSC_ERANGE;
-  if (batch == 0) return RSC_OK;
-  if (!slot_ids || !qkv || !conv_w || !a || !b || !A_log || !dt_bias || !out) return RSC_EINVAL;
-  if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(a, 16) ||
-      !aligned(dt_bias, 16) || !aligned(b, 4) || !aligned(A_log, 4) || !aligned(slot_ids, 4))
-    return RSC_EALIGN;
   rsc::DecodeExtras ex;
   ex.A_log = A_log;
   ex.dt_bias = dt_bias;
-  return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, a, b, out, ex,
-                            as_stream(stream));
+  return decode_impl(pool, layer, slot_ids, batch, qkv, conv_w, a, b, out, ex, false, true,
+                     stream);
 }
 
 int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tokens,

@@ -77,6 +77,25 @@ def test_calls_reject_bad_arguments_before_launch(rsc):
         assert L.kda_decode_step(h, 0, p, 1, None, p, p, p, p, None) == rsc.RSC_EINVAL
         assert L.kda_decode_step(h, 0, p, 1, ctypes.c_void_p(0x40008), p, p, p, p,
                                  None) == rsc.RSC_EALIGN
+        # the general call: option pairs must be complete, flags known
+        O = rsc.DecodeOpts
+        ob = lambda *a: ctypes.byref(O(*a))
+        assert L.kda_decode_step_ex(h, 0, p, 1, p, p, p, p, p, ob(None, None, None, None, 2),
+                                    None) == rsc.RSC_EINVAL
+        assert L.kda_decode_step_ex(h, 0, p, 1, p, p, p, p, p, ob(0x40000, None, None, None, 0),
+                                    None) == rsc.RSC_EINVAL
+        assert L.kda_decode_step_ex(h, 0, p, 1, p, p, p, p, p, ob(None, None, 0x40000, None, 1),
+                                    None) == rsc.RSC_EINVAL
+        assert L.kda_decode_step_ex(h, 0, p, 1, p, p, p, p, p,
+                                    ob(0x40000, 0x40008, None, None, 0), None) == rsc.RSC_EALIGN
+        assert L.kda_decode_step_ex(h, 0, p, 1, p, p, p, p, p,
+                                    ob(None, None, 0x40000, 0x40002, 0), None) == rsc.RSC_EALIGN
+        assert L.kda_decode_step_ex(h, 0, None, 0, None, None, None, None, None,
+                                    ob(0x40000, 0x40000, 0x40000, 0x40000, 1), None) == 0
+        assert L.kda_decode_step_ex(h, 5, p, 1, p, p, p, p, p, None, None) == rsc.RSC_ERANGE
+        # the tracked and gated forms still require their own pointers
+        assert L.kda_decode_step_track(h, 0, p, 1, p, p, p, p, p, None, p, None) == rsc.RSC_EINVAL
+        assert L.kda_decode_step_gated(h, 0, p, 1, p, p, p, p, p, None, p, None) == rsc.RSC_EINVAL
         # the overlapped form validates the same way
         assert L.kda_decode_step_overlap(h, 2, p, 1, p, p, p, p, p, None) == rsc.RSC_ERANGE
         assert L.kda_decode_step_overlap(h, 0, None, 0, None, None, None, None, None, None) == 0

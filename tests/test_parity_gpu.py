@@ -275,6 +275,46 @@ def test_decode_track_parity(cuda_dev, st, io, K, V):
     c.check_pool()
 
 
+@pytest.mark.parametrize("st,io,gate,K,V", [(1, 1, rsc.KDA, 128, 128), (0, 0, rsc.GDN, 64, 64)])
+def test_decode_ex_gating_tracking_overlap(cuda_dev, st, io, gate, K, V):
+    """kda_decode_step_ex with every option at once -- gates formed from raw projections, the
+    track copy fused, the overlapped launch -- over a chain of three layers: against the
+    oracle's gating followed by its decode and masked track copy, and bit-identical to the
+    same options without the overlap on a copy of the pool."""
+    H, B, L, P = 2, 4, 3, 12
+    c = Case(cuda_dev, 36, L=L, P=P, H=H, K=K, V=V, st=st, io=io, gate=gate)
+    plain = rsc.SlotPool(L, P, H, K, V, st, io, gate, cuda_dev, ssm=c.pool.ssm.clone(),
+                         conv=c.pool.conv.clone())
+    n = K if gate == rsc.KDA else 1
+    slots = np.int32([2, 5, 7, 9])
+    track = np.int32([11, 1, 12, 3])
+    mask = np.uint8([1, 0, 1, 1])
+    A_log = c.r.normal(0, 0.5, size=(H,)).astype(np.float32)
+    dt = c.r.normal(0, 1, size=(H, n)).astype(np.float32)
+    dev = lambda a: to_dev(a, c.dev)
+    dt_dev = dev(dt if n > 1 else dt[:, 0].copy())
+    xs = [c.proj((B,)) for _ in range(L)]
+    raws = [(c.r.normal(0, 2, size=(B, H, n)).astype(np.float32),
+             c.r.normal(0, 2, size=(B, H)).astype(np.float32)) for _ in range(L)]
+    a_dev = [dev(a if n > 1 else a[:, :, 0].copy()) for a, _ in raws]
+    b_dev = [dev(b) for _, b in raws]
+    args = dict(A_log=dev(A_log), dt_bias=dt_dev, track_mask=dev(mask), track_slots=dev(track))
+    sl = dev(slots)
+    torch.cuda.synchronize()
+    outs = [rsc.kda_decode_step_ex(c.pool, l, sl, dev(xs[l]), c.w_dev, a_dev[l], b_dev[l],
+                                   overlap=True, **args) for l in range(L)]
+    outs_plain = [rsc.kda_decode_step_ex(plain, l, sl, dev(xs[l]), c.w_dev, a_dev[l], b_dev[l],
+                                         **args) for l in range(L)]
+    torch.cuda.synchronize()
+    for l in range(L):
+        g, beta = oracle.gates_from_raw(c.ref, raws[l][0], raws[l][1], A_log, dt)
+        o_ref = oracle.decode_step_track(c.ref, l, slots, xs[l], c.w, g, beta, mask, track)
+        assert max_rel_err(widen(to_np(outs[l])), widen(o_ref)) <= tol(st, io), f"layer {l}"
+        assert torch.equal(outs[l], outs_plain[l]), f"layer {l}: overlap != plain"
+    c.check_pool()
+    assert torch.equal(c.pool.ssm, plain.ssm) and torch.equal(c.pool.conv, plain.conv)
+
+
 def test_allocator_track_plan_and_fused_track_copy(cuda_dev):
     """Host slot management driving the fused track copy: live and ping-pong track slots from
     the allocator, the plan of two steps (lengths crossing the interval), each tracked
