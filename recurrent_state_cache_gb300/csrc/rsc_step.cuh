@@ -242,6 +242,27 @@ __device__ __forceinline__ void delta_rule_tile2(
   }
 }
 
+// Butterfly reduce-scatter over the M lanes of an aligned lane group (M a power of two, at
+// most 32): on entry every lane holds M partial values x[0..M); on return lane i of the group
+// holds the sum over the group of entry i.  M - 1 shuffles in all, where M separate group
+// sums take M log2(M).  x is clobbered.
+template <int M>
+__device__ __forceinline__ float group_reduce_scatter(float (&x)[M]) {
+  const int li = threadIdx.x & (M - 1);
+#pragma unroll
+  for (int n = M; n > 1; n >>= 1) {
+    const int m = n >> 1;
+    const bool up = (li & m) != 0;  // this lane keeps the upper half of the current list
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = up ? x[i] : x[i + m];
+      const float keep = up ? x[i + m] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return x[0];
+}
+
 // The conv of one channel: taps 0..2 on the window rows (oldest first), tap 3 on x.
 __device__ __forceinline__ float conv4(const float4 &w, float w0, float w1, float w2, float x) {
   return fmaf(w.w, x, fmaf(w.z, w2, fmaf(w.y, w1, w.x * w0)));

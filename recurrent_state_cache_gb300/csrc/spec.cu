@@ -20,21 +20,39 @@
 // REPLAY (ReplaySSM, same page, ReplaySSM section): the same pass, but instead of S_t each
 // token leaves its records in the slot's rings at entry (pos + t) mod depth: the delta d
 // (rows of the tile, by their owner), the normalised key, the pre-norm key (the CTA owning
-// the key channels' windows), the log-decay and beta (tile 0).  COMMIT of the replay path
-// replays the accepted tokens from the slot state out of those records.
+// the key channels' windows), the log-decay and beta (tile 0).  No intermediate state is
+// stored, so the token loop is replaced by a closed form per block of eight tokens (every
+// row's outputs and deltas from the tile at the block start: 16 independent row dots, one
+// butterfly reduction, an 8x8 triangular solve; see replay_block), on a whole head per CTA.
+// COMMIT of the replay path replays the accepted tokens from the slot state out of those
+// records.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
 namespace rsc {
 
-// Minimum resident CTAs per SM the record-mode verify and the replay commit are compiled
-// for (4: 128 registers; the snapshot verify keeps its unbounded register budget).
-#ifndef RSC_VERIFY_MINB
-#define RSC_VERIFY_MINB 4
+// Resident CTAs per SM the replay commit is compiled for (4: 128 registers); it runs on the
+// snapshot verify's CTA shape (64 rows, 4 warps: measured 23.8 against 25.3 us with a whole
+// head per CTA).
+#ifndef RSC_COMMIT_MINB
+#define RSC_COMMIT_MINB 4
+#endif
+// Record-mode verify: state rows and warps per CTA (rows = 16 x warps, so that the block's
+// row dots reduce to one value per lane), and the resident CTAs it is compiled for.  A whole
+// head per CTA does the head's conv, norms, records and coefficients once instead of once
+// per row tile.
+#ifndef RSC_REPLAY_ROWS
+#define RSC_REPLAY_ROWS 128
+#endif
+#ifndef RSC_REPLAY_WARPS
+#define RSC_REPLAY_WARPS 8
+#endif
+#ifndef RSC_REPLAY_MINB
+#define RSC_REPLAY_MINB 2
 #endif
 
 template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE, bool REPLAY>
-__global__ void __launch_bounds__(NW * 32, REPLAY ? RSC_VERIFY_MINB : 1)
+__global__ void __launch_bounds__(NW * 32, REPLAY ? RSC_REPLAY_MINB * RSC_REPLAY_WARPS / NW : 1)
 kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
                        int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
                        const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -64,8 +82,19 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   // k_hat (in place of the conv outputs), the value rows, alpha = exp(g), k_hat . q_hat.
   __shared__ __align__(16) float s_qk[TS][2 * K];
   __shared__ float s_v[TS][VT];
-  __shared__ __align__(16) float s_al[TS][GW];
+  __shared__ __align__(16) float s_al[REPLAY ? 1 : TS][GW];
   __shared__ float s_kq[TS];
+  // Record mode only (the block in closed form, see below): cumulative log-decays of the
+  // block G_t, the decayed keys and queries k_hat_t . e^G_t and q_hat_t . e^G_t, the keys
+  // decayed to the block's last token k_hat_t . e^(G_last - G_t), and the coefficients
+  // A[t][s] = sum_k k_hat_s k_hat_t e^(G_t - G_s), P[t][s] = sum_k k_hat_s q_hat_t e^(G_t - G_s).
+  constexpr int RS = REPLAY ? TS : 1;
+  __shared__ __align__(16) float s_G[RS][GW];
+  __shared__ __align__(16) float s_kk[RS][K];
+  __shared__ __align__(16) float s_qq[RS][K];
+  __shared__ __align__(16) float s_c[RS][K];
+  __shared__ float s_A[RS][TS], s_P[RS][TS];
+  __shared__ float s_d[RS][VT];  // the block's deltas by row, for the tile update at its end
 
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -141,6 +170,185 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
 
   const int k0 = G::kofs();
   int cur = 0;
+
+  // Record mode: the block's tokens in closed form.  With G_t the cumulative log-decay from
+  // the block start and S0 the tile at the block start,
+  //   S_{t-1} Diag(alpha_t) = S0 Diag(e^G_t) + sum_{s<t} d_s (k_hat_s . e^(G_t - G_s))^T,
+  // so every row's u_t = a_t + sum_{s<t} A[t][s] d_s with a_t = S0 (k_hat_t . e^G_t), and
+  // o_t = S_t q_hat_t = b_t + sum_{s<=t} P[t][s] d_s with b_t = S0 (q_hat_t . e^G_t).  The 2 TS
+  // row dots of the block are independent of each other (one butterfly reduction for all
+  // of them instead of two per token), then d_t = beta_t (v_t - u_t) is an 8x8 triangular
+  // solve per row.  The tile itself changes only at the block end, if another block follows:
+  //   S <- S0 Diag(e^G_last) + sum_s d_s (k_hat_s . e^(G_last - G_s))^T.
+  auto replay_block = [&](int t0, int cnt) {
+    constexpr int LPR = G::LPR, NP = G::NP, E2 = G::EPL / 2;
+    static_assert(2 * NP == LPR, "the reduction leaves one value per lane");
+    const bool more = t0 + TS < T;
+    auto gk = [](int k) { return GW == 1 ? 0 : k; };
+    for (int i = tid; i < cnt * K; i += NT) {
+      const int tau = i / K, k = i % K;
+      const float Gt = s_G[tau][gk(k)];
+      const float e = expf(Gt);
+      s_kk[tau][k] = s_qk[tau][K + k] * e;
+      s_qq[tau][k] = s_qk[tau][k] * e;
+      if (more) s_c[tau][k] = s_qk[tau][K + k] * expf(s_G[cnt - 1][gk(k)] - Gt);
+    }
+    {
+      // the pairs (t, s), s < t, eight per warp (pair 8 warp + i); a lane covers CPL
+      // consecutive channels of one half of K (lanes 0-15 the first half, 16-31 the
+      // second), so a warp's shared-memory reads are contiguous
+      static_assert(NW * 8 >= TS * (TS - 1) / 2, "eight pairs per warp");
+      constexpr int CPL = K / 32;
+      static_assert(CPL == 2 || CPL == 4, "channels per lane");
+      const int c0 = (lane >> 4) * (K / 2) + CPL * (lane & 15);
+      auto ldv = [&](const float *p, float (&v)[CPL]) {
+        if constexpr (CPL == 4) {
+          const float4 u = *reinterpret_cast<const float4 *>(p);
+          v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+        } else {
+          const float2 u = *reinterpret_cast<const float2 *>(p);
+          v[0] = u.x; v[1] = u.y;
+        }
+      };
+      auto pair_of = [](int pi, int &t, int &s2) {
+        t = 1;
+        while (t * (t + 1) / 2 <= pi) ++t;
+        s2 = pi - t * (t - 1) / 2;
+      };
+      float x[16];  // A of the warp's eight pairs, then P
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int t, s2;
+        pair_of(8 * warp + i, t, s2);
+        float a = 0.f, p = 0.f;
+        if (8 * warp + i < TS * (TS - 1) / 2 && t < cnt) {  // uniform over the warp
+          float ks[CPL], kt[CPL], qt[CPL], gt[CPL], gs[CPL];
+          ldv(&s_qk[s2][K + c0], ks);
+          ldv(&s_qk[t][K + c0], kt);
+          ldv(&s_qk[t][c0], qt);
+          if constexpr (GW == 1) {
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) { gt[e] = s_G[t][0]; gs[e] = s_G[s2][0]; }
+          } else {
+            ldv(&s_G[t][c0], gt);
+            ldv(&s_G[s2][c0], gs);
+          }
+#pragma unroll
+          for (int e = 0; e < CPL; ++e) {
+            const float kd = ks[e] * expf(gt[e] - gs[e]);
+            a = fmaf(kd, kt[e], a);
+            p = fmaf(kd, qt[e], p);
+          }
+        }
+        x[i] = a;
+        x[8 + i] = p;
+      }
+      // the 16 sums over each half's 16 lanes, then over the two halves
+      float r = group_reduce_scatter<16>(x);
+      r += __shfl_xor_sync(0xffffffffu, r, 16);
+      if (lane < 16) {
+        const int i = lane & 7;
+        int t, s2;
+        pair_of(8 * warp + i, t, s2);
+        if (8 * warp + i < TS * (TS - 1) / 2 && t < cnt) (lane < 8 ? s_A : s_P)[t][s2] = r;
+      }
+    }
+    __syncthreads();
+    // the row dots: lane i of a row group ends with entry i, a_t of pass i (i < NP) or b_t
+    // of pass i - NP
+    const int li = lane & (LPR - 1);
+    const bool is_a = li < NP;
+    const int row = G::row(is_a ? li : li - NP);
+    float val[TS];
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      val[t] = 0.f;
+      if (t < cnt) {
+        float2 kv[E2], qv[E2];
+#pragma unroll
+        for (int e = 0; e < E2; ++e) {
+          kv[e] = *reinterpret_cast<const float2 *>(&s_kk[t][k0 + 2 * e]);
+          qv[e] = *reinterpret_cast<const float2 *>(&s_qq[t][k0 + 2 * e]);
+        }
+        // first butterfly level (lanes NP apart) as each pass's pair of dots completes,
+        // so the 2 NP partials never live at once: lanes with bit NP keep the b half
+        float y[NP];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float2 u = make_float2(0.f, 0.f), w = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < E2; ++e) {
+            u = __ffma2_rn(s[p][e], kv[e], u);
+            w = __ffma2_rn(s[p][e], qv[e], w);
+          }
+          const float pa = u.x + u.y, pb = w.x + w.y;
+          y[p] = (is_a ? pa : pb) + __shfl_xor_sync(0xffffffffu, is_a ? pb : pa, NP);
+        }
+        val[t] = group_reduce_scatter<NP>(y);
+      }
+    }
+    // deltas (meaningful on the a lanes), then handed to the b lane of the same row
+    float d[TS];
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      d[t] = 0.f;
+      if (t < cnt) {
+        float u = val[t];
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) u = fmaf(s_A[t][s2], d[s2], u);
+        d[t] = s_b[cur][t] * (s_v[t][row] - u);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      const float da = __shfl_up_sync(0xffffffffu, d[t], NP, LPR);
+      if (!is_a) d[t] = da;
+    }
+    // records (a lanes) and outputs (b lanes)
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      if (t < cnt) {
+        if (is_a) {
+          static_cast<ST *>(rv.d)[ent(t0 + t) * V + (size_t)j * VT + row] = from_f32<ST>(d[t]);
+          if (more) s_d[t][row] = d[t];
+        } else {
+          float o = fmaf(s_kq[t], d[t], val[t]);
+#pragma unroll
+          for (int s2 = 0; s2 < t; ++s2) o = fmaf(s_P[t][s2], d[s2], o);
+          out[(((size_t)b * T + t0 + t) * H + h) * V + (size_t)j * VT + row] = from_f32<IO>(o);
+        }
+      }
+    }
+    if (more) {
+      // the tile at the block end; each row's deltas from its a lane, through shared memory
+      // (the rows of a lane group are written by a lanes of the same warp)
+      __syncwarp();
+      float2 gl[E2];
+#pragma unroll
+      for (int e = 0; e < E2; ++e)
+        gl[e] = make_float2(expf(s_G[cnt - 1][gk(k0 + 2 * e)]), expf(s_G[cnt - 1][gk(k0 + 2 * e + 1)]));
+#pragma unroll
+      for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int e = 0; e < E2; ++e) s[p][e] = __fmul2_rn(s[p][e], gl[e]);
+#pragma unroll 1
+      for (int t = 0; t < cnt; ++t) {
+        {
+          float2 c[E2];
+#pragma unroll
+          for (int e = 0; e < E2; ++e) c[e] = *reinterpret_cast<const float2 *>(&s_c[t][k0 + 2 * e]);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            const float dp = s_d[t][G::row(p)];
+            const float2 d2 = make_float2(dp, dp);
+#pragma unroll
+            for (int e = 0; e < E2; ++e) s[p][e] = __ffma2_rn(d2, c[e], s[p][e]);
+          }
+        }
+      }
+    }
+  };
+
   for (int t0 = 0; t0 < T; t0 += TS) {
     cp_async_wait_all();
     __syncthreads();  // block `cur` landed; every reader of block cur^1 and of s_qk is done
@@ -176,7 +384,15 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
           static_cast<ST *>(rv.rawv)[ent(t0 + tau) * V + (size_t)j * VT + tid] = from_f32<ST>(y);
       }
     }
-    if (GATE == RSC_GATE_KDA) {
+    if constexpr (REPLAY) {
+      for (int c = tid; c < GW; c += NT) {  // G_t = g_0 + ... + g_t, a thread per channel
+        float acc = 0.f;
+        for (int tau = 0; tau < cnt; ++tau) {
+          acc += s_g[cur][tau][c];
+          s_G[tau][c] = acc;
+        }
+      }
+    } else if (GATE == RSC_GATE_KDA) {
       for (int i = tid; i < cnt * K; i += NT) s_al[i / K][i % K] = expf(s_g[cur][i / K][i % K]);
     } else if (tid < cnt) {
       s_al[tid][0] = expf(s_g[cur][tid][0]);
@@ -214,36 +430,30 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       }
     }
 
-    // the block's tokens: delta rule on the register tile, no barrier inside
-    for (int tau = 0; tau < cnt; ++tau) {
-      const int t = t0 + tau;
-      const size_t bt = (size_t)b * T + t;
-      float2 qh[G::EPL / 2], kh[G::EPL / 2], al[G::EPL / 2];
+    if constexpr (REPLAY) {
+      replay_block(t0, cnt);
+    } else {
+      // the block's tokens: delta rule on the register tile, no barrier inside
+      for (int tau = 0; tau < cnt; ++tau) {
+        const int t = t0 + tau;
+        const size_t bt = (size_t)b * T + t;
+        float2 qh[G::EPL / 2], kh[G::EPL / 2], al[G::EPL / 2];
 #pragma unroll
-      for (int e = 0; e < G::EPL / 2; ++e) {
-        qh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][k0 + 2 * e]);
-        kh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][K + k0 + 2 * e]);
-        al[e] = GATE == RSC_GATE_KDA ? *reinterpret_cast<const float2 *>(&s_al[tau][k0 + 2 * e])
-                                     : make_float2(s_al[tau][0], s_al[tau][0]);
-      }
-      float o[G::NP];
-      if constexpr (REPLAY) {
-        float dd[G::NP];
-        delta_rule_tile2<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, dd);
-        if (k0 == 0) {
-          ST *dr = static_cast<ST *>(rv.d) + ent(t) * V + (size_t)j * VT;
-#pragma unroll
-          for (int p = 0; p < G::NP; ++p) dr[G::row(p)] = from_f32<ST>(dd[p]);
+        for (int e = 0; e < G::EPL / 2; ++e) {
+          qh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][k0 + 2 * e]);
+          kh[e] = *reinterpret_cast<const float2 *>(&s_qk[tau][K + k0 + 2 * e]);
+          al[e] = GATE == RSC_GATE_KDA ? *reinterpret_cast<const float2 *>(&s_al[tau][k0 + 2 * e])
+                                       : make_float2(s_al[tau][0], s_al[tau][0]);
         }
-      } else {
+        float o[G::NP];
         delta_rule_tile2<ST, K, VT, VPL, NW>(s, qh, kh, al, s_b[cur][tau], s_kq[tau], s_v[tau], o, nullptr);
         ST *Se = spec_ssm + ((((size_t)b * L + t) * H + h) * V + (size_t)j * VT) * K;
         tile_store2<ST, K, VT, VPL, NW>(Se, s);
-      }
-      if (k0 == 0) {
-        IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
+        if (k0 == 0) {
+          IO *ob = out + (bt * H + h) * V + (size_t)j * VT;
 #pragma unroll
-        for (int p = 0; p < G::NP; ++p) ob[G::row(p)] = from_f32<IO>(o[p]);
+          for (int p = 0; p < G::NP; ++p) ob[G::row(p)] = from_f32<IO>(o[p]);
+        }
       }
     }
     cur ^= 1;
@@ -287,8 +497,10 @@ struct ReplayVerifyLaunch {
   static int run(const LayerArgs *a, const RingView *rv, const int32_t *slots, const int32_t *pos,
                  int B, int T, void *spec_conv, const void *qkv, const float *conv_w,
                  const float *g, const float *beta, void *out, cudaStream_t s) {
-    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
-    constexpr int NW = RSC_VERIFY_WARPS;
+    constexpr int ROWS = RSC_REPLAY_ROWS < V ? RSC_REPLAY_ROWS : V;
+    constexpr int NVT = V / ROWS;
+    constexpr int NW = ROWS / 16;
+    static_assert(RSC_REPLAY_ROWS == 16 * RSC_REPLAY_WARPS, "rows = 16 x warps");
     dim3 grid(NVT, a->pv.H, B);
     kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE, true><<<grid, NW * 32, 0, s>>>(
         a->pv, a->layer, slots, T, rv->depth, nullptr, static_cast<IO *>(spec_conv),
@@ -312,7 +524,7 @@ int launch_replay_verify(const LayerArgs &a, const RingView &rv, const int32_t *
 // back.  The CTA also restores its share of the window from snapshot accept[b] (the same
 // channel ownership as the verify pass), so every byte of the slot has one writer.
 template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE>
-__global__ void __launch_bounds__(NW * 32, RSC_VERIFY_MINB)
+__global__ void __launch_bounds__(NW * 32, RSC_COMMIT_MINB)
 kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__restrict__ slots,
                          const int32_t *__restrict__ pos, int T, const IO *__restrict__ spec_conv,
                          const int32_t *__restrict__ accept) {

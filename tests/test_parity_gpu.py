@@ -354,14 +354,18 @@ def _rings_np(rings):
     return {n: to_np(getattr(rings, n)) for n in ("d", "k", "rawv", "rawk", "g", "beta")}
 
 
-@pytest.mark.parametrize("st,io,gate,K,V", [
-    (0, 0, rsc.KDA, 64, 64), (1, 1, rsc.KDA, 128, 128), (1, 1, rsc.GDN, 128, 128),
-    (0, 1, rsc.KDA, 128, 64), (1, 0, rsc.KDA, 64, 128),
+@pytest.mark.parametrize("st,io,gate,K,V,T,depth", [
+    (0, 0, rsc.KDA, 64, 64, 5, 16), (1, 1, rsc.KDA, 128, 128, 5, 16),
+    (1, 1, rsc.GDN, 128, 128, 5, 16), (0, 1, rsc.KDA, 128, 64, 5, 16),
+    (1, 0, rsc.KDA, 64, 128, 5, 16),
+    (1, 1, rsc.KDA, 128, 128, 8, 16),   # one full block of eight tokens
+    (0, 0, rsc.KDA, 128, 128, 11, 32),  # a full block, then three tokens from its end state
+    (1, 1, rsc.GDN, 64, 64, 16, 32),    # two full blocks
 ])
-def test_replay_verify_commit_parity(cuda_dev, st, io, gate, K, V):
+def test_replay_verify_commit_parity(cuda_dev, st, io, gate, K, V, T, depth):
     """Verify: outputs and ring records match the oracle, windows bit-exact, slot untouched;
     commit: the replayed state matches the oracle's replay, windows bit-exact."""
-    H, B, T, depth = 2, 3, 5, 16
+    H, B = 2, 3
     c = Case(cuda_dev, 31, L=2, P=6, H=H, K=K, V=V, st=st, io=io, gate=gate)
     slots = np.int32([5, 2, 4])
     pos = np.int32([0, 9, 14])  # the last request wraps around its ring
@@ -384,7 +388,7 @@ def test_replay_verify_commit_parity(cuda_dev, st, io, gate, K, V):
     g_ref = rings_ref.g if gate == rsc.KDA else rings_ref.g[..., 0]
     assert np.array_equal(got["g"], g_ref) and np.array_equal(got["beta"], rings_ref.beta)
     assert rsc.rsc_get_device_error(c.pool) == 0
-    accept = np.int32([0, 4, 2])
+    accept = np.int32([0, T - 1, T // 2])
     rsc.kda_replay_verify_commit(c.pool, rings, 1, rsc.COMMIT, slots_d, pos_d, T, spec_conv,
                                  accept=to_dev(accept, c.dev))
     oracle.replay_commit(c.ref, rings_ref, 1, slots, pos, T, depth, sC_ref, accept)
