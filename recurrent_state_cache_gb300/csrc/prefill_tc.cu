@@ -80,7 +80,10 @@ constexpr uint32_t kChX = 32768;     // [K.e^(G-R); Q.e^(G-R)]  K-major 128 x K
 constexpr uint32_t kChKi = 65536;    // K.e^(R-G)              K-major 64 x K
 constexpr uint32_t kChBT = 81920;    // B^T                    K-major K x 64
 constexpr uint32_t kChPP = 98304;    // P                      K-major 64 x 64
-constexpr uint32_t kChSmem = 106496; // two CTAs per SM
+// Phase 1 also: the conv taps of the head's channels (float4 each), transposed so that the
+// lanes of a warp read consecutive vectors: the taps of channel 8 g + e at [e][g].
+constexpr uint32_t kChW = 106496;
+constexpr uint32_t kChSmem = kChW + (2 * kK + kVmax) * 16;  // 112640: two CTAs per SM
 // Phase 3 (over X and Ki once the A/P product has completed).
 constexpr int kAS = 68;                                  // fp32 row stride of A
 constexpr uint32_t kChA = 32768;     // A, then (I + A)^-1 in place, fp32 [64][68]
@@ -271,10 +274,16 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   if (tid == 0) mbar_init(&s_bar, 1);
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 256); tc::tmem_relinquish(); }
 
-  // the gates of this thread's rows and channels, requested now so their latency hides
-  // behind the conv
+  // the gates of this thread's rows and channels: their lines are prefetched into L2 at once,
+  // the registers filled after the q/k conv pass
   const int kg = tid >> 4, rsub = tid & 15;
   float G[4][8];
+  if (GATE == RSC_GATE_KDA && (kg & 3) == 0) {  // the rows' gate lines into L2 meanwhile
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (4 * rsub + i < Lc) prefetch_l2(g + ((size_t)(t0 + 4 * rsub + i) * H + h) * kK + 8 * kg);
+  }
+  auto load_gates = [&]() {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 4 * rsub + i;
@@ -294,6 +303,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       for (int e = 0; e < 8; ++e) G[i][e] = 0.f;
     }
   }
+  };
 
   // ---- 1. conv + L2 norm -> Y rows 0..63: q_hat | k_hat; v (zero beyond the chunk) -> KV
   auto src_channel = [&](int c) {  // channel c of the head -> column of the projections
@@ -323,64 +333,80 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
         st16(dst, make_uint4(0, 0, 0, 0));
       }
     }
+    float4 *sW = reinterpret_cast<float4 *>(smem + kChW);
+    for (int c = tid; c < CH; c += 256)
+      cp_async16(sW + (c % 8) * (CH / 8) + c / 8, conv_w + 4 * (size_t)src_channel(c));
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    for (int it = tid; it < 2 * CH; it += 256) {
-      const int c = it % CH, r0 = (it / CH) * (kC / 2);
-      const float4 w = reinterpret_cast<const float4 *>(conv_w)[src_channel(c)];
-      float x0 = __bfloat162float(stg[r0 * kRowElems + c]);
-      float x1 = __bfloat162float(stg[(r0 + 1) * kRowElems + c]);
-      float x2 = __bfloat162float(stg[(r0 + 2) * kRowElems + c]);
-#pragma unroll 8
-      for (int r = r0; r < r0 + kC / 2; ++r) {
-        const float x3 = __bfloat162float(stg[(r + 3) * kRowElems + c]);
-        Y[r * kRowElems + c] = __float2bfloat16_rn(conv4(w, x0, x1, x2, x3));
-        x0 = x1; x1 = x2; x2 = x3;
+    // q and k, conv and L2 norm in one pass: warp w takes tokens 8w .. 8w+7, lane l the eight
+    // channels 8l .. 8l+7 of [q | k] (lanes 0-15 q, 16-31 k, so each row's sum of squares is
+    // one reduction over a half warp); the fp32 conv outputs are normalised before rounding
+    {
+      const int g = lane;
+      float4 w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = sW[e * (CH / 8) + g];
+      const int r0 = 8 * warp;
+      float x0[8], x1[8], x2[8];
+      unpack16(ld16(stg + r0 * kRowElems + 8 * g), x0);
+      unpack16(ld16(stg + (r0 + 1) * kRowElems + 8 * g), x1);
+      unpack16(ld16(stg + (r0 + 2) * kRowElems + 8 * g), x2);
+#pragma unroll
+      for (int r = r0; r < r0 + 8; ++r) {
+        float x3[8], y[8];
+        unpack16(ld16(stg + (r + 3) * kRowElems + 8 * g), x3);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          y[e] = conv4(w[e], x0[e], x1[e], x2[e], x3[e]);
+          ss = fmaf(y[e], y[e], ss);
+          x0[e] = x1[e]; x1[e] = x2[e]; x2[e] = x3[e];
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float rn = r < Lc ? rsqrtf(ss + kNormEps) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] *= rn;
+        st16(Y + r * kRowElems + 8 * g, pack16(y));
+      }
+    }
+    load_gates();  // after the q/k pass, whose registers they would crowd
+    // v: thread (g, s) = (tid % 16, tid / 16) takes channels 8g .. 8g+7 of v on tokens
+    // 4s .. 4s+3 (zero beyond the chunk)
+    if (8 * (tid & 15) < V) {
+      const int g = tid & 15, r0 = 4 * (tid >> 4);
+      float4 w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = sW[e * (CH / 8) + 2 * kK / 8 + g];
+      const bf16 *xs = stg + 2 * kK + 8 * g;
+      float x0[8], x1[8], x2[8];
+      unpack16(ld16(xs + r0 * kRowElems), x0);
+      unpack16(ld16(xs + (r0 + 1) * kRowElems), x1);
+      unpack16(ld16(xs + (r0 + 2) * kRowElems), x2);
+#pragma unroll
+      for (int r = r0; r < r0 + 4; ++r) {
+        float x3[8], y[8];
+        unpack16(ld16(xs + (r + 3) * kRowElems), x3);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          y[e] = r < Lc ? conv4(w[e], x0[e], x1[e], x2[e], x3[e]) : 0.f;
+          x0[e] = x1[e]; x1[e] = x2[e]; x2[e] = x3[e];
+        }
+        st16(Y + r * kRowElems + 2 * kK + 8 * g, pack16(y));
       }
     }
     __syncthreads();  // the staged rows are dead from here
-    // a warp per token, two tokens at a time: lane l owns channels 4l..4l+3
-#pragma unroll
-    for (int r0 = warp; r0 < kC; r0 += 16) {
-      bf16 *yr[2] = {Y + r0 * kRowElems, Y + (r0 + 8) * kRowElems};
-      float q[2][4], k[2][4], qq[2], kk[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint2 qu = *reinterpret_cast<const uint2 *>(yr[u] + 4 * lane);
-        const uint2 ku = *reinterpret_cast<const uint2 *>(yr[u] + kK + 4 * lane);
-        q[u][0] = bf16lo(qu.x); q[u][1] = bf16hi(qu.x); q[u][2] = bf16lo(qu.y); q[u][3] = bf16hi(qu.y);
-        k[u][0] = bf16lo(ku.x); k[u][1] = bf16hi(ku.x); k[u][2] = bf16lo(ku.y); k[u][3] = bf16hi(ku.y);
-        qq[u] = q[u][0] * q[u][0] + q[u][1] * q[u][1] + q[u][2] * q[u][2] + q[u][3] * q[u][3];
-        kk[u] = k[u][0] * k[u][0] + k[u][1] * k[u][1] + k[u][2] * k[u][2] + k[u][3] * k[u][3];
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          qq[u] += __shfl_xor_sync(0xffffffffu, qq[u], o);
-          kk[u] += __shfl_xor_sync(0xffffffffu, kk[u], o);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = r0 + 8 * u;
-        const bool live = r < Lc;
-        const float rq = live ? rsqrtf(qq[u] + kNormEps) : 0.f;
-        const float rk = live ? rsqrtf(kk[u] + kNormEps) : 0.f;
-        *reinterpret_cast<uint2 *>(yr[u] + 4 * lane) =
-            make_uint2(pack_bf16x2(q[u][0] * rq, q[u][1] * rq), pack_bf16x2(q[u][2] * rq, q[u][3] * rq));
-        *reinterpret_cast<uint2 *>(yr[u] + kK + 4 * lane) =
-            make_uint2(pack_bf16x2(k[u][0] * rk, k[u][1] * rk), pack_bf16x2(k[u][2] * rk, k[u][3] * rk));
-        if (4 * lane < V) {
-          const uint2 vu = live ? *reinterpret_cast<const uint2 *>(yr[u] + 2 * kK + 4 * lane) : make_uint2(0, 0);
-          *reinterpret_cast<uint2 *>(sKV + tc::mnmajor_offset(kK + 4 * lane, r, NKV)) = vu;
-        }
-      }
+    // v into the V half of [K.Gamma | V] (over the staged rows): 16-byte pieces, token r,
+    // columns K + 8g .. +7
+    for (int i = tid; i < kC * (V / 8); i += 256) {
+      const int r = i / (V / 8), g = i % (V / 8);
+      st16(sKV + tc::mnmajor_offset(kK + 8 * g, r, NKV), ld16(Y + r * kRowElems + 2 * kK + 8 * g));
     }
   } else {
     // fp32 inputs: a warp per token straight from global memory (lane l owns channels
     // 4l..4l+3 of q, k, v).
+    load_gates();
     const int cq = h * kK + 4 * lane, ck = H * kK + h * kK + 4 * lane;
     const int cv = 2 * H * kK + h * V + 4 * lane;
     const bool has_v = 4 * lane < V;
@@ -518,6 +544,15 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     kv[i] = ld16(yr + kK + 8 * kg);
   }
   __syncthreads();  // Y is dead; the operands overlay it
+  // per channel: e^R and e^(G_last - R); with those, two exponentials per element instead of
+  // four (e^G = e^(G-R) e^R, e^(G_last - G) = e^(G_last - R) e^(R-G)).  Every factor is within
+  // e^(+-range/2) of one, which the range check keeps inside fp32.
+  float eR[8], eLR[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    eR[e] = exp2f(R[e] * kLog2e);
+    eLR[e] = exp2f((Gl[e] - R[e]) * kLog2e);
+  }
 #pragma unroll
   for (int ip = 0; ip < 4; ip += 2) {  // rows in pairs: B^T takes two rows per 4-byte store
     float bt[8][2];
@@ -531,13 +566,13 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float d = (G[i][e] - R[e]) * kLog2e;
-        const float ep = exp2f(d), en = exp2f(-d), gam = exp2f(G[i][e] * kLog2e);
+        const float ep = exp2f(d), en = exp2f(-d), gam = ep * eR[e];
         xk[e] = k8[e] * ep;
         xq[e] = q8[e] * ep;
         ki[e] = k8[e] * en;
         kgm[e] = k8[e] * gam;
         qgm[e] = q8[e] * gam;
-        bt[e][i - ip] = live ? k8[e] * exp2f((Gl[e] - G[i][e]) * kLog2e) : 0.f;
+        bt[e][i - ip] = live ? k8[e] * (eLR[e] * en) : 0.f;
       }
       st16(sX + tc::kmajor_offset(r, 8 * kg, kK), pack16(xk));
       st16(sX + tc::kmajor_offset(kC + r, 8 * kg, kK), pack16(xq));

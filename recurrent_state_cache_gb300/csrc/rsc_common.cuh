@@ -65,6 +65,10 @@ __device__ __forceinline__ uint4 ld16_stream(const void *p) {
 __device__ __forceinline__ void st16_stream(void *p, const uint4 &v) {
   __stcs(reinterpret_cast<uint4 *>(p), v);
 }
+// Ask for the 128-byte line holding p in L2, without a register or a wait.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
 __device__ __forceinline__ uint4 ld16(const void *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
