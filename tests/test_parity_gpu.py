@@ -80,6 +80,23 @@ def test_decode_variants(cuda_dev, st, io, gate, H, K, V, B):
     _decode_steps(c, slots, 3)
 
 
+@pytest.mark.parametrize("st,io,gate,H,B", [(1, 1, rsc.KDA, 10, 64), (0, 1, rsc.GDN, 32, 20)])
+def test_decode_large_batch(cuda_dev, st, io, gate, H, B):
+    """More CTAs than the GPU holds at once (several per SM, the headline's regime), plain and
+    overlapped launches, against the oracle."""
+    c = Case(cuda_dev, 9, L=2, P=B + 4, H=H, K=128, V=128, st=st, io=io, gate=gate)
+    slots = inputs.distinct_slots(c.r, B, B + 4)
+    slots_d = to_dev(slots, c.dev)
+    for layer, overlap in ((0, False), (1, True)):
+        x = c.proj((B,))
+        g, beta = c.gates((B,))
+        o_ref = oracle.decode_step(c.ref, layer, slots, x, c.w, g, beta)
+        o = rsc.kda_decode_step(c.pool, layer, slots_d, to_dev(x, c.dev), c.w_dev,
+                                to_dev(g, c.dev), to_dev(beta, c.dev), overlap=overlap)
+        assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(st, io)
+    c.check_pool()
+
+
 def test_decode_padding_slot_zero_is_legal(cuda_dev):
     c = Case(cuda_dev, 2, L=1, P=4, H=2, K=64, V=64, st=1, io=1, gate=rsc.KDA)
     _decode_steps(c, np.int32([0, 3]), 2)
