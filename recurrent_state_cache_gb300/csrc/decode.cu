@@ -331,9 +331,13 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #define RSC_DECODE_EARLY_CHUNKS 2
 #endif
 // The same for the overlapped launch, where the early chunks are requested before the wait
-// for the previous kernel.
+// for the previous kernel (69-layer graph, us per layer: 4 chunks with 1/2/3/4 early
+// 10.1/9.05/10.0/11.0; 8 chunks with 2/4/6 early 10.1/9.2/10.0; 2 chunks with 1 early 8.98).
+#ifndef RSC_DECODE_OVL_CHUNKS
+#define RSC_DECODE_OVL_CHUNKS 2
+#endif
 #ifndef RSC_DECODE_OVL_EARLY_CHUNKS
-#define RSC_DECODE_OVL_EARLY_CHUNKS 2
+#define RSC_DECODE_OVL_EARLY_CHUNKS 1
 #endif
 
 template <typename ST> struct DecodeTile;
@@ -356,9 +360,10 @@ struct DecodeLaunch {
     constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
     constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
     constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
-    constexpr int OEARLY = RSC_DECODE_OVL_EARLY_CHUNKS < NCH ? RSC_DECODE_OVL_EARLY_CHUNKS : NCH;
+    constexpr int ONCH = NP % RSC_DECODE_OVL_CHUNKS == 0 ? RSC_DECODE_OVL_CHUNKS : 1;
+    constexpr int OEARLY = RSC_DECODE_OVL_EARLY_CHUNKS < ONCH ? RSC_DECODE_OVL_EARLY_CHUNKS : ONCH;
     auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE, false>;
-    auto kern_ovl = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, OEARLY, GATE, true>;
+    auto kern_ovl = kda_decode_kernel<ST, IO, K, V, NVT, NW, ONCH, OEARLY, GATE, true>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
