@@ -195,6 +195,8 @@ __device__ __forceinline__ void tile_load2(const ST *base, Tile2<ST, K, VT, NW, 
     }
 }
 
+// Streaming (evict-first) stores: a stored tile is not read again soon (a spec cache entry
+// until its commit, a committed slot until that layer's next step).
 template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
 __device__ __forceinline__ void tile_store2(ST *base, const Tile2<ST, K, VT, NW, VPL> &s) {
   using G = TileGeom<ST, K, VT, NW, VPL>;
@@ -209,7 +211,7 @@ __device__ __forceinline__ void tile_store2(ST *base, const Tile2<ST, K, VT, NW,
         x[2 * e] = s[p][v * N16 / 2 + e].x;
         x[2 * e + 1] = s[p][v * N16 / 2 + e].y;
       }
-      st16(base + (size_t)G::row(p) * K + G::kofs() + v * N16, pack16(x));
+      st16_stream(base + (size_t)G::row(p) * K + G::kofs() + v * N16, pack16(x));
     }
 }
 
