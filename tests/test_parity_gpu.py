@@ -164,6 +164,33 @@ def test_decode_overlap_layer_chain(cuda_dev, st, io, gate, H, K, V, B):
     assert rsc.rsc_get_device_error(plain) == 0
 
 
+def test_decode_overlap_bad_slot_sets_flag_and_skips_row(cuda_dev):
+    """The overlapped launch reads the slot id before waiting for the previous kernel; a bad
+    one ends those CTAs before the wait with the error bit set and their rows untouched, and
+    the next call on the stream runs normally."""
+    c = Case(cuda_dev, 10, L=2, P=4, H=2, K=128, V=128, st=1, io=1, gate=rsc.KDA)
+    before_s, before_c = to_np(c.pool.ssm).copy(), to_np(c.pool.conv).copy()
+    slots = np.int32([3, 9])  # 9 > P
+    x = c.proj((2,))
+    g, beta = c.gates((2,))
+    rsc.kda_decode_step(c.pool, 0, to_dev(slots, c.dev), to_dev(x, c.dev), c.w_dev,
+                        to_dev(g, c.dev), to_dev(beta, c.dev), overlap=True)
+    good = np.int32([1, 2])
+    x2 = c.proj((2,))
+    g2, beta2 = c.gates((2,))
+    o2 = rsc.kda_decode_step(c.pool, 1, to_dev(good, c.dev), to_dev(x2, c.dev), c.w_dev,
+                             to_dev(g2, c.dev), to_dev(beta2, c.dev), overlap=True)
+    assert rsc.rsc_get_device_error(c.pool) == rsc.binding.DEVERR_SLOT
+    s_now, c_now = to_np(c.pool.ssm), to_np(c.pool.conv)
+    others = [0, 1, 2, 4]
+    assert np.array_equal(s_now[0, others], before_s[0, others])
+    assert np.array_equal(c_now[0, others], before_c[0, others])
+    oracle.decode_step(c.ref, 0, slots[:1], x[:1], c.w, g[:1], beta[:1])
+    o2_ref = oracle.decode_step(c.ref, 1, good, x2, c.w, g2, beta2)
+    assert max_rel_err(widen(to_np(o2)), widen(o2_ref)) <= tol(1, 1)
+    c.check_pool()
+
+
 # ------------------------------------------------------------------ slot copy
 
 @pytest.mark.parametrize("st,io,layer", [(1, 1, -1), (0, 1, 1), (0, 0, -1)])
