@@ -143,6 +143,41 @@ def test_unrolled_closed_form_of_the_pages():
     np.testing.assert_allclose(S, ref, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("T", [8, 11])
+def test_block_closed_form_outputs_and_deltas(T):
+    # The ReplaySSM verify computes each block of up to eight tokens in closed form from the
+    # state at the block start S0 (G_t the cumulative log-decay from there):
+    #   u_t = S0 (k_t . e^G_t) + sum_{s<t} A[t][s] d_s,  A[t][s] = sum_c k_s k_t e^(G_t - G_s)
+    #   d_t = beta_t (v_t - u_t)
+    #   o_t = S0 (q_t . e^G_t) + sum_{s<=t} P[t][s] d_s,  P[t][s] = sum_c k_s q_t e^(G_t - G_s)
+    # and the state at the block end by the pages' unrolled form.  Blocks chained this way give
+    # the recurrence's deltas and outputs.
+    q, k, v, g, beta, S0 = _head_case(11, T=T, K=6, V=5)
+    S_ref, o_ref, d_ref = oracle.recurrent_head(q, k, v, g, beta, S0)
+    S = S0.astype(np.float64).copy()
+    d_all, o_all = [], []
+    for t0 in range(0, T, 8):
+        kb, qb, vb, bb = k[t0:t0 + 8], q[t0:t0 + 8], v[t0:t0 + 8], beta[t0:t0 + 8]
+        G = np.cumsum(g[t0:t0 + 8], axis=0)
+        n = len(kb)
+        d = np.zeros((n, S.shape[0]))
+        for t in range(n):
+            u = S @ (kb[t] * np.exp(G[t]))
+            for s2 in range(t):
+                u = u + np.sum(kb[s2] * kb[t] * np.exp(G[t] - G[s2])) * d[s2]
+            d[t] = bb[t] * (vb[t] - u)
+            o = S @ (qb[t] * np.exp(G[t]))
+            for s2 in range(t + 1):
+                o = o + np.sum(kb[s2] * qb[t] * np.exp(G[t] - G[s2])) * d[s2]
+            d_all.append(d[t])
+            o_all.append(o)
+        S = S * np.exp(G[-1])[None, :] + sum(np.outer(d[s2], kb[s2] * np.exp(G[-1] - G[s2]))
+                                             for s2 in range(n))
+    np.testing.assert_allclose(np.array(d_all), d_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(np.array(o_all), o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(S, S_ref, rtol=1e-10, atol=1e-12)
+
+
 @pytest.mark.parametrize("T,K,V", [(1, 16, 16), (63, 16, 8), (64, 16, 16), (65, 8, 16),
                                    (130, 16, 16), (1312, 32, 32)])
 def test_chunkwise_equals_recurrence(T, K, V):
