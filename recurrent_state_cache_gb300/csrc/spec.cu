@@ -565,6 +565,24 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
   Tile2<ST, K, VT, NW, VPL> s;
   tile_load2<ST, K, VT, VPL, NW>(S, s);
   const int k0 = G::kofs();
+  // the window snapshot accept[b]: this CTA's q/k channels of the head and its value channels,
+  // requested now and written back at the end (its latency hides behind the replay)
+  const IO *E = spec_conv + ((size_t)b * rv.depth + acc) * 3 * (size_t)D;
+  IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
+  constexpr int NWIN = (3 * (OWN + VT) + NT - 1) / NT;
+  IO wsnap[NWIN];
+  auto win_index = [&](int i) {  // element i of this CTA's share -> offset in a [3][D] window
+    const int row = i / (OWN + VT), c = i % (OWN + VT);
+    const int i2 = j * OWN + c;
+    const int ch = c < OWN ? (i2 < K ? h * K + i2 : H * K + h * K + (i2 - K))
+                           : 2 * H * K + h * V + j * VT + (c - OWN);
+    return (size_t)row * D + ch;
+  };
+#pragma unroll
+  for (int u = 0; u < NWIN; ++u) {
+    const int i = tid + u * NT;
+    if (i < 3 * (OWN + VT)) wsnap[u] = E[win_index(i)];
+  }
 
   for (int t0 = 0; t0 < n; t0 += TS) {
     const int cnt = min(TS, n - t0);
@@ -621,16 +639,11 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
     }
   }
   tile_store2<ST, K, VT, VPL, NW>(S, s);
-
-  // window <- snapshot acc: this CTA's q/k channels of the head and its value channels
-  const IO *E = spec_conv + ((size_t)b * rv.depth + acc) * 3 * (size_t)D;
-  IO *W = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)D;
-  for (int i = tid; i < 3 * (OWN + VT); i += NT) {
-    const int row = i / (OWN + VT), c = i % (OWN + VT);
-    const int i2 = j * OWN + c;
-    const int ch = c < OWN ? (i2 < K ? h * K + i2 : H * K + h * K + (i2 - K))
-                           : 2 * H * K + h * V + j * VT + (c - OWN);
-    W[(size_t)row * D + ch] = E[(size_t)row * D + ch];
+  // window <- snapshot acc
+#pragma unroll
+  for (int u = 0; u < NWIN; ++u) {
+    const int i = tid + u * NT;
+    if (i < 3 * (OWN + VT)) W[win_index(i)] = wsnap[u];
   }
 }
 
