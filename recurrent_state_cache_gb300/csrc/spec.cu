@@ -185,19 +185,22 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     static_assert(2 * NP == LPR, "the reduction leaves one value per lane");
     const bool more = t0 + TS < T;
     auto gk = [](int k) { return GW == 1 ? 0 : k; };
+    // exponentials of log-decay sums over at most eight tokens (arguments of moderate size,
+    // non-positive for decaying gates): the fast intrinsic, ~1e-6 relative
     for (int i = tid; i < cnt * K; i += NT) {
       const int tau = i / K, k = i % K;
       const float Gt = s_G[tau][gk(k)];
-      const float e = expf(Gt);
+      const float e = __expf(Gt);
       s_kk[tau][k] = s_qk[tau][K + k] * e;
       s_qq[tau][k] = s_qk[tau][k] * e;
-      if (more) s_c[tau][k] = s_qk[tau][K + k] * expf(s_G[cnt - 1][gk(k)] - Gt);
+      if (more) s_c[tau][k] = s_qk[tau][K + k] * __expf(s_G[cnt - 1][gk(k)] - Gt);
     }
     {
-      // the pairs (t, s), s < t, eight per warp (pair 8 warp + i); a lane covers CPL
-      // consecutive channels of one half of K (lanes 0-15 the first half, 16-31 the
-      // second), so a warp's shared-memory reads are contiguous
-      static_assert(NW * 8 >= TS * (TS - 1) / 2, "eight pairs per warp");
+      // the pairs (t, s), s < t, PPW per warp (pair PPW warp + i) over all warps; a lane
+      // covers CPL consecutive channels of one half of K (lanes 0-15 the first half, 16-31
+      // the second), so a warp's shared-memory reads are contiguous
+      constexpr int PPW = NW >= 7 ? 4 : 8;
+      static_assert(NW * PPW >= TS * (TS - 1) / 2, "pairs per warp");
       constexpr int CPL = K / 32;
       static_assert(CPL == 2 || CPL == 4, "channels per lane");
       const int c0 = (lane >> 4) * (K / 2) + CPL * (lane & 15);
@@ -215,13 +218,13 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         while (t * (t + 1) / 2 <= pi) ++t;
         s2 = pi - t * (t - 1) / 2;
       };
-      float x[16];  // A of the warp's eight pairs, then P
+      float x[2 * PPW];  // A of the warp's pairs, then P
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < PPW; ++i) {
         int t, s2;
-        pair_of(8 * warp + i, t, s2);
+        pair_of(PPW * warp + i, t, s2);
         float a = 0.f, p = 0.f;
-        if (8 * warp + i < TS * (TS - 1) / 2 && t < cnt) {  // uniform over the warp
+        if (PPW * warp + i < TS * (TS - 1) / 2 && t < cnt) {  // uniform over the warp
           float ks[CPL], kt[CPL], qt[CPL], gt[CPL], gs[CPL];
           ldv(&s_qk[s2][K + c0], ks);
           ldv(&s_qk[t][K + c0], kt);
@@ -235,22 +238,30 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
           }
 #pragma unroll
           for (int e = 0; e < CPL; ++e) {
-            const float kd = ks[e] * expf(gt[e] - gs[e]);
+            const float kd = ks[e] * __expf(gt[e] - gs[e]);
             a = fmaf(kd, kt[e], a);
             p = fmaf(kd, qt[e], p);
           }
         }
         x[i] = a;
-        x[8 + i] = p;
+        x[PPW + i] = p;
       }
-      // the 16 sums over each half's 16 lanes, then over the two halves
-      float r = group_reduce_scatter<16>(x);
+      // the 2 PPW sums over each half's 16 lanes, then over the two halves
+      float r;
+      if constexpr (PPW == 8) {
+        r = group_reduce_scatter<16>(x);
+      } else {
+        float y[2 * PPW];
+#pragma unroll
+        for (int i = 0; i < 2 * PPW; ++i) y[i] = x[i] + __shfl_xor_sync(0xffffffffu, x[i], 8);
+        r = group_reduce_scatter<2 * PPW>(y);
+      }
       r += __shfl_xor_sync(0xffffffffu, r, 16);
-      if (lane < 16) {
-        const int i = lane & 7;
+      if (lane < 2 * PPW) {  // lane i: entry i (A of pair i, then P of pair i - PPW)
+        const int i = lane % PPW;
         int t, s2;
-        pair_of(8 * warp + i, t, s2);
-        if (8 * warp + i < TS * (TS - 1) / 2 && t < cnt) (lane < 8 ? s_A : s_P)[t][s2] = r;
+        pair_of(PPW * warp + i, t, s2);
+        if (PPW * warp + i < TS * (TS - 1) / 2 && t < cnt) (lane < PPW ? s_A : s_P)[t][s2] = r;
       }
     }
     __syncthreads();
