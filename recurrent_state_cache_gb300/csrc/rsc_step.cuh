@@ -123,58 +123,6 @@ __device__ __forceinline__ void delta_rule_tile(
     o[p] = delta_rule_row<G::EPL, G::LPR>(s[p], qh, kh, al, beta, kq, v_rows[G::row(p)]);
 }
 
-// delta_rule_tile that also returns each row's delta d (ReplaySSM records it).
-template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
-__device__ __forceinline__ void delta_rule_tile_d(
-    float (&s)[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL],
-    const float (&qh)[TileGeom<ST, K, VT, NW, VPL>::EPL],
-    const float (&kh)[TileGeom<ST, K, VT, NW, VPL>::EPL],
-    const float (&al)[TileGeom<ST, K, VT, NW, VPL>::EPL], float beta, float kq,
-    const float *v_rows, float (&o)[TileGeom<ST, K, VT, NW, VPL>::NP],
-    float (&dd)[TileGeom<ST, K, VT, NW, VPL>::NP]) {
-  using G = TileGeom<ST, K, VT, NW, VPL>;
-#pragma unroll
-  for (int p = 0; p < G::NP; ++p) {
-    float u = 0.f, w = 0.f;
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) {
-      s[p][e] *= al[e];
-      u = fmaf(s[p][e], kh[e], u);
-      w = fmaf(s[p][e], qh[e], w);
-    }
-    u = group_sum<G::LPR>(u);
-    w = group_sum<G::LPR>(w);
-    const float d = beta * (v_rows[G::row(p)] - u);
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) s[p][e] = fmaf(d, kh[e], s[p][e]);
-    o[p] = fmaf(d, kq, w);
-    dd[p] = d;
-  }
-}
-
-// The update alone, no output (a replayed token): s <- s . alpha; d = beta (v_r - s . k_hat);
-// s <- s + d k_hat, for every row of the tile.
-template <typename ST, int K, int VT, int VPL = 1, int NW = 4>
-__device__ __forceinline__ void delta_rule_tile_replay(
-    float (&s)[TileGeom<ST, K, VT, NW, VPL>::NP][TileGeom<ST, K, VT, NW, VPL>::EPL],
-    const float (&kh)[TileGeom<ST, K, VT, NW, VPL>::EPL],
-    const float (&al)[TileGeom<ST, K, VT, NW, VPL>::EPL], float beta, const float *v_rows) {
-  using G = TileGeom<ST, K, VT, NW, VPL>;
-#pragma unroll
-  for (int p = 0; p < G::NP; ++p) {
-    float u = 0.f;
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) {
-      s[p][e] *= al[e];
-      u = fmaf(s[p][e], kh[e], u);
-    }
-    u = group_sum<G::LPR>(u);
-    const float d = beta * (v_rows[G::row(p)] - u);
-#pragma unroll
-    for (int e = 0; e < G::EPL; ++e) s[p][e] = fmaf(d, kh[e], s[p][e]);
-  }
-}
-
 // ---- the same on a tile held as fp32 pairs: each lane's EPL elements of a row as EPL/2
 // float2, updated with the packed fp32 instructions (two lanes of arithmetic per issue).
 template <typename ST, int K, int VT, int NW = 4, int VPL = 1>
