@@ -49,7 +49,7 @@ DECODE_SOURCES = ("decode.cu", "rsc_step.cuh", "rsc_common.cuh")
 # Layers per host<->device copy in the end-to-end step (fewer, larger copies against a finer
 # overlap of copies and compute).
 E2E_GROUP = 8
-CAPTURED_DECODE_TRAFFIC = {"3de2aebca50da18e": 28_091_392}
+CAPTURED_DECODE_TRAFFIC = {"5b16fde349e60789": 28_077_056}
 
 
 # --------------------------------------------------------------------------- plumbing

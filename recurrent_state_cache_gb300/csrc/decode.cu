@@ -331,21 +331,31 @@ kda_decode_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #define RSC_DECODE_EARLY_CHUNKS 2
 #endif
 // The same for the overlapped launch, where the early chunks are requested before the wait
-// for the previous kernel (69-layer graph, us per layer: 4 chunks with 1/2/3/4 early
-// 10.1/9.05/10.0/11.0; 8 chunks with 2/4/6 early 10.1/9.2/10.0; 2 chunks with 1 early 8.98).
-#ifndef RSC_DECODE_OVL_CHUNKS
-#define RSC_DECODE_OVL_CHUNKS 2
+// for the previous kernel, per state dtype.  bf16, 69-layer KDA graph at batch 64, us per
+// layer: 4 chunks with 1/2/3/4 early 10.1/9.05/10.0/11.0; 8 with 2/4/6 early 10.1/9.2/10.0;
+// 2 with 1 early 8.98.  fp32 (64 KB tiles), 48-layer GDN graph at batch 1/16/64: 2 with 1
+// early 4.74/13.7/42.6; 4 with 2 early 4.23/13.1/42.3; 4 with 1 or 3 and 8 with 4 no better.
+#ifndef RSC_DECODE_OVL_CHUNKS_BF16
+#define RSC_DECODE_OVL_CHUNKS_BF16 2
 #endif
-#ifndef RSC_DECODE_OVL_EARLY_CHUNKS
-#define RSC_DECODE_OVL_EARLY_CHUNKS 1
+#ifndef RSC_DECODE_OVL_EARLY_BF16
+#define RSC_DECODE_OVL_EARLY_BF16 1
+#endif
+#ifndef RSC_DECODE_OVL_CHUNKS_F32
+#define RSC_DECODE_OVL_CHUNKS_F32 4
+#endif
+#ifndef RSC_DECODE_OVL_EARLY_F32
+#define RSC_DECODE_OVL_EARLY_F32 2
 #endif
 
 template <typename ST> struct DecodeTile;
 template <> struct DecodeTile<bf16> {
   static constexpr int ROWS = RSC_DECODE_ROWS_BF16, WARPS = RSC_DECODE_WARPS_BF16;
+  static constexpr int OVL_CHUNKS = RSC_DECODE_OVL_CHUNKS_BF16, OVL_EARLY = RSC_DECODE_OVL_EARLY_BF16;
 };
 template <> struct DecodeTile<float> {
   static constexpr int ROWS = RSC_DECODE_ROWS_F32, WARPS = RSC_DECODE_WARPS_F32;
+  static constexpr int OVL_CHUNKS = RSC_DECODE_OVL_CHUNKS_F32, OVL_EARLY = RSC_DECODE_OVL_EARLY_F32;
 };
 
 template <typename ST, typename IO, int K, int V, int GATE>
@@ -360,8 +370,8 @@ struct DecodeLaunch {
     constexpr int NP = TileGeom<ST, K, ROWS, NW>::NP;
     constexpr int NCH = NP % RSC_DECODE_CHUNKS == 0 ? RSC_DECODE_CHUNKS : 1;
     constexpr int EARLY = RSC_DECODE_EARLY_CHUNKS < NCH ? RSC_DECODE_EARLY_CHUNKS : NCH;
-    constexpr int ONCH = NP % RSC_DECODE_OVL_CHUNKS == 0 ? RSC_DECODE_OVL_CHUNKS : 1;
-    constexpr int OEARLY = RSC_DECODE_OVL_EARLY_CHUNKS < ONCH ? RSC_DECODE_OVL_EARLY_CHUNKS : ONCH;
+    constexpr int ONCH = NP % DecodeTile<ST>::OVL_CHUNKS == 0 ? DecodeTile<ST>::OVL_CHUNKS : 1;
+    constexpr int OEARLY = DecodeTile<ST>::OVL_EARLY < ONCH ? DecodeTile<ST>::OVL_EARLY : ONCH;
     auto kern = kda_decode_kernel<ST, IO, K, V, NVT, NW, NCH, EARLY, GATE, false>;
     auto kern_ovl = kda_decode_kernel<ST, IO, K, V, NVT, NW, ONCH, OEARLY, GATE, true>;
     static bool attr_set = false;  // per instantiation; set on the first (uncaptured) call
