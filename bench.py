@@ -357,31 +357,6 @@ def leg_copy(dev, peaks, stream, wl):
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
-_WRITE_PEAK = None
-
-
-def write_peak(dev):
-    """Measured rate of a pure device write stream (torch fill of 2 GiB), GB/s: the roof of
-    a kernel whose traffic is almost all writes."""
-    global _WRITE_PEAK
-    if _WRITE_PEAK is None:
-        import torch
-        x = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
-        for _ in range(3):
-            x.fill_(1.0)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(10):
-            x.fill_(2.0)
-        e1.record()
-        torch.cuda.synchronize()
-        _WRITE_PEAK = round(2 * (1 << 30) / (e0.elapsed_time(e1) / 10 * 1e-3) / 1e9, 1)
-        del x
-        torch.cuda.empty_cache()
-    return _WRITE_PEAK
-
-
 def leg_spec(dev, peaks, stream):
     import torch
     import recurrent_state_cache_gb300 as rsc
@@ -417,7 +392,6 @@ def leg_spec(dev, peaks, stream):
             "verify_ms": round(ms_v, 4), "verify_gbs": round(vb / (ms_v * 1e-3) / 1e9, 1),
             "verify_frac": round(vb / (ms_v * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "verify_write_gbs": round(vw / (ms_v * 1e-3) / 1e9, 1),
-            "write_peak_gbs": write_peak(dev),
             "commit_ms": round(ms_c, 4), "commit_gbs": round(cb / (ms_c * 1e-3) / 1e9, 1),
             "commit_frac": round(cb / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
