@@ -31,11 +31,28 @@
 
 namespace rsc {
 
-// Resident CTAs per SM the replay commit is compiled for (4: 128 registers); it runs on the
-// snapshot verify's CTA shape (64 rows, 4 warps: measured 23.8 against 25.3 us with a whole
-// head per CTA).
+// Replay commit: 64 state rows and 4 warps per CTA, compiled for 4 resident CTAs per SM (128
+// registers); measured 23.8 against 25.3 us with a whole head per CTA.
+#ifndef RSC_COMMIT_ROWS
+#define RSC_COMMIT_ROWS 64
+#endif
+#ifndef RSC_COMMIT_WARPS
+#define RSC_COMMIT_WARPS 4
+#endif
 #ifndef RSC_COMMIT_MINB
 #define RSC_COMMIT_MINB 4
+#endif
+// Snapshot verify: a whole head per CTA (8 warps) compiled for 2 resident CTAs per SM (128
+// registers).  B=64, T=8, H=12: 51.0 us; 64 rows x 4 warps 63.9 us unbounded (168 registers,
+// 3 CTAs per SM) and 61.4 us at 4 CTAs per SM; a whole head at 1 CTA per SM 66.5 us.
+#ifndef RSC_SNAPSHOT_ROWS
+#define RSC_SNAPSHOT_ROWS 128
+#endif
+#ifndef RSC_SNAPSHOT_WARPS
+#define RSC_SNAPSHOT_WARPS 8
+#endif
+#ifndef RSC_SNAPSHOT_MINB
+#define RSC_SNAPSHOT_MINB 2
 #endif
 // Record-mode verify: state rows and warps per CTA (rows = 16 x warps, so that the block's
 // row dots reduce to one value per lane), and the resident CTAs it is compiled for.  A whole
@@ -52,7 +69,8 @@ namespace rsc {
 #endif
 
 template <typename ST, typename IO, int K, int V, int NVT, int NW, int GATE, bool REPLAY>
-__global__ void __launch_bounds__(NW * 32, REPLAY ? RSC_REPLAY_MINB * RSC_REPLAY_WARPS / NW : 1)
+__global__ void __launch_bounds__(NW * 32, REPLAY ? RSC_REPLAY_MINB * RSC_REPLAY_WARPS / NW
+                                                   : RSC_SNAPSHOT_MINB)
 kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
                        int L, ST *__restrict__ spec_ssm, IO *__restrict__ spec_conv,
                        const IO *__restrict__ qkv, const float *__restrict__ conv_w,
@@ -182,7 +200,7 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   //   S <- S0 Diag(e^G_last) + sum_s d_s (k_hat_s . e^(G_last - G_s))^T.
   auto replay_block = [&](int t0, int cnt) {
     constexpr int LPR = G::LPR, NP = G::NP, E2 = G::EPL / 2;
-    static_assert(2 * NP == LPR, "the reduction leaves one value per lane");
+    static_assert(!REPLAY || 2 * NP == LPR, "the reduction leaves one value per lane");
     const bool more = t0 + TS < T;
     auto gk = [](int k) { return GW == 1 ? 0 : k; };
     // exponentials of log-decay sums over at most eight tokens (arguments of moderate size,
@@ -200,7 +218,7 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       // covers CPL consecutive channels of one half of K (lanes 0-15 the first half, 16-31
       // the second), so a warp's shared-memory reads are contiguous
       constexpr int PPW = NW >= 7 ? 4 : 8;
-      static_assert(NW * PPW >= TS * (TS - 1) / 2, "pairs per warp");
+      static_assert(!REPLAY || NW * PPW >= TS * (TS - 1) / 2, "pairs per warp");
       constexpr int CPL = K / 32;
       static_assert(CPL == 2 || CPL == 4, "channels per lane");
       const int c0 = (lane >> 4) * (K / 2) + CPL * (lane & 15);
@@ -471,21 +489,14 @@ kda_spec_verify_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   }
 }
 
-// State rows and warps per verify CTA.
-#ifndef RSC_VERIFY_ROWS
-#define RSC_VERIFY_ROWS 64
-#endif
-#ifndef RSC_VERIFY_WARPS
-#define RSC_VERIFY_WARPS 4
-#endif
 
 template <typename ST, typename IO, int K, int V, int GATE>
 struct VerifyLaunch {
   static int run(const LayerArgs *a, const int32_t *slots, int B, int T, int L,
                  void *spec_ssm, void *spec_conv, const void *qkv, const float *conv_w,
                  const float *g, const float *beta, void *out, cudaStream_t s) {
-    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
-    constexpr int NW = RSC_VERIFY_WARPS;
+    constexpr int NVT = V / (RSC_SNAPSHOT_ROWS < V ? RSC_SNAPSHOT_ROWS : V);
+    constexpr int NW = RSC_SNAPSHOT_WARPS;
     dim3 grid(NVT, a->pv.H, B);
     kda_spec_verify_kernel<ST, IO, K, V, NVT, NW, GATE, false><<<grid, NW * 32, 0, s>>>(
         a->pv, a->layer, slots, T, L, static_cast<ST *>(spec_ssm),
@@ -662,8 +673,8 @@ template <typename ST, typename IO, int K, int V, int GATE>
 struct ReplayCommitLaunch {
   static int run(const LayerArgs *a, const RingView *rv, const int32_t *slots, const int32_t *pos,
                  int B, int T, const void *spec_conv, const int32_t *accept, cudaStream_t s) {
-    constexpr int NVT = V / (RSC_VERIFY_ROWS < V ? RSC_VERIFY_ROWS : V);
-    constexpr int NW = RSC_VERIFY_WARPS;
+    constexpr int NVT = V / (RSC_COMMIT_ROWS < V ? RSC_COMMIT_ROWS : V);
+    constexpr int NW = RSC_COMMIT_WARPS;
     dim3 grid(NVT, a->pv.H, B);
     kda_replay_commit_kernel<ST, IO, K, V, NVT, NW, GATE><<<grid, NW * 32, 0, s>>>(
         a->pv, *rv, a->layer, slots, pos, T, static_cast<const IO *>(spec_conv), accept);
