@@ -44,7 +44,8 @@ namespace rsc {
 #endif
 // Snapshot verify: a whole head per CTA (8 warps) compiled for 2 resident CTAs per SM (128
 // registers).  B=64, T=8, H=12: 51.0 us; 64 rows x 4 warps 63.9 us unbounded (168 registers,
-// 3 CTAs per SM) and 61.4 us at 4 CTAs per SM; a whole head at 1 CTA per SM 66.5 us.
+// 3 CTAs per SM) and 61.4 us at 4 CTAs per SM; a whole head at 1 CTA per SM 66.5 us; a whole
+// head on 16 warps 81 us at 1 or 2 CTAs per SM.
 #ifndef RSC_SNAPSHOT_ROWS
 #define RSC_SNAPSHOT_ROWS 128
 #endif
