@@ -32,7 +32,9 @@
 namespace rsc {
 
 // Replay commit: 64 state rows and 4 warps per CTA, compiled for 4 resident CTAs per SM (128
-// registers); measured 23.8 against 25.3 us with a whole head per CTA.
+// registers); measured 23.8 against 25.3 us with a whole head per CTA.  At accept 0 / 7 for
+// every request: 15.0 / 27.0 us; 32-row tiles at 6 or 7 CTAs per SM 14.3-14.8 / 29.0; 64 rows at
+// 3 CTAs per SM 17.4 / 29.5.
 #ifndef RSC_COMMIT_ROWS
 #define RSC_COMMIT_ROWS 64
 #endif
