@@ -211,6 +211,34 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+# --------------------------------------------------------------------------- roofline arithmetic
+
+def decode_bytes_per_launch(B, H, K, V, state_bytes, io_bytes, per_channel_gate=True):
+    """Algorithmic bytes of one decode launch: per request the state read + written, the
+    window read + written, qkv, g, beta, out and its slot id; plus the layer's conv taps."""
+    D = H * (2 * K + V)
+    gw = K if per_channel_gate else 1
+    per_req = (2 * H * V * K * state_bytes + 2 * 3 * D * io_bytes + D * io_bytes + H * gw * 4
+               + H * 4 + H * V * io_bytes + 4)
+    return B * per_req + D * 4 * 4
+
+
+def prefill_flops(T, H, K, V, C=64):
+    """Algorithmic tensor flops of a chunked prefill of T tokens: per token and head
+    6CK + 4CV + 6KV (A, P, W; U', P U'; W S^T, Q S^T, U^T K)."""
+    return T * H * (6 * C * K + 4 * C * V + 6 * K * V)
+
+
+def spec_verify_bytes(B, T, H, K, V, state_bytes=2, io_bytes=2):
+    """Algorithmic bytes of a snapshot verify: per request the slot state read and T states
+    written, the window read and T window entries written, and per token qkv, g, beta, out;
+    plus the slot id."""
+    D = H * (2 * K + V)
+    S, Wb = H * V * K * state_bytes, 3 * D * io_bytes
+    return B * (S + T * S + Wb + T * Wb + T * D * io_bytes + T * H * K * 4 + T * H * 4
+                + T * H * V * io_bytes + 4)
+
+
 # --------------------------------------------------------------------------- workloads
 
 def _softplus_neg(t):
@@ -254,15 +282,10 @@ class DecodeWorkload:
                                 self.beta[l], self.out[l], overlap=self.overlap)
 
     def bytes_per_launch(self):
-        """Algorithmic bytes of one layer launch: per request the state read + written,
-        window read + written, qkv, g, beta, out and its slot id; plus the layer's taps."""
-        ss = 4 if self.st == 0 else 2
-        io = 4 if self.io == 0 else 2
-        H, K, V, D = self.H, self.K, self.V, self.D
-        gw = K if self.gate == 0 else 1
-        per_req = (2 * H * V * K * ss + 2 * 3 * D * io + D * io + H * gw * 4 + H * 4
-                   + H * V * io + 4)
-        return self.B * per_req + D * 4 * 4
+        """Algorithmic bytes of one layer launch (decode_bytes_per_launch)."""
+        return decode_bytes_per_launch(self.B, self.H, self.K, self.V,
+                                       4 if self.st == 0 else 2, 4 if self.io == 0 else 2,
+                                       self.gate == 0)
 
 
 # --------------------------------------------------------------------------- legs
@@ -326,7 +349,7 @@ def leg_prefill(dev, peaks, stream):
 
     graph = graph_of(run, stream)
     ms = timed(graph.replay, 5, 2, stream)
-    flops = T * H * (6 * 64 * K + 4 * 64 * V + 6 * K * V)
+    flops = prefill_flops(T, H, K, V)
     io_bytes = T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2
     res = {"config": "1 KDA layer, H=12, K=V=128, bf16, 13600 tokens as 6144/6144/1312, snapshot copy after each",
            "ms_per_prefill": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
@@ -385,7 +408,7 @@ def leg_spec(dev, peaks, stream):
     ms_v = timed(verify, 10, 3, stream)
     ms_c = timed(commit, 10, 3, stream)
     S, Wb = H * V * K * 2, 3 * D * 2
-    vb = B * (S + T * S + Wb + T * Wb + T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2 + 4)
+    vb = spec_verify_bytes(B, T, H, K, V)
     cb = B * 2 * (S + Wb)
     vw = B * (T * S + T * Wb + T * H * V * 2)  # bytes written by verify
     return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), cache depth 16",
