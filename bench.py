@@ -42,14 +42,15 @@ if ROOT not in sys.path:
 
 HEADLINE_METRIC = "decode tokens/s per layer and achieved HBM GB/s (% of peak); prefill tok/s"
 
-# DRAM bytes (read + write) per launch of the headline decode kernel in an ncu capture of the
-# same launch shape (64 requests; profiles/kda_decode_kimi_k3_b64.md), keyed by a hash of the
-# kernel's source files: reported only while the kernel is the one that was captured.
+# DRAM bytes (read + write) per launch of the headline decode kernel in a one-pass ncu capture
+# of the same launch shape (64 requests, 12 heads, second of two captured launches' first),
+# keyed by a hash of the kernel's source files: reported only while the kernel is the one
+# that was captured.
 DECODE_SOURCES = ("decode.cu", "rsc_step.cuh", "rsc_common.cuh")
 # Layers per host<->device copy in the end-to-end step (fewer, larger copies against a finer
 # overlap of copies and compute).
 E2E_GROUP = 8
-CAPTURED_DECODE_TRAFFIC = {"5b16fde349e60789": 28_077_056}
+CAPTURED_DECODE_TRAFFIC = {"3f787822c76e207d": 28_080_384}
 
 
 # --------------------------------------------------------------------------- plumbing
@@ -62,7 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="all", help="comma list of gdn,prefill,copy,spec,replay,gated,track or all/none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=2.0,
+                    help="wall seconds of each oracle baseline run (six runs)")
     ap.add_argument("--layers", type=int, default=69,
                     help="layers of the headline decode pool (69 = the Kimi-K3 shard; fewer "
                          "only for small profiling captures)")
@@ -532,69 +534,169 @@ def leg_replay(dev, peaks, stream):
 
 # --------------------------------------------------------------------------- oracle timing
 
-class OracleDecodeSample:
-    """One layer-step of the headline workload (64 requests, H=12, K=V=128, bf16 state
-    and io, KDA gate) on the CPU oracle; inputs built once, outside any timing."""
+class OracleWork:
+    """One unit of oracle work on synthetic inputs built once, outside any timing.
+    kind "kda_decode": a layer-step of `part` requests of the headline workload (H=12,
+      K=V=128, bf16 state and io, per-channel gate);
+    kind "gdn_decode": a layer-step of `part` requests of the GDN workload (H=32, K=V=128, fp32
+      state, bf16 io, per-head gate);
+    kind "prefill": a recurrent prefill call of `tokens` tokens over `part` heads of the
+      chunked-prefill workload (K=V=128, bf16), continuing from the slot.
+    units() = tokens processed per step (requests for decode, tokens for prefill; a prefill
+    over a share of the heads counts its tokens divided by the share)."""
 
-    def __init__(self, seed=0):
+    SHAPES = {"kda_decode": (12, 0, 0, 1, 1), "gdn_decode": (32, 1, 1, 0, 1),
+              "prefill": (12, 0, 0, 1, 1)}
+
+    def __init__(self, kind, part, seed=0, tokens=2048):
         import oracle
         from recurrent_state_cache_gb300 import inputs
-        self.oracle = oracle
-        H, K, V, B = 12, 128, 128, 64
-        self.B = B
+        self.oracle, self.kind, self.part = oracle, kind, part
+        H_full, gate, _, st, io = self.SHAPES[kind]
+        st = oracle.BF16 if st else oracle.F32
+        io = oracle.BF16 if io else oracle.F32
+        gate = oracle.GDN if gate else oracle.KDA
+        K = V = 128
         r = inputs.rng(seed)
-        ssm, conv = inputs.pool_arrays(r, 1, B, H, K, V, oracle.BF16, oracle.BF16)
-        self.pool = oracle.Pool(1, B, H, K, V, oracle.BF16, oracle.BF16, oracle.KDA, ssm, conv)
+        if kind == "prefill":
+            H, B, self.T = part, 1, tokens
+            self.share = part / H_full
+        else:
+            H, B = H_full, part
+            self.share = 1.0
+        ssm, conv = inputs.pool_arrays(r, 1, B, H, K, V, st, io)
+        self.pool = oracle.Pool(1, B, H, K, V, st, io, gate, ssm, conv)
         self.w = inputs.conv_weights(r, H, K, V)
         self.slots = inputs.distinct_slots(r, B, B)
-        self.x = inputs.projections(r, (B,), H, K, V, oracle.BF16)
-        self.g, self.beta = inputs.gates(r, (B,), H, K, oracle.KDA)
+        lead = (self.T,) if kind == "prefill" else (B,)
+        self.x = inputs.projections(r, lead, H, K, V, io)
+        self.g, self.beta = inputs.gates(r, lead, H, K, gate)
+        self.cu = np.int32([0, self.T]) if kind == "prefill" else None
 
     def step(self):
-        self.oracle.decode_step(self.pool, 0, self.slots, self.x, self.w, self.g, self.beta)
+        if self.kind == "prefill":
+            self.oracle.prefill(self.pool, 0, self.slots, self.cu, self.x, self.w, self.g, self.beta)
+        else:
+            self.oracle.decode_step(self.pool, 0, self.slots, self.x, self.w, self.g, self.beta)
+
+    def units(self):
+        return self.T * self.share if self.kind == "prefill" else self.part
 
 
-def oracle_decode_sample(seconds: float, seed=0):
-    """Time oracle layer-steps of the headline workload until `seconds` of CPU work;
-    returns (tokens/s per layer, description of the sample)."""
-    s = OracleDecodeSample(seed)
-    n = 0
+def _oracle_worker(kind, part, seed, tokens, steps, barrier, q):
+    w = OracleWork(kind, part, seed, tokens)
+    w.step()  # warm
+    barrier.wait()
+    t0 = time.time()
+    for _ in range(steps):
+        w.step()
+    q.put((t0, time.time(), w.units() * steps))
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _split(n, parts):
+    """n work items over at most `parts` workers, as even as possible (no empty share)."""
+    parts = max(1, min(parts, n))
+    return [n // parts + (1 if i < n % parts else 0) for i in range(parts)]
+
+
+def oracle_rate(kind, total, seconds, cores=1, seed=0, tokens=2048, steps=None):
+    """Oracle throughput (tokens/s) on `kind` over `total` requests (decode) or heads
+    (prefill), single-threaded (cores = 1) or split over `cores` worker processes (spawned,
+    each with its own share and inputs) that start together; the steps are sized to about
+    `seconds` of wall time unless given.  Returns (tokens/s, workers used, steps, wall s)."""
+    one = OracleWork(kind, total if cores == 1 else _split(total, cores)[0], seed, tokens)
     t0 = time.perf_counter()
-    while True:
-        s.step()
-        n += 1
+    one.step()
+    t_step = time.perf_counter() - t0
+    if steps is None:
+        steps = max(1, int(seconds / max(t_step, 1e-6)))
+    if cores == 1:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one.step()
         el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return s.B * n / el, f"{n} layer-steps of 64 requests (H=12, K=V=128, bf16) in {el:.1f} s"
+        return one.units() * steps / el, 1, steps, el
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    shares = _split(total, cores)
+    barrier = ctx.Barrier(len(shares))
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(kind, n, seed + i, tokens, steps, barrier, q))
+             for i, n in enumerate(shares)]
+    for p in procs:
+        p.start()
+    import queue
+    res = []
+    limit = time.time() + 120 + 20 * max(seconds, t_step * steps)
+    try:
+        while len(res) < len(procs):
+            try:
+                res.append(q.get(timeout=1.0))
+            except queue.Empty:
+                if any(p.exitcode not in (None, 0) for p in procs) or time.time() > limit:
+                    raise RuntimeError("an oracle worker process failed or did not finish")
+    finally:
+        for p in procs:
+            p.join(timeout=5)
+            if p.is_alive():
+                p.kill()
+    start = min(r[0] for r in res)
+    end = max(r[1] for r in res)
+    units = sum(r[2] for r in res)
+    return units / (end - start), len(shares), steps, end - start
+
+
+def oracle_baselines(seconds: float):
+    """The oracle on the machine's host cores, single-threaded and on all cores, for the three
+    workloads: KDA decode (64 requests), GDN decode (16 requests, one layer), chunked-prefill
+    workload in recurrent form (a 2048-token sample of the 13600-token prompt, 12 heads)."""
+    cores = host_cores()
+    out = {}
+    for name, kind, total in (("kda_decode_b64", "kda_decode", 64),
+                              ("gdn_decode_b16", "gdn_decode", 16),
+                              ("prefill_13600_sample2048", "prefill", 12)):
+        r1, _, n1, e1 = oracle_rate(kind, total, seconds, 1)
+        rn, used, nn, en = oracle_rate(kind, total, seconds, cores)
+        out[name] = {"single_core": round(r1, 3), "all_cores": round(rn, 3), "cores": used,
+                     "unit": "tokens/s per layer",
+                     "steps": [n1, nn], "seconds": [round(e1, 2), round(en, 2)]}
+    return cores, out
 
 
 # --------------------------------------------------------------------------- main
 
 def run_reference(args):
+    """The reference arm: the oracle itself on the host cores, on the headline workload.  A
+    step is one layer-step of the 64 requests, split by request over worker processes on all
+    host cores (the oracle's code as it stands, each worker with its share of the requests)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
     total_t0 = time.perf_counter()
-    sample = OracleDecodeSample(0)
-    for _ in range(args.warmup):
-        sample.step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        sample.step()
-    ms = 1e3 * (time.perf_counter() - t0) / args.steps
-    value = 64 / (ms * 1e-3)
+    cores = host_cores()
+    rate, used, steps, wall = oracle_rate("kda_decode", 64, 0.0, cores, steps=args.steps)
+    ms = 1e3 * wall / steps
+    value = rate
     line = {"metric": HEADLINE_METRIC, "value": round(value, 3), "unit": "tokens/s per layer",
             "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "kda_decode_kimi_k3_tp8_shard", "layers_per_step": 1,
                        "batch": 64, "H": 12, "K": 128, "V": 128, "state_dtype": "bf16"},
-            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s per layer", "cores": 1,
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s per layer", "cores": used,
                              "kind": "oracle",
-                             "sample": "each step: one layer-step of 64 requests of the headline workload"},
+                             "sample": f"each step: one layer-step of the 64 requests of the headline "
+                                       f"workload, split by request over {used} worker processes "
+                                       f"({cores} host cores); each worker warmed by one step"},
             "e2e": {"value": round(value, 3), "unit": "tokens/s per layer",
                     "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.perf_counter() - total_t0, 1)}
@@ -729,9 +831,15 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, sample = oracle_decode_sample(args.cpu_seconds)
-        cpu = {"value": round(v, 3), "unit": "tokens/s per layer", "cores": 1, "kind": "oracle",
-               "sample": sample}
+        cores, wls = oracle_baselines(args.cpu_seconds)
+        head = wls["kda_decode_b64"]
+        cpu = {"value": head["all_cores"], "unit": "tokens/s per layer", "cores": head["cores"],
+               "kind": "oracle",
+               "sample": f"layer-steps of the headline workload (64 requests, H=12, K=V=128, bf16) "
+                         f"split by request over {head['cores']} worker processes of the {cores} "
+                         f"host cores; about {args.cpu_seconds:g} s per run; single-threaded "
+                         f"{head['single_core']} tokens/s",
+               "single_core": head["single_core"], "host_cores": cores, "workloads": wls}
 
     clocks = clk.summary()
     line = {

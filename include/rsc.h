@@ -29,6 +29,9 @@
  *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  Host-side validation failures return a negative status before anything
  *     is launched.  A CUDA launch failure returns RSC_ECUDA.
+ *   - Every call that launches runs on the current device, which must be the device that
+ *     holds the pool's memory; otherwise it returns RSC_EDEVICE and launches nothing (the
+ *     device of the pool is looked up on its first launching call and remembered).
  *   - Values the host cannot see (slot ids, accept counts, sequence offsets: all device
  *     arrays) are checked on the device.  A bad row is skipped (nothing of that row is
  *     written) and a bit is OR-ed into the pool's device error word; read it with
@@ -55,6 +58,7 @@ extern "C" {
 #define RSC_EALIGN   -4 /* a vector-accessed pointer is not 16-byte aligned         */
 #define RSC_ECUDA    -5 /* a CUDA runtime call or launch failed                      */
 #define RSC_ENOSPACE -6 /* caller-provided workspace too small                       */
+#define RSC_EDEVICE  -7 /* the pool's memory is not device memory of the current device */
 
 /* Bits of the device error word. */
 #define RSC_DEVERR_SLOT   1 /* a slot id outside [0, num_slots]                      */
@@ -144,15 +148,19 @@ int kda_decode_step_ex(rsc_pool *pool, int layer, const int32_t *slot_ids, int b
 
 /* kda_decode_step as a programmatic dependent launch of the previous kernel on `stream`, so
  * that this layer's state reads overlap the tail of the work before it.  The kernel may
- * start while earlier kernels on the stream still run; BEFORE waiting for them it reads
- * slot_ids and layer `layer`'s state tiles and conv windows of those slots; qkv, conv_w, g
- * and beta are read, and every write is made, after the wait.  Caller precondition: no
- * earlier work on `stream` that may still be pending writes slot_ids or those state and
- * window rows.  In a model step the kernels before a layer's decode (its input projection,
- * the other layers' decodes) write neither; two consecutive calls on the same layer and
- * slots do -- use kda_decode_step there.  Results are bit-identical to kda_decode_step.
- * Measured on GB300 (69 layers x 64 requests, H=12, K=V=128, bf16, in a CUDA graph):
- * 8.97 instead of 11.31 us per layer.
+ * start while the kernel just before it on the stream still runs; BEFORE waiting for it, it
+ * reads slot_ids and layer `layer`'s state tiles and conv windows of those slots; qkv,
+ * conv_w, g and beta are read, and every write is made, after the wait.  The kernel
+ * releases its own dependents only after that wait, so when an overlapped call starts,
+ * every kernel before its immediate predecessor has completed: its early reads can overlap
+ * that one kernel alone.
+ * Caller precondition: the kernel immediately before this call on `stream` does not write
+ * slot_ids or those state and window rows (a caller's own programmatic-dependent kernel
+ * placed there must also release its dependents only after its own griddepcontrol.wait).
+ * Overlapped calls on different layers, one after another in any number and across steps
+ * (a model step's graph replayed back to back), meet it; two consecutive calls on the same
+ * layer and slots do not -- use kda_decode_step for the second.  Results are bit-identical
+ * to kda_decode_step.
  * Errors: as kda_decode_step. */
 int kda_decode_step_overlap(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch,
                             const void *qkv, const float *conv_w, const float *g,

@@ -66,5 +66,34 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+WAIT_TEST_LIB = os.path.join(BUILD, "librsc_waittest.so")
+WAIT_TEST_FLAGS = ["-DRSC_TEST_STARVE_FIRST_CHUNK", "-DRSC_MBAR_SPIN_LIMIT=65536u"]
+
+
+def build_wait_test() -> str:
+    """Test build of the decode path whose bounded wait runs out: decode.cu compiled with
+    RSC_TEST_STARVE_FIRST_CHUNK (request 0's first state chunk is armed on its mbarrier but
+    never copied) and a short spin limit, linked with the other objects of the library
+    build.  Used only by the test of the give-up path; returns the library's path."""
+    build()
+    nvcc = _nvcc()
+    src = os.path.join(CSRC, "decode.cu")
+    obj = os.path.join(BUILD, "decode_waittest.o")
+    r = subprocess.run([nvcc, *ARCH, *NVCC_FLAGS, *WAIT_TEST_FLAGS, "-c", src, "-o", obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on decode.cu (wait test):\n{r.stdout}\n{r.stderr}")
+    others = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+              for s in sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+              if os.path.basename(s) != "decode.cu"]
+    tmp = WAIT_TEST_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, obj, *others], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link of the wait-test library failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, WAIT_TEST_LIB)
+    return WAIT_TEST_LIB
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose=True))

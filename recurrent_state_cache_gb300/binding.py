@@ -18,8 +18,8 @@ F32, BF16 = 0, 1
 KDA, GDN = 0, 1
 VERIFY, COMMIT = 0, 1
 
-RSC_OK, RSC_EINVAL, RSC_ERANGE, RSC_EDTYPE, RSC_EALIGN, RSC_ECUDA, RSC_ENOSPACE = (
-    0, -1, -2, -3, -4, -5, -6)
+RSC_OK, RSC_EINVAL, RSC_ERANGE, RSC_EDTYPE, RSC_EALIGN, RSC_ECUDA, RSC_ENOSPACE, RSC_EDEVICE = (
+    0, -1, -2, -3, -4, -5, -6, -7)
 DEVERR_SLOT, DEVERR_ACCEPT, DEVERR_SEQ, DEVERR_TIMEOUT, DEVERR_GATE, DEVERR_RING = 1, 2, 4, 8, 16, 32
 
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
@@ -142,9 +142,31 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream(stream, pool):
+    """The call's stream: `stream`, else the current torch stream of the pool's device."""
+    s = stream if stream is not None else torch.cuda.current_stream(pool.device)
+    if s.device != pool.device:
+        raise ValueError(f"stream on {s.device}, the pool is on {pool.device}")
     return ctypes.c_void_p(s.cuda_stream)
+
+
+class _on:
+    """Makes the pool's device current for one library call (the library launches on the
+    current device and rejects a pool held by another one)."""
+
+    def __init__(self, pool):
+        self.dev = pool.device.index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.dev:
+            self.prev = cur
+            torch.cuda.set_device(self.dev)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
 
 
 def _need(t, name, dtype, shape, device):
@@ -236,9 +258,10 @@ def kda_decode_step(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, out=N
         out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
     _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
     fn = lib().kda_decode_step_overlap if overlap else lib().kda_decode_step
-    _check(fn(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w), _p(g), _p(beta),
-              _p(out), _stream(stream)),
-           "kda_decode_step_overlap" if overlap else "kda_decode_step")
+    with _on(pool):
+        _check(fn(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w), _p(g), _p(beta),
+                  _p(out), _stream(stream, pool)),
+               "kda_decode_step_overlap" if overlap else "kda_decode_step")
     return out
 
 
@@ -270,10 +293,11 @@ def kda_prefill_chunk(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, conv_w, 
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if workspace.dtype != torch.uint8 or workspace.device != dev:
         raise ValueError("workspace: a uint8 tensor on the pool's device")
-    _check(lib().kda_prefill_chunk(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N, T,
-                                   _p(has_initial_state), _p(qkv), _p(conv_w), _p(g), _p(beta),
-                                   _p(out), _p(workspace), workspace.numel(), _stream(stream)),
-           "kda_prefill_chunk")
+    with _on(pool):
+        _check(lib().kda_prefill_chunk(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N, T,
+                                       _p(has_initial_state), _p(qkv), _p(conv_w), _p(g), _p(beta),
+                                       _p(out), _p(workspace), workspace.numel(), _stream(stream, pool)),
+               "kda_prefill_chunk")
     return out
 
 
@@ -297,10 +321,11 @@ def kda_prefill_chunk_noalloc(pool: SlotPool, layer, slot_ids, cu_seqlens, qkv, 
     if out is None:
         out = torch.empty((T, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
     _need(out, "out", pool.io_dtype, (T, pool.H, pool.V), dev)
-    _check(lib().kda_prefill_chunk_noalloc(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N,
-                                           T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
-                                           _p(beta), _p(out), _stream(stream)),
-           "kda_prefill_chunk_noalloc")
+    with _on(pool):
+        _check(lib().kda_prefill_chunk_noalloc(pool.handle, layer, _p(slot_ids), _p(cu_seqlens), N,
+                                               T, _p(has_initial_state), _p(qkv), _p(conv_w), _p(g),
+                                               _p(beta), _p(out), _stream(stream, pool)),
+               "kda_prefill_chunk_noalloc")
     return out
 
 
@@ -330,9 +355,10 @@ def kda_decode_step_ex(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta, ou
     addr = lambda t: None if t is None else t.data_ptr()
     opts = DecodeOpts(addr(A_log), addr(dt_bias), addr(track_mask), addr(track_slots),
                       DECODE_OVERLAP if overlap else 0)
-    _check(lib().kda_decode_step_ex(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
-                                    _p(g), _p(beta), _p(out), ctypes.byref(opts),
-                                    _stream(stream)), "kda_decode_step_ex")
+    with _on(pool):
+        _check(lib().kda_decode_step_ex(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                        _p(g), _p(beta), _p(out), ctypes.byref(opts),
+                                        _stream(stream, pool)), "kda_decode_step_ex")
     return out
 
 
@@ -352,9 +378,10 @@ def kda_decode_step_track(pool: SlotPool, layer, slot_ids, qkv, conv_w, g, beta,
     if out is None:
         out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
     _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
-    _check(lib().kda_decode_step_track(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
-                                       _p(g), _p(beta), _p(out), _p(track_mask), _p(track_slots),
-                                       _stream(stream)), "kda_decode_step_track")
+    with _on(pool):
+        _check(lib().kda_decode_step_track(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                           _p(g), _p(beta), _p(out), _p(track_mask), _p(track_slots),
+                                           _stream(stream, pool)), "kda_decode_step_track")
     return out
 
 
@@ -375,9 +402,10 @@ def kda_decode_step_gated(pool: SlotPool, layer, slot_ids, qkv, conv_w, a, b, A_
     if out is None:
         out = torch.empty((B, pool.H, pool.V), dtype=pool.io_dtype, device=dev)
     _need(out, "out", pool.io_dtype, (B, pool.H, pool.V), dev)
-    _check(lib().kda_decode_step_gated(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
-                                       _p(a), _p(b), _p(A_log), _p(dt_bias), _p(out),
-                                       _stream(stream)), "kda_decode_step_gated")
+    with _on(pool):
+        _check(lib().kda_decode_step_gated(pool.handle, layer, _p(slot_ids), B, _p(qkv), _p(conv_w),
+                                           _p(a), _p(b), _p(A_log), _p(dt_bias), _p(out),
+                                           _stream(stream, pool)), "kda_decode_step_gated")
     return out
 
 
@@ -388,8 +416,9 @@ def ssm_slot_copy(pool: SlotPool, layer, src, dst, mask=None, stream=None):
     _need(dst, "dst", torch.int32, (n,), dev)
     if mask is not None:
         _need(mask, "mask", torch.uint8, (n,), dev)
-    _check(lib().ssm_slot_copy(pool.handle, layer, _p(src), _p(dst), _p(mask), n,
-                               _stream(stream)), "ssm_slot_copy")
+    with _on(pool):
+        _check(lib().ssm_slot_copy(pool.handle, layer, _p(src), _p(dst), _p(mask), n,
+                                   _stream(stream, pool)), "ssm_slot_copy")
 
 
 def kda_spec_verify_commit(pool: SlotPool, layer, mode, slot_ids, T, L, spec_ssm, spec_conv,
@@ -410,10 +439,11 @@ def kda_spec_verify_commit(pool: SlotPool, layer, mode, slot_ids, T, L, spec_ssm
         _need(out, "out", pool.io_dtype, (B, T, pool.H, pool.V), dev)
     else:
         _need(accept, "accept", torch.int32, (B,), dev)
-    _check(lib().kda_spec_verify_commit(pool.handle, layer, mode, _p(slot_ids), B, T, L,
-                                        _p(spec_ssm), _p(spec_conv), _p(qkv), _p(conv_w), _p(g),
-                                        _p(beta), _p(out), _p(accept), _stream(stream)),
-           "kda_spec_verify_commit")
+    with _on(pool):
+        _check(lib().kda_spec_verify_commit(pool.handle, layer, mode, _p(slot_ids), B, T, L,
+                                            _p(spec_ssm), _p(spec_conv), _p(qkv), _p(conv_w), _p(g),
+                                            _p(beta), _p(out), _p(accept), _stream(stream, pool)),
+               "kda_spec_verify_commit")
     return out
 
 
@@ -459,11 +489,12 @@ def kda_replay_verify_commit(pool: SlotPool, rings: ReplayRings, layer, mode, sl
     else:
         _need(accept, "accept", torch.int32, (B,), dev)
     d = rings.desc()
-    _check(lib().kda_replay_verify_commit(pool.handle, ctypes.byref(d), layer, mode,
-                                          _p(slot_ids), _p(ring_pos), B, T, _p(spec_conv),
-                                          _p(qkv), _p(conv_w), _p(g), _p(beta), _p(out),
-                                          _p(accept), _stream(stream)),
-           "kda_replay_verify_commit")
+    with _on(pool):
+        _check(lib().kda_replay_verify_commit(pool.handle, ctypes.byref(d), layer, mode,
+                                              _p(slot_ids), _p(ring_pos), B, T, _p(spec_conv),
+                                              _p(qkv), _p(conv_w), _p(g), _p(beta), _p(out),
+                                              _p(accept), _stream(stream, pool)),
+               "kda_replay_verify_commit")
     return out
 
 
@@ -529,6 +560,7 @@ def track_plan(seq_lens, interval: int, track_pairs, next_idx):
 
 def rsc_get_device_error(pool: SlotPool, stream=None) -> int:
     code = ctypes.c_int32()
-    _check(lib().rsc_get_device_error(pool.handle, ctypes.byref(code), _stream(stream)),
-           "rsc_get_device_error")
+    with _on(pool):
+        _check(lib().rsc_get_device_error(pool.handle, ctypes.byref(code), _stream(stream, pool)),
+               "rsc_get_device_error")
     return code.value

@@ -50,10 +50,26 @@ constexpr int kC = 64;      // chunk length
 constexpr int kK = 128;     // key dim of the tensor-core path
 constexpr int kVmax = 128;  // largest value dim
 constexpr int kVT = 32;     // state rows per state-pass CTA
-// Largest per-channel spread of the cumulative log gate inside one chunk for which the
-// split exponentials e^(+-(G - R)) stay far from the fp32 / bf16 range (e^80 ~ 5.5e34).
-constexpr float kGateSpreadLimit = 160.f;
+constexpr int kSub = 16;    // rows of a sub-chunk block (four per chunk)
+// A diagonal 16-row block pairs k_r e^(G_r - Gb) with k_j e^(Gb - G_j), Gb the cumulative
+// gate at the block's first row: the second factor grows with the block's own spread of the
+// cumulative log gate.  Up to this spread (e^64 ~ 6e27, far inside the fp32 / bf16 range,
+// and so is e^-64) the block stays on the tensor core; a wider block is recomputed in fp32
+// from the exponent differences.
+constexpr float kDiagSpread = 64.f;
+constexpr float kMaxInv = 1e30f;  // clamp of e^(Gb - G_j) in a block beyond kDiagSpread
+// A growing gate (g > 0) turns the references' exponents positive; beyond this exponent the
+// chunk is flagged (RSC_DEVERR_GATE).  A decaying gate never reaches it.
+constexpr float kGrowLimit = 60.f;
 constexpr float kLog2e = 1.4426950408889634f;
+// Layout of the A / P product.  Rows (tensor-memory lanes): block I's 16 key rows, then its 16
+// query rows, at 32 I -- so lane quadrant I holds block I alone.  Columns: one segment per row
+// block, at ap_seg(I), holding token j = 0 .. 16 I + 15 at ap_seg(I) + j: the earlier blocks'
+// tokens (factors k_j h_j t, exponents <= 0) and then block I's own (k_j / f_j).  A row of block
+// I reads its entries from one contiguous, warp-uniform window.
+__host__ __device__ constexpr int ap_seg(int I) { return 8 * I * (I + 1); }
+constexpr int kApN = ap_seg(4);  // 160 columns
+__host__ __device__ constexpr int ap_row(int r, int is_q) { return 32 * (r >> 4) + 16 * is_q + (r & 15); }
 
 // Per (chunk, head) operand block in the workspace (bytes).
 constexpr size_t kOffZ = 0;                          // Z   128 x K  bf16, K-major (KD = K)
@@ -76,14 +92,22 @@ constexpr uint32_t kChY = 53248;                           // >= 67 * 784
 // Phase 2: tensor-core operands (overlaying phase 1; the V half of KV is written by the
 // norm pass, once the staged rows are dead).
 constexpr uint32_t kChKV = 0;        // [K.Gamma | V]        MN-major B, N = K + V, KD = 64
-constexpr uint32_t kChX = 32768;     // [K.e^(G-R); Q.e^(G-R)]  K-major 128 x K
-constexpr uint32_t kChKi = 65536;    // K.e^(R-G)              K-major 64 x K
-constexpr uint32_t kChBT = 81920;    // B^T                    K-major K x 64
-constexpr uint32_t kChPP = 98304;    // P                      K-major 64 x 64
+constexpr uint32_t kChX = 32768;     // [K.f; Q.f]             K-major 128 x K
+constexpr uint32_t kChKc = 65536;    // columns of A / P       K-major 160 x K
+// Written once the A / P product has completed (over its spent column operand); B^T leaves
+// the registers it was formed in then.
+constexpr uint32_t kChBT = 73728;    // B^T                    K-major K x 64
+constexpr uint32_t kChPP = 90112;    // P                      K-major 64 x 64
 // Phase 1 also: the conv taps of the head's channels (float4 each), transposed so that the
 // lanes of a warp read consecutive vectors: the taps of channel 8 g + e at [e][g].
 constexpr uint32_t kChW = 106496;
 constexpr uint32_t kChSmem = kChW + (2 * kK + kVmax) * 16;  // 112640: two CTAs per SM
+// Wide diagonal blocks (between the norm pass and the operands): the block's exponents
+// G_r - Gb in fp32 (over the dead staged rows), and the exact diagonal-block values of A and
+// P (over the dead taps; per block 120 strictly lower A entries, then 136 P entries).
+constexpr int kGS = kK + 4;          // fp32 row stride of the staged exponents
+constexpr uint32_t kChG = 32768;
+constexpr uint32_t kChFb = kChW;
 // Phase 3 (over X and Ki once the A/P product has completed).
 constexpr int kAS = 68;                                  // fp32 row stride of A
 constexpr uint32_t kChA = 32768;     // A, then (I + A)^-1 in place, fp32 [64][68]
@@ -99,6 +123,9 @@ static_assert(kChY + kC * kRowElems * 2 <= kChSmem, "conv outputs");
 static_assert(kChKV + kC * (kK + kVmax) * 2 <= kChY, "V half of KV beside the conv outputs");
 static_assert(kChSt + 16 * kSS * 4 <= kChTH && kChTL + kC * kC * 2 <= kChBT, "phase 3");
 static_assert(kChWU + kC * (kK + kVmax) * 2 <= kChBT, "phase 4");
+static_assert(kChKc + kApN * kK * 2 == kChW && kChPP + kC * kC * 2 <= kChW, "A / P columns");
+static_assert(kChBT + kK * kC * 2 <= kChPP && kChX + 2 * kC * kK * 2 == kChKc, "operands");
+static_assert(kChG + kSub * kGS * 4 <= kChY && kChFb + 4 * 256 * 4 <= kChSmem, "wide blocks");
 
 // ---- state pass shared memory (bytes): four operand buffers and two S0 buffers
 constexpr uint32_t kSbZ = 0;                          // Z        128 x K K-major
@@ -190,6 +217,98 @@ __device__ __forceinline__ void inverse_stage(float *sA, float *sSt, unsigned ch
   __syncthreads();
 }
 
+// One lane's row rr of A (rows < 64 of the product) or of P, columns j0 .. j0+N-1, from N
+// accumulator values d.  A: beta_r x value below the diagonal, fp32 rows of sA; P: the value
+// on and below the diagonal of a live row, bf16 K-major.  In a block beyond kDiagSpread
+// (rwide) the row's own-block entries come from the exact values in fb.
+struct ApRow {
+  int rr, rb;
+  bool isP, rwide, live;
+  float br;
+};
+template <int N>
+__device__ __forceinline__ void ap_emit(const float *d, int j0, const ApRow &w, const float *fb,
+                                        float *sA, unsigned char *sPP) {
+#pragma unroll
+  for (int g8 = 0; g8 < N / 8; ++g8) {
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = j0 + 8 * g8 + e;
+      float x = d[8 * g8 + e];
+      if (w.rwide && (j >> 4) == w.rb && j <= w.rr) {
+        const int r = w.rr & 15, c = j & 15;
+        x = w.isP ? fb[w.rb * 256 + 120 + r * (r + 1) / 2 + c]
+                  : (c < r ? fb[w.rb * 256 + r * (r - 1) / 2 + c] : 0.f);
+      }
+      v[e] = w.isP ? (j <= w.rr && w.live ? x : 0.f) : (j < w.rr ? w.br * x : 0.f);
+    }
+    const int j = j0 + 8 * g8;
+    if (w.isP) {
+      st16(sPP + tc::kmajor_offset(w.rr, j, kC), pack16(v));
+    } else {
+      st4(sA + w.rr * kAS + j, make_float4(v[0], v[1], v[2], v[3]));
+      st4(sA + w.rr * kAS + j + 4, make_float4(v[4], v[5], v[6], v[7]));
+    }
+  }
+}
+
+// Exact diagonal block bI of A (raw, before beta) and P for a block beyond kDiagSpread, from
+// the block's rows of q_hat | k_hat (Y, bf16) and its exponents x = G - Gb (sG, fp32):
+// A[r][j] (j < r) = sum_c k_r k_j e^(x_r - x_j), P[r][j] (j <= r) = sum_c q_r k_j e^(x_r - x_j)
+// (every exponent <= 0 for a decaying gate).  Thread pair (2p, 2p+1) sums pair p of the strictly
+// lower triangle over the two channel halves; threads 240.. the P diagonal.  Out of line: the
+// rare path stays out of the kernel's instruction stream.
+__device__ __noinline__ void diag_block_exact(const bf16 *Y, const float *sG, float *fbb, int bI,
+                                              int tid) {
+  const int p = tid >> 1, hc = tid & 1;
+  int r = 1;
+  while ((r + 1) * r / 2 <= p) ++r;
+  const int j = p - r * (r - 1) / 2;
+  float a = 0.f, pp = 0.f;
+  if (p < 120) {
+    const bf16 *yr = Y + (kSub * bI + r) * kRowElems, *yj = Y + (kSub * bI + j) * kRowElems;
+    const float *gr = sG + r * kGS, *gj = sG + j * kGS;
+#pragma unroll 2
+    for (int c = 64 * hc; c < 64 * hc + 64; c += 8) {
+      float qr[8], kr[8], kj[8];
+      unpack16(ld16(yr + c), qr);
+      unpack16(ld16(yr + kK + c), kr);
+      unpack16(ld16(yj + kK + c), kj);
+      const float4 ra = ld4(gr + c), rb = ld4(gr + c + 4), ja = ld4(gj + c), jb = ld4(gj + c + 4);
+      const float dx[8] = {ra.x - ja.x, ra.y - ja.y, ra.z - ja.z, ra.w - ja.w,
+                           rb.x - jb.x, rb.y - jb.y, rb.z - jb.z, rb.w - jb.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float w = exp2f(dx[e] * kLog2e);
+        a = fmaf(kr[e] * kj[e], w, a);
+        pp = fmaf(qr[e] * kj[e], w, pp);
+      }
+    }
+  } else {
+    const bf16 *yr = Y + (kSub * bI + (tid - 240)) * kRowElems;
+#pragma unroll 2
+    for (int c = 0; c < kK; c += 8) {
+      float qr[8], kr[8];
+      unpack16(ld16(yr + c), qr);
+      unpack16(ld16(yr + kK + c), kr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pp = fmaf(qr[e], kr[e], pp);
+    }
+  }
+  const float a2 = __shfl_xor_sync(0xffffffffu, a, 1);
+  const float p2 = __shfl_xor_sync(0xffffffffu, pp, 1);
+  if (p < 120) {
+    if (hc == 0) {
+      fbb[r * (r - 1) / 2 + j] = a + a2;
+      fbb[120 + r * (r + 1) / 2 + j] = pp + p2;
+    }
+  } else {
+    const int rd = tid - 240;
+    fbb[120 + rd * (rd + 1) / 2 + rd] = pp;
+  }
+}
+
 }  // namespace
 
 size_t prefill_tc_chunk_capacity(int N, int T) { return (size_t)T / kC + (size_t)N; }
@@ -247,7 +366,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   constexpr int CH = 2 * kK + V;  // channels of one head
   extern __shared__ __align__(1024) unsigned char smem[];
   bf16 *Y = reinterpret_cast<bf16 *>(smem + kChY);
-  unsigned char *sKV = smem + kChKV, *sX = smem + kChX, *sKi = smem + kChKi;
+  unsigned char *sKV = smem + kChKV, *sX = smem + kChX;
   unsigned char *sBT = smem + kChBT, *sPP = smem + kChPP, *sWU = smem + kChWU;
   unsigned char *sTH = smem + kChTH, *sTL = smem + kChTL, *sQG = smem + kChQG;
   float *sA = reinterpret_cast<float *>(smem + kChA);
@@ -255,6 +374,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_bar;
   __shared__ float s_beta[kC];
+  __shared__ int s_wide, s_grow;  // blocks beyond kDiagSpread (bit per block); a growing gate
 
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -271,7 +391,11 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   char *blk = blocks + ((size_t)cid * H + h) * kBlockBytes;
   if (tid < kC) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
   // tensor memory and the MMA barrier, ready long before the first product
-  if (tid == 0) mbar_init(&s_bar, 1);
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    s_wide = 0;
+    s_grow = 0;
+  }
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 256); tc::tmem_relinquish(); }
 
   // the gates of this thread's rows and channels: their lines are prefetched into L2 at once,
@@ -406,6 +530,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   } else {
     // fp32 inputs: a warp per token straight from global memory (lane l owns channels
     // 4l..4l+3 of q, k, v).
+    __syncthreads();  // the flags of step 2 are initialised
     load_gates();
     const int cq = h * kK + 4 * lane, ck = H * kK + h * kK + 4 * lane;
     const int cv = 2 * H * kK + h * V + 4 * lane;
@@ -498,44 +623,84 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       for (int i = 0; i < 4; ++i) G[i][e] += ex;
     }
   }
-  float R[8], Gl[8];
+  // Sub-chunk references.  The chunk's rows form four 16-row blocks; this thread's rows lie
+  // in block I = rsub / 4.  With Gb(J) the cumulative gate at the first row of block J and
+  // G_last that of the chunk's last token, the factors
+  //   f_r = e^(G_r - Gb(I)),   h_r = e^(Gb(I+1) - G_r)   (block 3: e^(G_last - G_r))
+  // and, per channel, e^Gb(I), s = e^(G_last - Gb(I+1)), t_m = e^(Gb(I+m) - Gb(I+1)) all have
+  // exponents <= 0 for a decaying gate.  From them:
+  //   A / P rows          k_r f_r, q_r f_r
+  //   own-block columns   k_j / f_j           (the block's spread; see kDiagSpread)
+  //   earlier-block cols  k_j h_j t           (row block I' > J: t = e^(Gb(I') - Gb(J+1)))
+  //   K.Gamma, Q.Gamma    k_r f_r e^Gb(I), q_r f_r e^Gb(I)
+  //   B                   k_r h_r s
+  // A pair of different blocks multiplies two factors <= 1, so nothing overflows and what
+  // underflows is below fp32 range in the exact value too.  G is replaced by G - Gb(I).
+  const int I = rsub >> 2;
+  float d1[8], eGb[8], s1[8], t2[8], t3[8];
   {
-    float mn[8], mx[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      mn[e] = 3.0e38f;
-      mx[e] = -3.0e38f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (4 * rsub + i < Lc) { mn[e] = fminf(mn[e], G[i][e]); mx[e] = fmaxf(mx[e], G[i][e]); }
-    }
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], o, 16));
-        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], o, 16));
-      }
-    }
     const int last = Lc - 1, src = last >> 2, il = last & 3;
-    bool wide = false;
+    const int sb1 = 4 * min(I + 1, 3), sb2 = 4 * min(I + 2, 3);
+    bool wide = false, grow = false;
+    float gc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float gv = il == 0 ? G[0][e] : il == 1 ? G[1][e] : il == 2 ? G[2][e] : G[3][e];
-      Gl[e] = __shfl_sync(0xffffffffu, gv, src, 16);
-      R[e] = 0.5f * (mn[e] + mx[e]);
-      wide |= mx[e] - mn[e] > kGateSpreadLimit;
+      const float gl = __shfl_sync(0xffffffffu, gv, src, 16);
+      const float gb0 = __shfl_sync(0xffffffffu, G[0][e], 4 * I, 16);
+      const float gn = __shfl_sync(0xffffffffu, G[0][e], sb1, 16);
+      const float gb2 = __shfl_sync(0xffffffffu, G[0][e], sb2, 16);
+      const float gb3 = __shfl_sync(0xffffffffu, G[0][e], 12, 16);
+      const float gb1 = I == 3 ? gl : gn;
+      d1[e] = gb1 - gb0;
+      eGb[e] = exp2f(gb0 * kLog2e);
+      s1[e] = exp2f((gl - gb1) * kLog2e);
+      t2[e] = exp2f((gb2 - gb1) * kLog2e);
+      t3[e] = exp2f((gb3 - gb1) * kLog2e);
+      gc[e] = expf(gl);
+      grow |= gb0 > kGrowLimit || gl - gb1 > kGrowLimit || (I < 2 && gb2 - gb1 > kGrowLimit) ||
+              (I == 0 && gb3 - gb1 > kGrowLimit);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float x = G[i][e] - gb0;
+        G[i][e] = x;
+        wide |= -x > kDiagSpread;
+        grow |= x > kGrowLimit || d1[e] - x > kGrowLimit;
+      }
     }
+    if (wide) atomicOr(&s_wide, 1 << I);
+    if (grow) s_grow = 1;
     if (rsub == 0) {
-      if (wide) flag_error(pv.err, RSC_DEVERR_GATE);
-      float *gc = reinterpret_cast<float *>(blk + kOffGC) + 8 * kg;
-      st4(gc, make_float4(expf(Gl[0]), expf(Gl[1]), expf(Gl[2]), expf(Gl[3])));
-      st4(gc + 4, make_float4(expf(Gl[4]), expf(Gl[5]), expf(Gl[6]), expf(Gl[7])));
+      float *gp = reinterpret_cast<float *>(blk + kOffGC) + 8 * kg;
+      st4(gp, make_float4(gc[0], gc[1], gc[2], gc[3]));
+      st4(gp + 4, make_float4(gc[4], gc[5], gc[6], gc[7]));
     }
   }
 
   // ---- 3. operands
-  __syncthreads();  // the norm pass is complete
+  __syncthreads();  // the norm pass is complete; s_wide and s_grow are final
+  const int wide_blocks = s_wide;
+  if (tid == 0 && s_grow) flag_error(pv.err, RSC_DEVERR_GATE);
+  float *fb = reinterpret_cast<float *>(smem + kChFb);
+  if (wide_blocks) {
+    // Diagonal blocks beyond kDiagSpread, exactly (diag_block_exact), one block at a time:
+    // its exponents x = G - Gb staged in fp32, then the block's A and P entries into fb.
+    float *sG = reinterpret_cast<float *>(smem + kChG);
+    for (int bI = 0; bI < 4; ++bI) {
+      if (!((wide_blocks >> bI) & 1)) continue;
+      if (I == bI) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float *gp = sG + (4 * (rsub & 3) + i) * kGS + 8 * kg;
+          st4(gp, make_float4(G[i][0], G[i][1], G[i][2], G[i][3]));
+          st4(gp + 4, make_float4(G[i][4], G[i][5], G[i][6], G[i][7]));
+        }
+      }
+      __syncthreads();
+      diag_block_exact(Y, sG, fb + bI * 256, bI, tid);
+      __syncthreads();  // the staged exponents are reused by the next wide block
+    }
+  }
   uint4 qv[4], kv[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -544,15 +709,8 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     kv[i] = ld16(yr + kK + 8 * kg);
   }
   __syncthreads();  // Y is dead; the operands overlay it
-  // per channel: e^R and e^(G_last - R); with those, two exponentials per element instead of
-  // four (e^G = e^(G-R) e^R, e^(G_last - G) = e^(G_last - R) e^(R-G)).  Every factor is within
-  // e^(+-range/2) of one, which the range check keeps inside fp32.
-  float eR[8], eLR[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    eR[e] = exp2f(R[e] * kLog2e);
-    eLR[e] = exp2f((Gl[e] - R[e]) * kLog2e);
-  }
+  unsigned char *sKc = smem + kChKc;
+  uint32_t btp[2][8];  // B^T of the thread's rows, bf16 pairs (rows 4 rsub + 2 ip, + 1)
 #pragma unroll
   for (int ip = 0; ip < 4; ip += 2) {  // rows in pairs: B^T takes two rows per 4-byte store
     float bt[8][2];
@@ -560,33 +718,60 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     for (int i = ip; i < ip + 2; ++i) {
       const int r = 4 * rsub + i;
       const bool live = r < Lc;
-      float q8[8], k8[8], xk[8], xq[8], ki[8], kgm[8], qgm[8];
+      float q8[8], k8[8], xk[8], xq[8], kd[8], kh[8], kgm[8], qgm[8];
       unpack16(qv[i], q8);
       unpack16(kv[i], k8);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float d = (G[i][e] - R[e]) * kLog2e;
-        const float ep = exp2f(d), en = exp2f(-d), gam = ep * eR[e];
-        xk[e] = k8[e] * ep;
-        xq[e] = q8[e] * ep;
-        ki[e] = k8[e] * en;
+        const float x = G[i][e] * kLog2e;
+        const float f = exp2f(x), hh = exp2f(d1[e] * kLog2e - x);
+        const float fi = fminf(exp2f(-x), kMaxInv), gam = f * eGb[e];
+        xk[e] = k8[e] * f;
+        xq[e] = q8[e] * f;
+        kd[e] = k8[e] * fi;
+        kh[e] = k8[e] * hh;
         kgm[e] = k8[e] * gam;
         qgm[e] = q8[e] * gam;
-        bt[e][i - ip] = live ? k8[e] * (eLR[e] * en) : 0.f;
+        bt[e][i - ip] = live ? kh[e] * s1[e] : 0.f;
       }
-      st16(sX + tc::kmajor_offset(r, 8 * kg, kK), pack16(xk));
-      st16(sX + tc::kmajor_offset(kC + r, 8 * kg, kK), pack16(xq));
-      st16(sKi + tc::kmajor_offset(r, 8 * kg, kK), pack16(ki));
+      st16(sX + tc::kmajor_offset(ap_row(r, 0), 8 * kg, kK), pack16(xk));
+      st16(sX + tc::kmajor_offset(ap_row(r, 1), 8 * kg, kK), pack16(xq));
+      st16(sKc + tc::kmajor_offset(ap_seg(I) + r, 8 * kg, kK), pack16(kd));
+      if (I < 3) st16(sKc + tc::kmajor_offset(ap_seg(I + 1) + r, 8 * kg, kK), pack16(kh));
+      if (I < 2) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = kh[e] * t2[e];
+        st16(sKc + tc::kmajor_offset(ap_seg(I + 2) + r, 8 * kg, kK), pack16(y));
+      }
+      if (I < 1) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = kh[e] * t3[e];
+        st16(sKc + tc::kmajor_offset(ap_seg(3) + r, 8 * kg, kK), pack16(y));
+      }
       st16(sKV + tc::mnmajor_offset(8 * kg, r, NKV), pack16(kgm));
       st16(blk + kOffE + tc::kmajor_offset(r, 8 * kg, kK), pack16(qgm));  // Q.Gamma, E later
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      *reinterpret_cast<uint32_t *>(sBT + tc::kmajor_offset(8 * kg + e, 4 * rsub + ip, kC)) =
-          pack_bf16x2(bt[e][0], bt[e][1]);
+    for (int e = 0; e < 8; ++e) btp[ip >> 1][e] = pack_bf16x2(bt[e][0], bt[e][1]);
+  }
+  // B^T rows are 16 bytes of 8 consecutive tokens for one channel.  Lanes 2m and 2m+1 hold
+  // tokens 8m .. 8m+3 and 8m+4 .. 8m+7 of the same 8 channels: they swap half their channels,
+  // so that each ends with 4 channels x 8 tokens, i.e. four whole 16-byte rows.
+  const bool odd = rsub & 1;
+  uint4 btr[4];  // rows of channels 8 kg + 4 odd + c, tokens 8 (rsub / 2) .. +7
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t got[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      got[q] = __shfl_xor_sync(0xffffffffu, odd ? btp[q][c] : btp[q][4 + c], 1);
+    btr[c] = odd ? make_uint4(got[0], got[1], btp[0][4 + c], btp[1][4 + c])
+                 : make_uint4(btp[0][c], btp[1][c], got[0], got[1]);
   }
 
-  // ---- 4. A and P: [K.e^(G-R); Q.e^(G-R)] (128 x K) times (K.e^(R-G))^T -> 128 x 64
+  // ---- 4. A and P: [K.f; Q.f] (128 x K) times the 160 columns -> 128 x 160
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -595,36 +780,47 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   if (tid == 0) {
 #pragma unroll
     for (int ks = 0; ks < kK / 16; ++ks)
-      tc::mma_bf16(taddr, tc::kmajor_desc(sX, kK, ks), tc::kmajor_desc(sKi, kK, ks),
-                   tc::idesc_bf16<128, kC>(), ks > 0);
+      tc::mma_bf16(taddr, tc::kmajor_desc(sX, kK, ks), tc::kmajor_desc(sKc, kK, ks),
+                   tc::idesc_bf16<128, kApN>(), ks > 0);
     tc::mma_commit(&s_bar);
   }
   const int q4 = warp & 3, half = warp >> 2;
   bool ok = __syncthreads_and(mbar_wait(&s_bar, 0));
   tc::fence_after_sync();
   if (ok) {
-    // warp w reads lanes 32 (w % 4) .. +31 (rows) and columns 32 (w / 4) .. +31
-    const int row = 32 * q4 + lane, cb = 32 * half;
-    float d[32];
-    tc::tmem_ld32(tc::tmem_addr(taddr, 32 * q4, cb), d);
-    if (row < kC) {  // A (x beta, strictly lower) over the spent X operand
-      const float br = s_beta[row];
+    // B^T over the spent column operand: 16-byte rows, the channel order rotated by lane pair
+    // so that the 8 lanes of a quarter warp write 8 different 16-byte bank groups
+    {
+      const int m = rsub >> 1;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        float a[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = cb + 4 * m + e < row ? br * d[4 * m + e] : 0.f;
-        st4(sA + row * kAS + cb + 4 * m, make_float4(a[0], a[1], a[2], a[3]));
+      for (int c2 = 0; c2 < 4; ++c2) {
+        const int c = (c2 + m) & 3;
+        const uint4 v = c == 0 ? btr[0] : c == 1 ? btr[1] : c == 2 ? btr[2] : btr[3];
+        st16(sBT + tc::kmajor_offset(8 * kg + 4 * odd + c, 8 * m, kC), v);
       }
-    } else {         // P (lower incl. diagonal)
-      const int r = row - kC;
+    }
+    // Lane quadrant q4 is row block q4: lanes 0-15 its key rows (A), lanes 16-31 its query rows
+    // (P).  Row rr's entry j (j < 16 q4 + 16) is column ap_seg(q4) + j; the quadrant's two
+    // warps take alternate 16-column chunks.  P is zero beyond the block (an operand); A is
+    // read only below its diagonal blocks.
+    ApRow w;
+    w.rb = q4;
+    w.rr = 16 * q4 + (lane & 15);
+    w.isP = lane >= 16;
+    w.rwide = (wide_blocks >> q4) & 1;
+    w.live = w.rr < Lc;
+    w.br = s_beta[w.rr];
+#pragma unroll 1
+    for (int cidx = half; cidx < 4; cidx += 2) {
+      const bool have = cidx <= q4;  // warp-uniform
+      float d[16];
+      if (have) {
+        tc::tmem_ld16(tc::tmem_addr(taddr, 32 * q4, ap_seg(q4) + 16 * cidx), d);
+      } else {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = (cb + 8 * m + e <= r && r < Lc) ? d[8 * m + e] : 0.f;
-        st16(sPP + tc::kmajor_offset(r, cb + 8 * m, kC), pack16(x));
+        for (int e = 0; e < 16; ++e) d[e] = 0.f;
       }
+      if (have || w.isP) ap_emit<16>(d, 16 * cidx, w, fb, sA, sPP);
     }
   }
   tc::fence_before_sync();
@@ -1098,17 +1294,18 @@ static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *
   auto chunk_kernel = prefill_tc_chunk_kernel<IO, V, GATE>;
   auto state_kernel = prefill_tc_state_kernel<IO, V>;
   auto out_kernel = prefill_tc_out_kernel<IO, V>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kChSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStateSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kOutSmem) != cudaSuccess)
-      return RSC_ECUDA;
-    attr = true;
-  }
+  static PerDeviceFlag attr;  // per instantiation and device
+  const int rc = once_per_device(attr, [&] {
+    return cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kChSmem) == cudaSuccess &&
+                   cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kStateSmem) == cudaSuccess &&
+                   cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kOutSmem) == cudaSuccess
+               ? RSC_OK
+               : RSC_ECUDA;
+  });
+  if (rc != RSC_OK) return rc;
   const unsigned cap = (unsigned)prefill_tc_chunk_capacity(N, T);
   if (cap > 0 && T > 0) {
     chunk_kernel<<<dim3(cap, a.pv.H), 256, kChSmem, s>>>(a.pv, a.layer, slots, cu, chunk_base, N,

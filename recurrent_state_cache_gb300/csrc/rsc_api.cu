@@ -4,6 +4,7 @@
 // by the kernels, which skip the bad row and set a bit of the pool's error word.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <new>
 
 #include "rsc_internal.h"
@@ -11,6 +12,7 @@
 struct rsc_pool {
   rsc_pool_desc d;
   rsc::PoolView pv;
+  std::atomic<int> device{-1};  // device holding the pool's memory, looked up on first launch
 };
 
 namespace {
@@ -44,6 +46,25 @@ rsc::LayerArgs layer_args(const rsc_pool *p, int layer) {
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// The pool's memory must be device memory of the current device (the kernels run there and
+// dereference it).  Looked up once per pool, after every host check of the call has passed.
+int on_pool_device(rsc_pool *p) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return RSC_ECUDA;
+  int d = p->device.load(std::memory_order_relaxed);
+  if (d < 0) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p->d.ssm_base) != cudaSuccess) {
+      cudaGetLastError();  // an unregistered host pointer: clear the sticky status
+      return RSC_EDEVICE;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return RSC_EDEVICE;
+    d = at.device;
+    p->device.store(d, std::memory_order_relaxed);
+  }
+  return d == cur ? RSC_OK : RSC_EDEVICE;
+}
+
 // Shared checks and launch of every decode entry point; need_track / need_gate: the entry
 // point's own option pointers are required.
 int decode_impl(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch, const void *qkv,
@@ -61,6 +82,7 @@ int decode_impl(rsc_pool *pool, int layer, const int32_t *slot_ids, int batch, c
     return RSC_EALIGN;
   if (ex.A_log && (!aligned(ex.dt_bias, 16) || !aligned(ex.A_log, 4))) return RSC_EALIGN;
   if (ex.track_slots && !aligned(ex.track_slots, 4)) return RSC_EALIGN;
+  if (const int rc = on_pool_device(pool)) return rc;
   return rsc::launch_decode(layer_args(pool, layer), slot_ids, batch, qkv, conv_w, g, beta, out,
                             ex, as_stream(stream));
 }
@@ -191,6 +213,7 @@ int kda_prefill_chunk(rsc_pool *pool, int layer, const int32_t *slot_ids,
   if (total_tokens > 0 && (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(g, 16) ||
                            !aligned(beta, 4)))
     return RSC_EALIGN;
+  if (const int rc = on_pool_device(pool)) return rc;
   return rsc::launch_prefill(layer_args(pool, layer), slot_ids, cu_seqlens, num_seqs,
                              total_tokens, has_initial_state, qkv, conv_w, g, beta, out,
                              workspace, workspace_bytes, as_stream(stream));
@@ -206,6 +229,7 @@ int ssm_slot_copy(rsc_pool *pool, int layer, const int32_t *src, const int32_t *
   const int l0 = layer < 0 ? 0 : layer;
   const int nl = layer < 0 ? pool->d.num_layers : 1;
   if (nl > kMaxGrid) return RSC_ERANGE;
+  if (const int rc = on_pool_device(pool)) return rc;
   return rsc::launch_slot_copy(pool->pv, pool->d.state_dtype, pool->d.conv_dtype, l0, nl, src,
                                dst, mask, n, as_stream(stream));
 }
@@ -228,6 +252,7 @@ int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *s
   if (mode == RSC_SPEC_COMMIT) {
     if (!accept) return RSC_EINVAL;
     if (!aligned(accept, 4)) return RSC_EALIGN;
+    if (const int rc = on_pool_device(pool)) return rc;
     return rsc::launch_spec_commit(a, slot_ids, batch, T, L, spec_ssm, spec_conv, accept,
                                    as_stream(stream));
   }
@@ -235,6 +260,7 @@ int kda_spec_verify_commit(rsc_pool *pool, int layer, int mode, const int32_t *s
   if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
       !aligned(beta, 4))
     return RSC_EALIGN;
+  if (const int rc = on_pool_device(pool)) return rc;
   return rsc::launch_spec_verify(a, slot_ids, batch, T, L, spec_ssm, spec_conv, qkv, conv_w, g,
                                  beta, out, as_stream(stream));
 }
@@ -263,6 +289,7 @@ int kda_replay_verify_commit(rsc_pool *pool, const rsc_replay_rings *rings, int 
   if (mode == RSC_SPEC_COMMIT) {
     if (!accept) return RSC_EINVAL;
     if (!aligned(accept, 4)) return RSC_EALIGN;
+    if (const int rc = on_pool_device(pool)) return rc;
     return rsc::launch_replay_commit(a, rv, slot_ids, ring_pos, batch, T, spec_conv, accept,
                                      as_stream(stream));
   }
@@ -270,12 +297,14 @@ int kda_replay_verify_commit(rsc_pool *pool, const rsc_replay_rings *rings, int 
   if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(conv_w, 16) || !aligned(g, 16) ||
       !aligned(beta, 4))
     return RSC_EALIGN;
+  if (const int rc = on_pool_device(pool)) return rc;
   return rsc::launch_replay_verify(a, rv, slot_ids, ring_pos, batch, T, spec_conv, qkv, conv_w,
                                    g, beta, out, as_stream(stream));
 }
 
 int rsc_get_device_error(rsc_pool *pool, int32_t *code, void *stream) {
   if (!pool || !code) return RSC_EINVAL;
+  if (const int rc = on_pool_device(pool)) return rc;
   cudaStream_t s = as_stream(stream);
   int32_t host = 0;
   if (cudaMemcpyAsync(&host, pool->pv.err, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess)
@@ -296,6 +325,7 @@ const char *rsc_status_string(int status) {
     case RSC_EALIGN: return "pointer not aligned as required";
     case RSC_ECUDA: return "CUDA runtime error";
     case RSC_ENOSPACE: return "workspace too small";
+    case RSC_EDEVICE: return "the pool's memory is not device memory of the current device";
     default: return "unknown status";
   }
 }

@@ -146,7 +146,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Every wait is bounded: a wait that runs out sets RSC_DEVERR_TIMEOUT in the pool's
 // error word and the caller skips its work instead of spinning forever.
 
-constexpr uint32_t kMbarSpinLimit = 1u << 22;
+#ifndef RSC_MBAR_SPIN_LIMIT
+#define RSC_MBAR_SPIN_LIMIT (1u << 22)
+#endif
+constexpr uint32_t kMbarSpinLimit = RSC_MBAR_SPIN_LIMIT;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);

@@ -6,6 +6,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "rsc_common.cuh"
 
 namespace rsc {
@@ -80,6 +83,28 @@ int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_s
                    int N, int T, const uint8_t *has_init, const void *qkv,
                    const float *conv_w, const float *g, const float *beta, void *out,
                    void *ws, size_t ws_bytes, cudaStream_t s);
+
+// One-time set-up per device (kernel attributes such as the dynamic shared-memory limit are
+// per device): once_per_device(flag, setup) runs setup() with the current device until it
+// has succeeded once on that device.  Thread-safe; the common path is one atomic load.
+constexpr int kMaxDevices = 64;
+struct PerDeviceFlag {
+  std::atomic<uint64_t> done{0};
+  std::mutex mu;
+};
+template <typename F>
+int once_per_device(PerDeviceFlag &f, F setup) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RSC_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return RSC_ERANGE;
+  const uint64_t bit = 1ull << dev;
+  if (f.done.load(std::memory_order_acquire) & bit) return RSC_OK;
+  std::lock_guard<std::mutex> lock(f.mu);
+  if (f.done.load(std::memory_order_relaxed) & bit) return RSC_OK;
+  const int rc = setup();
+  if (rc == RSC_OK) f.done.fetch_or(bit, std::memory_order_release);
+  return rc;
+}
 
 inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? RSC_OK : RSC_ECUDA;

@@ -8,7 +8,8 @@ Distributions (workload statements of the hybrid-linear-attention cache pages; t
 conv taps are not given there and are drawn N(0, 0.5)):
   q, k, v projections   N(0, 1)
   beta                  sigmoid(N(0, 1))
-  log-decay gate g      -softplus(N(0, 1))     (alpha = exp(g) in (0, 1))
+  log-decay gate g      -softplus(N(0, 1))     (alpha = exp(g) in (0, 1)); tests of strong
+                        decay scale it, -s softplus(N(0, 1)) with s up to e^3
                         per key channel for KDA, one per head for GDN
   initial S, windows    N(0, 0.1)              (standard deviation 0.1)
   slot ids              distinct, uniform over the usable slots 1..P (row 0 is padding)
@@ -59,10 +60,11 @@ def distinct_slots(r: np.random.Generator, B: int, P: int) -> np.ndarray:
     return (r.permutation(P)[:B] + 1).astype(np.int32)
 
 
-def gates(r: np.random.Generator, lead: tuple, H: int, K: int, gate: int):
-    """(g, beta) for a leading shape (e.g. (B,), (T,), (B, T))."""
+def gates(r: np.random.Generator, lead: tuple, H: int, K: int, gate: int, scale: float = 1.0):
+    """(g, beta) for a leading shape (e.g. (B,), (T,), (B, T)).  scale multiplies the
+    log-decay draw: g = -scale * softplus(N(0, 1)) (strong decay for scale >> 1)."""
     gshape = lead + ((H, K) if gate == KDA else (H,))
-    g = _neg_softplus(r.standard_normal(gshape)).astype(np.float32)
+    g = (scale * _neg_softplus(r.standard_normal(gshape))).astype(np.float32)
     beta = _sigmoid(r.standard_normal(lead + (H,))).astype(np.float32)
     return g, beta
 

@@ -63,3 +63,75 @@ def test_full_size_decode_step_sampled(cuda_dev):
     for (l, s), (ssm0, conv0) in untouched.items():
         assert np.array_equal(to_np(wl.pool.ssm[l, s]), ssm0)
         assert np.array_equal(to_np(wl.pool.conv[l, s]), conv0)
+
+
+def test_full_size_chunked_prefill_13600_with_snapshots(cuda_dev):
+    """The chunked-prefill workload at full size, in the benchmark's launch configuration:
+    one KDA layer, H=12, K=V=128, bf16; a 13600-token prompt as calls of 6144, 6144 and 1312
+    tokens through one slot (the first from a fresh state), each followed by an ssm_slot_copy
+    of the slot into a fresh snapshot slot; the sequence captured in a CUDA graph and
+    replayed.  Every output token, the three snapshots and the final state against the
+    oracle's token-by-token run; windows bit-exact; the rest of the pool untouched."""
+    from recurrent_state_cache_gb300 import inputs
+    from tests.devio import to_dev
+    from tests.tolerances import TOL
+
+    torch.cuda.set_device(cuda_dev)
+    stream = torch.cuda.Stream(device=cuda_dev)
+    torch.cuda.set_stream(stream)
+    Hp, Pp, chunks = 12, 6, (6144, 6144, 1312)
+    slot, snaps = 1, (2, 3, 4)
+    r = inputs.rng(5)
+    ssm, conv = inputs.pool_arrays(r, 1, Pp, Hp, K, V, 1, 1)
+    ref = oracle.Pool(1, Pp, Hp, K, V, oracle.BF16, oracle.BF16, oracle.KDA, ssm, conv)
+    pool = rsc.SlotPool(1, Pp, Hp, K, V, rsc.BF16, rsc.BF16, rsc.KDA, cuda_dev,
+                        ssm=to_dev(ssm, cuda_dev), conv=to_dev(conv, cuda_dev))
+    w = inputs.conv_weights(r, Hp, K, V)
+    T = sum(chunks)
+    x = inputs.projections(r, (T,), Hp, K, V, 1)
+    g, beta = inputs.gates(r, (T,), Hp, K, oracle.KDA)
+    offs = np.cumsum((0,) + chunks)
+
+    xd, wd, gd, bd = (to_dev(a, cuda_dev) for a in (x, w, g, beta))
+    out = torch.empty((T, Hp, V), dtype=torch.bfloat16, device=cuda_dev)
+    ws = torch.empty(rsc.kda_prefill_workspace_size(pool, 1, max(chunks)), dtype=torch.uint8,
+                     device=cuda_dev)
+    slot_d = torch.tensor([slot], dtype=torch.int32, device=cuda_dev)
+    snap_d = [torch.tensor([s], dtype=torch.int32, device=cuda_dev) for s in snaps]
+    fresh = torch.tensor([0], dtype=torch.uint8, device=cuda_dev)
+    cus = [torch.tensor([0, c], dtype=torch.int32, device=cuda_dev) for c in chunks]
+
+    def run():
+        for i in range(len(chunks)):
+            a, e = int(offs[i]), int(offs[i + 1])
+            rsc.kda_prefill_chunk(pool, 0, slot_d, cus[i], xd[a:e], wd, gd[a:e], bd[a:e],
+                                  has_initial_state=fresh if i == 0 else None, out=out[a:e],
+                                  workspace=ws)
+            rsc.ssm_slot_copy(pool, 0, slot_d, snap_d[i])
+
+    # the sequence restarts from a fresh state, so the warm run inside graph_of and the
+    # replay leave identical results
+    graph = bench.graph_of(run, stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert rsc.rsc_get_device_error(pool) == 0
+
+    o_ref = []
+    for i, c in enumerate(chunks):
+        a, e = int(offs[i]), int(offs[i + 1])
+        o_ref.append(oracle.prefill(ref, 0, [slot], np.int32([0, c]), x[a:e], w, g[a:e], beta[a:e],
+                                    has_init=np.uint8([0 if i == 0 else 1])))
+        oracle.slot_copy(ref, 0, [slot], [snaps[i]])
+    o_gpu = widen(to_np(out))
+    for i in range(len(chunks)):
+        a, e = int(offs[i]), int(offs[i + 1])
+        err = max_rel_err(o_gpu[a:e], widen(o_ref[i]), tc=True)
+        assert err <= TOL[1], f"call {i} output max rel err {err}"
+    s_gpu, c_gpu = to_np(pool.ssm), to_np(pool.conv)
+    assert np.array_equal(c_gpu, ref.conv), "windows differ"
+    for s in (slot,) + snaps:
+        err = max_rel_err(widen(s_gpu[0, s]), widen(ref.ssm[0, s]), tc=True)
+        assert err <= TOL[1], f"slot {s} state max rel err {err}"
+    for s in range(Pp + 1):
+        if s not in (slot,) + snaps:
+            assert np.array_equal(s_gpu[0, s], ssm[0, s])

@@ -190,6 +190,46 @@ def test_chunkwise_equals_recurrence(T, K, V):
     assert np.max(np.abs(S_c - S_r)) <= 1e-11 * scale_s
 
 
+@pytest.mark.parametrize("mode", ["const4", "scale20", "mixed"])
+def test_chunkwise_equals_recurrence_under_strong_decay(mode):
+    """The chunkwise form stays equal to the recurrence when the cumulative log gate of a
+    chunk spans hundreds (g = -4 per token: 252 over 64 tokens; g = -e^3 softplus(N(0,1));
+    channels and stretches of tokens at very different rates, with full resets)."""
+    T, K, V = 200, 16, 8
+    q, k, v, g, beta, S0 = _head_case(77, T=T, K=K, V=V)
+    r = np.random.default_rng(78)
+    if mode == "const4":
+        g = np.full((T, K), -4.0)
+    elif mode == "scale20":
+        g = np.exp(3.0) * g
+    else:
+        g = g.copy()
+        g[70:140, : K // 2] *= 30.0
+        g[r.integers(0, T, 5)] = -300.0
+    S_r, o_r, _ = oracle.recurrent_head(q, k, v, g, beta, S0)
+    S_c, o_c = oracle.chunkwise_head(q, k, v, g, beta, S0, C=64)
+    assert np.max(np.abs(o_c - o_r)) <= 1e-11 * np.max(np.abs(o_r))
+    assert np.max(np.abs(S_c - S_r)) <= 1e-11 * np.max(np.abs(S_r))
+
+
+def test_full_decay_token_resets_the_state():
+    """alpha = exp(g) -> 0 on token t wipes the state: S_t = beta_t v_t k_t^T and
+    o_t = beta_t (k_t . q_t) v_t, whatever came before (the single-token closed form)."""
+    T, K, V = 40, 8, 6
+    q, k, v, g, beta, S0 = _head_case(79, T=T, K=K, V=V)
+    t = 23
+    g = g.copy()
+    g[t] = -1e4
+    S_r, o_r, _ = oracle.recurrent_head(q[: t + 1], k[: t + 1], v[: t + 1], g[: t + 1],
+                                       beta[: t + 1], S0)
+    np.testing.assert_allclose(S_r, beta[t] * np.outer(v[t], k[t]), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(o_r[t], beta[t] * (k[t] @ q[t]) * v[t], rtol=1e-12, atol=1e-14)
+    S_c, o_c = oracle.chunkwise_head(q, k, v, g, beta, S0, C=16)
+    S_f, o_f, _ = oracle.recurrent_head(q, k, v, g, beta, S0)
+    assert np.max(np.abs(o_c - o_f)) <= 1e-11 * np.max(np.abs(o_f))
+    assert np.max(np.abs(S_c - S_f)) <= 1e-11 * np.max(np.abs(S_f))
+
+
 # ----------------------------------------------------------------------- layer step
 
 def _pool_case(seed, H=2, K=8, V=6, P=5, st=oracle.F32, io=oracle.F32, gate=oracle.KDA):

@@ -37,11 +37,11 @@ class Case:
     def proj(self, lead):
         return inputs.projections(self.r, lead, self.H, self.K, self.V, self.io)
 
-    def check_pool(self, tol=None):
+    def check_pool(self, tol=None, tc=False):
         tol = TOL[self.st] if tol is None else tol
         s_gpu, c_gpu = to_np(self.pool.ssm), to_np(self.pool.conv)
         assert np.array_equal(c_gpu, self.ref.conv), "conv windows differ"
-        err = max_rel_err(widen(s_gpu), widen(self.ref.ssm))
+        err = max_rel_err(widen(s_gpu), widen(self.ref.ssm), tc=tc)
         assert err <= tol, f"state max rel err {err}"
         assert rsc.rsc_get_device_error(self.pool) == 0
 
@@ -162,6 +162,46 @@ def test_decode_overlap_layer_chain(cuda_dev, st, io, gate, H, K, V, B):
     c.check_pool()
     assert torch.equal(c.pool.ssm, plain.ssm) and torch.equal(c.pool.conv, plain.conv)
     assert rsc.rsc_get_device_error(plain) == 0
+
+
+@pytest.mark.parametrize("st", [0, 1])
+def test_decode_overlap_graph_replayed_back_to_back(cuda_dev, st):
+    """Every call overlapped, nothing in between: a CUDA graph of the two layers' decodes (one
+    request, one head, so each launch is a single small CTA and nothing but the library's
+    own ordering keeps a launch from running ahead) replayed 50 times without
+    synchronisation.  Layer 0 of each step follows layer 1 of the step before, whose
+    kernel was itself still free to start while layer 0 of that step ran; the early reads
+    of layer 0 must still see layer 0's previous write.  Against 51 oracle steps (the
+    capture helper runs the graph's calls once before capturing)."""
+    import bench
+    L, P, H, K, V, B, replays = 2, 3, 1, 128, 128, 1, 50
+    c = Case(cuda_dev, 13, L=L, P=P, H=H, K=K, V=V, st=st, io=st, gate=rsc.KDA)
+    slots = np.int32([2])
+    slots_d = to_dev(slots, c.dev)
+    xs = [c.proj((B,)) for _ in range(L)]
+    gb = [c.gates((B,)) for _ in range(L)]
+    xd = [to_dev(x, c.dev) for x in xs]
+    gd = [(to_dev(g, c.dev), to_dev(b, c.dev)) for g, b in gb]
+    outs = [torch.empty((B, H, V), dtype=c.pool.io_dtype, device=c.dev) for _ in range(L)]
+    stream = torch.cuda.Stream(device=c.dev)
+
+    def step():
+        for l in range(L):
+            rsc.kda_decode_step(c.pool, l, slots_d, xd[l], c.w_dev, gd[l][0], gd[l][1],
+                                out=outs[l], stream=stream, overlap=True)
+
+    graph = bench.graph_of(step, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(replays + 1):
+        o_ref = [oracle.decode_step(c.ref, l, slots, xs[l], c.w, gb[l][0], gb[l][1])
+                 for l in range(L)]
+    for l in range(L):
+        err = max_rel_err(widen(to_np(outs[l])), widen(o_ref[l]))
+        assert err <= tol(c.st, c.io), f"layer {l}: output max rel err {err}"
+    c.check_pool()
 
 
 def test_decode_overlap_bad_slot_sets_flag_and_skips_row(cuda_dev):
@@ -508,8 +548,9 @@ def test_prefill_parity(cuda_dev, st, io, gate, K, V, lens, init):
     o = rsc.kda_prefill_chunk(c.pool, 1, to_dev(slots, c.dev), to_dev(cu, c.dev),
                               to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
                               has_initial_state=to_dev(hi, c.dev))
-    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(st, io)
-    c.check_pool()
+    tc = st == 1 and K == 128  # the chunkwise tensor-core path
+    assert max_rel_err(widen(to_np(o)), widen(o_ref), tc=tc) <= tol(st, io)
+    c.check_pool(tc=tc)
 
 
 def test_prefill_bad_cu_seqlens_flags(cuda_dev):
@@ -535,16 +576,61 @@ def test_prefill_kimi_shaped_chunk(cuda_dev):
     o_ref = oracle.prefill(c.ref, 0, [2], cu, x, c.w, g, beta)
     o = rsc.kda_prefill_chunk(c.pool, 0, to_dev(np.int32([2]), c.dev), to_dev(cu, c.dev),
                               to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
-    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= TOL[1]
-    c.check_pool()
+    assert max_rel_err(widen(to_np(o)), widen(o_ref), tc=True) <= TOL[1]
+    c.check_pool(tc=True)
 
 
-def test_prefill_gate_spread_beyond_range_is_flagged(cuda_dev):
-    c = Case(cuda_dev, 11, L=1, P=2, H=1, K=128, V=64, st=1, io=1, gate=rsc.KDA)
+def _strong_gates(c, T, mode):
+    """Log-decay gates far beyond the usual draw: a constant -4 per token (a 64-token chunk
+    spans 252, a 16-token block 60), -e^3 softplus(N(0,1)) everywhere (every 16-token block
+    spans hundreds), or a mix: weak and strong stretches and channels, and full resets."""
+    if mode == "const4":
+        g, beta = c.gates((T,))
+        return np.full_like(g, -4.0), beta
+    if mode == "scale20":
+        return inputs.gates(c.r, (T,), c.H, c.K, c.gate, scale=float(np.exp(3.0)))
+    g, beta = c.gates((T,))
+    g = g.copy()
+    g[T // 3: 2 * T // 3, ..., : c.K // 2] *= 30.0
+    g[c.r.integers(0, T, 4)] = -300.0
+    return g, beta
+
+
+@pytest.mark.parametrize("gate,V,lens,init,mode", [
+    (rsc.KDA, 64, [64], [1], "const4"),
+    (rsc.KDA, 128, [200, 70], [1, 0], "scale20"),
+    (rsc.KDA, 128, [300], [1], "mixed"),
+    (rsc.GDN, 128, [130, 63], [0, 1], "scale20"),
+    (rsc.GDN, 64, [190], [1], "mixed"),
+])
+def test_prefill_strong_decay_matches_oracle(cuda_dev, gate, V, lens, init, mode):
+    """The tensor-core prefill under decay far beyond the usual draw (the diagonal 16-token
+    blocks then run exactly in fp32) against the oracle; no error bit."""
+    H, K = 2, 128
+    c = Case(cuda_dev, 11, L=1, P=4, H=H, K=K, V=V, st=1, io=1, gate=gate)
+    N = len(lens)
+    slots = inputs.distinct_slots(c.r, N, 4)
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    x = c.proj((T,))
+    g, beta = _strong_gates(c, T, mode)
+    hi = np.uint8(init)
+    o_ref = oracle.prefill(c.ref, 0, slots, cu, x, c.w, g, beta, has_init=hi)
+    o = rsc.kda_prefill_chunk(c.pool, 0, to_dev(slots, c.dev), to_dev(cu, c.dev),
+                              to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                              has_initial_state=to_dev(hi, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref), tc=True) <= TOL[1]
+    c.check_pool(tc=True)
+
+
+def test_prefill_growing_gate_is_flagged(cuda_dev):
+    """A gate that grows the state (g > 0) by more than the tensor-core form represents
+    within a chunk sets RSC_DEVERR_GATE; decaying gates never do (tests above)."""
+    c = Case(cuda_dev, 12, L=1, P=2, H=1, K=128, V=64, st=1, io=1, gate=rsc.KDA)
     T = 64
     x = c.proj((T,))
     _, beta = c.gates((T,))
-    g = np.full((T, 1, 128), -4.0, np.float32)  # cumulative spread 252 over the chunk
+    g = np.full((T, 1, 128), 2.0, np.float32)  # grows by 126 over the chunk
     rsc.kda_prefill_chunk(c.pool, 0, to_dev(np.int32([1]), c.dev), to_dev(np.int32([0, T]), c.dev),
                           to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
-    assert rsc.rsc_get_device_error(c.pool) & 16
+    assert rsc.rsc_get_device_error(c.pool) & rsc.binding.DEVERR_GATE

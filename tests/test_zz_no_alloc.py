@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import recurrent_state_cache_gb300 as rsc
 from recurrent_state_cache_gb300 import binding, inputs
 from tests.devio import to_dev, to_np, widen
@@ -18,26 +19,37 @@ pytestmark = pytest.mark.gpu
 def _pools(dev, st, H, K, V, P, seed):
     r = inputs.rng(seed)
     ssm, conv = inputs.pool_arrays(r, 1, P, H, K, V, st, st)
+    ref = oracle.Pool(1, P, H, K, V, st, st, oracle.KDA, ssm, conv)
     a = rsc.SlotPool(1, P, H, K, V, st, st, rsc.KDA, dev, ssm=to_dev(ssm, dev), conv=to_dev(conv, dev))
     b = rsc.SlotPool(1, P, H, K, V, st, st, rsc.KDA, dev, ssm=to_dev(ssm, dev), conv=to_dev(conv, dev))
-    return r, a, b
+    return r, ref, a, b
 
 
-@pytest.mark.parametrize("st", [rsc.F32, rsc.BF16])
-def test_noalloc_prefill_matches_workspace_prefill_twice(cuda_dev, st):
-    H, K, V, P = 2, 64, 128, 6
-    r, pool_ws, pool_na = _pools(cuda_dev, st, H, K, V, P, seed=31)
-    w = to_dev(inputs.conv_weights(r, H, K, V), cuda_dev)
-    slots = to_dev(np.int32([4, 2]), cuda_dev)
-    for call in range(2):  # second call continues from the state the first one left
+@pytest.mark.parametrize("st,K", [
+    (rsc.F32, 64),    # token-serial fp32 path
+    (rsc.BF16, 64),   # token-serial path of a bf16-state pool
+    (rsc.BF16, 128),  # chunkwise tensor-core path: chunk table and operand blocks in the array
+])
+def test_noalloc_prefill_matches_workspace_prefill_twice(cuda_dev, st, K):
+    """Two calls in a row on the shared static scratch (the second continues from the state
+    the first left, and meets the first call's leftovers in the array): outputs, states and
+    windows equal those of kda_prefill_chunk with a caller workspace, and the oracle's."""
+    H, V, P = 2, 128, 6
+    r, ref, pool_ws, pool_na = _pools(cuda_dev, st, H, K, V, P, seed=31)
+    w_np = inputs.conv_weights(r, H, K, V)
+    w = to_dev(w_np, cuda_dev)
+    slots_np = np.int32([4, 2])
+    slots = to_dev(slots_np, cuda_dev)
+    for call in range(2):
         lens = [97, 203] if call == 0 else [1, 130]
         cu = inputs.cu_seqlens(lens)
         T = int(cu[-1])
-        x = to_dev(inputs.projections(r, (T,), H, K, V, st), cuda_dev)
-        g, beta = inputs.gates(r, (T,), H, K, rsc.KDA)
-        g, beta = to_dev(g, cuda_dev), to_dev(beta, cuda_dev)
-        cu_d = to_dev(cu, cuda_dev)
-        hi = to_dev(np.uint8([call, 1]), cuda_dev)
+        x_np = inputs.projections(r, (T,), H, K, V, st)
+        g_np, beta_np = inputs.gates(r, (T,), H, K, rsc.KDA)
+        hi_np = np.uint8([call, 1])
+        o_ref = oracle.prefill(ref, 0, slots_np, cu, x_np, w_np, g_np, beta_np, has_init=hi_np)
+        x, g, beta = to_dev(x_np, cuda_dev), to_dev(g_np, cuda_dev), to_dev(beta_np, cuda_dev)
+        cu_d, hi = to_dev(cu, cuda_dev), to_dev(hi_np, cuda_dev)
         o_ws = rsc.kda_prefill_chunk(pool_ws, 0, slots, cu_d, x, w, g, beta, has_initial_state=hi)
         o_na = binding.kda_prefill_chunk_noalloc(pool_na, 0, slots, cu_d, x, w, g, beta,
                                                  has_initial_state=hi)
@@ -45,6 +57,10 @@ def test_noalloc_prefill_matches_workspace_prefill_twice(cuda_dev, st):
         assert max_rel_err(widen(to_np(o_na)), widen(to_np(o_ws))) <= TOL[st]
         assert max_rel_err(widen(to_np(pool_na.ssm)), widen(to_np(pool_ws.ssm))) <= TOL[st]
         assert np.array_equal(to_np(pool_na.conv), to_np(pool_ws.conv))
+        tc = st == rsc.BF16 and K == 128  # the chunkwise tensor-core path
+        assert max_rel_err(widen(to_np(o_na)), widen(o_ref), tc=tc) <= TOL[st]
+        assert max_rel_err(widen(to_np(pool_na.ssm)), widen(ref.ssm), tc=tc) <= TOL[st]
+        assert np.array_equal(to_np(pool_na.conv), ref.conv)
         assert rsc.rsc_get_device_error(pool_na) == 0
 
 

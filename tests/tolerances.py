@@ -1,21 +1,35 @@
 """Parity metric and tolerances shared by the tests.
 
-max relative error of a tensor = max_i |got_i - ref_i| / max_i |ref_i|  (infinity-norm
-relative error).  Bars: 1e-4 when the pool's state is fp32 and the compared tensor is
+The max relative error of a tensor is the larger of two forms, so that both must meet the
+bar:
+  norm-wise     max_i |got_i - ref_i| / max_i |ref_i|
+  element-wise  max_i |got_i - ref_i| / (|ref_i| + rms(ref))
+The element-wise form catches a large relative error on a small entry that the norm-wise
+form hides behind the tensor's largest entry; its floor rms(ref) keeps entries near zero,
+whose absolute error is set by the magnitude of the terms that meet in them, from failing a
+correct bf16 result.  Bars: 1e-4 when the pool's state is fp32 and the compared tensor is
 stored in fp32; 2e-2 when either is bf16 (a bf16 output carries its own rounding, and a
 bf16-state pool runs bf16 tensor-core operands).
+Results that pass through bf16 tensor-core operands (the chunked prefill of bf16-state pools,
+tc=True) hold the element-wise form to TC_ELEM_FACTOR times the bar: each of their entries is a
+sum of bf16-rounded products, so its absolute error follows the size of those products rather
+than of the entry.  Measured on GB300 against the oracle, before and after the sub-chunk gate
+form: RMS error 0.4-0.5% of the tensor's rms, the largest single entry 7.2% of rms (one of 9.4M
+outputs of a 6144-token call, 1-2 bf16 ulps on an entry five times below rms); the norm-wise
+form stays at or below 0.0094.
 Integer, index and byte results are compared bit for bit instead.
 """
 import numpy as np
 
 TOL = {0: 1e-4, 1: 2e-2}  # keyed by dtype: 0 = fp32, 1 = bf16
+TC_ELEM_FACTOR = 5.0
 
 
 def tol(state_dtype: int, tensor_dtype: int) -> float:
     return TOL[max(state_dtype, tensor_dtype)]
 
 
-def max_rel_err(got, ref) -> float:
+def norm_rel_err(got, ref) -> float:
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -26,3 +40,21 @@ def max_rel_err(got, ref) -> float:
     if denom == 0.0:
         return diff
     return diff / denom
+
+
+def elem_rel_err(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    floor = float(np.sqrt(np.mean(ref * ref)))
+    if floor == 0.0:
+        return float(np.max(np.abs(got - ref)))
+    return float(np.max(np.abs(got - ref) / (np.abs(ref) + floor)))
+
+
+def max_rel_err(got, ref, tc: bool = False) -> float:
+    """The larger of the two forms (the element-wise one scaled by 1 / TC_ELEM_FACTOR for
+    results of bf16 tensor-core operands), to be compared with the bar."""
+    return max(norm_rel_err(got, ref), elem_rel_err(got, ref) / (TC_ELEM_FACTOR if tc else 1.0))
