@@ -360,7 +360,37 @@ def leg_prefill(dev, peaks, stream):
            "io_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
            "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "path": "chunkwise, tcgen05 tensor cores"}
+    res["f32_state"] = leg_prefill_f32(dev, stream)
     return res
+
+
+def leg_prefill_f32(dev, stream, T=2048):
+    """The fp32-state prefill (exact token-serial recurrence, CUDA cores) on one 2048-token
+    call of the same head shape (H=12, K=V=128, bf16 inputs), from a fresh slot."""
+    import torch
+    import recurrent_state_cache_gb300 as rsc
+    from recurrent_state_cache_gb300 import binding as b
+    H, K, V = 12, 128, 128
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    D = H * (2 * K + V)
+    pool = rsc.SlotPool(1, 4, H, K, V, b.F32, b.BF16, b.KDA, dev)
+    qkv = torch.empty((T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((T, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((T, H), device=dev).normal_(0, 1, generator=gen))
+    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
+    out = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(rsc.kda_prefill_workspace_size(pool, 1, T), dtype=torch.uint8, device=dev)
+    slot = torch.tensor([1], dtype=torch.int32, device=dev)
+    fresh = torch.tensor([0], dtype=torch.uint8, device=dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    run = lambda: rsc.kda_prefill_chunk(pool, 0, slot, cu, qkv, w, g, beta,
+                                        has_initial_state=fresh, out=out, workspace=ws)
+    ms = timed(graph_of(run, stream).replay, 5, 2, stream)
+    return {"config": f"1 KDA layer, H=12, K=V=128, fp32 state, bf16 io, one {T}-token call",
+            "ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "us_per_token": round(ms * 1e3 / T, 4),
+            "path": "token-serial recurrence (prep, recurrent, window kernels)"}
 
 
 def leg_copy(dev, peaks, stream, wl):
@@ -382,38 +412,61 @@ def leg_copy(dev, peaks, stream, wl):
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+SPEC_ROTATIONS = 8  # distinct (layer, cache, accept) sets cycled through by the spec legs
+
+
+def _spec_inputs(dev, seed, R, B, T, H, K, V):
+    """Inputs of R verify calls of the speculative workload (one set per rotation)."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    D = H * (2 * K + V)
+    qkv = torch.empty((R, B, T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((R, B, T, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((R, B, T, H), device=dev).normal_(0, 1, generator=gen))
+    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
+    return gen, qkv, g, beta, w
+
+
 def leg_spec(dev, peaks, stream):
+    """Snapshot-form verify and commit on the speculative workload (B=64, T=8, cache depth
+    16).  Each timed graph cycles through SPEC_ROTATIONS calls on distinct pool layers, spec
+    caches and accept vectors, so a call's rows were last touched seven calls (>= 370 MB of
+    other traffic) earlier and are read from HBM, not from L2."""
     import torch
     import recurrent_state_cache_gb300 as rsc
     from recurrent_state_cache_gb300 import binding as b, inputs
-    H, K, V, B, T, L, P = 12, 128, 128, 64, 8, 16, 320
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(4)
+    H, K, V, B, T, L, P, R = 12, 128, 128, 64, 8, 16, 320, SPEC_ROTATIONS
     D = H * (2 * K + V)
-    ssm = torch.empty((1, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
-    conv = torch.empty((1, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
-    pool = rsc.SlotPool(1, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
+    gen, qkv, g, beta, w = _spec_inputs(dev, 4, R, B, T, H, K, V)
+    ssm = torch.empty((R, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    conv = torch.empty((R, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    pool = rsc.SlotPool(R, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
     r = inputs.rng(4)
-    slots = torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev)
-    accept = torch.from_numpy(inputs.accept_counts(r, B, T)).to(dev)
-    qkv = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
-    g = -torch.nn.functional.softplus(torch.empty((B, T, H, K), device=dev).normal_(0, 1, generator=gen))
-    beta = torch.sigmoid(torch.empty((B, T, H), device=dev).normal_(0, 1, generator=gen))
-    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
-    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
-    spec_ssm = torch.empty((B, L, H, V, K), dtype=torch.bfloat16, device=dev)
-    spec_conv = torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev)
-    verify = lambda: rsc.kda_spec_verify_commit(pool, 0, rsc.VERIFY, slots, T, L, spec_ssm, spec_conv,
-                                                qkv, w, g, beta, out)
-    commit = lambda: rsc.kda_spec_verify_commit(pool, 0, rsc.COMMIT, slots, T, L, spec_ssm, spec_conv,
-                                                accept=accept)
-    ms_v = timed(verify, 10, 3, stream)
-    ms_c = timed(commit, 10, 3, stream)
+    slots = [torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev) for _ in range(R)]
+    accept_np = [inputs.accept_counts(r, B, T) for _ in range(R)]
+    accept = [torch.from_numpy(a).to(dev) for a in accept_np]
+    out = torch.empty((R, B, T, H, V), dtype=torch.bfloat16, device=dev)
+    spec_ssm = [torch.empty((B, L, H, V, K), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    spec_conv = [torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def verify():
+        for i in range(R):
+            rsc.kda_spec_verify_commit(pool, i, rsc.VERIFY, slots[i], T, L, spec_ssm[i],
+                                       spec_conv[i], qkv[i], w, g[i], beta[i], out[i])
+
+    def commit():
+        for i in range(R):
+            rsc.kda_spec_verify_commit(pool, i, rsc.COMMIT, slots[i], T, L, spec_ssm[i],
+                                       spec_conv[i], accept=accept[i])
+    ms_v = timed(graph_of(verify, stream).replay, 20, 3, stream) / R
+    ms_c = timed(graph_of(commit, stream).replay, 20, 3, stream) / R
     S, Wb = H * V * K * 2, 3 * D * 2
     vb = spec_verify_bytes(B, T, H, K, V)
     cb = B * 2 * (S + Wb)
     vw = B * (T * S + T * Wb + T * H * V * 2)  # bytes written by verify
-    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), cache depth 16",
+    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), cache depth 16; "
+                      f"graphs of {R} calls on distinct layers, caches and accept vectors",
             "verify_ms": round(ms_v, 4), "verify_gbs": round(vb / (ms_v * 1e-3) / 1e9, 1),
             "verify_frac": round(vb / (ms_v * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "verify_write_gbs": round(vw / (ms_v * 1e-3) / 1e9, 1),
@@ -489,41 +542,46 @@ def leg_track(dev, peaks, stream, wl):
 def leg_replay(dev, peaks, stream):
     """ReplaySSM verify / commit on the speculative workload of leg_spec: verify writes ring
     records (d, k, rawv, rawk, g, beta) instead of 8 states per request; commit replays the
-    accepted tokens from the slot state."""
+    accepted tokens from the slot state.  Timed like leg_spec: graphs cycling through
+    SPEC_ROTATIONS distinct layers (each with its own rings), slot sets and accept vectors."""
     import torch
     import recurrent_state_cache_gb300 as rsc
     from recurrent_state_cache_gb300 import binding as b, inputs
-    H, K, V, B, T, L, P = 12, 128, 128, 64, 8, 16, 320
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(4)
+    H, K, V, B, T, L, P, R = 12, 128, 128, 64, 8, 16, 320, SPEC_ROTATIONS
     D = H * (2 * K + V)
-    ssm = torch.empty((1, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
-    conv = torch.empty((1, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
-    pool = rsc.SlotPool(1, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
+    gen, qkv, g, beta, w = _spec_inputs(dev, 5, R, B, T, H, K, V)
+    ssm = torch.empty((R, P + 1, H, V, K), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    conv = torch.empty((R, P + 1, 3, D), dtype=torch.bfloat16, device=dev).normal_(0, 0.1, generator=gen)
+    pool = rsc.SlotPool(R, P, H, K, V, b.BF16, b.BF16, b.KDA, dev, ssm=ssm, conv=conv)
     rings = rsc.ReplayRings(pool, L)
     r = inputs.rng(4)
-    slots = torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev)
-    accept_np = inputs.accept_counts(r, B, T)
-    accept = torch.from_numpy(accept_np).to(dev)
-    pos = torch.from_numpy(inputs.rng(5).integers(0, L, B).astype("int32")).to(dev)
-    qkv = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
-    g = -torch.nn.functional.softplus(torch.empty((B, T, H, K), device=dev).normal_(0, 1, generator=gen))
-    beta = torch.sigmoid(torch.empty((B, T, H), device=dev).normal_(0, 1, generator=gen))
-    w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
-    out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
-    spec_conv = torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev)
-    verify = lambda: rsc.kda_replay_verify_commit(pool, rings, 0, rsc.VERIFY, slots, pos, T, spec_conv,
-                                                  qkv, w, g, beta, out)
-    commit = lambda: rsc.kda_replay_verify_commit(pool, rings, 0, rsc.COMMIT, slots, pos, T, spec_conv,
-                                                  accept=accept)
-    ms_v = timed(verify, 10, 3, stream)
-    ms_c = timed(commit, 10, 3, stream)
+    slots = [torch.from_numpy(inputs.distinct_slots(r, B, P)).to(dev) for _ in range(R)]
+    accept_np = [inputs.accept_counts(r, B, T) for _ in range(R)]
+    accept = [torch.from_numpy(a).to(dev) for a in accept_np]
+    r5 = inputs.rng(5)
+    pos = [torch.from_numpy(r5.integers(0, L, B).astype("int32")).to(dev) for _ in range(R)]
+    out = torch.empty((R, B, T, H, V), dtype=torch.bfloat16, device=dev)
+    spec_conv = [torch.empty((B, L, 3, D), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def verify():
+        for i in range(R):
+            rsc.kda_replay_verify_commit(pool, rings, i, rsc.VERIFY, slots[i], pos[i], T,
+                                         spec_conv[i], qkv[i], w, g[i], beta[i], out[i])
+
+    def commit():
+        for i in range(R):
+            rsc.kda_replay_verify_commit(pool, rings, i, rsc.COMMIT, slots[i], pos[i], T,
+                                         spec_conv[i], accept=accept[i])
+    ms_v = timed(graph_of(verify, stream).replay, 20, 3, stream) / R
+    ms_c = timed(graph_of(commit, stream).replay, 20, 3, stream) / R
     S, Wb = H * V * K * 2, 3 * D * 2
     rec = H * (2 * V * 2 + 2 * K * 2 + K * 4 + 4)   # one token's records over the heads
     rep_ = H * (V * 2 + K * 2 + K * 4 + 4)          # what commit reads of one token's records
     vb = B * (S + T * rec + Wb + T * Wb + T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2 + 8)
-    cb = int(2 * B * S + 2 * B * Wb + int(accept_np.astype("int64").sum() + B) * rep_ + 12 * B)
-    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), ring depth 16",
+    acc_tokens = sum(int(a.astype("int64").sum()) + B for a in accept_np) / R
+    cb = int(2 * B * S + 2 * B * Wb + acc_tokens * rep_ + 12 * B)
+    return {"config": "KDA H=12 K=V=128 bf16, batch 64, T=8 (anchor+7 drafts), ring depth 16; "
+                      f"graphs of {R} calls on distinct layers, slot sets and accept vectors",
             "verify_ms": round(ms_v, 4), "verify_bytes": vb,
             "verify_gbs": round(vb / (ms_v * 1e-3) / 1e9, 1),
             "verify_frac": round(vb / (ms_v * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -794,6 +852,10 @@ def main(argv=None):
     e2e_steps = max(10, min(args.steps, 200))
     ms_e2e = timed(e2e_graph.replay, e2e_steps, args.warmup, stream, dist)
     ms_e2e = max_over_ranks(ms_e2e, dist, dev)
+    # The same step issued eagerly every time (69 binding calls through ctypes, their argument
+    # checks and launches, plus the stream forks and copies), without a graph.
+    ms_eager = timed(e2e_step, max(10, min(args.steps, 100)), args.warmup, stream, dist)
+    ms_eager = max_over_ranks(ms_eager, dist, dev)
     h2d = h_pack.numel()
     d2h = h_out.numel() * h_out.element_size()
 
@@ -868,7 +930,10 @@ def main(argv=None):
                 "how": "per step: pinned host->device copies of every layer's qkv, g, beta (packed per layer, one copy per group of layers), "
                        "the kda_decode_step_overlap calls, device->host copies of every layer's output, "
                        "overlapped layer by layer on a copy-in, a compute and a copy-out stream; "
-                       "captured once in a CUDA graph and replayed"},
+                       "captured once in a CUDA graph and replayed",
+                "eager_value": round(sum_over_ranks(units, dist, dev) / (ms_eager * 1e-3), 1),
+                "eager_ms_per_step": round(ms_eager, 4),
+                "eager_how": "the same step issued from Python every time, without a graph"},
         "gpu_launches": args.layers * args.steps,
         "clocks": clocks,
         "legs": legs,

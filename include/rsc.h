@@ -65,10 +65,11 @@ extern "C" {
 #define RSC_DEVERR_ACCEPT 2 /* an accept count outside [0, T-1]                      */
 #define RSC_DEVERR_SEQ    4 /* cu_seqlens not non-decreasing within [0, total]       */
 #define RSC_DEVERR_TIMEOUT 8 /* a bounded on-chip wait ran out; that tile was skipped  */
-#define RSC_DEVERR_GATE   16 /* tensor-core prefill: a 64-token chunk's cumulative log
-                                gate spans more than 160 in some channel; its split
-                                exponentials lose range and that chunk's result is not
-                                reliable (the gate must decay, g <= 0)                */
+#define RSC_DEVERR_GATE   16 /* tensor-core prefill: a growing gate (g > 0) raised a
+                                chunk's cumulative log gate by more than 60 above one
+                                of its 16-token reference points; that chunk's result
+                                is not reliable.  Never set for a decaying gate (g <= 0),
+                                however strong.                                       */
 #define RSC_DEVERR_RING   32 /* a ReplaySSM ring position outside [0, depth)            */
 
 typedef enum { RSC_F32 = 0, RSC_BF16 = 1 } rsc_dtype;
@@ -212,9 +213,9 @@ int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tok
  *   workspace         device, >= kda_prefill_workspace_size bytes, 16-byte aligned
  * bf16-state pools with head_k == 128 run the chunkwise form (chunk 64, every
  * contraction on the tcgen05 tensor cores with bf16 operands and fp32 accumulation);
- * it expects a decaying gate (g <= 0, as the models' gates are) and flags
- * RSC_DEVERR_GATE for a chunk whose gate range it cannot represent.  Other pools run the
- * recurrence token by token in fp32.
+ * any decaying gate (g <= 0, as the models' gates are) is exact to that precision,
+ * however strong; a growing gate beyond the range above flags RSC_DEVERR_GATE.  Other
+ * pools run the recurrence token by token in fp32.
  * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ENOSPACE, RSC_ECUDA. */
 int kda_prefill_chunk(rsc_pool *pool, int layer, const int32_t *slot_ids,
                       const int32_t *cu_seqlens, int num_seqs, int total_tokens,

@@ -25,18 +25,20 @@
 //   chunk table  one warp: chunk_base[n] = chunks before sequence n (64-token chunks).
 //   chunk        grid (chunk, head), 256 threads, two CTAs per SM: everything that does not
 //                depend on the state, from the raw projections.  Conv and L2 norm; the gate
-//                cumsum with a per-channel midpoint reference R (no split factor exceeds
-//                e^(range/2); a range beyond 160 sets an error bit); A and P as one
-//                128x64x128 MMA; (I + A)^-1 by 16x16 blocks in fp32; [W | U'] as one MMA of
+//                cumsum with one reference point per 16-token sub-chunk (every factor on
+//                the tensor cores has an exponent <= 0 for a decaying gate; a sub-chunk
+//                whose own spread is too wide gets its diagonal block in fp32); A and P as
+//                one MMA; (I + A)^-1 by 16x16 blocks in fp32; [W | U'] as one MMA of
 //                (I + A)^-1 Diag(beta) (split into bf16 high and low parts) with [K.Gamma | V];
 //                [Z | N^T] = B^T [W | U'] and [P W | F] = P [W | U'] as two more MMAs.  Writes
 //                per (chunk, head) a block of Z and E in the canonical K-major operand
 //                layout, N^T and F by 32-column tiles, and Gamma_c.
 //   state        grid (32-row tile of S, head, sequence): walks the sequence's chunks in
 //                order with the tile's state in fp32 registers (thread k holds column k); per
-//                chunk one MMA pair Z S0^T, E S0^T, then the state update and the outputs.
-//                Operand blocks arrive by TMA bulk copies two chunks ahead; a chunk's outputs
-//                are written while the next chunk's MMAs run.
+//                chunk one MMA Z S0^T (Z the A operand in tensor memory), then the state
+//                update; S0 of every chunk goes to the chunk's block.  Operand blocks arrive
+//                by TMA bulk copies three chunks ahead.
+//   output       grid (chunk, head): O = E S0^T + F, one MMA per chunk and head.
 //   window       prefill.cu's window kernel.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
