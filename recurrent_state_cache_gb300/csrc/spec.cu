@@ -28,6 +28,7 @@
 // records.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
+#include "rsc_tc.cuh"
 
 namespace rsc {
 
@@ -517,6 +518,278 @@ int launch_spec_verify(const LayerArgs &a, const int32_t *slots, int B, int T, i
                                     spec_ssm, spec_conv, qkv, conv_w, g, beta, out, s);
 }
 
+// Record-mode verify on the tensor cores: bf16 state, K = V = 128, one block of T <= 8
+// tokens (the pages' draft of seven tokens plus the anchor), one CTA per (head, request).
+// The same closed form as replay_block, with the 2 T row dots of the block as one tcgen05
+// product: D = S0 [k_hat_t . e^G_t | q_hat_t . e^G_t]^T (M = 128 state rows, N = 16,
+// K = 128), S0 the slot's tile (exactly bf16, copied into the canonical operand layout by
+// cp.async) and the 16 vectors as bf16 high and low parts (two accumulating products, so
+// the dots keep ~16 bits of the fp32 vectors).  Thread v (warps 0-3) then reads row v's 16
+// dots from tensor memory and runs the 8x8 triangular solve of its row.  No state tile in
+// registers: 256 threads at three CTAs per SM.
+namespace rtc {
+constexpr int K = 128, V = 128, TS = 8, CH = 2 * K + V, NT = 256;
+constexpr uint32_t kS0 = 0;                       // S0  bf16 K-major, 128 rows x K
+constexpr uint32_t kXH = kS0 + V * K * 2;         // X   bf16 K-major, 16 rows x K (high part)
+constexpr uint32_t kXL = kXH + 16 * K * 2;        //     low part
+constexpr uint32_t kSx = kXL + 16 * K * 2;        // raw inputs of the block [TS][CH] (io dtype)
+constexpr uint32_t kSy = kSx + TS * CH * 4;       // conv outputs fp32 [TS][CH]: q_hat | k_hat | v
+constexpr uint32_t kSg = kSy + TS * CH * 4;       // log-decays fp32 [TS][K]
+constexpr uint32_t kSG = kSg + TS * K * 4;        // cumulative log-decays fp32 [TS][K]
+constexpr uint32_t kSmem = kSG + TS * K * 4;      // 72 KB: three CTAs per SM
+}  // namespace rtc
+
+template <typename IO, int GATE>
+__global__ void __launch_bounds__(rtc::NT, 3)
+kda_replay_verify_tc_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots, int T,
+                            IO *__restrict__ spec_conv, const IO *__restrict__ qkv,
+                            const float *__restrict__ conv_w, const float *__restrict__ g,
+                            const float *__restrict__ beta, IO *__restrict__ out, RingView rv,
+                            const int32_t *__restrict__ pos) {
+  using namespace rtc;
+  using bf16_t = bf16;
+  constexpr int GW = GATE == RSC_GATE_KDA ? K : 1;
+  constexpr int XV = 16 / sizeof(IO);
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ float s_b[TS], s_kq[TS], s_A[TS][TS], s_P[TS][TS];
+  __shared__ uint32_t s_taddr;
+  __shared__ __align__(8) uint64_t s_bar;
+  IO *sx = reinterpret_cast<IO *>(smem + kSx);
+  float *sy = reinterpret_cast<float *>(smem + kSy);
+  float *sg = reinterpret_cast<float *>(smem + kSg);
+  float *sG = reinterpret_cast<float *>(smem + kSG);
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = pv.H, D = pv.D;
+
+  const int slot = slots[b];
+  if (slot < 0 || slot > pv.P) {
+    if (tid == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
+    return;
+  }
+  const int p0 = pos[b];
+  if (p0 < 0 || p0 >= rv.depth) {
+    if (tid == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_RING);
+    return;
+  }
+  const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+  auto ent = [&](int t) { return (prow * H + h) * (size_t)rv.depth + ((p0 + t) & (rv.depth - 1)); };
+  // channel c of the head (q | k | v) -> column of the projections and of the window
+  auto col = [&](int c) {
+    return c < K ? h * K + c : c < 2 * K ? H * K + h * K + (c - K) : 2 * H * K + h * V + (c - 2 * K);
+  };
+
+  if (tid == 0) mbar_init(&s_bar, 1);
+  if (warp == 0) { tc::tmem_alloc(&s_taddr, 32); tc::tmem_relinquish(); }
+
+  // 1. copies: the slot's tile into the operand layout (8 lanes with the same 16-byte column
+  //    take 8 consecutive rows: distinct bank groups), the block's raw inputs, gates, betas
+  const bf16_t *Sg = reinterpret_cast<const bf16_t *>(pv.ssm) + (prow * H + h) * (size_t)V * K;
+  for (int i = tid; i < V * K / 8; i += NT) {
+    const int v = ((i >> 7) << 3) | (i & 7), kc = (i >> 3) & 15;
+    cp_async16(smem + kS0 + tc::kmajor_offset(v, 8 * kc, K), Sg + (size_t)v * K + 8 * kc);
+  }
+  for (int i = tid; i < T * (CH / XV); i += NT) {
+    const int t = i / (CH / XV), c = (i % (CH / XV)) * XV;
+    cp_async16(sx + t * CH + c, qkv + ((size_t)b * T + t) * D + col(c));
+  }
+  if constexpr (GW == K) {
+    for (int i = tid; i < T * (K / 4); i += NT) {
+      const int t = i / (K / 4), c = (i % (K / 4)) * 4;
+      cp_async16(sg + t * K + c, g + (((size_t)b * T + t) * H + h) * K + c);
+    }
+  } else if (tid < T) {
+    cp_async4(sg + tid * K, g + ((size_t)b * T + tid) * H + h);
+  }
+  if (tid < T) cp_async4(&s_b[tid], beta + ((size_t)b * T + tid) * H + h);
+  cp_async_commit();
+  // taps and window rows of this thread's channels (tid, and tid + 256 below 384)
+  const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
+  float4 wt[2];
+  IO win[2][3];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int c = tid + u * NT;
+    if (c < CH) {
+      const int cc = col(c);
+      wt[u] = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)cc);
+      win[u][0] = W[cc]; win[u][1] = W[D + cc]; win[u][2] = W[2 * D + cc];
+    }
+  }
+  cp_async_wait_all();
+  tc::fence_smem_to_async();  // the tile is read by the tensor core
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t taddr = s_taddr;
+
+  // 2. conv of every token (each thread rolls its channels' windows, writes the window after
+  //    every token into the cache entry, rawk / rawv records), cumulative log-decays
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int c = tid + u * NT;
+    if (c >= CH) continue;
+    const int cc = col(c);
+    for (int t = 0; t < T; ++t) {
+      const IO xc = sx[t * CH + c];
+      const float y = conv4(wt[u], to_f32(win[u][0]), to_f32(win[u][1]), to_f32(win[u][2]), to_f32(xc));
+      sy[t * CH + c] = y;
+      win[u][0] = win[u][1]; win[u][1] = win[u][2]; win[u][2] = xc;
+      IO *E = spec_conv + ((size_t)b * rv.depth + t) * 3 * (size_t)D;
+      E[cc] = win[u][0]; E[D + cc] = win[u][1]; E[2 * D + cc] = win[u][2];
+      if (c >= 2 * K) static_cast<bf16_t *>(rv.rawv)[ent(t) * V + (c - 2 * K)] = __float2bfloat16_rn(y);
+      else if (c >= K) static_cast<bf16_t *>(rv.rawk)[ent(t) * K + (c - K)] = __float2bfloat16_rn(y);
+    }
+  }
+  if (tid < GW) {
+    float acc = 0.f;
+    for (int t = 0; t < T; ++t) {
+      const float x = sg[t * K + tid];
+      acc += x;
+      sG[t * K + tid] = acc;
+      rv.g[ent(t) * GW + tid] = x;
+    }
+  }
+  if (tid < T) rv.beta[ent(tid)] = s_b[tid];
+  __syncthreads();
+
+  // 3. L2 norms, a warp per token (lane l: channels l, l+32, l+64, l+96 of q and of k);
+  //    the normalised key's record
+  for (int t = warp; t < T; t += NT / 32) {
+    float *yq = sy + t * CH, *yk = yq + K;
+    float qq = 0.f, kk = 0.f, qk = 0.f;
+#pragma unroll
+    for (int e = 0; e < K / 32; ++e) {
+      const float a = yq[lane + 32 * e], c = yk[lane + 32 * e];
+      qq = fmaf(a, a, qq); kk = fmaf(c, c, kk); qk = fmaf(a, c, qk);
+    }
+    qq = group_sum<32>(qq); kk = group_sum<32>(kk); qk = group_sum<32>(qk);
+    const float rq = 1.0f / sqrtf(qq + kNormEps), rk = 1.0f / sqrtf(kk + kNormEps);
+#pragma unroll
+    for (int e = 0; e < K / 32; ++e) {
+      yq[lane + 32 * e] *= rq;
+      const float kh = yk[lane + 32 * e] * rk;
+      yk[lane + 32 * e] = kh;
+      static_cast<bf16_t *>(rv.k)[ent(t) * K + lane + 32 * e] = __float2bfloat16_rn(kh);
+    }
+    if (lane == 0) s_kq[t] = qk * rq * rk;
+  }
+  __syncthreads();
+
+  // 4. the product's B operand, rows n < 8: k_hat_n . e^G_n, rows 8 + n: q_hat_n . e^G_n (zero
+  //    beyond the block), as bf16 high and low parts; item i: row i % 16, eight channels
+  //    8 (i / 16) .. +7
+  {
+    const int n = tid & 15, kc = tid >> 4, t = n & 7;
+    float hi[8], lo[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float x = 0.f;
+      if (t < T) {
+        const int k = 8 * kc + e;
+        const float Gt = sG[t * K + (GW == 1 ? 0 : k)];
+        x = sy[t * CH + (n < 8 ? K : 0) + k] * __expf(Gt);
+      }
+      hi[e] = __bfloat162float(__float2bfloat16_rn(x));
+      lo[e] = x - hi[e];
+    }
+    const uint32_t off = tc::kmajor_offset(n, 8 * kc, K);
+    st16(smem + kXH + off, pack16(hi));
+    st16(smem + kXL + off, pack16(lo));
+  }
+  // coefficients of the pairs s < t: A[t][s] = sum_k k_s k_t e^(G_t - G_s), P[t][s] = sum_k
+  // k_s q_t e^(G_t - G_s); warp w takes pairs w, w + 8, ..., lane l channels 4l .. 4l+3
+  for (int pi = warp; pi < TS * (TS - 1) / 2; pi += NT / 32) {
+    int t = 1;
+    while (t * (t + 1) / 2 <= pi) ++t;
+    const int s2 = pi - t * (t - 1) / 2;
+    if (t >= T) continue;  // uniform over the warp
+    const float *ks = sy + s2 * CH + K, *kt = sy + t * CH + K, *qt = sy + t * CH;
+    float a = 0.f, p = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = 4 * lane + e;
+      const float dg = GW == 1 ? sG[t * K] - sG[s2 * K] : sG[t * K + k] - sG[s2 * K + k];
+      const float kd = ks[k] * __expf(dg);
+      a = fmaf(kd, kt[k], a);
+      p = fmaf(kd, qt[k], p);
+    }
+    a = group_sum<32>(a);
+    p = group_sum<32>(p);
+    if (lane == 0) { s_A[t][s2] = a; s_P[t][s2] = p; }
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // 5. D = S0 X^T on the tensor core (high part, then low part accumulated)
+  if (tid == 0) {
+    constexpr uint32_t idesc = tc::idesc_bf16<128, 16>();
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(smem + kS0, K, ks), tc::kmajor_desc(smem + kXH, K, ks),
+                   idesc, ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks)
+      tc::mma_bf16(taddr, tc::kmajor_desc(smem + kS0, K, ks), tc::kmajor_desc(smem + kXL, K, ks),
+                   idesc, true);
+    tc::mma_commit(&s_bar);
+  }
+  bool ok = true;
+  if (warp < 4) {
+    ok = mbar_wait(&s_bar, 0);
+    tc::fence_after_sync();
+  }
+  ok = __syncthreads_and(ok);
+  // 6. row v = tid (warps 0-3, their own lane quadrant): a_t, b_t; the triangular solve
+  //    d_t = beta_t (v_t - a_t - sum_{s<t} A[t][s] d_s), o_t = b_t + sum_{s<=t} P[t][s] d_s
+  if (ok && warp < 4) {
+    float dv[16];
+    tc::tmem_ld16(tc::tmem_addr(taddr, 32 * warp, 0), dv);
+    const int v = tid;
+    float d[TS];
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      d[t] = 0.f;
+      if (t < T) {
+        float u = dv[t];
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) u = fmaf(s_A[t][s2], d[s2], u);
+        d[t] = s_b[t] * (sy[t * CH + 2 * K + v] - u);
+        float o = fmaf(s_kq[t], d[t], dv[8 + t]);
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) o = fmaf(s_P[t][s2], d[s2], o);
+        static_cast<bf16_t *>(rv.d)[ent(t) * V + v] = __float2bfloat16_rn(d[t]);
+        out[(((size_t)b * T + t) * H + h) * V + v] = from_f32<IO>(o);
+      }
+    }
+  } else if (!ok && tid == 0) {
+    flag_error(pv.err, RSC_DEVERR_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(taddr, 32);
+}
+
+template <typename IO, int GATE>
+static int launch_replay_verify_tc(const LayerArgs &a, const RingView &rv, const int32_t *slots,
+                                   const int32_t *pos, int B, int T, void *spec_conv,
+                                   const void *qkv, const float *conv_w, const float *g,
+                                   const float *beta, void *out, cudaStream_t s) {
+  auto kern = kda_replay_verify_tc_kernel<IO, GATE>;
+  static PerDeviceFlag attr;
+  const int rc = once_per_device(attr, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)rtc::kSmem) == cudaSuccess ? RSC_OK : RSC_ECUDA;
+  });
+  if (rc != RSC_OK) return rc;
+  kern<<<dim3(a.pv.H, B), rtc::NT, rtc::kSmem, s>>>(
+      a.pv, a.layer, slots, T, static_cast<IO *>(spec_conv), static_cast<const IO *>(qkv),
+      conv_w, g, beta, static_cast<IO *>(out), rv, pos);
+  return launch_status();
+}
+
 template <typename ST, typename IO, int K, int V, int GATE>
 struct ReplayVerifyLaunch {
   static int run(const LayerArgs *a, const RingView *rv, const int32_t *slots, const int32_t *pos,
@@ -538,6 +811,18 @@ int launch_replay_verify(const LayerArgs &a, const RingView &rv, const int32_t *
                          const int32_t *pos, int B, int T, void *spec_conv, const void *qkv,
                          const float *conv_w, const float *g, const float *beta, void *out,
                          cudaStream_t s) {
+  if (a.st == RSC_BF16 && a.pv.K == 128 && a.pv.V == 128 && T >= 1 && T <= rtc::TS) {
+    const bool kda = a.gate == RSC_GATE_KDA;
+    if (a.io == RSC_BF16)
+      return kda ? launch_replay_verify_tc<bf16, RSC_GATE_KDA>(a, rv, slots, pos, B, T, spec_conv,
+                                                               qkv, conv_w, g, beta, out, s)
+                 : launch_replay_verify_tc<bf16, RSC_GATE_GDN>(a, rv, slots, pos, B, T, spec_conv,
+                                                               qkv, conv_w, g, beta, out, s);
+    return kda ? launch_replay_verify_tc<float, RSC_GATE_KDA>(a, rv, slots, pos, B, T, spec_conv,
+                                                              qkv, conv_w, g, beta, out, s)
+               : launch_replay_verify_tc<float, RSC_GATE_GDN>(a, rv, slots, pos, B, T, spec_conv,
+                                                              qkv, conv_w, g, beta, out, s);
+  }
   return dispatch_all<ReplayVerifyLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, &rv, slots,
                                           pos, B, T, spec_conv, qkv, conv_w, g, beta, out, s);
 }

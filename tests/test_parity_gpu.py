@@ -443,6 +443,7 @@ def _rings_np(rings):
     (1, 1, rsc.GDN, 128, 128, 5, 16), (0, 1, rsc.KDA, 128, 64, 5, 16),
     (1, 0, rsc.KDA, 64, 128, 5, 16),
     (1, 1, rsc.KDA, 128, 128, 8, 16),   # one full block of eight tokens
+    (1, 0, rsc.KDA, 128, 128, 7, 16),   # fp32 io on the tensor-core verify
     (0, 0, rsc.KDA, 128, 128, 11, 32),  # a full block, then three tokens from its end state
     (1, 1, rsc.GDN, 64, 64, 16, 32),    # two full blocks
 ])
