@@ -582,13 +582,10 @@ kda_replay_verify_tc_kernel(PoolView pv, int layer, const int32_t *__restrict__ 
   if (tid == 0) mbar_init(&s_bar, 1);
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 32); tc::tmem_relinquish(); }
 
-  // 1. copies: the slot's tile into the operand layout (8 lanes with the same 16-byte column
-  //    take 8 consecutive rows: distinct bank groups), the block's raw inputs, gates, betas
-  const bf16_t *Sg = reinterpret_cast<const bf16_t *>(pv.ssm) + (prow * H + h) * (size_t)V * K;
-  for (int i = tid; i < V * K / 8; i += NT) {
-    const int v = ((i >> 7) << 3) | (i & 7), kc = (i >> 3) & 15;
-    cp_async16(smem + kS0 + tc::kmajor_offset(v, 8 * kc, K), Sg + (size_t)v * K + 8 * kc);
-  }
+  // 1. copies in two groups: the block's raw inputs, gates and betas (waited for before the
+  //    conv), then the slot's tile into the operand layout (8 lanes with the same 16-byte
+  //    column take 8 consecutive rows: distinct bank groups), waited for only before the
+  //    product, so its latency hides behind the conv, the norms and the coefficients
   for (int i = tid; i < T * (CH / XV); i += NT) {
     const int t = i / (CH / XV), c = (i % (CH / XV)) * XV;
     cp_async16(sx + t * CH + c, qkv + ((size_t)b * T + t) * D + col(c));
@@ -603,6 +600,12 @@ kda_replay_verify_tc_kernel(PoolView pv, int layer, const int32_t *__restrict__ 
   }
   if (tid < T) cp_async4(&s_b[tid], beta + ((size_t)b * T + tid) * H + h);
   cp_async_commit();
+  const bf16_t *Sg = reinterpret_cast<const bf16_t *>(pv.ssm) + (prow * H + h) * (size_t)V * K;
+  for (int i = tid; i < V * K / 8; i += NT) {
+    const int v = ((i >> 7) << 3) | (i & 7), kc = (i >> 3) & 15;
+    cp_async16(smem + kS0 + tc::kmajor_offset(v, 8 * kc, K), Sg + (size_t)v * K + 8 * kc);
+  }
+  cp_async_commit();
   // taps and window rows of this thread's channels (tid, and tid + 256 below 384)
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + prow * 3 * (size_t)D;
   float4 wt[2];
@@ -616,8 +619,7 @@ kda_replay_verify_tc_kernel(PoolView pv, int layer, const int32_t *__restrict__ 
       win[u][0] = W[cc]; win[u][1] = W[D + cc]; win[u][2] = W[2 * D + cc];
     }
   }
-  cp_async_wait_all();
-  tc::fence_smem_to_async();  // the tile is read by the tensor core
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // the inputs (the tile may be in flight)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -718,7 +720,8 @@ kda_replay_verify_tc_kernel(PoolView pv, int layer, const int32_t *__restrict__ 
     p = group_sum<32>(p);
     if (lane == 0) { s_A[t][s2] = a; s_P[t][s2] = p; }
   }
-  tc::fence_smem_to_async();
+  cp_async_wait_all();        // this thread's pieces of the tile
+  tc::fence_smem_to_async();  // the tile and X are read by the tensor core
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
