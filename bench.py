@@ -407,7 +407,7 @@ def leg_copy(dev, peaks, stream, wl):
     row = wl.H * wl.V * wl.K * ss + 3 * wl.D * io
     nbytes = 2 * row * wl.layers * 64
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"config": "64 pairs x 69 layers of the decode pool, one launch pair",
+    return {"config": "64 pairs x 69 layers of the decode pool, one launch",
             "ms": round(ms, 4), "bytes": nbytes, "hbm_gbs": round(gbs, 1),
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 

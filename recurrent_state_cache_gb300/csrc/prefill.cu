@@ -282,18 +282,6 @@ int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t 
   return launch_status();
 }
 
-int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
-                          int T, const uint8_t *has_init, const void *qkv, cudaStream_t s) {
-  const dim3 grid((a.pv.D + 127) / 128, N);
-  if (a.io == RSC_BF16)
-    prefill_window_kernel<bf16><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
-                                                     static_cast<const bf16 *>(qkv));
-  else
-    prefill_window_kernel<float><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
-                                                      static_cast<const float *>(qkv));
-  return launch_status();
-}
-
 static bool use_tc(const PoolView &pv, int st) { return st == RSC_BF16 && pv.K == 128; }
 
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T) {
@@ -313,10 +301,9 @@ int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_s
                                  out, ws, s);
   int32_t *chunk_base = static_cast<int32_t *>(ws);
   char *blocks = static_cast<char *>(ws) + align256((size_t)(N + 1) * 4);
-  int rc = launch_prefill_tc(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta, out,
-                             chunk_base, blocks, s);
-  if (rc != RSC_OK) return rc;
-  return launch_prefill_window(a, slots, cu_seqlens, N, T, has_init, qkv, s);
+  // the tensor-core path writes the windows in its state pass
+  return launch_prefill_tc(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta, out,
+                           chunk_base, blocks, s);
 }
 
 }  // namespace rsc

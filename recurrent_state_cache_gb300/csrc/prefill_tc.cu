@@ -38,8 +38,8 @@
 //                chunk one MMA Z S0^T (Z the A operand in tensor memory), then the state
 //                update; S0 of every chunk goes to the chunk's block.  Operand blocks arrive
 //                by TMA bulk copies three chunks ahead.
+//                The state pass also writes the slot's new conv window.
 //   output       grid (chunk, head): O = E S0^T + F, one MMA per chunk and head.
-//   window       prefill.cu's window kernel.
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 #include "rsc_tc.cuh"
@@ -1037,7 +1037,8 @@ template <typename IO, int V>
 __global__ void __launch_bounds__(kStateThreads)
 prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                         const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_base,
-                        int T, const uint8_t *__restrict__ has_init, char *__restrict__ blocks) {
+                        int T, const uint8_t *__restrict__ has_init, char *__restrict__ blocks,
+                        const IO *__restrict__ qkv) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_lbar[kNBuf];  // a buffer's operand block landed
@@ -1059,6 +1060,30 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
   bf16 *Sg = reinterpret_cast<bf16 *>(pv.ssm) + ((prow * H + h) * V + (size_t)vt * kVT) * kK;
   auto block = [&](int c) { return blocks + ((size_t)(chunk_base[n] + c) * H + h) * kBlockBytes; };
+
+  // The slot's window after the sequence: the last three raw inputs (rows before the
+  // sequence's start come from the old window, or zero for a fresh sequence).  The chunk
+  // kernel, which read the old window, has completed; this tile writes CHT of the head's
+  // window channels (thread t: channel vt * CHT + t), the new rows requested now and stored
+  // at the end.
+  constexpr int CH = 2 * kK + V, CHT = CH / (V / kVT);
+  static_assert(CHT <= kStateThreads, "a window channel per thread");
+  IO *Wn = reinterpret_cast<IO *>(pv.conv) + prow * 3 * (size_t)pv.D;
+  IO wnew[3];
+  int wcol = -1;
+  if (tid < CHT) {
+    const int c = vt * CHT + tid;
+    wcol = c < kK ? h * kK + c : c < 2 * kK ? H * kK + h * kK + (c - kK) : 2 * H * kK + h * V + (c - 2 * kK);
+    const int len = end - start;
+    IO old[3];
+#pragma unroll
+    for (int m = 0; m < 3; ++m) old[m] = init ? Wn[(size_t)m * pv.D + wcol] : from_f32<IO>(0.f);
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const int pp = len - 3 + m;
+      wnew[m] = pp >= 0 ? qkv[(size_t)(start + pp) * pv.D + wcol] : old[3 + pp];
+    }
+  }
 
   const bool owner = tid < kK;      // warps 0-3: thread k holds column k of the state tile
   const bool issuer = tid == kK;    // warp 4, lane 0: products and operand copies
@@ -1202,6 +1227,10 @@ prefill_tc_state_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 #pragma unroll
     for (int v = 0; v < kVT; ++v) Sg[(size_t)v * kK + tid] = __float2bfloat16_rn(S[v]);
   }
+  if (wcol >= 0) {
+#pragma unroll
+    for (int m = 0; m < 3; ++m) Wn[(size_t)m * pv.D + wcol] = wnew[m];
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tDZ, 256);
@@ -1315,8 +1344,8 @@ static int launch_tc_v(const LayerArgs &a, const int32_t *slots, const int32_t *
                                                           conv_w, g, beta, blocks);
     if (launch_status() != RSC_OK) return RSC_ECUDA;
   }
-  state_kernel<<<dim3(V / kVT, a.pv.H, N), kStateThreads, kStateSmem, s>>>(a.pv, a.layer, slots, cu,
-                                                                   chunk_base, T, has_init, blocks);
+  state_kernel<<<dim3(V / kVT, a.pv.H, N), kStateThreads, kStateSmem, s>>>(
+      a.pv, a.layer, slots, cu, chunk_base, T, has_init, blocks, static_cast<const IO *>(qkv));
   if (launch_status() != RSC_OK) return RSC_ECUDA;
   if (cap > 0 && T > 0)
     out_kernel<<<dim3(cap, a.pv.H), 128, kOutSmem, s>>>(a.pv, slots, cu, chunk_base, N, blocks,
