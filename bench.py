@@ -50,7 +50,7 @@ DECODE_SOURCES = ("decode.cu", "rsc_step.cuh", "rsc_common.cuh")
 # Layers per host<->device copy in the end-to-end step (fewer, larger copies against a finer
 # overlap of copies and compute).
 E2E_GROUP = 8
-CAPTURED_DECODE_TRAFFIC = {"3f787822c76e207d": 28_080_384}
+CAPTURED_DECODE_TRAFFIC = {"3f787822c76e207d": 28_088_320}
 
 
 # --------------------------------------------------------------------------- plumbing
