@@ -222,13 +222,13 @@ __device__ __forceinline__ void inverse_stage(float *sA, float *sSt, unsigned ch
 // One lane's row rr of A (rows < 64 of the product) or of P, columns j0 .. j0+N-1, from N
 // accumulator values d.  A: beta_r x value below the diagonal, fp32 rows of sA; P: the value
 // on and below the diagonal of a live row, bf16 K-major.  In a block beyond kDiagSpread
-// (rwide) the row's own-block entries come from the exact values in fb.
+// (WIDE) the row's own-block entries come from the exact values in fb.
 struct ApRow {
   int rr, rb;
   bool isP, rwide, live;
   float br;
 };
-template <int N>
+template <int N, bool WIDE>
 __device__ __forceinline__ void ap_emit(const float *d, int j0, const ApRow &w, const float *fb,
                                         float *sA, unsigned char *sPP) {
 #pragma unroll
@@ -238,10 +238,12 @@ __device__ __forceinline__ void ap_emit(const float *d, int j0, const ApRow &w, 
     for (int e = 0; e < 8; ++e) {
       const int j = j0 + 8 * g8 + e;
       float x = d[8 * g8 + e];
-      if (w.rwide && (j >> 4) == w.rb && j <= w.rr) {
-        const int r = w.rr & 15, c = j & 15;
-        x = w.isP ? fb[w.rb * 256 + 120 + r * (r + 1) / 2 + c]
-                  : (c < r ? fb[w.rb * 256 + r * (r - 1) / 2 + c] : 0.f);
+      if constexpr (WIDE) {
+        if ((j >> 4) == w.rb && j <= w.rr) {
+          const int r = w.rr & 15, c = j & 15;
+          x = w.isP ? fb[w.rb * 256 + 120 + r * (r + 1) / 2 + c]
+                    : (c < r ? fb[w.rb * 256 + r * (r - 1) / 2 + c] : 0.f);
+        }
       }
       v[e] = w.isP ? (j <= w.rr && w.live ? x : 0.f) : (j < w.rr ? w.br * x : 0.f);
     }
@@ -822,7 +824,12 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
 #pragma unroll
         for (int e = 0; e < 16; ++e) d[e] = 0.f;
       }
-      if (have || w.isP) ap_emit<16>(d, 16 * cidx, w, fb, sA, sPP);
+      if (have || w.isP) {
+        // the exact diagonal values only in a block beyond kDiagSpread (warp-uniform), so the
+        // common path never touches them
+        if (w.rwide) ap_emit<16, true>(d, 16 * cidx, w, fb, sA, sPP);
+        else ap_emit<16, false>(d, 16 * cidx, w, fb, sA, sPP);
+      }
     }
   }
   tc::fence_before_sync();
