@@ -554,6 +554,48 @@ def test_prefill_parity(cuda_dev, st, io, gate, K, V, lens, init):
     c.check_pool(tc=tc)
 
 
+@pytest.mark.parametrize("gate,V", [(rsc.KDA, 128), (rsc.GDN, 64)])
+def test_prefill_many_packed_sequences(cuda_dev, gate, V):
+    """The tensor-core path over 24 packed sequences: empty ones (fresh and continued), single
+    tokens, exact multiples of the 64-token chunk, ragged tails; every output, state and
+    window against the oracle (the windows written by the state pass, bit for bit)."""
+    H, K = 2, 128
+    c = Case(cuda_dev, 14, L=1, P=30, H=H, K=K, V=V, st=1, io=1, gate=gate)
+    lens = [0, 1, 64, 0, 2, 3, 128, 65, 17, 0, 191, 64, 1, 5, 250, 63, 0, 33, 129, 2, 70, 3, 0, 96]
+    init = [1, 0, 1, 0, 1, 0, 1, 1, 0, 1, 0, 1, 0, 1, 1, 0, 1, 1, 0, 1, 0, 1, 1, 0]
+    N = len(lens)
+    slots = inputs.distinct_slots(c.r, N, 30)
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    x = c.proj((T,))
+    g, beta = c.gates((T,))
+    hi = np.uint8(init)
+    o_ref = oracle.prefill(c.ref, 0, slots, cu, x, c.w, g, beta, has_init=hi)
+    o = rsc.kda_prefill_chunk(c.pool, 0, to_dev(slots, c.dev), to_dev(cu, c.dev),
+                              to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                              has_initial_state=to_dev(hi, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref), tc=True) <= TOL[1]
+    c.check_pool(tc=True)
+
+
+@pytest.mark.parametrize("st,K", [(1, 128), (0, 64)])
+def test_prefill_call_of_empty_sequences(cuda_dev, st, K):
+    """A call whose sequences are all empty (zero tokens): fresh ones get a zero state and
+    window, continued ones keep theirs; the rest of the pool is untouched."""
+    c = Case(cuda_dev, 15, L=1, P=6, H=2, K=K, V=64, st=st, io=st, gate=rsc.KDA)
+    lens, init = [0, 0, 0], [1, 0, 1]
+    slots = np.int32([4, 1, 6])
+    cu = inputs.cu_seqlens(lens)
+    x = c.proj((0,))
+    g, beta = c.gates((0,))
+    hi = np.uint8(init)
+    oracle.prefill(c.ref, 0, slots, cu, x, c.w, g, beta, has_init=hi)
+    rsc.kda_prefill_chunk(c.pool, 0, to_dev(slots, c.dev), to_dev(cu, c.dev), to_dev(x, c.dev),
+                          c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                          has_initial_state=to_dev(hi, c.dev))
+    c.check_pool(tc=st == 1 and K == 128)
+
+
 def test_prefill_bad_cu_seqlens_flags(cuda_dev):
     c = Case(cuda_dev, 9, L=1, P=4, H=1, K=64, V=64, st=0, io=0, gate=rsc.KDA)
     x = c.proj((10,))
