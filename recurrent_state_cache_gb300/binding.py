@@ -138,21 +138,35 @@ def _check(rc: int, what: str):
         raise RscError(rc, what)
 
 
+# The per-call marshalling below runs once per library call, so it keeps to cheap operations:
+# raw pointers and stream handles as plain ints (the argtypes convert them), device checks by
+# index.  Every check of the argument still happens.
+
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+# torch's current stream of a device as its raw handle, without building a Stream object
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream, pool):
-    """The call's stream: `stream`, else the current torch stream of the pool's device."""
-    s = stream if stream is not None else torch.cuda.current_stream(pool.device)
-    if s.device != pool.device:
-        raise ValueError(f"stream on {s.device}, the pool is on {pool.device}")
-    return ctypes.c_void_p(s.cuda_stream)
+    """The call's stream (raw handle): `stream`, else the current torch stream of the pool's
+    device."""
+    if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(pool.device.index)
+        stream = torch.cuda.current_stream(pool.device)
+    if stream.device != pool.device:
+        raise ValueError(f"stream on {stream.device}, the pool is on {pool.device}")
+    return stream.cuda_stream
 
 
 class _on:
     """Makes the pool's device current for one library call (the library launches on the
     current device and rejects a pool held by another one)."""
+
+    __slots__ = ("dev", "prev")
 
     def __init__(self, pool):
         self.dev = pool.device.index
@@ -170,11 +184,11 @@ class _on:
 
 
 def _need(t, name, dtype, shape, device):
-    if t.dtype != dtype:
+    if t.dtype is not dtype:
         raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
-    if t.device != device:
+    if t.get_device() != device.index:
         raise ValueError(f"{name}: on {t.device}, expected {device}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
