@@ -49,7 +49,23 @@ HEADLINE_METRIC = "decode tokens/s per layer and achieved HBM GB/s (% of peak); 
 DECODE_SOURCES = ("decode.cu", "rsc_step.cuh", "rsc_common.cuh")
 # Layers per host<->device copy in the end-to-end step (fewer, larger copies against a finer
 # overlap of copies and compute).
-E2E_GROUP = 8
+E2E_GROUP = 16
+
+
+def e2e_bounds(layers: int, mid: int = E2E_GROUP) -> list:
+    """Group boundaries of the end-to-end step: small groups first (nothing hides the first
+    input copy), then `mid`-layer groups, then a short and a 2-layer group (nothing hides the
+    last output copy).  69 layers: [0, 2, 6, 14, 30, 46, 62, 67, 69]."""
+    b = [0]
+    for s in (2, 4, 8):
+        if b[-1] + s < layers - 7:
+            b.append(b[-1] + s)
+    while b[-1] + mid <= layers - 7:
+        b.append(b[-1] + mid)
+    if b[-1] < layers - 2:
+        b.append(layers - 2)
+    b.append(layers)
+    return b
 CAPTURED_DECODE_TRAFFIC = {"3f787822c76e207d": 28_088_320}
 
 
@@ -814,16 +830,16 @@ def main(argv=None):
     ev_in = [torch.cuda.Event() for _ in range(wl.layers)]
     ev_out = [torch.cuda.Event() for _ in range(wl.layers)]
 
-    def e2e_step(group=E2E_GROUP):
-        # pipelined by groups of layers: a group's inputs arrive while the previous group
-        # computes, and its outputs leave while the next one computes; every stream joins back
-        # before the step ends
+    def e2e_step():
+        # pipelined by groups of layers (e2e_bounds): a group's inputs arrive while the previous
+        # group computes, and its outputs leave while the next one computes; every stream joins
+        # back before the step ends
         cur = torch.cuda.current_stream()
         fork = torch.cuda.Event()
         fork.record(cur)
         cin.wait_event(fork)
         cout.wait_event(fork)
-        bounds = list(range(0, wl.layers, group)) + [wl.layers]
+        bounds = e2e_bounds(wl.layers)
         with torch.cuda.stream(cin):
             for i in range(len(bounds) - 1):
                 a, z = bounds[i], bounds[i + 1]
@@ -927,7 +943,7 @@ def main(argv=None):
         "e2e": {"value": round(sum_over_ranks(units, dist, dev) / (ms_e2e * 1e-3), 1),
                 "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "per step: pinned host->device copies of every layer's qkv, g, beta (packed per layer, one copy per group of layers), "
+                "how": "per step: pinned host->device copies of every layer's qkv, g, beta (packed per layer, one copy per group of layers: 2, 4, 8, then 16-layer groups, then 5 and 2), "
                        "the kda_decode_step_overlap calls, device->host copies of every layer's output, "
                        "overlapped layer by layer on a copy-in, a compute and a copy-out stream; "
                        "captured once in a CUDA graph and replayed",

@@ -37,3 +37,11 @@ def test_traffic_is_keyed_by_the_current_decode_sources():
     # the roofline traffic is reported only for the decode kernel the counters came from
     assert bench.decode_source_hash() in bench.CAPTURED_DECODE_TRAFFIC
     assert all(v > 27_000_000 for v in bench.CAPTURED_DECODE_TRAFFIC.values())
+
+
+def test_end_to_end_groups_cover_every_layer_once():
+    assert bench.e2e_bounds(69) == [0, 2, 6, 14, 30, 46, 62, 67, 69]
+    for layers in (1, 2, 7, 8, 9, 16, 48, 69, 100):
+        b = bench.e2e_bounds(layers)
+        assert b[0] == 0 and b[-1] == layers
+        assert all(x < y for x, y in zip(b, b[1:])), (layers, b)
