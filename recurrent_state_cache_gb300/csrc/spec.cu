@@ -874,6 +874,30 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
   auto ent = [&](int t) { return (prow * H + h) * (size_t)rv.depth + ((p0 + t) & (rv.depth - 1)); };
   const int n = acc + 1;  // tokens to replay
 
+  // the records of tokens t0 .. t0 + cnt - 1 into shared memory (cp.async, one group)
+  auto stage = [&](int t0, int cnt) {
+    for (int i = tid; i < cnt * (K / XS); i += NT) {
+      const int tau = i / (K / XS), c = (i % (K / XS)) * XS;
+      cp_async16(&s_rk[tau][c], static_cast<const ST *>(rv.rawk) + ent(t0 + tau) * K + c);
+    }
+    for (int i = tid; i < cnt * (VT / XS); i += NT) {
+      const int tau = i / (VT / XS), c = (i % (VT / XS)) * XS;
+      cp_async16(&s_rv[tau][c], static_cast<const ST *>(rv.rawv) + ent(t0 + tau) * V + (size_t)j * VT + c);
+    }
+    if (GATE == RSC_GATE_KDA) {
+      for (int i = tid; i < cnt * (K / 4); i += NT) {
+        const int tau = i / (K / 4), c = (i % (K / 4)) * 4;
+        cp_async16(&s_g[tau][c], rv.g + ent(t0 + tau) * K + c);
+      }
+    } else if (tid < cnt) {
+      cp_async4(&s_g[tid][0], rv.g + ent(t0 + tid));
+    }
+    if (tid < cnt) cp_async4(&s_b[tid], rv.beta + ent(t0 + tid));
+    cp_async_commit();
+  };
+  // the first block's records are requested before the state tile, which is needed only
+  // after their norms: the two latencies overlap
+  stage(0, min(TS, n));
   ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
   Tile2<ST, K, VT, NW, VPL> s;
   tile_load2<ST, K, VT, VPL, NW>(S, s);
@@ -899,25 +923,10 @@ kda_replay_commit_kernel(PoolView pv, RingView rv, int layer, const int32_t *__r
 
   for (int t0 = 0; t0 < n; t0 += TS) {
     const int cnt = min(TS, n - t0);
-    __syncthreads();  // the previous block's readers are done
-    for (int i = tid; i < cnt * (K / XS); i += NT) {
-      const int tau = i / (K / XS), c = (i % (K / XS)) * XS;
-      cp_async16(&s_rk[tau][c], static_cast<const ST *>(rv.rawk) + ent(t0 + tau) * K + c);
+    if (t0 > 0) {
+      __syncthreads();  // the previous block's readers are done
+      stage(t0, cnt);
     }
-    for (int i = tid; i < cnt * (VT / XS); i += NT) {
-      const int tau = i / (VT / XS), c = (i % (VT / XS)) * XS;
-      cp_async16(&s_rv[tau][c], static_cast<const ST *>(rv.rawv) + ent(t0 + tau) * V + (size_t)j * VT + c);
-    }
-    if (GATE == RSC_GATE_KDA) {
-      for (int i = tid; i < cnt * (K / 4); i += NT) {
-        const int tau = i / (K / 4), c = (i % (K / 4)) * 4;
-        cp_async16(&s_g[tau][c], rv.g + ent(t0 + tau) * K + c);
-      }
-    } else if (tid < cnt) {
-      cp_async4(&s_g[tid][0], rv.g + ent(t0 + tid));
-    }
-    if (tid < cnt) cp_async4(&s_b[tid], rv.beta + ent(t0 + tid));
-    cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
     // normalised keys (a warp per token), alpha = exp(g), value rows to fp32
