@@ -17,7 +17,8 @@
 //              rounded once to the state dtype and written back.
 //   window     grid (channel block, sequence): the slot's window becomes the last three
 //              raw inputs of the sequence (fewer than three tokens shift the old window).
-// This is the exact fp32 recurrence; it is the path of fp32-state pools.
+// This is the exact fp32 recurrence; it is the path of pools with head_k 64 (fp32-state
+// pools with head_k 128 take the same recurrence eight tokens at a time, prefill_blocked.cu).
 #include "rsc_internal.h"
 #include "rsc_step.cuh"
 
@@ -250,6 +251,18 @@ struct PrefillSerialLaunch {
   }
 };
 
+int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                          int T, const uint8_t *has_init, const void *qkv, cudaStream_t s) {
+  const dim3 grid((a.pv.D + 127) / 128, N);
+  if (a.io == RSC_BF16)
+    prefill_window_kernel<bf16><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
+                                                     static_cast<const bf16 *>(qkv));
+  else
+    prefill_window_kernel<float><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, T, has_init,
+                                                      static_cast<const float *>(qkv));
+  return launch_status();
+}
+
 int launch_prefill_serial(const LayerArgs &a, const int32_t *slots, const int32_t *cu,
                           int N, int T, const uint8_t *has_init, const void *qkv,
                           const float *conv_w, const float *g, const float *beta,
@@ -283,11 +296,13 @@ int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t 
 }
 
 static bool use_tc(const PoolView &pv, int st) { return st == RSC_BF16 && pv.K == 128; }
+static bool use_blocked(const PoolView &pv, int st) { return st == RSC_F32 && pv.K == 128; }
 
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T) {
   if (use_tc(pv, st))
     return align256((size_t)(N + 1) * 4) +
            prefill_tc_chunk_capacity(N, T) * (size_t)pv.H * prefill_tc_block_bytes();
+  if (use_blocked(pv, st)) return prefill_blocked_bytes(pv, T);
   return prefill_prep_bytes(pv, T);
 }
 
@@ -296,6 +311,9 @@ int launch_prefill(const LayerArgs &a, const int32_t *slots, const int32_t *cu_s
                    const float *conv_w, const float *g, const float *beta, void *out,
                    void *ws, size_t ws_bytes, cudaStream_t s) {
   if (ws_bytes < prefill_workspace_bytes(a.pv, a.st, N, T)) return RSC_ENOSPACE;
+  if (use_blocked(a.pv, a.st))
+    return launch_prefill_blocked(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta,
+                                  out, ws, s);
   if (!use_tc(a.pv, a.st))
     return launch_prefill_serial(a, slots, cu_seqlens, N, T, has_init, qkv, conv_w, g, beta,
                                  out, ws, s);

@@ -1,0 +1,501 @@
+// prefill_blocked.cu -- prefill of fp32-state pools with head_k 128: the exact recurrence
+// taken eight tokens at a time in closed form.
+//
+// Sources: "SGLang之KV Cache内存池机制" §8.5 forward_extend (each sequence starts from its
+// slot's state or from zero, the final state goes back to the slot; sequences packed by
+// cu_seqlens) and "SGLang Qwen3/kimi-k3 Hybrid Linear Mamba KV cache管理", ReplaySSM section
+// (the recurrence over several tokens unrolled into one closed form from the first state).
+//
+// The closed form.  Within a block of tokens 0..c-1 of one sequence, with S0 the state
+// before the block and Gam_t the cumulative log-decay from the block start up to and
+// including token t (per key channel for KDA, per head for GDN):
+//   S_{t-1} Diag(alpha_t) = S0 Diag(e^Gam_t) + sum_{s<t} d_s (k_s . e^(Gam_t - Gam_s))^T
+// so every state row's u_t = a_t + sum_{s<t} A[t][s] d_s and o_t = b_t + sum_{s<=t} P[t][s] d_s
+// with a_t = S0 (k_t . e^Gam_t), b_t = S0 (q_t . e^Gam_t), A[t][s] = sum_k k_s k_t e^(Gam_t - Gam_s)
+// and P[t][s] = sum_k k_s q_t e^(Gam_t - Gam_s); d_t = beta_t (v_t - u_t) is then a forward
+// substitution, and S_end = S0 Diag(e^Gam_end) + sum_s d_s (k_s . e^(Gam_end - Gam_s))^T.
+// This is exact algebra: the result is the token-by-token recurrence up to rounding order.
+//
+// Three launches:
+//   blk        grid (block, head): conv and L2 norms of the block's tokens, then its scaled
+//              keys and queries, the end-scaled keys, e^Gam_end and the A / P rows.  The
+//              2 x 36 sums over channels are one butterfly reduce-scatter per warp and a
+//              4-warp add.
+//   recurrent  grid (row tile, head, sequence): S in registers across the sequence; per
+//              block the 16 row dots of every row (one butterfly reduce-scatter: 16 shuffles
+//              where the token loop spends 80), the 8x8 forward substitution, the outputs
+//              and the block-end state.  Block operands are staged one block ahead by
+//              cp.async, double-buffered.
+//   window     (prefill.cu) the slot's window becomes the sequence's last three inputs.
+// Blocks start at each sequence start, so a sequence of n tokens has ceil(n / 8) blocks;
+// block b of the grid belongs to the last sequence i with cu[i] / 8 + i <= b (these bases are
+// strictly increasing and leave room for every block of each sequence).
+#include "rsc_internal.h"
+#include "rsc_step.cuh"
+
+namespace rsc {
+
+namespace {
+
+constexpr int TS = 8;      // tokens per block
+constexpr int KB = 128;    // head_k of the blocked form
+constexpr int NCO = 16;    // per token: its A row (8), then its P row (8)
+constexpr float kMaxRise = 80.f;  // largest growth of a log gate within a block
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct BlockedWs {
+  float *ke;  // [T][H][K]  k_hat_t . e^(Gam_end - Gam_t)
+  float *eg;  // [T][H][K]  e^Gam_end, in the row of the block's first token
+  float *co;  // [T][H][16] A row, P row of the token within its block
+};
+
+BlockedWs blocked_carve(void *ws, const PoolView &pv, int T) {
+  char *p = static_cast<char *>(ws) + prefill_prep_bytes(pv, T);
+  const size_t nk = align256((size_t)T * pv.H * KB * 4);
+  BlockedWs b;
+  b.ke = reinterpret_cast<float *>(p);
+  b.eg = reinterpret_cast<float *>(p + nk);
+  b.co = reinterpret_cast<float *>(p + 2 * nk);
+  return b;
+}
+
+// Pair indices of the 64 coefficient sums: A[t][s] (s < t) at t(t-1)/2 + s, then P[t][s]
+// (s <= t) at 28 + t(t+1)/2 + s.
+__host__ __device__ constexpr int ia(int t, int s) { return t * (t - 1) / 2 + s; }
+__host__ __device__ constexpr int ip(int t, int s) { return 28 + t * (t + 1) / 2 + s; }
+
+// Per (block, head): the conv of the head's q / k / v channels over the block's tokens (one
+// thread per key channel, also owning value channel k when k < V), the L2 norms of q and k,
+// then the block's operands.  A thread reads its channels' 11 inputs once (3 before the
+// block: the sequence, the slot's window before the sequence start, or zero for a fresh
+// sequence) where a conv per token would read 32.
+template <typename IO, int V, int GATE>
+__global__ void __launch_bounds__(128)
+prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
+                   const int32_t *__restrict__ cu, int N, int T,
+                   const uint8_t *__restrict__ has_init, const IO *__restrict__ qkv,
+                   const float *__restrict__ conv_w, PrefillWs w, BlockedWs bw,
+                   const float *__restrict__ g) {
+  static_assert(V <= KB, "a thread per key channel covers the value channels");
+  __shared__ float red[4][64];
+  __shared__ float nrm[2 * TS];  // 1/|q_t|, 1/|k_t|
+  const int b = blockIdx.x, h = blockIdx.y, k = threadIdx.x, lane = k & 31, warp = k >> 5;
+  const int H = pv.H, D = pv.D;
+  if (b == 0 && h == 0 && k == 0 && (cu[0] != 0 || cu[N] != T)) flag_error(pv.err, RSC_DEVERR_SEQ);
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] / TS + mid <= b) lo = mid; else hi = mid - 1;
+  }
+  const int start = cu[lo], end = cu[lo + 1];
+  if (start < 0 || end < start || end > T) return;  // flagged by the recurrence
+  const int t0 = start + TS * (b - (start / TS + lo));
+  if (t0 < start || t0 >= end) return;
+  const int cnt = min(TS, end - t0);
+  const int slot = slots[lo];
+  if (slot < 0 || slot > pv.P) return;  // flagged by the recurrence
+  const bool init = has_init == nullptr || has_init[lo] != 0;
+  const IO *W = reinterpret_cast<const IO *>(pv.conv) + ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
+
+  auto conv_rows = [&](int c, float (&y)[TS]) {
+    float x[TS + 3];  // inputs at tokens t0 - 3 .. t0 + 7 (oldest first)
+#pragma unroll
+    for (int i = 0; i < TS + 3; ++i) {
+      const int pos = t0 - start + i - 3;  // position within the sequence
+      x[i] = 0.f;
+      if (i < cnt + 3)
+        x[i] = pos >= 0 ? to_f32(qkv[(size_t)(start + pos) * D + c])
+                        : (init ? to_f32(W[(size_t)(3 + pos) * D + c]) : 0.f);
+    }
+    const float4 wc = *reinterpret_cast<const float4 *>(conv_w + 4 * (size_t)c);
+#pragma unroll
+    for (int t = 0; t < TS; ++t) y[t] = t < cnt ? conv4(wc, x[t], x[t + 1], x[t + 2], x[t + 3]) : 0.f;
+  };
+  float q[TS], kk[TS];
+  conv_rows(h * KB + k, q);
+  conv_rows(H * KB + h * KB + k, kk);
+  if (k < V) {
+    float y[TS];
+    conv_rows(2 * H * KB + h * V + k, y);
+#pragma unroll
+    for (int t = 0; t < TS; ++t)
+      if (t < cnt) w.v[((size_t)(t0 + t) * H + h) * V + k] = y[t];
+  }
+  {
+    float part[32];  // |q_t|^2, then |k_t|^2, summed over the head's channels
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      part[t] = q[t] * q[t];
+      part[TS + t] = kk[t] * kk[t];
+    }
+#pragma unroll
+    for (int i = 2 * TS; i < 32; ++i) part[i] = 0.f;
+    red[warp][lane] = group_reduce_scatter<32>(part);
+    __syncthreads();
+    if (k < 2 * TS) nrm[k] = 1.0f / sqrtf(red[0][k] + red[1][k] + red[2][k] + red[3][k] + kNormEps);
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      q[t] *= nrm[t];
+      kk[t] *= nrm[TS + t];
+    }
+  }
+
+  float Gm[TS];
+  float acc = 0.f, gl = 0.f, low = 0.f, rise = 0.f;
+#pragma unroll
+  for (int t = 0; t < TS; ++t) {
+    if (t < cnt) {
+      const size_t th = (size_t)(t0 + t) * H + h;
+      acc += GATE == RSC_GATE_KDA ? g[th * KB + k] : g[th];
+      gl = acc;
+      rise = fmaxf(rise, acc - low);
+      low = fminf(low, acc);
+    }
+    Gm[t] = acc;
+  }
+  if (rise > kMaxRise) flag_error(pv.err, RSC_DEVERR_GATE);
+#pragma unroll
+  for (int t = 0; t < TS; ++t)
+    if (t < cnt) {
+      const size_t o = ((size_t)(t0 + t) * H + h) * KB + k;
+      const float e = expf(Gm[t]);
+      w.q[o] = q[t] * e;
+      w.k[o] = kk[t] * e;
+      bw.ke[o] = kk[t] * expf(gl - Gm[t]);
+    }
+  bw.eg[((size_t)t0 * H + h) * KB + k] = expf(gl);
+
+  // this channel's terms of the 64 sums (rows t >= cnt come out zero: their q, k are zero)
+  float x[64];
+#pragma unroll
+  for (int t = 0; t < TS; ++t) {
+    x[ip(t, t)] = kk[t] * q[t];
+#pragma unroll
+    for (int s = 0; s < t; ++s) {
+      const float e = kk[s] * expf(Gm[t] - Gm[s]);
+      x[ia(t, s)] = e * kk[t];
+      x[ip(t, s)] = e * q[t];
+    }
+  }
+  float lo32[32], hi32[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) { lo32[i] = x[i]; hi32[i] = x[32 + i]; }
+  red[warp][lane] = group_reduce_scatter<32>(lo32);
+  red[warp][32 + lane] = group_reduce_scatter<32>(hi32);
+  __syncthreads();
+  for (int i = k; i < cnt * NCO; i += 128) {
+    const int t = i / NCO, c = i % NCO;
+    float v = 0.f;
+    if (c < TS) {
+      if (c < t) { const int j = ia(t, c); v = red[0][j] + red[1][j] + red[2][j] + red[3][j]; }
+    } else if (c - TS <= t) {
+      const int j = ip(t, c - TS);
+      v = red[0][j] + red[1][j] + red[2][j] + red[3][j];
+    }
+    bw.co[((size_t)(t0 + t) * H + h) * NCO + c] = v;
+  }
+}
+
+// Block operands in shared memory, one stage per block of tokens.
+template <int VT>
+struct Stage {
+  float kq[2 * TS][KB];  // rows 0-7: scaled keys, rows 8-15: scaled queries
+  float ke[TS][KB];
+  float eg[KB];
+  float co[TS][NCO];
+  float v[TS][VT < 4 ? 4 : VT];
+  float b[TS];
+  float pad[4];
+};
+
+// One CTA: rows [j VT, (j+1) VT) of head h of sequence n's state, VT = NW R: NW warps of R
+// rows each, a row across a whole warp (lane i holds key channels 4i .. 4i+3).  The block
+// operands are staged by cp.async NS blocks ahead (the loop's per-block work is shorter than
+// the latency of a fetch from L2 or HBM; one block ahead left each block waiting).  Per block a
+// lane loads its channels of the block's scaled keys, queries and end-scaled keys into
+// registers once and applies them to its R rows.  Per row: the 16 row dots, one butterfly
+// reduce-scatter (lane t then holds a_t, lane 8+t holds b_t), the 8 a's gathered, the forward
+// substitution, o_t written by lane 8+t, the row moved to the block end.
+template <typename IO, int V, int NW, int R, int NS>
+__global__ void __launch_bounds__(32 * NW)
+prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
+                       const int32_t *__restrict__ cu, int T, const uint8_t *__restrict__ has_init,
+                       PrefillWs w, BlockedWs bw, const float *__restrict__ beta,
+                       IO *__restrict__ out) {
+  constexpr int NT = 32 * NW, VT = NW * R;
+  static_assert(V % VT == 0, "row tile");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Stage<VT> *stg = reinterpret_cast<Stage<VT> *>(smem_raw);
+
+  const int j = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5, k0 = 4 * lane;
+  const int H = pv.H;
+  const int start = cu[n], end = cu[n + 1];
+  if (start < 0 || end < start || end > T) {
+    if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SEQ);
+    return;
+  }
+  const int slot = slots[n];
+  if (slot < 0 || slot > pv.P) {
+    if (tid == 0 && j == 0 && h == 0) flag_error(pv.err, RSC_DEVERR_SLOT);
+    return;
+  }
+  const bool init = has_init == nullptr || has_init[n] != 0;
+  const size_t prow = (size_t)layer * (pv.P + 1) + slot;
+  float *S = reinterpret_cast<float *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * KB;
+  float2 s[R][2];  // rows warp R + p, channels k0 .. k0+3
+#pragma unroll
+  for (int p = 0; p < R; ++p) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (init) x = *reinterpret_cast<const float4 *>(S + (size_t)(warp * R + p) * KB + k0);
+    s[p][0] = make_float2(x.x, x.y);
+    s[p][1] = make_float2(x.z, x.w);
+  }
+
+  // Block operands; rows past the sequence end are zero, which makes their deltas zero.
+  auto stage = [&](int buf, int t0) {
+    Stage<VT> &st = stg[buf];
+    const int cnt = min(TS, end - t0);
+    for (int i = tid; i < TS * (KB / 4); i += NT) {
+      const int t = i / (KB / 4), c4 = (i % (KB / 4)) * 4;
+      if (t < cnt) {
+        const size_t o = ((size_t)(t0 + t) * H + h) * KB + c4;
+        cp_async16(&st.kq[t][c4], w.k + o);
+        cp_async16(&st.kq[TS + t][c4], w.q + o);
+        cp_async16(&st.ke[t][c4], bw.ke + o);
+      } else {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(&st.kq[t][c4]) = z;
+        *reinterpret_cast<float4 *>(&st.kq[TS + t][c4]) = z;
+        *reinterpret_cast<float4 *>(&st.ke[t][c4]) = z;
+      }
+    }
+    for (int i = tid; i < KB / 4; i += NT)
+      cp_async16(&st.eg[4 * i], bw.eg + ((size_t)t0 * H + h) * KB + 4 * i);
+    constexpr int VC = VT < 4 ? 0 : VT / 4;  // 16-byte chunks of a token's value rows
+    for (int i = tid; i < TS * (NCO / 4 + VC); i += NT) {
+      const int t = i / (NCO / 4 + VC), c = i % (NCO / 4 + VC);
+      const size_t th = (size_t)(t0 + t) * H + h;
+      float *dst = c < NCO / 4 ? &st.co[t][4 * c] : &st.v[t][4 * (c - NCO / 4)];
+      if (t < cnt) {
+        cp_async16(dst, c < NCO / 4 ? bw.co + th * NCO + 4 * c
+                                    : w.v + th * V + (size_t)j * VT + 4 * (c - NCO / 4));
+      } else {
+        *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if constexpr (VT < 4) {
+      for (int i = tid; i < TS * VT; i += NT) {
+        const int t = i / VT, c = i % VT;
+        if (t < cnt) cp_async4(&st.v[t][c], w.v + ((size_t)(t0 + t) * H + h) * V + (size_t)j * VT + c);
+        else st.v[t][c] = 0.f;
+      }
+    }
+    if (tid < TS) {
+      if (tid < cnt) cp_async4(&st.b[tid], beta + (size_t)(t0 + tid) * H + h);
+      else st.b[tid] = 0.f;
+    }
+    cp_async_commit();
+  };
+
+  const int to = lane & 7;  // lanes 8-15 end with b_to
+  // One commit group per block (empty past the end), so that "all but the newest NS - 2
+  // groups" is always "this block's".
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) {
+    if (start + i * TS < end) stage(i, start + i * TS);
+    else cp_async_commit();
+  }
+  int cur = 0;
+  for (int t0 = start; t0 < end; t0 += TS) {
+    cp_async_wait_group<NS - 2>();
+    __syncthreads();  // block `cur` landed; everyone is done with the previous block's stage
+    {
+      const int tn = t0 + (NS - 1) * TS;
+      const int nb = cur == 0 ? NS - 1 : cur - 1;
+      if (tn < end) stage(nb, tn);
+      else cp_async_commit();
+    }
+    const Stage<VT> &st = stg[cur];
+    const int cnt = min(TS, end - t0);
+    float A[TS][TS], bt[TS], Pr[TS];
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      bt[t] = st.b[t];
+      Pr[t] = st.co[to][TS + t];  // P[to][t]
+#pragma unroll
+      for (int u = 0; u < t; ++u) A[t][u] = st.co[t][u];
+    }
+    // Slot i of this lane holds operand row i ^ (lane & 15) (a scaled key for rows < 8, a
+    // scaled query above): then at every level of the reduce-scatter below the values this
+    // lane keeps sit in the lower slots and the ones it hands over in the upper slots, for
+    // every lane, so the butterfly needs no per-lane selects.
+    const int perm = lane & 15;
+    float2 kq[2 * TS][2], ke[TS][2], eg[2];
+#pragma unroll
+    for (int i = 0; i < 2 * TS; ++i) {
+      const float4 a = *reinterpret_cast<const float4 *>(&st.kq[i ^ perm][k0]);
+      kq[i][0] = make_float2(a.x, a.y); kq[i][1] = make_float2(a.z, a.w);
+    }
+#pragma unroll
+    for (int t = 0; t < TS; ++t) {
+      const float4 c = *reinterpret_cast<const float4 *>(&st.ke[t][k0]);
+      ke[t][0] = make_float2(c.x, c.y); ke[t][1] = make_float2(c.z, c.w);
+    }
+    {
+      const float4 e = *reinterpret_cast<const float4 *>(&st.eg[k0]);
+      eg[0] = make_float2(e.x, e.y); eg[1] = make_float2(e.z, e.w);
+    }
+#pragma unroll
+    for (int p = 0; p < R; ++p) {
+      const int row = warp * R + p;
+      float x[2 * TS];  // x[i]: this lane's part of the dot with operand row i ^ perm
+#pragma unroll
+      for (int i = 0; i < 2 * TS; ++i) {
+        const float2 u = __ffma2_rn(s[p][1], kq[i][1], __fmul2_rn(s[p][0], kq[i][0]));
+        x[i] = u.x + u.y;
+      }
+#pragma unroll
+      for (int m = TS; m >= 1; m >>= 1)
+#pragma unroll
+        for (int i = 0; i < m; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i + m], m);
+      // lane i (and i + 16) now holds the whole dot with row i: a_i for i < 8, b_(i-8) above
+      const float val = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
+      float r[TS], d[TS];
+#pragma unroll
+      for (int t = 0; t < TS; ++t) r[t] = st.v[t][row] - __shfl_sync(0xffffffffu, val, t);
+#pragma unroll
+      for (int u = 0; u < TS; ++u) {
+        d[u] = bt[u] * r[u];
+#pragma unroll
+        for (int t = u + 1; t < TS; ++t) r[t] = fmaf(-A[t][u], d[u], r[t]);
+      }
+      if (lane >= TS && lane < 2 * TS && to < cnt) {
+        float o = val;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) o = fmaf(Pr[u], d[u], o);
+        out[((size_t)(t0 + to) * H + h) * V + (size_t)j * VT + row] = from_f32<IO>(o);
+      }
+      s[p][0] = __fmul2_rn(s[p][0], eg[0]);
+      s[p][1] = __fmul2_rn(s[p][1], eg[1]);
+#pragma unroll
+      for (int u = 0; u < TS; ++u) {
+        const float2 du = make_float2(d[u], d[u]);
+        s[p][0] = __ffma2_rn(du, ke[u][0], s[p][0]);
+        s[p][1] = __ffma2_rn(du, ke[u][1], s[p][1]);
+      }
+    }
+    cur = cur == NS - 1 ? 0 : cur + 1;
+  }
+  cp_async_wait_all();  // no copy into shared memory outlives the CTA
+#pragma unroll
+  for (int p = 0; p < R; ++p)
+    st16_stream(S + (size_t)(warp * R + p) * KB + k0,
+                make_uint4(__float_as_uint(s[p][0].x), __float_as_uint(s[p][0].y),
+                           __float_as_uint(s[p][1].x), __float_as_uint(s[p][1].y)));
+}
+
+#ifndef RSC_BLK_STAGES
+#define RSC_BLK_STAGES 2
+#endif
+
+template <typename IO, int V, int NW, int R>
+int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
+                const uint8_t *has_init, const PrefillWs &w, const BlockedWs &bw,
+                const float *beta, void *out, cudaStream_t s) {
+  constexpr int VT = NW * R, NS = RSC_BLK_STAGES;
+  static_assert(NS >= 2 && sizeof(Stage<VT>) % 16 == 0, "stages");
+  constexpr size_t smem = NS * sizeof(Stage<VT>);
+  auto *kern = prefill_blocked_kernel<IO, V, NW, R, NS>;
+  static PerDeviceFlag attr;
+  const int rc = once_per_device(attr, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                   cudaSuccess
+               ? RSC_OK
+               : RSC_ECUDA;
+  });
+  if (rc != RSC_OK) return rc;
+  kern<<<dim3(V / VT, a.pv.H, N), 32 * NW, smem, s>>>(a.pv, a.layer, slots, cu, T, has_init, w,
+                                                      bw, beta, static_cast<IO *>(out));
+  return launch_status();
+}
+
+// Row tiles: few (sequence, head) pairs get small tiles so that the grid still spreads over
+// the GPU; many get wide ones (fewer copies of each block's operands staged).
+#ifndef RSC_BLOCKED_MIN_CTAS
+#define RSC_BLOCKED_MIN_CTAS 304
+#endif
+#ifndef RSC_BLK_SMALL_NW
+#define RSC_BLK_SMALL_NW 2
+#endif
+#ifndef RSC_BLK_SMALL_R
+#define RSC_BLK_SMALL_R 2
+#endif
+#ifndef RSC_BLK_WIDE_NW
+#define RSC_BLK_WIDE_NW 4
+#endif
+#ifndef RSC_BLK_WIDE_R
+#define RSC_BLK_WIDE_R 8
+#endif
+
+template <typename IO, int V>
+int run_blocked_v(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
+                  const uint8_t *has_init, const PrefillWs &w, const BlockedWs &bw,
+                  const float *beta, void *out, cudaStream_t s) {
+  const long wide = (long)(V / 32) * a.pv.H * N;
+  if (wide >= RSC_BLOCKED_MIN_CTAS)
+    return run_blocked<IO, V, RSC_BLK_WIDE_NW, RSC_BLK_WIDE_R>(a, slots, cu, N, T, has_init, w,
+                                                                bw, beta, out, s);
+  return run_blocked<IO, V, RSC_BLK_SMALL_NW, RSC_BLK_SMALL_R>(a, slots, cu, N, T, has_init, w,
+                                                                bw, beta, out, s);
+}
+
+}  // namespace
+
+size_t prefill_blocked_bytes(const PoolView &pv, int T) {
+  return prefill_prep_bytes(pv, T) + 2 * align256((size_t)T * pv.H * KB * 4) +
+         align256((size_t)T * pv.H * NCO * 4);
+}
+
+int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
+                           int T, const uint8_t *has_init, const void *qkv,
+                           const float *conv_w, const float *g, const float *beta, void *out,
+                           void *ws, cudaStream_t s) {
+  if (a.st != RSC_F32 || a.pv.K != KB) return RSC_EDTYPE;
+  const PrefillWs w = prefill_carve(ws, a.pv, T);
+  const BlockedWs bw = blocked_carve(ws, a.pv, T);
+  const bool bf = a.io == RSC_BF16, kda = a.gate == RSC_GATE_KDA;
+  int rc = RSC_OK;
+  if (T > 0) {
+    const dim3 grid((unsigned)(T / TS + N), a.pv.H);
+#define RSC_BLK(IO_, V_, G_)                                                                  \
+  prefill_blk_kernel<IO_, V_, G_><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, N, T, has_init, \
+                                                       static_cast<const IO_ *>(qkv), conv_w, w, \
+                                                       bw, g)
+    if (a.pv.V == 128) {
+      if (bf) { if (kda) RSC_BLK(bf16, 128, RSC_GATE_KDA); else RSC_BLK(bf16, 128, RSC_GATE_GDN); }
+      else { if (kda) RSC_BLK(float, 128, RSC_GATE_KDA); else RSC_BLK(float, 128, RSC_GATE_GDN); }
+    } else if (a.pv.V == 64) {
+      if (bf) { if (kda) RSC_BLK(bf16, 64, RSC_GATE_KDA); else RSC_BLK(bf16, 64, RSC_GATE_GDN); }
+      else { if (kda) RSC_BLK(float, 64, RSC_GATE_KDA); else RSC_BLK(float, 64, RSC_GATE_GDN); }
+    } else {
+      return RSC_EDTYPE;
+    }
+#undef RSC_BLK
+    if ((rc = launch_status()) != RSC_OK) return rc;
+  }
+  if (a.pv.V == 128)
+    rc = bf ? run_blocked_v<bf16, 128>(a, slots, cu, N, T, has_init, w, bw, beta, out, s)
+            : run_blocked_v<float, 128>(a, slots, cu, N, T, has_init, w, bw, beta, out, s);
+  else if (a.pv.V == 64)
+    rc = bf ? run_blocked_v<bf16, 64>(a, slots, cu, N, T, has_init, w, bw, beta, out, s)
+            : run_blocked_v<float, 64>(a, slots, cu, N, T, has_init, w, bw, beta, out, s);
+  else
+    return RSC_EDTYPE;
+  if (rc != RSC_OK) return rc;
+  return launch_prefill_window(a, slots, cu, N, T, has_init, qkv, s);
+}
+
+}  // namespace rsc

@@ -525,10 +525,14 @@ def test_replay_bad_ring_position_flags(cuda_dev):
 # ------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("st,io,gate,K,V,lens,init", [
-    # token-serial fp32 path (fp32 state, or K = 64)
+    # token-serial fp32 path (K = 64)
     (0, 0, rsc.KDA, 64, 64, [1, 70, 2, 129], [1, 1, 0, 1]),
-    (0, 1, rsc.GDN, 128, 128, [200], [1]),
     (1, 1, rsc.KDA, 64, 128, [65, 3], [1, 0]),
+    # blocked fp32 path (fp32 state, K = 128): whole and ragged 8-token blocks
+    (0, 1, rsc.GDN, 128, 128, [200], [1]),
+    (0, 0, rsc.KDA, 128, 128, [1, 7, 8, 9, 200], [1, 0, 1, 1, 0]),
+    (0, 1, rsc.KDA, 128, 64, [70, 3], [0, 1]),
+    (0, 0, rsc.GDN, 128, 64, [33, 16, 2], [1, 1, 0]),
     # chunkwise tensor-core path (bf16 state, K = 128): ragged chunks, fresh / continued
     (1, 1, rsc.KDA, 128, 128, [64, 1, 131], [1, 0, 1]),
     (1, 1, rsc.KDA, 128, 128, [300], [1]),
@@ -664,6 +668,74 @@ def test_prefill_strong_decay_matches_oracle(cuda_dev, gate, V, lens, init, mode
                               has_initial_state=to_dev(hi, c.dev))
     assert max_rel_err(widen(to_np(o)), widen(o_ref), tc=True) <= TOL[1]
     c.check_pool(tc=True)
+
+
+@pytest.mark.parametrize("gate,V,lens,init,mode", [
+    (rsc.KDA, 128, [64, 13], [1, 0], "const4"),
+    (rsc.KDA, 128, [200, 70], [1, 0], "scale20"),
+    (rsc.KDA, 64, [300], [1], "mixed"),
+    (rsc.GDN, 128, [130, 63], [0, 1], "scale20"),
+    (rsc.KDA, 128, [77], [1], "grow"),
+    (rsc.GDN, 64, [41], [1], "grow"),
+])
+def test_prefill_blocked_fp32_gates(cuda_dev, gate, V, lens, init, mode):
+    """The blocked fp32 prefill under decay far beyond the usual draw, and under a growing
+    gate (g = +0.5 per token, about e^4 per 8-token block), against the oracle at the fp32 bar;
+    no error bit."""
+    H, K = 2, 128
+    c = Case(cuda_dev, 16, L=1, P=4, H=H, K=K, V=V, st=0, io=0, gate=gate)
+    N = len(lens)
+    slots = inputs.distinct_slots(c.r, N, 4)
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    x = c.proj((T,))
+    if mode == "grow":
+        g, beta = c.gates((T,))
+        g = np.full_like(g, 0.5)
+    else:
+        g, beta = _strong_gates(c, T, mode)
+    hi = np.uint8(init)
+    o_ref = oracle.prefill(c.ref, 0, slots, cu, x, c.w, g, beta, has_init=hi)
+    o = rsc.kda_prefill_chunk(c.pool, 0, to_dev(slots, c.dev), to_dev(cu, c.dev),
+                              to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                              has_initial_state=to_dev(hi, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= TOL[0]
+    c.check_pool()
+
+
+@pytest.mark.parametrize("gate,H,V,N", [(rsc.KDA, 12, 128, 8), (rsc.GDN, 16, 64, 10)])
+def test_prefill_blocked_fp32_many_sequences(cuda_dev, gate, H, V, N):
+    """Enough sequences x heads for the 32-row tiles of the blocked fp32 prefill (the smaller
+    cases above run 8-row tiles); lengths cover empty, single-token, whole and ragged blocks."""
+    K = 128
+    c = Case(cuda_dev, 17, L=1, P=N + 2, H=H, K=K, V=V, st=0, io=1, gate=gate)
+    lens = [0, 1, 8, 23, 64, 5, 17, 40, 9, 3][:N]
+    init = [1, 0, 1, 1, 0, 1, 0, 1, 1, 0][:N]
+    slots = inputs.distinct_slots(c.r, N, N + 2)
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    x = c.proj((T,))
+    g, beta = c.gates((T,))
+    hi = np.uint8(init)
+    o_ref = oracle.prefill(c.ref, 0, slots, cu, x, c.w, g, beta, has_init=hi)
+    o = rsc.kda_prefill_chunk(c.pool, 0, to_dev(slots, c.dev), to_dev(cu, c.dev),
+                              to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev),
+                              has_initial_state=to_dev(hi, c.dev))
+    assert max_rel_err(widen(to_np(o)), widen(o_ref)) <= tol(0, 1)
+    c.check_pool()
+
+
+def test_prefill_blocked_fp32_steep_growth_is_flagged(cuda_dev):
+    """A growing gate that raises a log gate by more than 80 within an 8-token block (11 per
+    token) sets RSC_DEVERR_GATE on the blocked fp32 path."""
+    c = Case(cuda_dev, 18, L=1, P=2, H=1, K=128, V=64, st=0, io=0, gate=rsc.KDA)
+    T = 16
+    x = c.proj((T,))
+    _, beta = c.gates((T,))
+    g = np.full((T, 1, 128), 11.0, np.float32)
+    rsc.kda_prefill_chunk(c.pool, 0, to_dev(np.int32([1]), c.dev), to_dev(np.int32([0, T]), c.dev),
+                          to_dev(x, c.dev), c.w_dev, to_dev(g, c.dev), to_dev(beta, c.dev))
+    assert rsc.rsc_get_device_error(c.pool) & rsc.binding.DEVERR_GATE
 
 
 def test_prefill_growing_gate_is_flagged(cuda_dev):

@@ -27,6 +27,7 @@ def _pools(dev, st, H, K, V, P, seed):
 
 @pytest.mark.parametrize("st,K", [
     (rsc.F32, 64),    # token-serial fp32 path
+    (rsc.F32, 128),   # blocked fp32 path
     (rsc.BF16, 64),   # token-serial path of a bf16-state pool
     (rsc.BF16, 128),  # chunkwise tensor-core path: chunk table and operand blocks in the array
 ])
