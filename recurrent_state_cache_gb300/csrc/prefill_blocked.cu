@@ -44,6 +44,12 @@ constexpr float kMaxRise = 80.f;  // largest growth of a log gate within a block
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Wait until at most N of this thread's most recent cp.async groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 struct BlockedWs {
   float *ke;  // [T][H][K]  k_hat_t . e^(Gam_end - Gam_t)
   float *eg;  // [T][H][K]  e^Gam_end, in the row of the block's first token
