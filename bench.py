@@ -14,7 +14,9 @@ Legs reported in the same line (each timed separately with CUDA events):
   gdn_decode   GDN decode, H=32, K=V=128, fp32 state, 48 layers, 1024-slot pool,
                batch 1/16/64/256
   prefill      one KDA layer, 13600 tokens in chunked-prefill calls of 6144/6144/1312,
-               a slot snapshot (ssm_slot_copy) after each call
+               a slot snapshot (ssm_slot_copy) after each call; bf16 state (tensor cores),
+               then fp32 state (blocked closed form) on the same prompt and on 64 packed
+               212-token sequences
   slot_copy    64 (src, dst) pairs of the 69-layer decode pool, all layers, one launch
   spec         verify of 8 tokens (anchor + 7 drafts) for 64 requests into a 16-deep
                cache, then commit of a seeded accept count per request
@@ -334,17 +336,23 @@ def leg_gdn(dev, peaks, stream, batches=(1, 16, 64, 256)):
     return res
 
 
-def leg_prefill(dev, peaks, stream):
+PROMPT_CHUNKS = (6144, 6144, 1312)
+
+
+def _prompt_ms(dev, stream, st, seed):
+    """ms per 13600-token prompt: three kda_prefill_chunk calls of 6144/6144/1312 tokens chained
+    through one slot of a 1-layer pool (H=12, K=V=128, bf16 inputs, state dtype st), a slot
+    snapshot after each; captured once in a CUDA graph and replayed."""
     import torch
     import recurrent_state_cache_gb300 as rsc
-    from recurrent_state_cache_gb300 import binding as b, inputs
+    from recurrent_state_cache_gb300 import binding as b
     H, K, V = 12, 128, 128
-    chunks = (6144, 6144, 1312)
+    chunks = PROMPT_CHUNKS
     T = sum(chunks)
     gen = torch.Generator(device=dev)
-    gen.manual_seed(2)
+    gen.manual_seed(seed)
     D = H * (2 * K + V)
-    pool = rsc.SlotPool(1, 8, H, K, V, b.BF16, b.BF16, b.KDA, dev)
+    pool = rsc.SlotPool(1, 8, H, K, V, st, b.BF16, b.KDA, dev)
     qkv = torch.empty((T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
     g = -torch.nn.functional.softplus(torch.empty((T, H, K), device=dev).normal_(0, 1, generator=gen))
     beta = torch.sigmoid(torch.empty((T, H), device=dev).normal_(0, 1, generator=gen))
@@ -365,8 +373,17 @@ def leg_prefill(dev, peaks, stream):
                                   workspace=ws)
             rsc.ssm_slot_copy(pool, 0, slot, snaps[i])
 
-    graph = graph_of(run, stream)
-    ms = timed(graph.replay, 5, 2, stream)
+    ms = timed(graph_of(run, stream).replay, 5, 2, stream)
+    assert rsc.rsc_get_device_error(pool) == 0
+    return ms
+
+
+def leg_prefill(dev, peaks, stream):
+    from recurrent_state_cache_gb300 import binding as b
+    H, K, V = 12, 128, 128
+    T = sum(PROMPT_CHUNKS)
+    D = H * (2 * K + V)
+    ms = _prompt_ms(dev, stream, b.BF16, 2)
     flops = prefill_flops(T, H, K, V)
     io_bytes = T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2
     res = {"config": "1 KDA layer, H=12, K=V=128, bf16, 13600 tokens as 6144/6144/1312, snapshot copy after each",
@@ -380,33 +397,41 @@ def leg_prefill(dev, peaks, stream):
     return res
 
 
-def leg_prefill_f32(dev, stream, T=2048):
-    """The fp32-state prefill (exact token-serial recurrence, CUDA cores) on one 2048-token
-    call of the same head shape (H=12, K=V=128, bf16 inputs), from a fresh slot."""
+def leg_prefill_f32(dev, stream, nseq=64, seqlen=212):
+    """The fp32-state prefill (the recurrence eight tokens at a time in closed form, fp32 on the
+    CUDA cores) at the same head shape (H=12, K=V=128, bf16 inputs): the 13600-token prompt as
+    in the bf16 leg, and a batch of 64 packed 212-token sequences from fresh slots."""
     import torch
     import recurrent_state_cache_gb300 as rsc
     from recurrent_state_cache_gb300 import binding as b
+    T = sum(PROMPT_CHUNKS)
+    ms_prompt = _prompt_ms(dev, stream, b.F32, 3)
     H, K, V = 12, 128, 128
+    Tb = nseq * seqlen
     gen = torch.Generator(device=dev)
-    gen.manual_seed(3)
+    gen.manual_seed(4)
     D = H * (2 * K + V)
-    pool = rsc.SlotPool(1, 4, H, K, V, b.F32, b.BF16, b.KDA, dev)
-    qkv = torch.empty((T, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
-    g = -torch.nn.functional.softplus(torch.empty((T, H, K), device=dev).normal_(0, 1, generator=gen))
-    beta = torch.sigmoid(torch.empty((T, H), device=dev).normal_(0, 1, generator=gen))
+    pool = rsc.SlotPool(1, nseq + 1, H, K, V, b.F32, b.BF16, b.KDA, dev)
+    qkv = torch.empty((Tb, D), dtype=torch.bfloat16, device=dev).normal_(0, 1, generator=gen)
+    g = -torch.nn.functional.softplus(torch.empty((Tb, H, K), device=dev).normal_(0, 1, generator=gen))
+    beta = torch.sigmoid(torch.empty((Tb, H), device=dev).normal_(0, 1, generator=gen))
     w = torch.empty((D, 4), device=dev).normal_(0, 0.5, generator=gen)
-    out = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(rsc.kda_prefill_workspace_size(pool, 1, T), dtype=torch.uint8, device=dev)
-    slot = torch.tensor([1], dtype=torch.int32, device=dev)
-    fresh = torch.tensor([0], dtype=torch.uint8, device=dev)
-    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
-    run = lambda: rsc.kda_prefill_chunk(pool, 0, slot, cu, qkv, w, g, beta,
+    out = torch.empty((Tb, H, V), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(rsc.kda_prefill_workspace_size(pool, nseq, Tb), dtype=torch.uint8, device=dev)
+    slots = torch.arange(1, nseq + 1, dtype=torch.int32, device=dev)
+    fresh = torch.zeros(nseq, dtype=torch.uint8, device=dev)
+    cu = torch.arange(0, Tb + 1, seqlen, dtype=torch.int32, device=dev)
+    run = lambda: rsc.kda_prefill_chunk(pool, 0, slots, cu, qkv, w, g, beta,
                                         has_initial_state=fresh, out=out, workspace=ws)
-    ms = timed(graph_of(run, stream).replay, 5, 2, stream)
-    return {"config": f"1 KDA layer, H=12, K=V=128, fp32 state, bf16 io, one {T}-token call",
-            "ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
-            "us_per_token": round(ms * 1e3 / T, 4),
-            "path": "token-serial recurrence (prep, recurrent, window kernels)"}
+    ms_batch = timed(graph_of(run, stream).replay, 5, 2, stream)
+    assert rsc.rsc_get_device_error(pool) == 0
+    return {"config": f"1 KDA layer, H=12, K=V=128, fp32 state, bf16 io: the {T}-token prompt as "
+                      f"6144/6144/1312 with snapshots; {nseq} packed {seqlen}-token sequences",
+            "ms_per_prefill": round(ms_prompt, 4), "tokens_per_s": round(T / (ms_prompt * 1e-3), 1),
+            "us_per_token": round(ms_prompt * 1e3 / T, 4),
+            "batch_ms": round(ms_batch, 4), "batch_tokens_per_s": round(Tb / (ms_batch * 1e-3), 1),
+            "path": "8-token blocks in closed form (per-block conv/norm/operand kernel, blocked "
+                    "recurrence, window kernel)"}
 
 
 def leg_copy(dev, peaks, stream, wl):

@@ -267,8 +267,23 @@ int launch_prefill_serial(const LayerArgs &a, const int32_t *slots, const int32_
                           int N, int T, const uint8_t *has_init, const void *qkv,
                           const float *conv_w, const float *g, const float *beta,
                           void *out, void *ws, cudaStream_t s) {
-  return dispatch_all<PrefillSerialLaunch>(a.st, a.io, a.pv.K, a.pv.V, a.gate, &a, slots, cu,
-                                           N, T, has_init, qkv, conv_w, g, beta, out, ws, s);
+  // head_k 64 only: head_k 128 pools take the tensor-core or the blocked form
+  if (a.pv.K != 64) return RSC_EDTYPE;
+  if (a.st == RSC_F32)
+    return a.io == RSC_F32
+               ? dispatch_v<PrefillSerialLaunch, float, float, 64>(a.pv.V, a.gate, &a, slots, cu,
+                                                                   N, T, has_init, qkv, conv_w,
+                                                                   g, beta, out, ws, s)
+               : dispatch_v<PrefillSerialLaunch, float, bf16, 64>(a.pv.V, a.gate, &a, slots, cu,
+                                                                  N, T, has_init, qkv, conv_w, g,
+                                                                  beta, out, ws, s);
+  return a.io == RSC_F32
+             ? dispatch_v<PrefillSerialLaunch, bf16, float, 64>(a.pv.V, a.gate, &a, slots, cu, N,
+                                                                T, has_init, qkv, conv_w, g, beta,
+                                                                out, ws, s)
+             : dispatch_v<PrefillSerialLaunch, bf16, bf16, 64>(a.pv.V, a.gate, &a, slots, cu, N,
+                                                               T, has_init, qkv, conv_w, g, beta,
+                                                               out, ws, s);
 }
 
 int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
