@@ -212,7 +212,7 @@ struct Stage {
   float eg[KB];
   float co[TS][NCO];
   float v[TS][VT < 4 ? 4 : VT];
-  float b[TS];
+  float b[TS];  // 16-byte aligned: every member above is a multiple of 16 bytes
   float pad[4];
 };
 
@@ -264,13 +264,17 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   auto stage = [&](int buf, int t0) {
     Stage<VT> &st = stg[buf];
     const int cnt = min(TS, end - t0);
-    for (int i = tid; i < TS * (KB / 4); i += NT) {
-      const int t = i / (KB / 4), c4 = (i % (KB / 4)) * 4;
+    const float *kb = w.k + (size_t)t0 * H * KB, *qb = w.q + (size_t)t0 * H * KB;
+    const float *eb = bw.ke + (size_t)t0 * H * KB;
+    static_assert((TS * KB / 4) % NT == 0, "whole staging passes");
+#pragma unroll
+    for (int it = 0; it < TS * KB / 4 / NT; ++it) {
+      const int i = tid + it * NT, t = i / (KB / 4), c4 = (i % (KB / 4)) * 4;
+      const int o = (t * H + h) * KB + c4;  // within the block's rows
       if (t < cnt) {
-        const size_t o = ((size_t)(t0 + t) * H + h) * KB + c4;
-        cp_async16(&st.kq[t][c4], w.k + o);
-        cp_async16(&st.kq[TS + t][c4], w.q + o);
-        cp_async16(&st.ke[t][c4], bw.ke + o);
+        cp_async16(&st.kq[t][c4], kb + o);
+        cp_async16(&st.kq[TS + t][c4], qb + o);
+        cp_async16(&st.ke[t][c4], eb + o);
       } else {
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4 *>(&st.kq[t][c4]) = z;
@@ -326,13 +330,19 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     }
     const Stage<VT> &st = stg[cur];
     const int cnt = min(TS, end - t0);
-    float A[TS][TS], bt[TS], Pr[TS];
+    float A[TS][TS], bt[TS], Pr[TS];  // 16-byte loads: A rows, beta, this lane's P row
+    auto ld = [](const float *p, float *d) {
+      const float4 x = *reinterpret_cast<const float4 *>(p);
+      d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+    };
+    ld(&st.b[0], bt);
+    ld(&st.b[4], bt + 4);
+    ld(&st.co[to][TS], Pr);  // P[to][t]
+    ld(&st.co[to][TS + 4], Pr + 4);
 #pragma unroll
-    for (int t = 0; t < TS; ++t) {
-      bt[t] = st.b[t];
-      Pr[t] = st.co[to][TS + t];  // P[to][t]
-#pragma unroll
-      for (int u = 0; u < t; ++u) A[t][u] = st.co[t][u];
+    for (int t = 1; t < TS; ++t) {
+      ld(&st.co[t][0], A[t]);
+      if (t > 4) ld(&st.co[t][4], A[t] + 4);
     }
     // Slot i of this lane holds operand row i ^ (lane & 15) (a scaled key for rows < 8, a
     // scaled query above): then at every level of the reduce-scatter below the values this
