@@ -19,8 +19,9 @@
 // Three launches:
 //   blk        grid (block, head): conv and L2 norms of the block's tokens, then its scaled
 //              keys and queries, the end-scaled keys, e^Gam_end and the A / P rows.  The
-//              2 x 36 sums over channels are one butterfly reduce-scatter per warp and a
-//              4-warp add.
+//              2 x 32 sums over channels are one butterfly reduce-scatter per warp and a
+//              4-warp add (a shared-memory transpose instead costs the CTAs per SM that this
+//              latency-bound kernel needs).
 //   recurrent  grid (row tile, head, sequence): S in registers across the sequence; per
 //              block the 16 row dots of every row (one butterfly reduce-scatter: 16 shuffles
 //              where the token loop spends 80), the 8x8 forward substitution, the outputs
@@ -129,15 +130,15 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       if (t < cnt) w.v[((size_t)(t0 + t) * H + h) * V + k] = y[t];
   }
   {
-    float part[32];  // |q_t|^2, then |k_t|^2, summed over the head's channels
+    float sq[2 * TS];  // |q_t|^2, then |k_t|^2, summed over the head's channels
 #pragma unroll
     for (int t = 0; t < TS; ++t) {
-      part[t] = q[t] * q[t];
-      part[TS + t] = kk[t] * kk[t];
+      sq[t] = q[t] * q[t];
+      sq[TS + t] = kk[t] * kk[t];
     }
-#pragma unroll
-    for (int i = 2 * TS; i < 32; ++i) part[i] = 0.f;
-    red[warp][lane] = group_reduce_scatter<32>(part);
+    float v16 = group_reduce_scatter<2 * TS>(sq);  // lane i: entry i & 15 over its half-warp
+    v16 += __shfl_xor_sync(0xffffffffu, v16, 16);
+    if (lane < 2 * TS) red[warp][lane] = v16;
     __syncthreads();
     if (k < 2 * TS) nrm[k] = 1.0f / sqrtf(red[0][k] + red[1][k] + red[2][k] + red[3][k] + kNormEps);
     __syncthreads();
@@ -148,41 +149,52 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     }
   }
 
-  float Gm[TS];
-  float acc = 0.f, gl = 0.f, low = 0.f, rise = 0.f;
+  // Decays alpha_t = e^(g_t) (1 past the sequence end); every factor e^(Gam_t - Gam_s) below
+  // is a product of alphas, the token recurrence's own arithmetic, to at most 7 roundings.
+  float al[TS];
+  float acc = 0.f, low = 0.f, rise = 0.f;
 #pragma unroll
   for (int t = 0; t < TS; ++t) {
+    al[t] = 1.f;
     if (t < cnt) {
       const size_t th = (size_t)(t0 + t) * H + h;
-      acc += GATE == RSC_GATE_KDA ? g[th * KB + k] : g[th];
-      gl = acc;
+      const float gt = GATE == RSC_GATE_KDA ? g[th * KB + k] : g[th];
+      al[t] = expf(gt);
+      acc += gt;
       rise = fmaxf(rise, acc - low);
       low = fminf(low, acc);
     }
-    Gm[t] = acc;
   }
   if (rise > kMaxRise) flag_error(pv.err, RSC_DEVERR_GATE);
+  float eg[TS], ee[TS];  // e^Gam_t, e^(Gam_end - Gam_t)
+  {
+    float f = 1.f, b2 = 1.f;
+#pragma unroll
+    for (int t = 0; t < TS; ++t) { f *= al[t]; eg[t] = f; }
+#pragma unroll
+    for (int t = TS - 1; t >= 0; --t) { ee[t] = b2; b2 *= al[t]; }
+  }
 #pragma unroll
   for (int t = 0; t < TS; ++t)
     if (t < cnt) {
       const size_t o = ((size_t)(t0 + t) * H + h) * KB + k;
-      const float e = expf(Gm[t]);
-      w.q[o] = q[t] * e;
-      w.k[o] = kk[t] * e;
-      bw.ke[o] = kk[t] * expf(gl - Gm[t]);
+      w.q[o] = q[t] * eg[t];
+      w.k[o] = kk[t] * eg[t];
+      bw.ke[o] = kk[t] * ee[t];
     }
-  bw.eg[((size_t)t0 * H + h) * KB + k] = expf(gl);
+  bw.eg[((size_t)t0 * H + h) * KB + k] = eg[TS - 1];
 
   // this channel's terms of the 64 sums (rows t >= cnt come out zero: their q, k are zero)
   float x[64];
 #pragma unroll
-  for (int t = 0; t < TS; ++t) {
-    x[ip(t, t)] = kk[t] * q[t];
+  for (int s2 = 0; s2 < TS; ++s2) {
+    x[ip(s2, s2)] = kk[s2] * q[s2];
+    float f = kk[s2];
 #pragma unroll
-    for (int s = 0; s < t; ++s) {
-      const float e = kk[s] * expf(Gm[t] - Gm[s]);
-      x[ia(t, s)] = e * kk[t];
-      x[ip(t, s)] = e * q[t];
+    for (int t = s2 + 1; t < TS; ++t) {
+      f *= al[t];  // k_s e^(Gam_t - Gam_s)
+      x[ia(t, s2)] = f * kk[t];
+      x[ip(t, s2)] = f * q[t];
     }
   }
   float lo32[32], hi32[32];
@@ -195,10 +207,10 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     const int t = i / NCO, c = i % NCO;
     float v = 0.f;
     if (c < TS) {
-      if (c < t) { const int j = ia(t, c); v = red[0][j] + red[1][j] + red[2][j] + red[3][j]; }
+      if (c < t) { const int e = ia(t, c); v = red[0][e] + red[1][e] + red[2][e] + red[3][e]; }
     } else if (c - TS <= t) {
-      const int j = ip(t, c - TS);
-      v = red[0][j] + red[1][j] + red[2][j] + red[3][j];
+      const int e = ip(t, c - TS);
+      v = red[0][e] + red[1][e] + red[2][e] + red[3][e];
     }
     bw.co[((size_t)(t0 + t) * H + h) * NCO + c] = v;
   }
