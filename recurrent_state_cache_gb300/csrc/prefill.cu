@@ -317,7 +317,7 @@ size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T) {
   if (use_tc(pv, st))
     return align256((size_t)(N + 1) * 4) +
            prefill_tc_chunk_capacity(N, T) * (size_t)pv.H * prefill_tc_block_bytes();
-  if (use_blocked(pv, st)) return prefill_blocked_bytes(pv, T);
+  if (use_blocked(pv, st)) return prefill_blocked_bytes(pv, N, T);
   return prefill_prep_bytes(pv, T);
 }
 

@@ -18,15 +18,16 @@
 //
 // Three launches:
 //   blk        grid (block, head): conv and L2 norms of the block's tokens, then its scaled
-//              keys and queries, the end-scaled keys, e^Gam_end and the A / P rows.  The
+//              keys and queries, the end-scaled keys, e^Gam_end and the A / P rows, written
+//              with beta and the values as one contiguous record per (block, head).  The
 //              2 x 32 sums over channels are one butterfly reduce-scatter per warp and a
 //              4-warp add (a shared-memory transpose instead costs the CTAs per SM that this
 //              latency-bound kernel needs).
 //   recurrent  grid (row tile, head, sequence): S in registers across the sequence; per
 //              block the 16 row dots of every row (one butterfly reduce-scatter: 16 shuffles
 //              where the token loop spends 80), the 8x8 forward substitution, the outputs
-//              and the block-end state.  Block operands are staged one block ahead by
-//              cp.async, double-buffered.
+//              and the block-end state.  Each block's record is staged by two bulk copies
+//              (TMA) from one thread, a few blocks ahead.
 //   window     (prefill.cu) the slot's window becomes the sequence's last three inputs.
 // Blocks start at each sequence start, so a sequence of n tokens has ceil(n / 8) blocks;
 // block b of the grid belongs to the last sequence i with cu[i] / 8 + i <= b (these bases are
@@ -43,29 +44,19 @@ constexpr int KB = 128;    // head_k of the blocked form
 constexpr int NCO = 16;    // per token: its A row (8), then its P row (8)
 constexpr float kMaxRise = 80.f;  // largest growth of a log gate within a block
 
-inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// Wait until at most N of this thread's most recent cp.async groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
-struct BlockedWs {
-  float *ke;  // [T][H][K]  k_hat_t . e^(Gam_end - Gam_t)
-  float *eg;  // [T][H][K]  e^Gam_end, in the row of the block's first token
-  float *co;  // [T][H][16] A row, P row of the token within its block
-};
-
-BlockedWs blocked_carve(void *ws, const PoolView &pv, int T) {
-  char *p = static_cast<char *>(ws) + prefill_prep_bytes(pv, T);
-  const size_t nk = align256((size_t)T * pv.H * KB * 4);
-  BlockedWs b;
-  b.ke = reinterpret_cast<float *>(p);
-  b.eg = reinterpret_cast<float *>(p + nk);
-  b.co = reinterpret_cast<float *>(p + 2 * nk);
-  return b;
-}
+// One record per (block, head) in the workspace, fp32, in the order the recurrence stages it:
+// scaled keys (rows 0-7) and queries (rows 8-15) [16][K], end-scaled keys [8][K], e^Gam_end
+// [K], the A rows then the P rows [8][16], beta [8] (+8 zero), then the values [V][8] (value
+// channel-major, so a row tile's values are one contiguous run).  Rows past the sequence end
+// are zero, which makes their deltas zero.
+constexpr int kOffKQ = 0;
+constexpr int kOffKE = kOffKQ + 2 * TS * KB;
+constexpr int kOffEG = kOffKE + TS * KB;
+constexpr int kOffCO = kOffEG + KB;
+constexpr int kOffB = kOffCO + TS * NCO;
+constexpr int kOffV = kOffB + 2 * TS;  // also the floats of the shared part of a record
+__host__ __device__ constexpr int rec_floats(int V) { return kOffV + TS * V; }
+static_assert((kOffV * 4) % 16 == 0, "16-byte bulk copies");
 
 // Pair indices of the 64 coefficient sums: A[t][s] (s < t) at t(t-1)/2 + s, then P[t][s]
 // (s <= t) at 28 + t(t+1)/2 + s.
@@ -82,8 +73,8 @@ __global__ void __launch_bounds__(128)
 prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                    const int32_t *__restrict__ cu, int N, int T,
                    const uint8_t *__restrict__ has_init, const IO *__restrict__ qkv,
-                   const float *__restrict__ conv_w, PrefillWs w, BlockedWs bw,
-                   const float *__restrict__ g) {
+                   const float *__restrict__ conv_w, const float *__restrict__ g,
+                   const float *__restrict__ beta, float *__restrict__ recs) {
   static_assert(V <= KB, "a thread per key channel covers the value channels");
   __shared__ float red[4][64];
   __shared__ float nrm[2 * TS];  // 1/|q_t|, 1/|k_t|
@@ -104,6 +95,7 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   if (slot < 0 || slot > pv.P) return;  // flagged by the recurrence
   const bool init = has_init == nullptr || has_init[lo] != 0;
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
+  float *rec = recs + ((size_t)b * H + h) * rec_floats(V);
 
   auto conv_rows = [&](int c, float (&y)[TS]) {
     float x[TS + 3];  // inputs at tokens t0 - 3 .. t0 + 7 (oldest first)
@@ -125,9 +117,9 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   if (k < V) {
     float y[TS];
     conv_rows(2 * H * KB + h * V + k, y);
-#pragma unroll
-    for (int t = 0; t < TS; ++t)
-      if (t < cnt) w.v[((size_t)(t0 + t) * H + h) * V + k] = y[t];
+    float4 *dv = reinterpret_cast<float4 *>(rec + kOffV + TS * k);
+    dv[0] = make_float4(y[0], y[1], y[2], y[3]);
+    dv[1] = make_float4(y[4], y[5], y[6], y[7]);
   }
   {
     float sq[2 * TS];  // |q_t|^2, then |k_t|^2, summed over the head's channels
@@ -175,14 +167,13 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
     for (int t = TS - 1; t >= 0; --t) { ee[t] = b2; b2 *= al[t]; }
   }
 #pragma unroll
-  for (int t = 0; t < TS; ++t)
-    if (t < cnt) {
-      const size_t o = ((size_t)(t0 + t) * H + h) * KB + k;
-      w.q[o] = q[t] * eg[t];
-      w.k[o] = kk[t] * eg[t];
-      bw.ke[o] = kk[t] * ee[t];
-    }
-  bw.eg[((size_t)t0 * H + h) * KB + k] = eg[TS - 1];
+  for (int t = 0; t < TS; ++t) {  // zero past the sequence end: q, k are
+    rec[kOffKQ + t * KB + k] = kk[t] * eg[t];
+    rec[kOffKQ + (TS + t) * KB + k] = q[t] * eg[t];
+    rec[kOffKE + t * KB + k] = kk[t] * ee[t];
+  }
+  rec[kOffEG + k] = eg[TS - 1];
+  if (k < 2 * TS) rec[kOffB + k] = k < cnt ? beta[(size_t)(t0 + k) * H + h] : 0.f;
 
   // this channel's terms of the 64 sums (rows t >= cnt come out zero: their q, k are zero)
   float x[64];
@@ -203,8 +194,9 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   red[warp][lane] = group_reduce_scatter<32>(lo32);
   red[warp][32 + lane] = group_reduce_scatter<32>(hi32);
   __syncthreads();
-  for (int i = k; i < cnt * NCO; i += 128) {
-    const int t = i / NCO, c = i % NCO;
+  static_assert(TS * NCO == 128, "a thread per coefficient");
+  {
+    const int t = k / NCO, c = k % NCO;
     float v = 0.f;
     if (c < TS) {
       if (c < t) { const int e = ia(t, c); v = red[0][e] + red[1][e] + red[2][e] + red[3][e]; }
@@ -212,40 +204,38 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       const int e = ip(t, c - TS);
       v = red[0][e] + red[1][e] + red[2][e] + red[3][e];
     }
-    bw.co[((size_t)(t0 + t) * H + h) * NCO + c] = v;
+    rec[kOffCO + k] = v;  // rows past the end: zero sums
   }
 }
 
-// Block operands in shared memory, one stage per block of tokens.
+// One stage of block operands in shared memory: the record's shared part and this tile's
+// values, each one bulk copy.
 template <int VT>
 struct Stage {
-  float kq[2 * TS][KB];  // rows 0-7: scaled keys, rows 8-15: scaled queries
-  float ke[TS][KB];
-  float eg[KB];
-  float co[TS][NCO];
-  float v[TS][VT < 4 ? 4 : VT];
-  float b[TS];  // 16-byte aligned: every member above is a multiple of 16 bytes
-  float pad[4];
+  float rec[kOffV];
+  float v[VT][TS];  // values of the tile's rows, [row][token]
 };
 
 // One CTA: rows [j VT, (j+1) VT) of head h of sequence n's state, VT = NW R: NW warps of R
-// rows each, a row across a whole warp (lane i holds key channels 4i .. 4i+3).  The block
-// operands are staged by cp.async NS blocks ahead (the loop's per-block work is shorter than
-// the latency of a fetch from L2 or HBM; one block ahead left each block waiting).  Per block a
-// lane loads its channels of the block's scaled keys, queries and end-scaled keys into
-// registers once and applies them to its R rows.  Per row: the 16 row dots, one butterfly
-// reduce-scatter (lane t then holds a_t, lane 8+t holds b_t), the 8 a's gathered, the forward
-// substitution, o_t written by lane 8+t, the row moved to the block end.
+// rows each, a row across a whole warp (lane i holds key channels 4i .. 4i+3).  Thread 0
+// stages each block's record with two bulk copies (TMA) NS - 1 blocks ahead, completing on
+// that stage's mbarrier.  Per block a lane loads its channels of the block's scaled keys,
+// queries and end-scaled keys into registers once and applies them to its R rows.  Per row:
+// the 16 row dots, one butterfly reduce-scatter (lane t then holds a_t, lane 8+t holds b_t),
+// the 8 a's gathered, the forward substitution, o_t written by lane 8+t, the row moved to the
+// block end.
 template <typename IO, int V, int NW, int R, int NS>
 __global__ void __launch_bounds__(32 * NW)
 prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                        const int32_t *__restrict__ cu, int T, const uint8_t *__restrict__ has_init,
-                       PrefillWs w, BlockedWs bw, const float *__restrict__ beta,
-                       IO *__restrict__ out) {
-  constexpr int NT = 32 * NW, VT = NW * R;
-  static_assert(V % VT == 0, "row tile");
+                       const float *__restrict__ recs, IO *__restrict__ out) {
+  constexpr int VT = NW * R;
+  constexpr uint32_t kBytesRec = kOffV * 4, kBytesV = VT * TS * 4;
+  static_assert(V % VT == 0 && kBytesV % 16 == 0, "row tile");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Stage<VT> *stg = reinterpret_cast<Stage<VT> *>(smem_raw);
+  __shared__ __align__(8) uint64_t s_bar[NS];
+  __shared__ int s_fail;
 
   const int j = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5, k0 = 4 * lane;
@@ -272,128 +262,88 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     s[p][1] = make_float2(x.z, x.w);
   }
 
-  // Block operands; rows past the sequence end are zero, which makes their deltas zero.
-  auto stage = [&](int buf, int t0) {
-    Stage<VT> &st = stg[buf];
-    const int cnt = min(TS, end - t0);
-    const float *kb = w.k + (size_t)t0 * H * KB, *qb = w.q + (size_t)t0 * H * KB;
-    const float *eb = bw.ke + (size_t)t0 * H * KB;
-    static_assert((TS * KB / 4) % NT == 0, "whole staging passes");
-#pragma unroll
-    for (int it = 0; it < TS * KB / 4 / NT; ++it) {
-      const int i = tid + it * NT, t = i / (KB / 4), c4 = (i % (KB / 4)) * 4;
-      const int o = (t * H + h) * KB + c4;  // within the block's rows
-      if (t < cnt) {
-        cp_async16(&st.kq[t][c4], kb + o);
-        cp_async16(&st.kq[TS + t][c4], qb + o);
-        cp_async16(&st.ke[t][c4], eb + o);
-      } else {
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(&st.kq[t][c4]) = z;
-        *reinterpret_cast<float4 *>(&st.kq[TS + t][c4]) = z;
-        *reinterpret_cast<float4 *>(&st.ke[t][c4]) = z;
-      }
-    }
-    for (int i = tid; i < KB / 4; i += NT)
-      cp_async16(&st.eg[4 * i], bw.eg + ((size_t)t0 * H + h) * KB + 4 * i);
-    constexpr int VC = VT < 4 ? 0 : VT / 4;  // 16-byte chunks of a token's value rows
-    for (int i = tid; i < TS * (NCO / 4 + VC); i += NT) {
-      const int t = i / (NCO / 4 + VC), c = i % (NCO / 4 + VC);
-      const size_t th = (size_t)(t0 + t) * H + h;
-      float *dst = c < NCO / 4 ? &st.co[t][4 * c] : &st.v[t][4 * (c - NCO / 4)];
-      if (t < cnt) {
-        cp_async16(dst, c < NCO / 4 ? bw.co + th * NCO + 4 * c
-                                    : w.v + th * V + (size_t)j * VT + 4 * (c - NCO / 4));
-      } else {
-        *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    if constexpr (VT < 4) {
-      for (int i = tid; i < TS * VT; i += NT) {
-        const int t = i / VT, c = i % VT;
-        if (t < cnt) cp_async4(&st.v[t][c], w.v + ((size_t)(t0 + t) * H + h) * V + (size_t)j * VT + c);
-        else st.v[t][c] = 0.f;
-      }
-    }
-    if (tid < TS) {
-      if (tid < cnt) cp_async4(&st.b[tid], beta + (size_t)(t0 + tid) * H + h);
-      else st.b[tid] = 0.f;
-    }
-    cp_async_commit();
+  const int nb = (end - start + TS - 1) / TS;
+  const float *rec0 = recs + ((size_t)(start / TS + n) * H + h) * rec_floats(V);
+  auto issue = [&](int i) {  // thread 0: block i of the sequence into stage i % NS
+    Stage<VT> &st = stg[i % NS];
+    const float *rec = rec0 + (size_t)i * H * rec_floats(V);
+    mbar_arrive_expect_tx(&s_bar[i % NS], kBytesRec + kBytesV);
+    bulk_g2s(st.rec, rec, kBytesRec, &s_bar[i % NS]);
+    bulk_g2s(st.v, rec + kOffV + (size_t)j * VT * TS, kBytesV, &s_bar[i % NS]);
   };
+  int issued = 0;
+  if (tid == 0) {
+    for (int b = 0; b < NS; ++b) mbar_init(&s_bar[b], 1);
+    s_fail = 0;
+    for (; issued < NS - 1 && issued < nb; ++issued) issue(issued);
+  }
+  __syncthreads();
 
   const int to = lane & 7;  // lanes 8-15 end with b_to
-  // One commit group per block (empty past the end), so that "all but the newest NS - 2
-  // groups" is always "this block's".
-#pragma unroll
-  for (int i = 0; i < NS - 1; ++i) {
-    if (start + i * TS < end) stage(i, start + i * TS);
-    else cp_async_commit();
-  }
-  int cur = 0;
-  for (int t0 = start; t0 < end; t0 += TS) {
-    cp_async_wait_group<NS - 2>();
-    __syncthreads();  // block `cur` landed; everyone is done with the previous block's stage
-    {
-      const int tn = t0 + (NS - 1) * TS;
-      const int nb = cur == 0 ? NS - 1 : cur - 1;
-      if (tn < end) stage(nb, tn);
-      else cp_async_commit();
-    }
-    const Stage<VT> &st = stg[cur];
-    const int cnt = min(TS, end - t0);
+  const int perm = lane & 15;
+  bool ok = true;
+  int i = 0;
+  for (; i < nb; ++i) {
+    // block i landed; everyone is done with the stage of block i - 1
+    ok = __syncthreads_and(mbar_wait(&s_bar[i % NS], (i / NS) & 1));
+    if (!ok) break;
+    if (tid == 0 && issued < nb) issue(issued++);
+    const Stage<VT> &st = stg[i % NS];
+    const float *rc = st.rec;
+    const int t0 = start + i * TS, cnt = min(TS, end - t0);
     float A[TS][TS], bt[TS], Pr[TS];  // 16-byte loads: A rows, beta, this lane's P row
     auto ld = [](const float *p, float *d) {
       const float4 x = *reinterpret_cast<const float4 *>(p);
       d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
     };
-    ld(&st.b[0], bt);
-    ld(&st.b[4], bt + 4);
-    ld(&st.co[to][TS], Pr);  // P[to][t]
-    ld(&st.co[to][TS + 4], Pr + 4);
+    ld(rc + kOffB, bt);
+    ld(rc + kOffB + 4, bt + 4);
+    ld(rc + kOffCO + to * NCO + TS, Pr);  // P[to][t]
+    ld(rc + kOffCO + to * NCO + TS + 4, Pr + 4);
 #pragma unroll
     for (int t = 1; t < TS; ++t) {
-      ld(&st.co[t][0], A[t]);
-      if (t > 4) ld(&st.co[t][4], A[t] + 4);
+      ld(rc + kOffCO + t * NCO, A[t]);
+      if (t > 4) ld(rc + kOffCO + t * NCO + 4, A[t] + 4);
     }
     // Slot i of this lane holds operand row i ^ (lane & 15) (a scaled key for rows < 8, a
     // scaled query above): then at every level of the reduce-scatter below the values this
     // lane keeps sit in the lower slots and the ones it hands over in the upper slots, for
     // every lane, so the butterfly needs no per-lane selects.
-    const int perm = lane & 15;
     float2 kq[2 * TS][2], ke[TS][2], eg[2];
 #pragma unroll
-    for (int i = 0; i < 2 * TS; ++i) {
-      const float4 a = *reinterpret_cast<const float4 *>(&st.kq[i ^ perm][k0]);
-      kq[i][0] = make_float2(a.x, a.y); kq[i][1] = make_float2(a.z, a.w);
+    for (int q = 0; q < 2 * TS; ++q) {
+      const float4 a = *reinterpret_cast<const float4 *>(rc + kOffKQ + (q ^ perm) * KB + k0);
+      kq[q][0] = make_float2(a.x, a.y); kq[q][1] = make_float2(a.z, a.w);
     }
 #pragma unroll
     for (int t = 0; t < TS; ++t) {
-      const float4 c = *reinterpret_cast<const float4 *>(&st.ke[t][k0]);
+      const float4 c = *reinterpret_cast<const float4 *>(rc + kOffKE + t * KB + k0);
       ke[t][0] = make_float2(c.x, c.y); ke[t][1] = make_float2(c.z, c.w);
     }
     {
-      const float4 e = *reinterpret_cast<const float4 *>(&st.eg[k0]);
+      const float4 e = *reinterpret_cast<const float4 *>(rc + kOffEG + k0);
       eg[0] = make_float2(e.x, e.y); eg[1] = make_float2(e.z, e.w);
     }
 #pragma unroll
     for (int p = 0; p < R; ++p) {
       const int row = warp * R + p;
-      float x[2 * TS];  // x[i]: this lane's part of the dot with operand row i ^ perm
+      float x[2 * TS];  // x[q]: this lane's part of the dot with operand row q ^ perm
 #pragma unroll
-      for (int i = 0; i < 2 * TS; ++i) {
-        const float2 u = __ffma2_rn(s[p][1], kq[i][1], __fmul2_rn(s[p][0], kq[i][0]));
-        x[i] = u.x + u.y;
+      for (int q = 0; q < 2 * TS; ++q) {
+        const float2 u = __ffma2_rn(s[p][1], kq[q][1], __fmul2_rn(s[p][0], kq[q][0]));
+        x[q] = u.x + u.y;
       }
 #pragma unroll
       for (int m = TS; m >= 1; m >>= 1)
 #pragma unroll
-        for (int i = 0; i < m; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i + m], m);
-      // lane i (and i + 16) now holds the whole dot with row i: a_i for i < 8, b_(i-8) above
+        for (int q = 0; q < m; ++q) x[q] += __shfl_xor_sync(0xffffffffu, x[q + m], m);
+      // lane q (and q + 16) now holds the whole dot with row q: a_q for q < 8, b_(q-8) above
       const float val = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
       float r[TS], d[TS];
+      ld(st.v[row], r);
+      ld(st.v[row] + 4, r + 4);
 #pragma unroll
-      for (int t = 0; t < TS; ++t) r[t] = st.v[t][row] - __shfl_sync(0xffffffffu, val, t);
+      for (int t = 0; t < TS; ++t) r[t] -= __shfl_sync(0xffffffffu, val, t);
 #pragma unroll
       for (int u = 0; u < TS; ++u) {
         d[u] = bt[u] * r[u];
@@ -415,9 +365,15 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         s[p][1] = __ffma2_rn(du, ke[u][1], s[p][1]);
       }
     }
-    cur = cur == NS - 1 ? 0 : cur + 1;
   }
-  cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  if (!ok) {
+    if (tid == 0) {
+      flag_error(pv.err, RSC_DEVERR_TIMEOUT);
+      // let every requested bulk copy land before the shared memory is released
+      for (int k = i; k < issued; ++k) mbar_wait(&s_bar[k % NS], (k / NS) & 1);
+    }
+    return;  // the slot's rows stay as they were
+  }
 #pragma unroll
   for (int p = 0; p < R; ++p)
     st16_stream(S + (size_t)(warp * R + p) * KB + k0,
@@ -426,13 +382,12 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
 }
 
 #ifndef RSC_BLK_STAGES
-#define RSC_BLK_STAGES 2
+#define RSC_BLK_STAGES 3
 #endif
 
 template <typename IO, int V, int NW, int R>
 int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                const uint8_t *has_init, const PrefillWs &w, const BlockedWs &bw,
-                const float *beta, void *out, cudaStream_t s) {
+                const uint8_t *has_init, const float *recs, void *out, cudaStream_t s) {
   constexpr int VT = NW * R, NS = RSC_BLK_STAGES;
   static_assert(NS >= 2 && sizeof(Stage<VT>) % 16 == 0, "stages");
   constexpr size_t smem = NS * sizeof(Stage<VT>);
@@ -445,8 +400,8 @@ int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int
                : RSC_ECUDA;
   });
   if (rc != RSC_OK) return rc;
-  kern<<<dim3(V / VT, a.pv.H, N), 32 * NW, smem, s>>>(a.pv, a.layer, slots, cu, T, has_init, w,
-                                                      bw, beta, static_cast<IO *>(out));
+  kern<<<dim3(V / VT, a.pv.H, N), 32 * NW, smem, s>>>(a.pv, a.layer, slots, cu, T, has_init, recs,
+                                                      static_cast<IO *>(out));
   return launch_status();
 }
 
@@ -470,21 +425,21 @@ int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int
 
 template <typename IO, int V>
 int run_blocked_v(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                  const uint8_t *has_init, const PrefillWs &w, const BlockedWs &bw,
-                  const float *beta, void *out, cudaStream_t s) {
+                  const uint8_t *has_init, const float *recs, void *out, cudaStream_t s) {
   const long wide = (long)(V / 32) * a.pv.H * N;
   if (wide >= RSC_BLOCKED_MIN_CTAS)
-    return run_blocked<IO, V, RSC_BLK_WIDE_NW, RSC_BLK_WIDE_R>(a, slots, cu, N, T, has_init, w,
-                                                                bw, beta, out, s);
-  return run_blocked<IO, V, RSC_BLK_SMALL_NW, RSC_BLK_SMALL_R>(a, slots, cu, N, T, has_init, w,
-                                                                bw, beta, out, s);
+    return run_blocked<IO, V, RSC_BLK_WIDE_NW, RSC_BLK_WIDE_R>(a, slots, cu, N, T, has_init, recs,
+                                                                out, s);
+  return run_blocked<IO, V, RSC_BLK_SMALL_NW, RSC_BLK_SMALL_R>(a, slots, cu, N, T, has_init, recs,
+                                                                out, s);
 }
 
 }  // namespace
 
-size_t prefill_blocked_bytes(const PoolView &pv, int T) {
-  return prefill_prep_bytes(pv, T) + 2 * align256((size_t)T * pv.H * KB * 4) +
-         align256((size_t)T * pv.H * NCO * 4);
+// Blocks of the grid: sequence i's ceil(len_i / 8) blocks start at floor(cu[i] / 8) + i, so
+// floor(T / 8) + N records per head cover every block.
+size_t prefill_blocked_bytes(const PoolView &pv, int N, int T) {
+  return ((size_t)T / TS + N) * pv.H * rec_floats(pv.V) * 4;
 }
 
 int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
@@ -492,16 +447,15 @@ int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32
                            const float *conv_w, const float *g, const float *beta, void *out,
                            void *ws, cudaStream_t s) {
   if (a.st != RSC_F32 || a.pv.K != KB) return RSC_EDTYPE;
-  const PrefillWs w = prefill_carve(ws, a.pv, T);
-  const BlockedWs bw = blocked_carve(ws, a.pv, T);
+  float *recs = static_cast<float *>(ws);
   const bool bf = a.io == RSC_BF16, kda = a.gate == RSC_GATE_KDA;
   int rc = RSC_OK;
   if (T > 0) {
     const dim3 grid((unsigned)(T / TS + N), a.pv.H);
 #define RSC_BLK(IO_, V_, G_)                                                                  \
   prefill_blk_kernel<IO_, V_, G_><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, N, T, has_init, \
-                                                       static_cast<const IO_ *>(qkv), conv_w, w, \
-                                                       bw, g)
+                                                       static_cast<const IO_ *>(qkv), conv_w, g, \
+                                                       beta, recs)
     if (a.pv.V == 128) {
       if (bf) { if (kda) RSC_BLK(bf16, 128, RSC_GATE_KDA); else RSC_BLK(bf16, 128, RSC_GATE_GDN); }
       else { if (kda) RSC_BLK(float, 128, RSC_GATE_KDA); else RSC_BLK(float, 128, RSC_GATE_GDN); }
@@ -515,11 +469,11 @@ int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32
     if ((rc = launch_status()) != RSC_OK) return rc;
   }
   if (a.pv.V == 128)
-    rc = bf ? run_blocked_v<bf16, 128>(a, slots, cu, N, T, has_init, w, bw, beta, out, s)
-            : run_blocked_v<float, 128>(a, slots, cu, N, T, has_init, w, bw, beta, out, s);
+    rc = bf ? run_blocked_v<bf16, 128>(a, slots, cu, N, T, has_init, recs, out, s)
+            : run_blocked_v<float, 128>(a, slots, cu, N, T, has_init, recs, out, s);
   else if (a.pv.V == 64)
-    rc = bf ? run_blocked_v<bf16, 64>(a, slots, cu, N, T, has_init, w, bw, beta, out, s)
-            : run_blocked_v<float, 64>(a, slots, cu, N, T, has_init, w, bw, beta, out, s);
+    rc = bf ? run_blocked_v<bf16, 64>(a, slots, cu, N, T, has_init, recs, out, s)
+            : run_blocked_v<float, 64>(a, slots, cu, N, T, has_init, recs, out, s);
   else
     return RSC_EDTYPE;
   if (rc != RSC_OK) return rc;

@@ -73,7 +73,7 @@ int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t 
 int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
                           int T, const uint8_t *has_init, const void *qkv, cudaStream_t s);
 // Blocked fp32 path (fp32 state, K = 128): the recurrence eight tokens at a time.
-size_t prefill_blocked_bytes(const PoolView &pv, int T);
+size_t prefill_blocked_bytes(const PoolView &pv, int N, int T);
 int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
                            int T, const uint8_t *has_init, const void *qkv,
                            const float *conv_w, const float *g, const float *beta, void *out,
