@@ -20,7 +20,8 @@ Legs reported in the same line (each timed separately with CUDA events):
   slot_copy    64 (src, dst) pairs of the 69-layer decode pool, all layers, one launch
   spec         verify of 8 tokens (anchor + 7 drafts) for 64 requests into a 16-deep
                cache, then commit of a seeded accept count per request
-The oracle (plain fp64 C, one host core) is timed on a bounded sample as cpu_baseline.
+The oracle (plain fp64 C) is timed on a bounded sample, on one and on all host cores, as
+cpu_baseline.
 
 --impl reference times the oracle itself on the same workload (rank 0 only).
 Multi-GPU: replicas only (the layer step has no exchange between requests or heads);

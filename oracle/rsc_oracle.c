@@ -18,7 +18,7 @@
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - L2 norm: x / sqrt(sum x^2 + eps) with eps = 1e-6 ([p1] replay step prints eps, no value).
- *  - q is not scaled (the spec output is o = S q).
+ *  - q is not scaled: the output is o = S q.
  *  - conv: no bias, no activation; taps w[c][0..2] act on the window rows (oldest first),
  *    w[c][3] on the current input.
  *  - channel split of the conv output: [q: H*K | k: H*K | v: H*V], head-major in each block.
