@@ -68,8 +68,8 @@ extern "C" {
 #define RSC_DEVERR_GATE   16 /* prefill: a growing gate (g > 0) raised a cumulative log
                                 gate beyond what the blocked forms represent -- on the
                                 tensor-core path by more than 60 above one of a chunk's
-                                16-token reference points, on the fp32 head_k 128 path
-                                by more than 80 within an 8-token block; that block's
+                                16-token reference points, on the other pools' blocked
+                                path by more than 80 within an 8-token block; that block's
                                 result is not reliable.  Never set for a decaying gate
                                 (g <= 0), however strong.                             */
 #define RSC_DEVERR_RING   32 /* a ReplaySSM ring position outside [0, depth)            */
@@ -217,9 +217,9 @@ int kda_prefill_workspace_size(const rsc_pool *pool, int num_seqs, int total_tok
  * contraction on the tcgen05 tensor cores with bf16 operands and fp32 accumulation);
  * any decaying gate (g <= 0, as the models' gates are) is exact to that precision,
  * however strong; a growing gate beyond the range above flags RSC_DEVERR_GATE.
- * fp32-state pools with head_k == 128 run the recurrence eight tokens at a time in a
- * closed form (exact algebra, fp32 on the CUDA cores; the same gate rule, with its own
- * range).  Pools with head_k == 64 run it token by token in fp32.
+ * Every other pool (fp32 state, or head_k == 64) runs the recurrence eight tokens at a
+ * time in a closed form (exact algebra, fp32 on the CUDA cores, the state rounded once at
+ * the end of the call; the same gate rule, with its own range).
  * Errors: RSC_EINVAL, RSC_ERANGE, RSC_EALIGN, RSC_ENOSPACE, RSC_ECUDA. */
 int kda_prefill_chunk(rsc_pool *pool, int layer, const int32_t *slot_ids,
                       const int32_t *cu_seqlens, int num_seqs, int total_tokens,

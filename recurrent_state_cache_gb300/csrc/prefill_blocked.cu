@@ -1,5 +1,5 @@
-// prefill_blocked.cu -- prefill of fp32-state pools with head_k 128: the exact recurrence
-// taken eight tokens at a time in closed form.
+// prefill_blocked.cu -- prefill of every pool the tensor-core form does not take (fp32 state,
+// or head_k 64): the exact recurrence taken eight tokens at a time in closed form, in fp32.
 //
 // Sources: "SGLang之KV Cache内存池机制" §8.5 forward_extend (each sequence starts from its
 // slot's state or from zero, the final state goes back to the slot; sequences packed by
@@ -40,7 +40,6 @@ namespace rsc {
 namespace {
 
 constexpr int TS = 8;      // tokens per block
-constexpr int KB = 128;    // head_k of the blocked form
 constexpr int NCO = 16;    // per token: its A row (8), then its P row (8)
 constexpr float kMaxRise = 80.f;  // largest growth of a log gate within a block
 
@@ -49,33 +48,37 @@ constexpr float kMaxRise = 80.f;  // largest growth of a log gate within a block
 // [K], the A rows then the P rows [8][16], beta [8] (+8 zero), then the values [V][8] (value
 // channel-major, so a row tile's values are one contiguous run).  Rows past the sequence end
 // are zero, which makes their deltas zero.
-constexpr int kOffKQ = 0;
-constexpr int kOffKE = kOffKQ + 2 * TS * KB;
-constexpr int kOffEG = kOffKE + TS * KB;
-constexpr int kOffCO = kOffEG + KB;
-constexpr int kOffB = kOffCO + TS * NCO;
-constexpr int kOffV = kOffB + 2 * TS;  // also the floats of the shared part of a record
-__host__ __device__ constexpr int rec_floats(int V) { return kOffV + TS * V; }
-static_assert((kOffV * 4) % 16 == 0, "16-byte bulk copies");
+template <int K>
+struct Rec {
+  static constexpr int KQ = 0;
+  static constexpr int KE = KQ + 2 * TS * K;
+  static constexpr int EG = KE + TS * K;
+  static constexpr int CO = EG + K;
+  static constexpr int B = CO + TS * NCO;
+  static constexpr int V = B + 2 * TS;  // also the floats of the shared part of a record
+  static_assert((V * 4) % 16 == 0, "16-byte bulk copies");
+  __host__ __device__ static constexpr int floats(int Vd) { return V + TS * Vd; }
+};
 
 // Pair indices of the 64 coefficient sums: A[t][s] (s < t) at t(t-1)/2 + s, then P[t][s]
 // (s <= t) at 28 + t(t+1)/2 + s.
 __host__ __device__ constexpr int ia(int t, int s) { return t * (t - 1) / 2 + s; }
 __host__ __device__ constexpr int ip(int t, int s) { return 28 + t * (t + 1) / 2 + s; }
 
-// Per (block, head): the conv of the head's q / k / v channels over the block's tokens (one
-// thread per key channel, also owning value channel k when k < V), the L2 norms of q and k,
+// Per (block, head): the conv of the head's q / k / v channels over the block's tokens (thread
+// k owns key channel k when k < K and value channel k when k < V), the L2 norms of q and k,
 // then the block's operands.  A thread reads its channels' 11 inputs once (3 before the
 // block: the sequence, the slot's window before the sequence start, or zero for a fresh
 // sequence) where a conv per token would read 32.
-template <typename IO, int V, int GATE>
+template <typename IO, int K, int V, int GATE>
 __global__ void __launch_bounds__(128)
 prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                    const int32_t *__restrict__ cu, int N, int T,
                    const uint8_t *__restrict__ has_init, const IO *__restrict__ qkv,
                    const float *__restrict__ conv_w, const float *__restrict__ g,
                    const float *__restrict__ beta, float *__restrict__ recs) {
-  static_assert(V <= KB, "a thread per key channel covers the value channels");
+  using L = Rec<K>;
+  static_assert(K <= 128 && V <= 128, "a thread per channel");
   __shared__ float red[4][64];
   __shared__ float nrm[2 * TS];  // 1/|q_t|, 1/|k_t|
   const int b = blockIdx.x, h = blockIdx.y, k = threadIdx.x, lane = k & 31, warp = k >> 5;
@@ -95,7 +98,7 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
   if (slot < 0 || slot > pv.P) return;  // flagged by the recurrence
   const bool init = has_init == nullptr || has_init[lo] != 0;
   const IO *W = reinterpret_cast<const IO *>(pv.conv) + ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
-  float *rec = recs + ((size_t)b * H + h) * rec_floats(V);
+  float *rec = recs + ((size_t)b * H + h) * L::floats(V);
 
   auto conv_rows = [&](int c, float (&y)[TS]) {
     float x[TS + 3];  // inputs at tokens t0 - 3 .. t0 + 7 (oldest first)
@@ -111,13 +114,18 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #pragma unroll
     for (int t = 0; t < TS; ++t) y[t] = t < cnt ? conv4(wc, x[t], x[t + 1], x[t + 2], x[t + 3]) : 0.f;
   };
+  const bool key = k < K;  // this thread's key channel; threads past K add zeros
   float q[TS], kk[TS];
-  conv_rows(h * KB + k, q);
-  conv_rows(H * KB + h * KB + k, kk);
+#pragma unroll
+  for (int t = 0; t < TS; ++t) q[t] = kk[t] = 0.f;
+  if (key) {
+    conv_rows(h * K + k, q);
+    conv_rows(H * K + h * K + k, kk);
+  }
   if (k < V) {
     float y[TS];
-    conv_rows(2 * H * KB + h * V + k, y);
-    float4 *dv = reinterpret_cast<float4 *>(rec + kOffV + TS * k);
+    conv_rows(2 * H * K + h * V + k, y);
+    float4 *dv = reinterpret_cast<float4 *>(rec + L::V + TS * k);
     dv[0] = make_float4(y[0], y[1], y[2], y[3]);
     dv[1] = make_float4(y[4], y[5], y[6], y[7]);
   }
@@ -148,9 +156,9 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #pragma unroll
   for (int t = 0; t < TS; ++t) {
     al[t] = 1.f;
-    if (t < cnt) {
+    if (t < cnt && key) {
       const size_t th = (size_t)(t0 + t) * H + h;
-      const float gt = GATE == RSC_GATE_KDA ? g[th * KB + k] : g[th];
+      const float gt = GATE == RSC_GATE_KDA ? g[th * K + k] : g[th];
       al[t] = expf(gt);
       acc += gt;
       rise = fmaxf(rise, acc - low);
@@ -166,14 +174,16 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
 #pragma unroll
     for (int t = TS - 1; t >= 0; --t) { ee[t] = b2; b2 *= al[t]; }
   }
+  if (key) {
 #pragma unroll
-  for (int t = 0; t < TS; ++t) {  // zero past the sequence end: q, k are
-    rec[kOffKQ + t * KB + k] = kk[t] * eg[t];
-    rec[kOffKQ + (TS + t) * KB + k] = q[t] * eg[t];
-    rec[kOffKE + t * KB + k] = kk[t] * ee[t];
+    for (int t = 0; t < TS; ++t) {  // zero past the sequence end: q, k are
+      rec[L::KQ + t * K + k] = kk[t] * eg[t];
+      rec[L::KQ + (TS + t) * K + k] = q[t] * eg[t];
+      rec[L::KE + t * K + k] = kk[t] * ee[t];
+    }
+    rec[L::EG + k] = eg[TS - 1];
   }
-  rec[kOffEG + k] = eg[TS - 1];
-  if (k < 2 * TS) rec[kOffB + k] = k < cnt ? beta[(size_t)(t0 + k) * H + h] : 0.f;
+  if (k < 2 * TS) rec[L::B + k] = k < cnt ? beta[(size_t)(t0 + k) * H + h] : 0.f;
 
   // this channel's terms of the 64 sums (rows t >= cnt come out zero: their q, k are zero)
   float x[64];
@@ -204,41 +214,83 @@ prefill_blk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
       const int e = ip(t, c - TS);
       v = red[0][e] + red[1][e] + red[2][e] + red[3][e];
     }
-    rec[kOffCO + k] = v;  // rows past the end: zero sums
+    rec[L::CO + k] = v;  // rows past the end: zero sums
   }
 }
 
 // One stage of block operands in shared memory: the record's shared part and this tile's
 // values, each one bulk copy.
-template <int VT>
+template <int K, int VT>
 struct Stage {
-  float rec[kOffV];
+  float rec[Rec<K>::V];
   float v[VT][TS];  // values of the tile's rows, [row][token]
 };
 
+// E consecutive fp32 values (E = 2 or 4, 8- or 16-byte aligned) as E/2 pairs.
+template <int E>
+__device__ __forceinline__ void ld_pairs(const float *p, float2 (&d)[E / 2]) {
+  if constexpr (E == 4) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    d[0] = make_float2(x.x, x.y);
+    d[1] = make_float2(x.z, x.w);
+  } else {
+    d[0] = *reinterpret_cast<const float2 *>(p);
+  }
+}
+// A lane's E state entries in the state dtype.
+template <typename ST, int E>
+__device__ __forceinline__ void ld_state(const ST *p, float2 (&d)[E / 2]) {
+  if constexpr (sizeof(ST) == 4) {
+    ld_pairs<E>(reinterpret_cast<const float *>(p), d);
+  } else if constexpr (E == 4) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    d[0] = make_float2(bf16lo(u.x), bf16hi(u.x));
+    d[1] = make_float2(bf16lo(u.y), bf16hi(u.y));
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+    d[0] = make_float2(bf16lo(u), bf16hi(u));
+  }
+}
+template <typename ST, int E>
+__device__ __forceinline__ void st_state(ST *p, const float2 (&d)[E / 2]) {
+  if constexpr (sizeof(ST) == 4) {
+    if constexpr (E == 4)
+      st16_stream(p, make_uint4(__float_as_uint(d[0].x), __float_as_uint(d[0].y),
+                                __float_as_uint(d[1].x), __float_as_uint(d[1].y)));
+    else
+      *reinterpret_cast<float2 *>(p) = d[0];
+  } else if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(p) =
+        make_uint2(pack_bf16x2(d[0].x, d[0].y), pack_bf16x2(d[1].x, d[1].y));
+  } else {
+    *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(d[0].x, d[0].y);
+  }
+}
+
 // One CTA: rows [j VT, (j+1) VT) of head h of sequence n's state, VT = NW R: NW warps of R
-// rows each, a row across a whole warp (lane i holds key channels 4i .. 4i+3).  Thread 0
-// stages each block's record with two bulk copies (TMA) NS - 1 blocks ahead, completing on
-// that stage's mbarrier.  Per block a lane loads its channels of the block's scaled keys,
-// queries and end-scaled keys into registers once and applies them to its R rows.  Per row:
-// the 16 row dots, one butterfly reduce-scatter (lane t then holds a_t, lane 8+t holds b_t),
-// the 8 a's gathered, the forward substitution, o_t written by lane 8+t, the row moved to the
-// block end.
-template <typename IO, int V, int NW, int R, int NS>
+// rows each, a row across a whole warp (lane i holds key channels E i .. E i + E - 1, E =
+// K / 32).  Thread 0 stages each block's record with two bulk copies (TMA) NS - 1 blocks
+// ahead, completing on that stage's mbarrier.  Per block a lane loads its channels of the
+// block's scaled keys, queries and end-scaled keys into registers once and applies them to
+// its R rows.  Per row: the 16 row dots, one butterfly reduce-scatter (lane t then holds a_t,
+// lane 8+t holds b_t), the 8 a's gathered, the forward substitution, o_t written by lane 8+t,
+// the row moved to the block end.  The state stays in fp32 registers for the whole call and
+// is rounded to the state dtype once, at the end.
+template <typename ST, typename IO, int K, int V, int NW, int R, int NS>
 __global__ void __launch_bounds__(32 * NW)
 prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots,
                        const int32_t *__restrict__ cu, int T, const uint8_t *__restrict__ has_init,
                        const float *__restrict__ recs, IO *__restrict__ out) {
-  constexpr int VT = NW * R;
-  constexpr uint32_t kBytesRec = kOffV * 4, kBytesV = VT * TS * 4;
-  static_assert(V % VT == 0 && kBytesV % 16 == 0, "row tile");
+  using L = Rec<K>;
+  constexpr int VT = NW * R, E = K / 32, E2 = E / 2;
+  constexpr uint32_t kBytesRec = L::V * 4, kBytesV = VT * TS * 4;
+  static_assert(V % VT == 0 && kBytesV % 16 == 0 && (E == 2 || E == 4), "row tile, lanes");
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Stage<VT> *stg = reinterpret_cast<Stage<VT> *>(smem_raw);
+  Stage<K, VT> *stg = reinterpret_cast<Stage<K, VT> *>(smem_raw);
   __shared__ __align__(8) uint64_t s_bar[NS];
-  __shared__ int s_fail;
 
   const int j = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5, k0 = 4 * lane;
+  const int lane = tid & 31, warp = tid >> 5, k0 = E * lane;
   const int H = pv.H;
   const int start = cu[n], end = cu[n + 1];
   if (start < 0 || end < start || end > T) {
@@ -252,29 +304,30 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
   }
   const bool init = has_init == nullptr || has_init[n] != 0;
   const size_t prow = (size_t)layer * (pv.P + 1) + slot;
-  float *S = reinterpret_cast<float *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * KB;
-  float2 s[R][2];  // rows warp R + p, channels k0 .. k0+3
+  ST *S = reinterpret_cast<ST *>(pv.ssm) + ((prow * H + h) * V + (size_t)j * VT) * K;
+  float2 s[R][E2];  // rows warp R + p, channels k0 .. k0 + E - 1
 #pragma unroll
   for (int p = 0; p < R; ++p) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init) x = *reinterpret_cast<const float4 *>(S + (size_t)(warp * R + p) * KB + k0);
-    s[p][0] = make_float2(x.x, x.y);
-    s[p][1] = make_float2(x.z, x.w);
+    if (init) {
+      ld_state<ST, E>(S + (size_t)(warp * R + p) * K + k0, s[p]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E2; ++e) s[p][e] = make_float2(0.f, 0.f);
+    }
   }
 
   const int nb = (end - start + TS - 1) / TS;
-  const float *rec0 = recs + ((size_t)(start / TS + n) * H + h) * rec_floats(V);
+  const float *rec0 = recs + ((size_t)(start / TS + n) * H + h) * L::floats(V);
   auto issue = [&](int i) {  // thread 0: block i of the sequence into stage i % NS
-    Stage<VT> &st = stg[i % NS];
-    const float *rec = rec0 + (size_t)i * H * rec_floats(V);
+    Stage<K, VT> &st = stg[i % NS];
+    const float *rec = rec0 + (size_t)i * H * L::floats(V);
     mbar_arrive_expect_tx(&s_bar[i % NS], kBytesRec + kBytesV);
     bulk_g2s(st.rec, rec, kBytesRec, &s_bar[i % NS]);
-    bulk_g2s(st.v, rec + kOffV + (size_t)j * VT * TS, kBytesV, &s_bar[i % NS]);
+    bulk_g2s(st.v, rec + L::V + (size_t)j * VT * TS, kBytesV, &s_bar[i % NS]);
   };
   int issued = 0;
   if (tid == 0) {
     for (int b = 0; b < NS; ++b) mbar_init(&s_bar[b], 1);
-    s_fail = 0;
     for (; issued < NS - 1 && issued < nb; ++issued) issue(issued);
   }
   __syncthreads();
@@ -288,7 +341,7 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     ok = __syncthreads_and(mbar_wait(&s_bar[i % NS], (i / NS) & 1));
     if (!ok) break;
     if (tid == 0 && issued < nb) issue(issued++);
-    const Stage<VT> &st = stg[i % NS];
+    const Stage<K, VT> &st = stg[i % NS];
     const float *rc = st.rec;
     const int t0 = start + i * TS, cnt = min(TS, end - t0);
     float A[TS][TS], bt[TS], Pr[TS];  // 16-byte loads: A rows, beta, this lane's P row
@@ -296,41 +349,34 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
       const float4 x = *reinterpret_cast<const float4 *>(p);
       d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
     };
-    ld(rc + kOffB, bt);
-    ld(rc + kOffB + 4, bt + 4);
-    ld(rc + kOffCO + to * NCO + TS, Pr);  // P[to][t]
-    ld(rc + kOffCO + to * NCO + TS + 4, Pr + 4);
+    ld(rc + L::B, bt);
+    ld(rc + L::B + 4, bt + 4);
+    ld(rc + L::CO + to * NCO + TS, Pr);  // P[to][t]
+    ld(rc + L::CO + to * NCO + TS + 4, Pr + 4);
 #pragma unroll
     for (int t = 1; t < TS; ++t) {
-      ld(rc + kOffCO + t * NCO, A[t]);
-      if (t > 4) ld(rc + kOffCO + t * NCO + 4, A[t] + 4);
+      ld(rc + L::CO + t * NCO, A[t]);
+      if (t > 4) ld(rc + L::CO + t * NCO + 4, A[t] + 4);
     }
-    // Slot i of this lane holds operand row i ^ (lane & 15) (a scaled key for rows < 8, a
+    // Slot q of this lane holds operand row q ^ (lane & 15) (a scaled key for rows < 8, a
     // scaled query above): then at every level of the reduce-scatter below the values this
     // lane keeps sit in the lower slots and the ones it hands over in the upper slots, for
     // every lane, so the butterfly needs no per-lane selects.
-    float2 kq[2 * TS][2], ke[TS][2], eg[2];
+    float2 kq[2 * TS][E2], ke[TS][E2], eg[E2];
 #pragma unroll
-    for (int q = 0; q < 2 * TS; ++q) {
-      const float4 a = *reinterpret_cast<const float4 *>(rc + kOffKQ + (q ^ perm) * KB + k0);
-      kq[q][0] = make_float2(a.x, a.y); kq[q][1] = make_float2(a.z, a.w);
-    }
+    for (int q = 0; q < 2 * TS; ++q) ld_pairs<E>(rc + L::KQ + (q ^ perm) * K + k0, kq[q]);
 #pragma unroll
-    for (int t = 0; t < TS; ++t) {
-      const float4 c = *reinterpret_cast<const float4 *>(rc + kOffKE + t * KB + k0);
-      ke[t][0] = make_float2(c.x, c.y); ke[t][1] = make_float2(c.z, c.w);
-    }
-    {
-      const float4 e = *reinterpret_cast<const float4 *>(rc + kOffEG + k0);
-      eg[0] = make_float2(e.x, e.y); eg[1] = make_float2(e.z, e.w);
-    }
+    for (int t = 0; t < TS; ++t) ld_pairs<E>(rc + L::KE + t * K + k0, ke[t]);
+    ld_pairs<E>(rc + L::EG + k0, eg);
 #pragma unroll
     for (int p = 0; p < R; ++p) {
       const int row = warp * R + p;
       float x[2 * TS];  // x[q]: this lane's part of the dot with operand row q ^ perm
 #pragma unroll
       for (int q = 0; q < 2 * TS; ++q) {
-        const float2 u = __ffma2_rn(s[p][1], kq[q][1], __fmul2_rn(s[p][0], kq[q][0]));
+        float2 u = __fmul2_rn(s[p][0], kq[q][0]);
+#pragma unroll
+        for (int e = 1; e < E2; ++e) u = __ffma2_rn(s[p][e], kq[q][e], u);
         x[q] = u.x + u.y;
       }
 #pragma unroll
@@ -356,13 +402,13 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
         for (int u = 0; u < TS; ++u) o = fmaf(Pr[u], d[u], o);
         out[((size_t)(t0 + to) * H + h) * V + (size_t)j * VT + row] = from_f32<IO>(o);
       }
-      s[p][0] = __fmul2_rn(s[p][0], eg[0]);
-      s[p][1] = __fmul2_rn(s[p][1], eg[1]);
+#pragma unroll
+      for (int e = 0; e < E2; ++e) s[p][e] = __fmul2_rn(s[p][e], eg[e]);
 #pragma unroll
       for (int u = 0; u < TS; ++u) {
         const float2 du = make_float2(d[u], d[u]);
-        s[p][0] = __ffma2_rn(du, ke[u][0], s[p][0]);
-        s[p][1] = __ffma2_rn(du, ke[u][1], s[p][1]);
+#pragma unroll
+        for (int e = 0; e < E2; ++e) s[p][e] = __ffma2_rn(du, ke[u][e], s[p][e]);
       }
     }
   }
@@ -375,23 +421,20 @@ prefill_blocked_kernel(PoolView pv, int layer, const int32_t *__restrict__ slots
     return;  // the slot's rows stay as they were
   }
 #pragma unroll
-  for (int p = 0; p < R; ++p)
-    st16_stream(S + (size_t)(warp * R + p) * KB + k0,
-                make_uint4(__float_as_uint(s[p][0].x), __float_as_uint(s[p][0].y),
-                           __float_as_uint(s[p][1].x), __float_as_uint(s[p][1].y)));
+  for (int p = 0; p < R; ++p) st_state<ST, E>(S + (size_t)(warp * R + p) * K + k0, s[p]);
 }
 
 #ifndef RSC_BLK_STAGES
 #define RSC_BLK_STAGES 3
 #endif
 
-template <typename IO, int V, int NW, int R>
+template <typename ST, typename IO, int K, int V, int NW, int R>
 int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
                 const uint8_t *has_init, const float *recs, void *out, cudaStream_t s) {
   constexpr int VT = NW * R, NS = RSC_BLK_STAGES;
-  static_assert(NS >= 2 && sizeof(Stage<VT>) % 16 == 0, "stages");
-  constexpr size_t smem = NS * sizeof(Stage<VT>);
-  auto *kern = prefill_blocked_kernel<IO, V, NW, R, NS>;
+  static_assert(NS >= 2 && sizeof(Stage<K, VT>) % 16 == 0, "stages");
+  constexpr size_t smem = NS * sizeof(Stage<K, VT>);
+  auto *kern = prefill_blocked_kernel<ST, IO, K, V, NW, R, NS>;
   static PerDeviceFlag attr;
   const int rc = once_per_device(attr, [&] {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
@@ -423,61 +466,60 @@ int run_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int
 #define RSC_BLK_WIDE_R 8
 #endif
 
-template <typename IO, int V>
-int run_blocked_v(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N, int T,
-                  const uint8_t *has_init, const float *recs, void *out, cudaStream_t s) {
-  const long wide = (long)(V / 32) * a.pv.H * N;
-  if (wide >= RSC_BLOCKED_MIN_CTAS)
-    return run_blocked<IO, V, RSC_BLK_WIDE_NW, RSC_BLK_WIDE_R>(a, slots, cu, N, T, has_init, recs,
-                                                                out, s);
-  return run_blocked<IO, V, RSC_BLK_SMALL_NW, RSC_BLK_SMALL_R>(a, slots, cu, N, T, has_init, recs,
-                                                                out, s);
-}
+template <typename ST, typename IO, int K, int V, int GATE>
+struct BlockedLaunch {
+  static int run(const LayerArgs *a, const int32_t *slots, const int32_t *cu, int N, int T,
+                 const uint8_t *has_init, const void *qkv, const float *conv_w, const float *g,
+                 const float *beta, void *out, float *recs, cudaStream_t s) {
+    if (T > 0) {
+      prefill_blk_kernel<IO, K, V, GATE><<<dim3((unsigned)(T / TS + N), a->pv.H), 128, 0, s>>>(
+          a->pv, a->layer, slots, cu, N, T, has_init, static_cast<const IO *>(qkv), conv_w, g,
+          beta, recs);
+      if (launch_status() != RSC_OK) return RSC_ECUDA;
+    }
+    const long wide = (long)(V / 32) * a->pv.H * N;
+    const int rc =
+        wide >= RSC_BLOCKED_MIN_CTAS
+            ? run_blocked<ST, IO, K, V, RSC_BLK_WIDE_NW, RSC_BLK_WIDE_R>(*a, slots, cu, N, T,
+                                                                          has_init, recs, out, s)
+            : run_blocked<ST, IO, K, V, RSC_BLK_SMALL_NW, RSC_BLK_SMALL_R>(*a, slots, cu, N, T,
+                                                                            has_init, recs, out, s);
+    if (rc != RSC_OK) return rc;
+    return launch_prefill_window(*a, slots, cu, N, T, has_init, qkv, s);
+  }
+};
 
 }  // namespace
 
 // Blocks of the grid: sequence i's ceil(len_i / 8) blocks start at floor(cu[i] / 8) + i, so
 // floor(T / 8) + N records per head cover every block.
 size_t prefill_blocked_bytes(const PoolView &pv, int N, int T) {
-  return ((size_t)T / TS + N) * pv.H * rec_floats(pv.V) * 4;
+  const size_t rec = pv.K == 64 ? Rec<64>::floats(pv.V) : Rec<128>::floats(pv.V);
+  return ((size_t)T / TS + N) * pv.H * rec * 4;
 }
 
 int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
                            int T, const uint8_t *has_init, const void *qkv,
                            const float *conv_w, const float *g, const float *beta, void *out,
                            void *ws, cudaStream_t s) {
-  if (a.st != RSC_F32 || a.pv.K != KB) return RSC_EDTYPE;
   float *recs = static_cast<float *>(ws);
-  const bool bf = a.io == RSC_BF16, kda = a.gate == RSC_GATE_KDA;
-  int rc = RSC_OK;
-  if (T > 0) {
-    const dim3 grid((unsigned)(T / TS + N), a.pv.H);
-#define RSC_BLK(IO_, V_, G_)                                                                  \
-  prefill_blk_kernel<IO_, V_, G_><<<grid, 128, 0, s>>>(a.pv, a.layer, slots, cu, N, T, has_init, \
-                                                       static_cast<const IO_ *>(qkv), conv_w, g, \
-                                                       beta, recs)
-    if (a.pv.V == 128) {
-      if (bf) { if (kda) RSC_BLK(bf16, 128, RSC_GATE_KDA); else RSC_BLK(bf16, 128, RSC_GATE_GDN); }
-      else { if (kda) RSC_BLK(float, 128, RSC_GATE_KDA); else RSC_BLK(float, 128, RSC_GATE_GDN); }
-    } else if (a.pv.V == 64) {
-      if (bf) { if (kda) RSC_BLK(bf16, 64, RSC_GATE_KDA); else RSC_BLK(bf16, 64, RSC_GATE_GDN); }
-      else { if (kda) RSC_BLK(float, 64, RSC_GATE_KDA); else RSC_BLK(float, 64, RSC_GATE_GDN); }
-    } else {
-      return RSC_EDTYPE;
-    }
-#undef RSC_BLK
-    if ((rc = launch_status()) != RSC_OK) return rc;
-  }
-  if (a.pv.V == 128)
-    rc = bf ? run_blocked_v<bf16, 128>(a, slots, cu, N, T, has_init, recs, out, s)
-            : run_blocked_v<float, 128>(a, slots, cu, N, T, has_init, recs, out, s);
-  else if (a.pv.V == 64)
-    rc = bf ? run_blocked_v<bf16, 64>(a, slots, cu, N, T, has_init, recs, out, s)
-            : run_blocked_v<float, 64>(a, slots, cu, N, T, has_init, recs, out, s);
-  else
-    return RSC_EDTYPE;
-  if (rc != RSC_OK) return rc;
-  return launch_prefill_window(a, slots, cu, N, T, has_init, qkv, s);
+  if (a.st == RSC_F32)
+    return a.io == RSC_F32
+               ? dispatch_k<BlockedLaunch, float, float>(a.pv.K, a.pv.V, a.gate, &a, slots, cu, N,
+                                                          T, has_init, qkv, conv_w, g, beta, out,
+                                                          recs, s)
+               : dispatch_k<BlockedLaunch, float, bf16>(a.pv.K, a.pv.V, a.gate, &a, slots, cu, N,
+                                                         T, has_init, qkv, conv_w, g, beta, out,
+                                                         recs, s);
+  // bf16 state: head_k 64 here, head_k 128 takes the tensor-core form
+  if (a.pv.K != 64) return RSC_EDTYPE;
+  return a.io == RSC_F32
+             ? dispatch_v<BlockedLaunch, bf16, float, 64>(a.pv.V, a.gate, &a, slots, cu, N, T,
+                                                          has_init, qkv, conv_w, g, beta, out,
+                                                          recs, s)
+             : dispatch_v<BlockedLaunch, bf16, bf16, 64>(a.pv.V, a.gate, &a, slots, cu, N, T,
+                                                         has_init, qkv, conv_w, g, beta, out,
+                                                         recs, s);
 }
 
 }  // namespace rsc

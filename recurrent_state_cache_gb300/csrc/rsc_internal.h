@@ -59,20 +59,11 @@ int launch_slot_copy(const PoolView &pv, int st, int io, int layer0, int nlayers
 
 size_t prefill_workspace_bytes(const PoolView &pv, int st, int N, int T);
 
-// Per-token prefill operands written by the prep kernel (fp32): q_hat, k_hat [T][H][K],
-// conv'd v [T][H][V], k_hat . q_hat [T][H].
-struct PrefillWs {
-  float *q, *k, *v, *kq;
-};
-size_t prefill_prep_bytes(const PoolView &pv, int T);
-PrefillWs prefill_carve(void *ws, const PoolView &pv, int T);
-int launch_prefill_prep(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
-                        int T, const uint8_t *has_init, const void *qkv, const float *conv_w,
-                        const PrefillWs &w, cudaStream_t s);
 // The slot's window becomes the last three raw inputs of each sequence.
 int launch_prefill_window(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
                           int T, const uint8_t *has_init, const void *qkv, cudaStream_t s);
-// Blocked fp32 path (fp32 state, K = 128): the recurrence eight tokens at a time.
+// Recurrent form of every pool the tensor-core form does not take: the recurrence eight tokens
+// at a time in closed form, fp32.
 size_t prefill_blocked_bytes(const PoolView &pv, int N, int T);
 int launch_prefill_blocked(const LayerArgs &a, const int32_t *slots, const int32_t *cu, int N,
                            int T, const uint8_t *has_init, const void *qkv,

@@ -525,10 +525,11 @@ def test_replay_bad_ring_position_flags(cuda_dev):
 # ------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("st,io,gate,K,V,lens,init", [
-    # token-serial fp32 path (K = 64)
+    # blocked path, K = 64 (fp32 and bf16 state, 2 key channels a lane)
     (0, 0, rsc.KDA, 64, 64, [1, 70, 2, 129], [1, 1, 0, 1]),
     (1, 1, rsc.KDA, 64, 128, [65, 3], [1, 0]),
-    # blocked fp32 path (fp32 state, K = 128): whole and ragged 8-token blocks
+    (1, 0, rsc.GDN, 64, 64, [9, 40], [0, 1]),
+    # blocked path, fp32 state, K = 128: whole and ragged 8-token blocks
     (0, 1, rsc.GDN, 128, 128, [200], [1]),
     (0, 0, rsc.KDA, 128, 128, [1, 7, 8, 9, 200], [1, 0, 1, 1, 0]),
     (0, 1, rsc.KDA, 128, 64, [70, 3], [0, 1]),

@@ -26,9 +26,9 @@ def _pools(dev, st, H, K, V, P, seed):
 
 
 @pytest.mark.parametrize("st,K", [
-    (rsc.F32, 64),    # token-serial fp32 path
-    (rsc.F32, 128),   # blocked fp32 path
-    (rsc.BF16, 64),   # token-serial path of a bf16-state pool
+    (rsc.F32, 64),    # blocked path, 2 key channels a lane
+    (rsc.F32, 128),   # blocked path, 4 key channels a lane
+    (rsc.BF16, 64),   # blocked path of a bf16-state pool
     (rsc.BF16, 128),  # chunkwise tensor-core path: chunk table and operand blocks in the array
 ])
 def test_noalloc_prefill_matches_workspace_prefill_twice(cuda_dev, st, K):
