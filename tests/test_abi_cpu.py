@@ -143,6 +143,25 @@ def test_calls_reject_bad_arguments_before_launch(rsc):
         L.ssm_pool_destroy(h)
 
 
+def test_prefill_workspace_of_the_blocked_form(rsc):
+    """Pools outside the tensor-core form (fp32 state, or head_k 64) size their prefill
+    workspace as one record per (8-token block, head): floor(T/8) + N blocks, each holding the
+    scaled keys and queries [16][K], end-scaled keys [8][K], e^Gamma_end [K], the A / P rows
+    [8][16], beta [8] and 8 of padding, and the values [V][8], in fp32."""
+    L = rsc.lib()
+    for st, K, V in [(rsc.F32, 128, 128), (rsc.F32, 64, 128), (rsc.BF16, 64, 64), (rsc.F32, 128, 64)]:
+        rc, h = _create(rsc, _desc(rsc, head_k=K, head_v=V, state_dtype=st))
+        assert rc == rsc.RSC_OK
+        try:
+            rec = 16 * K + 8 * K + K + 8 * 16 + 16 + 8 * V
+            for N, T in [(1, 0), (1, 7), (1, 8), (3, 100), (64, 13568)]:
+                n = ctypes.c_size_t()
+                assert L.kda_prefill_workspace_size(h, N, T, ctypes.byref(n)) == 0
+                assert n.value == (T // 8 + N) * 3 * rec * 4, (st, K, V, N, T)
+        finally:
+            L.ssm_pool_destroy(h)
+
+
 def test_pool_bytes_agree_with_oracle_layout(rsc):
     import oracle
     for (layers, slots, H, K, V, st, io) in [(69, 80, 12, 128, 128, 1, 1), (48, 1024, 32, 128, 128, 0, 1),
