@@ -377,6 +377,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   float *sSt = reinterpret_cast<float *>(smem + kChSt);
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_sbar;  // the staged rows (bulk copies)
   __shared__ float s_beta[kC];
   __shared__ int s_wide, s_grow;  // blocks beyond kDiagSpread (bit per block); a growing gate
 
@@ -397,10 +398,12 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   // tensor memory and the MMA barrier, ready long before the first product
   if (tid == 0) {
     mbar_init(&s_bar, 1);
+    mbar_init(&s_sbar, 1);
     s_wide = 0;
     s_grow = 0;
   }
   if (warp == 0) { tc::tmem_alloc(&s_taddr, 256); tc::tmem_relinquish(); }
+  bool staged = true;  // the staging barrier completed (false: it timed out)
 
   // the gates of this thread's rows and channels: their lines are prefetched into L2 at once,
   // the registers filled after the q/k conv pass
@@ -440,25 +443,31 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
   };
   if constexpr (sizeof(IO) == 2) {
     // bf16 inputs: the chunk's rows (3 before it, from the sequence or the slot's window,
-    // or zero for a fresh sequence) staged with cp.async, then a sliding window per
-    // (channel, half of the rows).
+    // or zero for a fresh sequence) staged by bulk copies, three contiguous runs a row (the
+    // head's q, k and v channels), completing on one barrier; then a sliding window per
+    // (channel, half of the rows).  (Per-thread 16-byte copies took 3216 requests a chunk.)
     bf16 *stg = reinterpret_cast<bf16 *>(smem + kChStg);
     const IO *Wn = reinterpret_cast<const IO *>(pv.conv) +
                    ((size_t)layer * (pv.P + 1) + slot) * 3 * (size_t)D;
     const int p0 = t0 - seq0 - 3;   // sequence position of staged row 0
-    for (int i = tid; i < kStageRows * (CH / 8); i += 256) {
-      const int row = i / (CH / 8), c8 = (i % (CH / 8)) * 8;
+    auto copied = [&](int row) { return row - 3 < Lc && (p0 + row >= 0 || init); };
+    __syncthreads();  // the staging barrier is initialised before any copy names it
+    if (tid == 0) {
+      uint32_t bytes = 0;
+      for (int row = 0; row < kStageRows; ++row)
+        if (copied(row)) bytes += CH * 2;
+      mbar_arrive_expect_tx(&s_sbar, bytes);
+    }
+    for (int i = tid; i < kStageRows * 3; i += 256) {
+      const int row = i / 3, c0 = (i % 3) * kK;  // runs start at channels 0, K, 2K
+      const uint32_t nbytes = (c0 < 2 * kK ? kK : V) * 2;
       const int pos = p0 + row;
-      const int src_c = src_channel(c8);
-      bf16 *dst = stg + row * kRowElems + c8;
-      if (row - 3 >= Lc) {
-        st16(dst, make_uint4(0, 0, 0, 0));
-      } else if (pos >= 0) {
-        cp_async16(dst, qkv + (size_t)(seq0 + pos) * D + src_c);
-      } else if (init) {
-        cp_async16(dst, Wn + (size_t)(3 + pos) * D + src_c);
+      bf16 *dst = stg + row * kRowElems + c0;
+      if (copied(row)) {
+        const IO *src = pos >= 0 ? qkv + (size_t)(seq0 + pos) * D : Wn + (size_t)(3 + pos) * D;
+        bulk_g2s(dst, src + src_channel(c0), nbytes, &s_sbar);
       } else {
-        st16(dst, make_uint4(0, 0, 0, 0));
+        for (uint32_t o = 0; o < nbytes; o += 16) st16(reinterpret_cast<char *>(dst) + o, make_uint4(0, 0, 0, 0));
       }
     }
     float4 *sW = reinterpret_cast<float4 *>(smem + kChW);
@@ -466,6 +475,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
       cp_async16(sW + (c % 8) * (CH / 8) + c / 8, conv_w + 4 * (size_t)src_channel(c));
     cp_async_commit();
     cp_async_wait_all();
+    staged = mbar_wait(&s_sbar, 0);
     __syncthreads();
     // q and k, conv and L2 norm in one pass: warp w takes tokens 8w .. 8w+7, lane l the eight
     // channels 8l .. 8l+7 of [q | k] (lanes 0-15 q, 16-31 k, so each row's sum of squares is
@@ -789,7 +799,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     tc::mma_commit(&s_bar);
   }
   const int q4 = warp & 3, half = warp >> 2;
-  bool ok = __syncthreads_and(mbar_wait(&s_bar, 0));
+  bool ok = __syncthreads_and(staged && mbar_wait(&s_bar, 0));
   tc::fence_after_sync();
   if (ok) {
     // B^T over the spent column operand: 16-byte rows, the channel order rotated by lane pair
@@ -1026,6 +1036,7 @@ prefill_tc_chunk_kernel(PoolView pv, int layer, const int32_t *__restrict__ slot
     }
   } else if (tid == 0) {
     flag_error(pv.err, RSC_DEVERR_TIMEOUT);
+    if (!staged) mbar_wait(&s_sbar, 0);  // the staged rows land before shared memory is released
   }
   tc::fence_before_sync();
   __syncthreads();
