@@ -145,8 +145,8 @@ def test_unrolled_closed_form_of_the_pages():
 
 @pytest.mark.parametrize("T", [8, 11])
 def test_block_closed_form_outputs_and_deltas(T):
-    # The ReplaySSM verify computes each block of up to eight tokens in closed form from the
-    # state at the block start S0 (G_t the cumulative log-decay from there):
+    # The ReplaySSM verify and the blocked prefill compute each block of up to eight tokens in
+    # closed form from the state at the block start S0 (G_t the cumulative log-decay from there):
     #   u_t = S0 (k_t . e^G_t) + sum_{s<t} A[t][s] d_s,  A[t][s] = sum_c k_s k_t e^(G_t - G_s)
     #   d_t = beta_t (v_t - u_t)
     #   o_t = S0 (q_t . e^G_t) + sum_{s<=t} P[t][s] d_s,  P[t][s] = sum_c k_s q_t e^(G_t - G_s)
