@@ -16,7 +16,8 @@ Legs reported in the same line (each timed separately with CUDA events):
   prefill      one KDA layer, 13600 tokens in chunked-prefill calls of 6144/6144/1312,
                a slot snapshot (ssm_slot_copy) after each call; bf16 state (tensor cores),
                then fp32 state (blocked closed form) on the same prompt and on 64 packed
-               212-token sequences
+               212-token sequences; the two forms' outputs and final states on the prompt
+               are compared (cross_check)
   slot_copy    64 (src, dst) pairs of the 69-layer decode pool, all layers, one launch
   spec         verify of 8 tokens (anchor + 7 drafts) for 64 requests into a 16-deep
                cache, then commit of a seeded accept count per request
@@ -340,10 +341,12 @@ def leg_gdn(dev, peaks, stream, batches=(1, 16, 64, 256)):
 PROMPT_CHUNKS = (6144, 6144, 1312)
 
 
-def _prompt_ms(dev, stream, st, seed):
+def _prompt_run(dev, stream, st, seed):
     """ms per 13600-token prompt: three kda_prefill_chunk calls of 6144/6144/1312 tokens chained
     through one slot of a 1-layer pool (H=12, K=V=128, bf16 inputs, state dtype st), a slot
-    snapshot after each; captured once in a CUDA graph and replayed."""
+    snapshot after each; captured once in a CUDA graph and replayed.  Also returns the outputs
+    and the slot's final state (every replay starts the prompt from a fresh state, so they are
+    the prompt's)."""
     import torch
     import recurrent_state_cache_gb300 as rsc
     from recurrent_state_cache_gb300 import binding as b
@@ -376,7 +379,12 @@ def _prompt_ms(dev, stream, st, seed):
 
     ms = timed(graph_of(run, stream).replay, 5, 2, stream)
     assert rsc.rsc_get_device_error(pool) == 0
-    return ms
+    return ms, out, pool.ssm[0, 1]
+
+
+def _max_rel_err(got, ref) -> float:
+    got, ref = got.float(), ref.float()
+    return float((got - ref).abs().max() / ref.abs().max().clamp_min(1e-30))
 
 
 def leg_prefill(dev, peaks, stream):
@@ -384,7 +392,7 @@ def leg_prefill(dev, peaks, stream):
     H, K, V = 12, 128, 128
     T = sum(PROMPT_CHUNKS)
     D = H * (2 * K + V)
-    ms = _prompt_ms(dev, stream, b.BF16, 2)
+    ms, out_tc, state_tc = _prompt_run(dev, stream, b.BF16, 2)
     flops = prefill_flops(T, H, K, V)
     io_bytes = T * D * 2 + T * H * K * 4 + T * H * 4 + T * H * V * 2
     res = {"config": "1 KDA layer, H=12, K=V=128, bf16, 13600 tokens as 6144/6144/1312, snapshot copy after each",
@@ -394,19 +402,28 @@ def leg_prefill(dev, peaks, stream):
            "io_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
            "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "path": "chunkwise, tcgen05 tensor cores"}
-    res["f32_state"] = leg_prefill_f32(dev, stream)
+    res["f32_state"], out_f32, state_f32 = leg_prefill_f32(dev, stream)
+    # The two forms on the same prompt (same seed): the tensor-core form's bf16 operands
+    # against the fp32 closed form, at the bf16 bar (max |difference| / max |fp32 value|).
+    res["cross_check"] = {
+        "what": "bf16-state tensor-core prefill against the fp32-state blocked prefill on the same "
+                "13600-token prompt: every output, and the final state",
+        "out_max_rel_err": round(_max_rel_err(out_tc, out_f32), 5),
+        "state_max_rel_err": round(_max_rel_err(state_tc, state_f32), 5),
+        "bar": 0.02}
     return res
 
 
 def leg_prefill_f32(dev, stream, nseq=64, seqlen=212):
     """The fp32-state prefill (the recurrence eight tokens at a time in closed form, fp32 on the
-    CUDA cores) at the same head shape (H=12, K=V=128, bf16 inputs): the 13600-token prompt as
-    in the bf16 leg, and a batch of 64 packed 212-token sequences from fresh slots."""
+    CUDA cores) at the same head shape (H=12, K=V=128, bf16 inputs): the bf16 leg's 13600-token
+    prompt (same inputs), and a batch of 64 packed 212-token sequences from fresh slots.
+    Returns the leg's figures, and the prompt's outputs and final state."""
     import torch
     import recurrent_state_cache_gb300 as rsc
     from recurrent_state_cache_gb300 import binding as b
     T = sum(PROMPT_CHUNKS)
-    ms_prompt = _prompt_ms(dev, stream, b.F32, 3)
+    ms_prompt, out_prompt, state_prompt = _prompt_run(dev, stream, b.F32, 2)
     H, K, V = 12, 128, 128
     Tb = nseq * seqlen
     gen = torch.Generator(device=dev)
@@ -426,13 +443,14 @@ def leg_prefill_f32(dev, stream, nseq=64, seqlen=212):
                                         has_initial_state=fresh, out=out, workspace=ws)
     ms_batch = timed(graph_of(run, stream).replay, 5, 2, stream)
     assert rsc.rsc_get_device_error(pool) == 0
-    return {"config": f"1 KDA layer, H=12, K=V=128, fp32 state, bf16 io: the {T}-token prompt as "
+    leg = {"config": f"1 KDA layer, H=12, K=V=128, fp32 state, bf16 io: the {T}-token prompt as "
                       f"6144/6144/1312 with snapshots; {nseq} packed {seqlen}-token sequences",
             "ms_per_prefill": round(ms_prompt, 4), "tokens_per_s": round(T / (ms_prompt * 1e-3), 1),
             "us_per_token": round(ms_prompt * 1e3 / T, 4),
             "batch_ms": round(ms_batch, 4), "batch_tokens_per_s": round(Tb / (ms_batch * 1e-3), 1),
             "path": "8-token blocks in closed form (per-block conv/norm/operand kernel, blocked "
                     "recurrence, window kernel)"}
+    return leg, out_prompt, state_prompt
 
 
 def leg_copy(dev, peaks, stream, wl):
